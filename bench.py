@@ -1,0 +1,420 @@
+"""Benchmark: paged decode attention on one GB300 (or N independent replicas).
+
+A step is one decode iteration of one attention layer over the whole batch:
+pa_kv_append of every sequence's new token, then pa_decode_attention (and its
+split-K merge when the plan has more than one partition).  The metric is the
+KV-read bandwidth of that step, counted from the algorithmic bytes (K/V of
+every cached token read once, q read, out written) and also reported as
+sequence-steps per second and as a fraction of the measured HBM peak.
+
+    python bench.py [--workload 8b|70b|long|fp8prefix] [--steps K] [--warmup W]
+                    [--splits S] [--impl ours|reference] [--gpus N]
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) every rank runs an
+independent replica of the workload on its own GPU (the path has no exchange
+step); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak), seq-steps/sec"
+UNIT = "GB/s"
+FALLBACK_HBM = 6800.0
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM, "fallback"
+
+
+def algorithmic_bytes(w):
+    """K/V bytes of every cached token of every sequence (logical, once per sequence),
+    plus q read and out written.  Unique-physical KV bytes reported beside it."""
+    elt = 1 if w.kv == "fp8" else 2
+    tok = 2 * w.Hkv * w.d * elt
+    lens = np.asarray(w.seq_lens, dtype=np.int64)
+    qo = 2 * w.B * w.Hq * w.d * 2
+    return int(lens.sum()) * tok + qo, int(lens.sum()) * tok, qo
+
+
+def unique_kv_bytes(w, tables):
+    elt = 1 if w.kv == "fp8" else 2
+    blocks = set()
+    for b, L in enumerate(w.seq_lens):
+        nb = -(-int(L) // w.bs)
+        blocks.update(int(x) for x in tables[b, :nb])
+    # a block holds full pages; count tokens actually cached in each distinct block
+    return len(blocks) * w.bs * 2 * w.Hkv * w.d * elt
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        except Exception:
+            sel = str(device_index)
+        self.cmd = ["nvidia-smi", "-i", sel, "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                    "-lms", "200"]
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("pa_decode.cu", "pa_device.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_294_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload, splits_used):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash() and e.get("splits") == splits_used:
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+        return dist, dist.get_rank(), ws
+    return None, 0, 1
+
+
+def cpu_oracle_baseline(w, tables, budget_s=10.0, threads=None):
+    """The fp64 oracle's step (append of the new token + decode attention) on a bounded
+    sample of the batch, repeated until ~budget_s of wall time.  Returns dict."""
+    import oracle.run
+    threads = threads or os.cpu_count() or 1
+    rng = np.random.default_rng(0)
+    order = rng.permutation(w.B)
+    # grow the sample until one oracle step takes ~1/5 of the budget
+    n = min(w.B, max(1, threads))
+    while True:
+        seqs = sorted(order[:n].tolist())
+        st = oracle.run.OracleStep(w, seqs=seqs, tables=tables)
+        t0 = time.perf_counter()
+        st.append()
+        st.decode(threads=threads)
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 5 or n >= w.B:
+            break
+        n = min(w.B, n * 2)
+    reps, total = 1, dt
+    while total < budget_s and reps < 50:
+        st = oracle.run.OracleStep(w, seqs=seqs, tables=tables)
+        t0 = time.perf_counter()
+        st.append()
+        st.decode(threads=threads)
+        total += time.perf_counter() - t0
+        reps += 1
+    lens = np.asarray(w.seq_lens, dtype=np.int64)[seqs]
+    elt = 1 if w.kv == "fp8" else 2
+    byts = int(lens.sum()) * 2 * w.Hkv * w.d * elt + 2 * len(seqs) * w.Hq * w.d * 2
+    per_step = total / reps
+    return {"value": byts / per_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d of %d sequences (%d tokens), fp64 C oracle append+decode, %d reps, %.1f s" %
+                      (len(seqs), w.B, int(lens.sum()), reps, total),
+            "seq_steps_per_s": len(seqs) / per_step}
+
+
+def run_reference(args):
+    """The oracle arm: the fp64 CPU oracle timed on the host cores, rank 0 only."""
+    dist, rank, world = dist_init()
+    if rank != 0:
+        return
+    w = workloads.make(args.workload, device="cpu")
+    import oracle.run
+    tables = oracle.run.tables_of(w)
+    threads = os.cpu_count() or 1
+    # per step: a bounded sample of the batch sized for ~2 s of CPU work
+    rng = np.random.default_rng(1)
+    n = max(1, min(w.B, threads))
+    seqs = sorted(rng.permutation(w.B)[:n].tolist())
+    times = []
+    for i in range(args.warmup + args.steps):
+        st = oracle.run.OracleStep(w, seqs=seqs, tables=tables)
+        t0 = time.perf_counter()
+        st.append()
+        st.decode(threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    lens = np.asarray(w.seq_lens, dtype=np.int64)[seqs]
+    elt = 1 if w.kv == "fp8" else 2
+    byts = int(lens.sum()) * 2 * w.Hkv * w.d * elt + 2 * len(seqs) * w.Hq * w.d * 2
+    t = sum(times)
+    value = byts * len(times) / t / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "seq_steps_per_s": len(seqs) * len(times) / t,
+            "config": {"workload": args.workload, "desc": w.desc, "sample_sequences": len(seqs)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d of %d sequences per step, fp64 C oracle append+decode" %
+                                       (len(seqs), w.B)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def run_ours(args):
+    import paged_kv_cache_294_gb300 as pa
+    from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
+    import oracle.run
+
+    dist, rank, world = dist_init()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pa.load()
+
+    w = workloads.make(args.workload, device=dev)
+    layer = PagedDecodeLayer.from_workload(w, dev)
+    S = layer.num_splits(args.splits)
+    layer.ensure_workspace(args.splits)
+    alg, kv_bytes, qo_bytes = algorithmic_bytes(w)
+    uniq = unique_kv_bytes(w, layer.tables_host)
+
+    # parity once, before timing: the step's output on sampled sequences vs the oracle
+    pa.pa_get_device_error(clear=True)
+    layer.step(num_splits=args.splits)
+    torch.cuda.synchronize()
+    flags = pa.pa_get_device_error()
+    sample = sorted({0, w.B - 1, w.B // 2})
+    st = oracle.run.OracleStep(w, seqs=sample, tables=layer.tables_host)
+    st.append()
+    ref = st.decode(threads=os.cpu_count() or 1)
+    err = float(np.max(np.abs(layer.out.float().cpu().numpy()[sample] - ref)))
+    tol = 5e-2 if w.kv == "fp8" else 1e-2
+    parity = {"max_abs_err": err, "tol": tol, "sequences": sample, "ok": bool(err <= tol and flags == 0)}
+    if not parity["ok"]:
+        print("parity check failed: %s flags=%#x" % (parity, flags), file=sys.stderr)
+        sys.exit(3)
+
+    # the cache must hold exactly the history before each timed append: re-running the
+    # append of the same token to the same slot rewrites identical bytes (bf16) and, for
+    # fp8, keeps the block scale (max(old, same absmax)) -- every step does identical work.
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 2 x L2
+    stream = torch.cuda.current_stream(dev)
+    launches_per_step = 2 + (1 if S > 1 else 0)
+
+    def one_step():
+        layer.append_step()
+        layer.decode(num_splits=args.splits)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        one_step()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()                       # evict the previous step's lines from L2 (untimed)
+            ev[i][0].record(stream)
+            layer.append_step()
+            ev[i][1].record(stream)
+            layer.decode(num_splits=args.splits)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    t_step = sum(step_ms) / 1e3
+    t_dec = sum(dec_ms) / 1e3
+    if dist:
+        t = torch.tensor([t_step, t_dec], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_step, t_dec = float(t[0]), float(t[1])
+    K = args.steps
+    value = world * alg * K / t_step / 1e9
+    dec_gbs = alg * K / t_dec / 1e9
+    peak, peak_kind = hbm_peak()
+
+    # end to end through the public API with host buffers: H2D of the step's inputs from
+    # pinned memory, append + decode, D2H of the output, all inside the timed region
+    h_q = w.q.cpu().pin_memory()
+    h_kn = w.k_new.cpu().pin_memory()
+    h_vn = w.v_new.cpu().pin_memory()
+    h_slots = torch.from_numpy(layer.step_slots_host).pin_memory()
+    h_tab = torch.from_numpy(layer.tables_host).pin_memory()
+    h_len = torch.from_numpy(layer.lens_host).pin_memory()
+    h_out = torch.empty(tuple(layer.out.shape), dtype=torch.bfloat16).pin_memory()
+    d_q, d_kn, d_vn = torch.empty_like(layer.q), torch.empty_like(layer.k_new), torch.empty_like(layer.v_new)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tab, h_len))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q.copy_(h_q, non_blocking=True)
+        d_kn.copy_(h_kn, non_blocking=True)
+        d_vn.copy_(h_vn, non_blocking=True)
+        layer.step_slots.copy_(h_slots, non_blocking=True)
+        layer.block_tables.copy_(h_tab, non_blocking=True)
+        layer.seq_lens.copy_(h_len, non_blocking=True)
+        layer.append_step(d_kn, d_vn)
+        layer.decode(q=d_q, num_splits=args.splits)
+        h_out.copy_(layer.out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        ee[i][0].record(stream)
+        e2e_step()
+        ee[i][1].record(stream)
+    torch.cuda.synchronize()
+    t_e2e = sum(a.elapsed_time(b) for a, b in ee) / 1e3
+    if dist:
+        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t[0])
+    e2e_value = world * alg * K / t_e2e / 1e9
+
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_baseline(w, layer.tables_host, budget_s=args.cpu_seconds)
+    clk = clocks.summary()
+    traffic = ncu_traffic(args.workload, S)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_step / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3-cache/f16-mma/f32-softmax" if w.kv == "fp8" else "bf16-cache/bf16-mma/f32-softmax",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "desc": w.desc, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+                   "head_dim": w.d, "block_size": w.bs, "kv": w.kv, "num_splits": S,
+                   "tokens": int(np.sum(w.seq_lens)), "parallelism": "replicas" if world > 1 else "1 gpu",
+                   "l2": "512 MiB memset between timed steps (untimed); step reads > L2"},
+        "seq_steps_per_s": world * w.B * K / t_step,
+        "hbm_frac_of_%s" % peak_kind: (value / world) / peak,
+        "decode_only": {"GBps": dec_gbs, "us_per_call": 1e6 * t_dec / K},
+        "bytes_per_step": {"algorithmic": alg, "kv_logical": kv_bytes, "q_out": qo_bytes,
+                           "kv_unique_physical": uniq},
+        "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(dec_gbs / peak, 4), "traffic": traffic,
+                     "peak_source": peak_kind, "kernel": "pa_decode_attention (decode + merge)"},
+        "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "parity": parity,
+        "wall_s_timed_region": wall,
+    }
+    if cpu:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="8b", choices=sorted(workloads.CONFIGS))
+    ap.add_argument("--splits", type=int, default=0, help="split-K partitions (0 = automatic)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,252 @@
+/*
+ * pa.h - C ABI of libpagedattn.so: single-token decode attention over a
+ * paged KV cache, for NVIDIA GB300 (sm_103a).
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [P1] "KV cache & continuous batching" (docs.masst.dev/ai/inference/kv-cache-batching)
+ *   [P2] "LLM Serving - KV Cache, Batching, Speculative Decoding"
+ *        (dineshblog.com/blog/session-124-llm-serving)
+ *   [P3] "LLM Inference Optimization: KV Cache, Batching, and Speculative
+ *        Decoding" (adaptiverecall.com/open-source-llms/inference-optimization.php)
+ *
+ * Conventions for every call
+ *   - Device pointers are owned by the caller (for example allocated by
+ *     PyTorch).  The device entry points allocate no device memory, never
+ *     synchronise the device, and enqueue their kernels on the caller's
+ *     stream, passed as `void* stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Host pointers are read only during the call.
+ *   - Errors are return codes (pa_status); nothing throws, nothing aborts.
+ *     Argument errors are found on the host before any launch and leave every
+ *     buffer untouched.
+ *   - Values that only the device can check (block ids read from a block
+ *     table, lengths read from seq_lens, slots read from slot_mapping) are
+ *     range-checked inside the kernels: an offending element is skipped or
+ *     clamped (no out-of-bounds access is ever made) and a bit is set in a
+ *     per-device error word that pa_get_device_error() returns.
+ *
+ * Memory layout (all row-major, innermost last)
+ *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
+ *                     bf16 (PA_KV_BF16) or e4m3 bytes (PA_KV_FP8_E4M3).
+ *                     One (block, kv_head) page is contiguous.
+ *   k_scale, v_scale  [num_blocks][num_kv_heads] fp32 (fp8 cache only)
+ *   q, out            [batch][num_q_heads][head_dim] bf16
+ *   k_new, v_new      [num_tokens][num_kv_heads][head_dim] bf16
+ *   block_tables      [batch][max_blocks_per_seq] int32: physical block of
+ *                     logical block j of sequence b ([P1] "2. PagedAttention")
+ *   seq_lens          [batch] int32, tokens of each sequence including the one
+ *                     appended this step
+ *   slot_mapping      [num_tokens] int64, slot = block * block_size + offset
+ *
+ * Query head i reads KV head i / (num_q_heads / num_kv_heads) (grouped-query
+ * attention, [P1] "KV cache memory math"; consecutive query heads share a KV
+ * head, the pages leave the order open).
+ */
+#ifndef PAGEDATTN_PA_H
+#define PAGEDATTN_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID = 1,     /* bad argument (shape, null pointer, range, workspace too small) */
+    PA_ERR_OOM = 2,         /* allocator: not enough free blocks (nothing was taken) */
+    PA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
+    PA_ERR_UNSUPPORTED = 4  /* valid request this build does not implement (e.g. fp8 with head_dim 64) */
+} pa_status;
+
+typedef enum {
+    PA_KV_BF16 = 0,
+    PA_KV_FP8_E4M3 = 1
+} pa_kv_dtype;
+
+/* Bits of the per-device error word (pa_get_device_error). */
+#define PA_DEVERR_BLOCK_ID   0x1u   /* a block table entry outside [0, num_blocks) (clamped to block 0) */
+#define PA_DEVERR_SEQ_LEN    0x2u   /* seq_len < 0 or > max_blocks_per_seq * block_size (clamped) */
+#define PA_DEVERR_SLOT       0x4u   /* slot >= num_blocks * block_size (token skipped) */
+#define PA_DEVERR_TIMEOUT    0x8u   /* a pipeline wait exceeded its bound; the kernel gave up */
+
+/* Human-readable name of a status code (static string). */
+const char* pa_status_string(pa_status s);
+
+/* ---------------------------------------------------------------------------
+ * pa_kv_append - write the K/V of new tokens into the paged cache.
+ *
+ * Defines: [P2] "Recall and stretch" item 3 (keys/values are written in
+ * prefill and appended in decode) and [P1] "The core insight" (decode
+ * computes K/V for the new token only).  Token t, KV head h is written to
+ * cache[slot / block_size][h][slot % block_size][:], slot = slot_mapping[t];
+ * a negative slot skips the token.
+ *
+ * PA_KV_BF16: an exact copy of the bf16 bits; k_scale / v_scale must be NULL.
+ *
+ * PA_KV_FP8_E4M3 ([P1] "KV cache memory math": fp8 = 1 byte per element;
+ * [P3] "Memory Bandwidth Optimization": KV-cache quantization): one fp32
+ * scale per (block, kv_head), separately for K and V.  For each block p that
+ * this call writes, with f = the smallest offset written:
+ *     old = 0 if f == 0 else scale[p][h]
+ *     s   = max(old, fp32(max|x| over the new values) / 448)
+ *     if s > old > 0, each older entry (offset < f) is re-encoded as
+ *         E4M3(fp32(value(e) * old) / s)
+ *     each new value x is stored as E4M3(x / s) (round to nearest even,
+ *     saturating at +-448); all codes are +0 when s == 0;  scale[p][h] = s.
+ * Precondition (fp8 only): the tokens a call writes into one block form one
+ * run of consecutive entries of slot_mapping with increasing offsets (true for
+ * one decode token per sequence and for a prefill of one sequence).  A
+ * violation gives unspecified cache contents but no out-of-bounds access.
+ *
+ * num_blocks * num_kv_heads * block_size must be below 2^31.  head_dim in
+ * {64, 128} (fp8: 128), block_size in {16, 32}.  num_tokens == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                       const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                       int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                       int block_size, int kv_dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Split-K (flash-decoding) planning for pa_decode_attention.
+ *
+ * With S = num_splits the tokens of every sequence are cut into partitions
+ * of P = ceil(max_blocks_per_seq / S) blocks; sequence b uses
+ * ceil(ceil(seq_len_b / block_size) / P) partitions.  Each partition yields a
+ * normalised partial output and its log-sum-exp, combined as
+ *     out = sum_i exp(lse_i - L) o_i,  L = log sum_i exp(lse_i)
+ * which equals the unsplit result in exact arithmetic.  num_splits == 0
+ * picks S from the batch shape and the current device's SM count.
+ *
+ * pa_decode_resolve_splits returns the S that pa_decode_attention will use for
+ * the request (0 asks for the automatic choice); the workspace must hold
+ * pa_decode_workspace_bytes(...) bytes for that S (0 bytes when S == 1).
+ * Workspace layout: o_part fp32 [batch][num_q_heads][S][head_dim], then
+ * lse fp32 [batch][num_q_heads][S], 256-byte aligned.
+ * ------------------------------------------------------------------------- */
+int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits);
+size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int num_splits);
+
+/* ---------------------------------------------------------------------------
+ * pa_decode_attention - one decode step's attention for a batch.
+ *
+ * Defines: [P1] "The core insight" (the new token's query attends over all
+ * cached K and V), [P2] "Hands-on: cache equivalence and scheduling oracles"
+ * (cached attention = softmax(q . K^T * scale) . V, the last row of causal
+ * attention), [P1] "2. PagedAttention" (K and V gathered through the block
+ * table, blocks need not be contiguous), [P3] "FlashAttention" (scores,
+ * softmax and P.V fused on chip, fp32 online softmax).
+ *
+ *   out[b][i][:] = sum_t softmax_t(scale * q[b][i] . K_t) V_t,
+ *   t = 0 .. seq_lens[b]-1,  K_t = k_cache[block_tables[b][t / bs]][i / G][t % bs]
+ * fp8: K_t and V_t elements are value(code) * scale[block][kv_head].
+ * A sequence with seq_len 0 gives a zero row.  The outputs are bf16.
+ *
+ * num_blocks * num_kv_heads * block_size must be below 2^31; head_dim in
+ * {64, 128} (fp8: 128); block_size in {16, 32}; num_q_heads a multiple of
+ * num_kv_heads with a group size of at most 8.  batch == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, int kv_dtype, void* stream);
+
+/* Read (and optionally clear) the current device's error word; synchronises
+ * the device.  *flags receives an OR of PA_DEVERR_* bits set since the last
+ * clear. */
+pa_status pa_get_device_error(uint32_t* flags, int clear);
+
+/* Enqueue a one-warp kernel that waits on a shared-memory barrier phase that
+ * nothing completes, through the same bounded wait the decode pipeline uses.
+ * The wait gives up after about two seconds, the kernel ends normally and
+ * PA_DEVERR_TIMEOUT is set in the device error word: a check, without any
+ * GPU fault, that no barrier wait in this library can hang a GPU. */
+pa_status pa_selftest_bounded_wait(void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host side: block allocator, accounting, slots, scheduler simulator.
+ * No device access.  Not thread-safe per allocator object.
+ * ------------------------------------------------------------------------- */
+
+/* Paged KV-block pool: [P1] "2. PagedAttention" (fixed-size blocks allocated
+ * on demand and freed when done, not necessarily contiguous) and [P2] "KV
+ * memory, paging and prefix identity" (physical blocks shared between
+ * sequences).  Reference counted; an allocation takes the lowest free ids in
+ * increasing order (a deterministic policy: the pages fix none). */
+typedef struct pa_allocator pa_allocator;
+
+/* NULL on bad arguments (num_blocks < 0, block_size <= 0) or out of memory. */
+pa_allocator* pa_allocator_create(int num_blocks, int block_size);
+void pa_allocator_destroy(pa_allocator* a);
+/* n blocks, all or nothing; ids written to out_ids[0..n-1].  PA_ERR_OOM if
+ * fewer than n are free (nothing taken). */
+pa_status pa_block_alloc(pa_allocator* a, int n, int32_t* out_ids);
+/* Drop one reference per listed id; a block is free again at zero.  Any id
+ * out of range or without enough references: PA_ERR_INVALID and no change. */
+pa_status pa_block_free(pa_allocator* a, const int32_t* ids, int n);
+/* Take one more reference per listed id (prefix sharing, [P3] "KV Cache
+ * Management": 100 requests sharing one system prompt).  Every id must be
+ * allocated; otherwise PA_ERR_INVALID and no change. */
+pa_status pa_block_share(pa_allocator* a, const int32_t* ids, int n);
+int pa_allocator_num_free(const pa_allocator* a);
+int pa_allocator_num_blocks(const pa_allocator* a);
+/* References held on block id (0 = free); -1 if id is out of range. */
+int pa_allocator_refcount(const pa_allocator* a, int32_t id);
+
+/* Blocks needed for `tokens` tokens: ceil(tokens / block_size) ([P1] "Visual:
+ * the lifecycle of a request": 50 tokens use 4 blocks, 5000 use 313).
+ * 0 for tokens <= 0 or block_size <= 0. */
+int64_t pa_blocks_for_tokens(int64_t tokens, int block_size);
+
+/* KV-cache bytes: 2 x layers x kv_heads x head_dim x tokens x batch x
+ * dtype_bits / 8 ([P1] "KV cache memory math"; [P2] "KV memory, paging and
+ * prefix identity": GQA/MQA count KV heads).  dtype_bits 16 for bf16/fp16, 8
+ * for fp8/int8, 4 for int4.  Returns 0 if an argument is negative. */
+uint64_t pa_kv_bytes(int layers, int kv_heads, int head_dim, int dtype_bits, int64_t tokens,
+                     int64_t batch);
+
+/* slots[t] = block_tables[seq_ids[t]][positions[t] / block_size] * block_size
+ *            + positions[t] % block_size
+ * ([P1] "2. PagedAttention": the table maps logical positions to physical
+ * blocks).  PA_ERR_INVALID if a position is negative or beyond the table. */
+pa_status pa_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* seq_ids, const int32_t* positions, int num_tokens,
+                          int block_size, int64_t* slots);
+
+/* Unit-time scheduler simulator ([P2] "Static versus continuous scheduling"
+ * and "Hands-on"): mode 0 = static cohorts of `slots` requests (each cohort
+ * lasts as long as its longest member), mode 1 = iteration-level (a freed
+ * slot is refilled before the next iteration).  out_lens are the requests'
+ * output lengths in arrival order.  Requires slots > 0 and out_lens > 0
+ * (zero slots would never finish): otherwise PA_ERR_INVALID.  n == 0 gives
+ * 0 iterations.  [5,20,10,15,10] with 3 slots: 35 static, 20 continuous. */
+pa_status pa_sched_simulate(const int64_t* out_lens, int n, int slots, int mode, int64_t* iters);
+
+/* Iteration-level scheduler with KV admission ([P1] "1. Continuous
+ * (iteration-level) batching": admit while KV blocks remain, decode one
+ * token for every active request, free a finished request's blocks at once;
+ * [P1] "Pitfalls" 1 and 5: a request is admitted only when its reserved
+ * tokens fit, at most max_num_seqs run at once).
+ * Request r needs prompt_lens[r] + out_lens[r] tokens; admission reserves
+ * blocks for them all (pa_blocks_for_tokens) from `a`, in arrival order, and
+ * the head of the queue blocks later ones when it does not fit.  Runs until
+ * every request has finished or until `stop_iter` iterations (stop_iter < 0:
+ * run to the end).  Outputs (may be NULL): *iters = iterations run;
+ * admitted_at[r] / finished_at[r] = iteration of admission / completion
+ * (-1 if not reached); tables (n x max_blocks_per_seq, -1 padded) and
+ * lens (tokens held) of the requests still active when it stops.
+ * PA_ERR_INVALID on bad arguments or if a single request can never fit. */
+pa_status pa_sched_continuous_kv(pa_allocator* a, const int64_t* prompt_lens,
+                                 const int64_t* out_lens, int n, int max_num_seqs,
+                                 int64_t stop_iter, int max_blocks_per_seq, int64_t* iters,
+                                 int64_t* admitted_at, int64_t* finished_at, int32_t* tables,
+                                 int32_t* lens);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_PA_H */

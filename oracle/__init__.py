@@ -17,6 +17,8 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
   e4m3_encode/value       nearest-value brute force over the 256-code table, format facts
   kv_bytes/blocks_for     the pages' printed per-token sizes and block counts
   sched_*                 the pages' printed iteration counts
+  sched_continuous_kv     equals sched_continuous when memory never binds; equal-size
+                          requests under a pool of k reservations behave as k slots
   Allocator               lowest-id / refcount invariants on hand-checked traces
 """
 from __future__ import annotations
@@ -74,6 +76,7 @@ def _load():
             "or_alloc_share": (i32, [P, P, i32]),
             "or_alloc_refcount": (i32, [P, i32]),
             "or_slot_mapping": (i32, [P, i32, P, P, i32, i32, P]),
+            "or_sched_continuous_kv": (i32, [P, i32, P, P, i32, i32, i64, i32, P, P, P, P, P]),
             "or_kv_append_bf16": (i32, [P, P, P, P, P, i32, i64, i32, i32, i32]),
             "or_kv_append_fp8": (i32, [P, P, P, P, P, P, P, i32, i64, i32, i32, i32]),
             "or_decode_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
@@ -194,6 +197,27 @@ class Allocator:
 
     def refcount(self, i: int) -> int:
         return int(self._lib.or_alloc_refcount(self._h, int(i)))
+
+
+def sched_continuous_kv(alloc: Allocator, block_size: int, prompt_lens, out_lens, max_num_seqs: int,
+                        stop_iter: int = -1, M: int = 0) -> dict:
+    """Iteration-level scheduling with KV admission on `alloc` (see the C file)."""
+    p = np.ascontiguousarray(np.asarray(prompt_lens, dtype=np.int64))
+    o = np.ascontiguousarray(np.asarray(out_lens, dtype=np.int64))
+    n = len(p)
+    it = np.zeros(1, np.int64)
+    adm = np.zeros(max(n, 1), np.int64)
+    fin = np.zeros(max(n, 1), np.int64)
+    tables = np.zeros((max(n, 1), max(M, 1)), np.int32)
+    lens = np.zeros(max(n, 1), np.int32)
+    rc = _load().or_sched_continuous_kv(alloc._h, int(block_size), _p(p) if n else None,
+                                        _p(o) if n else None, n, int(max_num_seqs), int(stop_iter),
+                                        int(M), _p(it), _p(adm), _p(fin), _p(tables) if M > 0 else None,
+                                        _p(lens))
+    if rc != 0:
+        raise ValueError("invalid scheduler arguments")
+    return dict(iters=int(it[0]), admitted_at=adm[:n], finished_at=fin[:n], tables=tables[:n, :M],
+                lens=lens[:n])
 
 
 # ---------------------------------------------------------------- slots

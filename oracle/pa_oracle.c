@@ -520,3 +520,79 @@ int or_decode_attention_split(double* out, const uint16_t* q, const void* k_cach
     free(plse);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Iteration-level scheduling with KV admission: [P1] "1. Continuous        */
+/* (iteration-level) batching" (admit while KV memory remains, decode one    */
+/* token for every active request in one pass, free a finished request's     */
+/* blocks immediately) and [P1] "Pitfalls" 1 and 5 (a request reserves KV    */
+/* for its whole budget; admission is refused when it does not fit; at most  */
+/* max_seqs requests run).  Request r reserves ceil((prompt+out)/bs) blocks. */
+/* Waiting requests are admitted strictly in arrival order.                  */
+/* ------------------------------------------------------------------------ */
+int or_sched_continuous_kv(or_alloc* a, int bs, const int64_t* prompt, const int64_t* outl, int n,
+                           int max_seqs, int64_t stop_iter, int M, int64_t* iters, int64_t* admitted,
+                           int64_t* finished, int32_t* tables, int32_t* lens) {
+    int r, j, head = 0, active = 0;
+    int64_t it = 0;
+    int* state;          /* 0 waiting, 1 active, 2 done */
+    int64_t* gen;
+    int64_t* nblk;
+    int32_t* blocks;     /* n x maxb */
+    int64_t maxb = 1;
+    if (n < 0 || max_seqs <= 0 || bs <= 0) return -1;
+    for (r = 0; r < n; r++) {
+        int64_t need;
+        if (prompt[r] < 0 || outl[r] <= 0) return -1;
+        need = or_blocks_for_tokens(prompt[r] + outl[r], bs);
+        if (need > a->n || (tables && need > M)) return -1;
+        if (need > maxb) maxb = need;
+    }
+    state = (int*)calloc((size_t)(n > 0 ? n : 1), sizeof(int));
+    gen = (int64_t*)calloc((size_t)(n > 0 ? n : 1), sizeof(int64_t));
+    nblk = (int64_t*)calloc((size_t)(n > 0 ? n : 1), sizeof(int64_t));
+    blocks = (int32_t*)calloc((size_t)(n > 0 ? n : 1) * (size_t)maxb, sizeof(int32_t));
+    if (!state || !gen || !nblk || !blocks) { free(state); free(gen); free(nblk); free(blocks); return -1; }
+    for (r = 0; r < n; r++) {
+        if (admitted) admitted[r] = -1;
+        if (finished) finished[r] = -1;
+    }
+    while ((head < n || active > 0) && (stop_iter < 0 || it < stop_iter)) {
+        /* admit from the head of the queue */
+        while (head < n && active < max_seqs) {
+            int64_t need = or_blocks_for_tokens(prompt[head] + outl[head], bs);
+            if (or_alloc_num_free(a) < need) break;
+            or_alloc_alloc(a, (int)need, blocks + (int64_t)head * maxb);
+            nblk[head] = need;
+            state[head] = 1;
+            if (admitted) admitted[head] = it;
+            active++;
+            head++;
+        }
+        if (active == 0) { free(state); free(gen); free(nblk); free(blocks); return -1; }
+        /* one iteration: every active request emits a token */
+        for (r = 0; r < n; r++) {
+            if (state[r] != 1) continue;
+            gen[r]++;
+            if (gen[r] >= outl[r]) {
+                or_alloc_free(a, blocks + (int64_t)r * maxb, (int)nblk[r]);
+                state[r] = 2;
+                active--;
+                if (finished) finished[r] = it;
+            }
+        }
+        it++;
+    }
+    if (iters) *iters = it;
+    for (r = 0; r < n; r++) {
+        if (lens) lens[r] = state[r] == 1 ? (int32_t)(prompt[r] + gen[r]) : 0;
+        if (tables)
+            for (j = 0; j < M; j++)
+                tables[(int64_t)r * M + j] = (state[r] == 1 && j < nblk[r]) ? blocks[(int64_t)r * maxb + j] : -1;
+    }
+    free(state);
+    free(gen);
+    free(nblk);
+    free(blocks);
+    return 0;
+}

@@ -1,0 +1,301 @@
+"""Paged-KV decode attention for NVIDIA GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over libpagedattn.so whose functions carry the C ABI's
+names (include/pa.h).  It converts torch tensors to device pointers and
+checks dtypes and shapes; every step of the computation runs in the
+library's CUDA kernels.  There is no fallback: if the library cannot be
+loaded, every call raises.
+
+Tensor layouts (row-major):
+  k_cache, v_cache  [num_blocks, Hkv, block_size, head_dim] bf16, or uint8 (e4m3 codes)
+  k_scale, v_scale  [num_blocks, Hkv] float32 (fp8 cache only)
+  q, out            [B, Hq, head_dim] bf16
+  k_new, v_new      [T, Hkv, head_dim] bf16
+  block_tables      [B, M] int32;  seq_lens [B] int32;  slot_mapping [T] int64
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _build
+
+PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = range(5)
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_lib = None
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s" % (what, status_string(status)))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libpagedattn.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and not _build.up_to_date():
+        _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError("libpagedattn.so is not built (%s); run __graft_entry__.build()" % path)
+    lib = ctypes.CDLL(path)
+    P, i32, i64, u64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64, ctypes.c_size_t
+    sig = {
+        "pa_status_string": (ctypes.c_char_p, [i32]),
+        "pa_kv_append": (i32, [P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]),
+        "pa_decode_resolve_splits": (i32, [i32, i32, i32, i32]),
+        "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
+        "pa_decode_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                      ctypes.c_float, i32, P, sz, i32, P]),
+        "pa_get_device_error": (i32, [P, i32]),
+        "pa_selftest_bounded_wait": (i32, [P]),
+        "pa_allocator_create": (P, [i32, i32]),
+        "pa_allocator_destroy": (None, [P]),
+        "pa_block_alloc": (i32, [P, i32, P]),
+        "pa_block_free": (i32, [P, P, i32]),
+        "pa_block_share": (i32, [P, P, i32]),
+        "pa_allocator_num_free": (i32, [P]),
+        "pa_allocator_num_blocks": (i32, [P]),
+        "pa_allocator_refcount": (i32, [P, i32]),
+        "pa_blocks_for_tokens": (i64, [i64, i32]),
+        "pa_kv_bytes": (u64, [i32, i32, i32, i32, i64, i64]),
+        "pa_slot_mapping": (i32, [P, i32, P, P, i32, i32, P]),
+        "pa_sched_simulate": (i32, [P, i32, i32, i32, P]),
+        "pa_sched_continuous_kv": (i32, [P, P, P, i32, i32, i64, i32, P, P, P, P, P]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(lib, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(s: int) -> str:
+    return load().pa_status_string(int(s)).decode()
+
+
+def _check(status: int, what: str):
+    if status != PA_OK:
+        raise PagedAttnError(status, what)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _np_ptr(a: Optional[np.ndarray]):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _kv_dtype(cache: torch.Tensor) -> int:
+    if cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if cache.dtype == torch.uint8:
+        return PA_KV_FP8_E4M3
+    raise TypeError("cache dtype must be bfloat16 or uint8 (e4m3 codes)")
+
+
+def _need(t: torch.Tensor, dtype, name: str, dim: Optional[int] = None):
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dim is not None and t.dim() != dim:
+        raise ValueError("%s must have %d dimensions" % (name, dim))
+
+
+# ------------------------------------------------------------------ device ops
+def pa_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
+                 v_scale: Optional[torch.Tensor], k_new: torch.Tensor, v_new: torch.Tensor,
+                 slot_mapping: torch.Tensor, stream=None) -> None:
+    lib = load()
+    kvd = _kv_dtype(k_cache)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    if kvd == PA_KV_FP8_E4M3:
+        _need(k_scale, torch.float32, "k_scale", 2)
+        _need(v_scale, torch.float32, "v_scale", 2)
+    nb, hkv, bs, d = k_cache.shape
+    T = slot_mapping.shape[0]
+    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d) or v_cache.shape != k_cache.shape:
+        raise ValueError("shape mismatch between caches, new K/V and slot_mapping")
+    _check(lib.pa_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(k_new),
+                            _ptr(v_new), _ptr(slot_mapping), T, nb, hkv, d, bs, kvd, _stream(stream)),
+           "pa_kv_append")
+
+
+def pa_decode_resolve_splits(batch: int, num_kv_heads: int, max_blocks_per_seq: int,
+                             num_splits: int = 0) -> int:
+    return int(load().pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits))
+
+
+def pa_decode_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                              max_blocks_per_seq: int, num_splits: int = 0) -> int:
+    return int(load().pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                max_blocks_per_seq, num_splits))
+
+
+def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor],
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                        num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> None:
+    lib = load()
+    kvd = _kv_dtype(k_cache)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, dc = k_cache.shape
+    M = block_tables.shape[1]
+    if dc != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                   _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d,
+                                   bs, M, nb, float(scale), int(num_splits), _ptr(workspace), ws,
+                                   kvd, _stream(stream)),
+           "pa_decode_attention")
+
+
+def pa_get_device_error(clear: bool = True) -> int:
+    v = ctypes.c_uint32(0)
+    _check(load().pa_get_device_error(ctypes.byref(v), 1 if clear else 0), "pa_get_device_error")
+    return int(v.value)
+
+
+def pa_selftest_bounded_wait(stream=None) -> None:
+    _check(load().pa_selftest_bounded_wait(_stream(stream)), "pa_selftest_bounded_wait")
+
+
+# ------------------------------------------------------------------ host side
+class pa_allocator:
+    """Reference-counted KV block pool (lowest free ids first)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._lib = load()
+        self._h = self._lib.pa_allocator_create(int(num_blocks), int(block_size))
+        if not self._h:
+            raise ValueError("invalid allocator arguments")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pa_allocator_destroy(h)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def alloc(self, n: int) -> np.ndarray:
+        return pa_block_alloc(self, n)
+
+    def free(self, ids) -> None:
+        pa_block_free(self, ids)
+
+    def share(self, ids) -> None:
+        pa_block_share(self, ids)
+
+    def num_free(self) -> int:
+        return int(self._lib.pa_allocator_num_free(self._h))
+
+    def refcount(self, i: int) -> int:
+        return int(self._lib.pa_allocator_refcount(self._h, int(i)))
+
+
+def pa_block_alloc(a: pa_allocator, n: int) -> np.ndarray:
+    out = np.zeros(max(int(n), 1), dtype=np.int32)
+    _check(load().pa_block_alloc(a.handle, int(n), _np_ptr(out)), "pa_block_alloc")
+    return out[:n]
+
+
+def pa_block_free(a: pa_allocator, ids: Sequence[int]) -> None:
+    arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    _check(load().pa_block_free(a.handle, _np_ptr(arr) if arr.size else None, int(arr.size)),
+           "pa_block_free")
+
+
+def pa_block_share(a: pa_allocator, ids: Sequence[int]) -> None:
+    arr = np.ascontiguousarray(np.asarray(ids, dtype=np.int32))
+    _check(load().pa_block_share(a.handle, _np_ptr(arr) if arr.size else None, int(arr.size)),
+           "pa_block_share")
+
+
+def pa_blocks_for_tokens(tokens: int, block_size: int) -> int:
+    return int(load().pa_blocks_for_tokens(int(tokens), int(block_size)))
+
+
+def pa_kv_bytes(layers: int, kv_heads: int, head_dim: int, dtype_bits: int, tokens: int, batch: int) -> int:
+    return int(load().pa_kv_bytes(layers, kv_heads, head_dim, dtype_bits, tokens, batch))
+
+
+def pa_slot_mapping(block_tables: np.ndarray, seq_ids: np.ndarray, positions: np.ndarray,
+                    block_size: int) -> np.ndarray:
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    s = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    p = np.ascontiguousarray(positions, dtype=np.int32)
+    out = np.zeros(max(len(s), 1), dtype=np.int64)
+    _check(load().pa_slot_mapping(_np_ptr(t), int(t.shape[1]), _np_ptr(s), _np_ptr(p), int(len(s)),
+                                  int(block_size), _np_ptr(out)), "pa_slot_mapping")
+    return out[: len(s)]
+
+
+def pa_sched_simulate(out_lens: Sequence[int], slots: int, mode: int) -> int:
+    arr = np.ascontiguousarray(np.asarray(out_lens, dtype=np.int64))
+    it = ctypes.c_int64(0)
+    _check(load().pa_sched_simulate(_np_ptr(arr) if arr.size else None, int(arr.size), int(slots),
+                                    int(mode), ctypes.byref(it)), "pa_sched_simulate")
+    return int(it.value)
+
+
+def pa_sched_continuous_kv(a: pa_allocator, prompt_lens, out_lens, max_num_seqs: int,
+                           stop_iter: int = -1, max_blocks_per_seq: int = 0):
+    """Returns dict(iters, admitted_at, finished_at, tables, lens)."""
+    p = np.ascontiguousarray(np.asarray(prompt_lens, dtype=np.int64))
+    o = np.ascontiguousarray(np.asarray(out_lens, dtype=np.int64))
+    n = len(p)
+    it = ctypes.c_int64(0)
+    adm = np.zeros(max(n, 1), np.int64)
+    fin = np.zeros(max(n, 1), np.int64)
+    tables = np.zeros((max(n, 1), max(max_blocks_per_seq, 1)), np.int32)
+    lens = np.zeros(max(n, 1), np.int32)
+    _check(load().pa_sched_continuous_kv(a.handle, _np_ptr(p) if n else None, _np_ptr(o) if n else None,
+                                         n, int(max_num_seqs), int(stop_iter), int(max_blocks_per_seq),
+                                         ctypes.byref(it), _np_ptr(adm), _np_ptr(fin),
+                                         _np_ptr(tables) if max_blocks_per_seq > 0 else None,
+                                         _np_ptr(lens)),
+           "pa_sched_continuous_kv")
+    return dict(iters=int(it.value), admitted_at=adm[:n], finished_at=fin[:n],
+                tables=tables[:n, :max_blocks_per_seq], lens=lens[:n])

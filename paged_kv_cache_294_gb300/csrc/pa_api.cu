@@ -1,0 +1,269 @@
+// C entry points for the device operations of libpagedattn.so: argument
+// validation, split planning, TMA descriptor encoding, dispatch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "../../include/pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+bool shape_ok(int num_blocks, int Hkv, int d, int bs, int kv_dtype) {
+    if (num_blocks <= 0 || Hkv <= 0 || bs <= 0 || d <= 0) return false;
+    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return false;
+    if ((int64_t)num_blocks * Hkv * bs >= (int64_t)1 << 31) return false;  // TMA row coordinate
+    return true;
+}
+
+// PA_OK, PA_ERR_INVALID or PA_ERR_UNSUPPORTED for head_dim / block_size / dtype.
+pa_status kernel_shape(int d, int bs, int kv_dtype) {
+    if (bs != 16 && bs != 32) return PA_ERR_UNSUPPORTED;
+    if (kv_dtype == PA_KV_FP8_E4M3) return d == 128 ? PA_OK : PA_ERR_UNSUPPORTED;
+    return (d == 64 || d == 128) ? PA_OK : PA_ERR_UNSUPPORTED;
+}
+
+// ---------------------------------------------------------------- TMA maps
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+struct MapKey {
+    const void* ptr;
+    int64_t rows;
+    int d, bs, dtype, device;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && rows == o.rows && d == o.d && bs == o.bs && dtype == o.dtype &&
+               device == o.device;
+    }
+};
+
+struct MapCache {
+    static constexpr int N = 32;
+    MapKey key[N];
+    CUtensorMap map[N];
+    bool used[N] = {};
+    int next = 0;
+    std::mutex mu;
+};
+
+MapCache& map_cache() {
+    static MapCache c;
+    return c;
+}
+
+// The cache viewed as a 2-D tensor: rows = num_blocks * Hkv * bs token rows of
+// d elements; one box = bs rows x 128 bytes, written to shared memory with
+// the 128-byte swizzle (a page of head_dim 128 bf16 takes two boxes).
+bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, CUtensorMap* out) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return false;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    const MapKey k{base, rows, d, bs, dtype, dev};
+    MapCache& c = map_cache();
+    std::lock_guard<std::mutex> lock(c.mu);
+    for (int i = 0; i < MapCache::N; ++i)
+        if (c.used[i] && c.key[i] == k) {
+            *out = c.map[i];
+            return true;
+        }
+    const bool fp8 = dtype == PA_KV_FP8_E4M3;
+    const int elt = fp8 ? 1 : 2;
+    cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+    cuuint64_t gstride[1] = {(cuuint64_t)d * elt};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)bs};
+    cuuint32_t estride[2] = {1, 1};
+    CUtensorMap m;
+    CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(base), gdim, gstride, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    const int slot = c.next;
+    c.next = (c.next + 1) % MapCache::N;
+    c.key[slot] = k;
+    c.map[slot] = m;
+    c.used[slot] = true;
+    *out = m;
+    return true;
+}
+
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+        return 148;
+    return sms;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Blocks per partition for a resolved split count.
+int part_blocks_for(int M, int S) { return (int)ceil_div(M, S < 1 ? 1 : S); }
+
+}  // namespace
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID: return "PA_ERR_INVALID";
+        case PA_ERR_OOM: return "PA_ERR_OOM";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                       const void* k_new, const void* v_new, const int64_t* slot_mapping,
+                       int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
+                       int block_size, int kv_dtype, void* stream) {
+    if (num_tokens < 0 || !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
+        return PA_ERR_INVALID;
+    const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
+    if (ks != PA_OK) return ks;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_cache || !v_cache || !k_new || !v_new || !slot_mapping) return PA_ERR_INVALID;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+        return PA_ERR_INVALID;
+    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return PA_ERR_INVALID;
+    pa::AppendLaunch L{k_cache, v_cache, k_scale, v_scale, k_new, v_new, slot_mapping,
+                       num_tokens, num_blocks, num_kv_heads, head_dim, block_size, fp8};
+    return cuda_status(pa::launch_kv_append(L, static_cast<cudaStream_t>(stream)));
+}
+
+int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits) {
+    if (batch <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return 1;
+    const int M = max_blocks_per_seq;
+    if (num_splits > 0) {
+        const int S = num_splits > M ? M : num_splits;
+        return (int)ceil_div(M, part_blocks_for(M, S));
+    }
+    // Automatic: aim for ~12 CTAs per SM over the batch (several waves of the
+    // three CTAs an SM holds) assuming tables half full on average; a
+    // partition holds 16 .. 128 blocks.
+    const int64_t pages = (int64_t)batch * num_kv_heads * M / 2;
+    const int64_t target = (int64_t)device_sms() * 12;
+    int64_t P = ceil_div(pages, target);
+    if (P < 16) P = 16;
+    if (P > 128) P = 128;
+    if (P > M) P = M;
+    return (int)ceil_div(M, P);
+}
+
+size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int max_blocks_per_seq, int num_splits) {
+    if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
+    if (S <= 1) return 0;
+    const size_t rows = (size_t)batch * num_q_heads * S;
+    const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) & ~(size_t)255;
+    return o_bytes + rows * sizeof(float);
+}
+
+pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, int kv_dtype,
+                              void* stream) {
+    if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_splits < 0 ||
+        !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
+        return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+    if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;  // grid y / z
+    if ((int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31) return PA_ERR_INVALID;
+    const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
+    if (ks != PA_OK) return ks;
+    if (!(scale == scale)) return PA_ERR_INVALID;  // NaN
+    if (batch == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return PA_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PA_ERR_INVALID;
+    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+    if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+    const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
+    const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  max_blocks_per_seq, num_splits);
+    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+        return PA_ERR_INVALID;
+
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
+    CUtensorMap tm_k, tm_v;
+    if (!encode_cache_map(k_cache, rows, head_dim, block_size, kv_dtype, &tm_k) ||
+        !encode_cache_map(v_cache, rows, head_dim, block_size, kv_dtype, &tm_v))
+        return PA_ERR_CUDA;
+
+    pa::DecodeLaunch L;
+    L.out = out;
+    L.q = q;
+    L.k_scale = k_scale;
+    L.v_scale = v_scale;
+    L.tables = block_tables;
+    L.lens = seq_lens;
+    L.o_part = nullptr;
+    L.lse = nullptr;
+    if (S > 1) {
+        const size_t o_rows = (size_t)batch * num_q_heads * S;
+        const size_t o_bytes = (o_rows * head_dim * sizeof(float) + 255) & ~(size_t)255;
+        L.o_part = static_cast<float*>(workspace);
+        L.lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+    }
+    L.tm_k = &tm_k;
+    L.tm_v = &tm_v;
+    L.B = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.d = head_dim;
+    L.bs = block_size;
+    L.M = max_blocks_per_seq;
+    L.num_blocks = num_blocks;
+    L.part_blocks = part_blocks_for(max_blocks_per_seq, S);
+    L.S = S;
+    L.scale = scale;
+    L.fp8 = fp8;
+    return cuda_status(pa::launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_selftest_bounded_wait(void* stream) {
+    return cuda_status(pa::launch_wait_selftest(static_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_get_device_error(uint32_t* flags, int clear) {
+    if (!flags) return PA_ERR_INVALID;
+    unsigned int a = 0, d = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = pa::append_unit_error(&a, clear != 0);
+    if (e == cudaSuccess) e = pa::decode_unit_error(&d, clear != 0);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    *flags = a | d;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,183 @@
+// KV append: scatter the new tokens' K/V into the paged cache through
+// slot_mapping (bf16 copy, or fp8 e4m3 quantisation with per-(block,
+// kv_head) absmax scales).
+//
+// Definitions: "LLM Serving - KV Cache, Batching, Speculative Decoding",
+// section "Recall and stretch" item 3 (keys/values appended in decode);
+// "KV cache & continuous batching", sections "The core insight" and "KV cache
+// memory math" (fp8 = 1 byte per element); "LLM Inference Optimization",
+// section "Memory Bandwidth Optimization" (KV-cache quantization).
+#include <cuda_fp8.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+// One thread per 16-byte unit of one (token, kv_head) row, K and V.
+__global__ void __launch_bounds__(256) kv_append_bf16_kernel(
+    uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k_new,
+    const uint4* __restrict__ v_new, const int64_t* __restrict__ slots, int T, int Hkv, int units,
+    int bs, int64_t cap_slots) {
+    const int64_t total = (int64_t)T * Hkv * units;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int u = (int)(i % units);
+        const int64_t th = i / units;
+        const int h = (int)(th % Hkv);
+        const int64_t t = th / Hkv;
+        const int64_t slot = slots[t];
+        if (slot < 0) continue;
+        if (slot >= cap_slots) {
+            if (u == 0 && h == 0) raise_error(PA_DEVERR_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / bs, off = slot - blk * bs;
+        const int64_t dst = ((blk * Hkv + h) * bs + off) * units + u;
+        const int64_t src = (t * Hkv + h) * units + u;
+        k_cache[dst] = k_new[src];
+        v_cache[dst] = v_new[src];
+    }
+}
+
+// e4m3 code -> fp32, exact (the e4m3 -> f16 conversion is exact).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+    const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(code & 0xFF));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
+}
+
+__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
+    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
+    return __uint_as_float(bits16 << 16);
+}
+
+// Quantise one run of tokens that land in one block, for one kv head, into
+// `page` (bs rows of 128 codes) with its scale.  One warp; lane owns bytes
+// 4*lane .. 4*lane+3 of every row.
+__device__ void fp8_run_one(uint8_t* __restrict__ page, float* __restrict__ scale_p,
+                            const uint16_t* __restrict__ src, const int64_t* __restrict__ slots,
+                            int t0, int r, int h, int Hkv, int bs, int first) {
+    const int lane = threadIdx.x & 31;
+    float a = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < r; ++j) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src + ((int64_t)(t0 + j) * Hkv + h) * 128 +
+                                                        lane * 4);
+        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x & 0xFFFF)));
+        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x >> 16)));
+        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y & 0xFFFF)));
+        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y >> 16)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float old = (first == 0) ? 0.f : *scale_p;
+    float s = __fdiv_rn(a, 448.0f);
+    if (old > s) s = old;
+    if (s > old && old > 0.f) {
+#pragma unroll 1
+        for (int o = 0; o < first; ++o) {
+            uint32_t* row = reinterpret_cast<uint32_t*>(page + o * 128) + lane;
+            const uint32_t w = *row;
+            uint32_t nw = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float v = e4m3_to_f32((w >> (8 * e)) & 0xFF);
+                nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
+            }
+            *row = nw;
+        }
+    }
+#pragma unroll 1
+    for (int j = 0; j < r; ++j) {
+        const int off = (int)(slots[t0 + j] % bs);
+        const uint2 w = *reinterpret_cast<const uint2*>(src + ((int64_t)(t0 + j) * Hkv + h) * 128 +
+                                                        lane * 4);
+        const float x[4] = {bf16_bits_to_f32(w.x & 0xFFFF), bf16_bits_to_f32(w.x >> 16),
+                            bf16_bits_to_f32(w.y & 0xFFFF), bf16_bits_to_f32(w.y >> 16)};
+        uint32_t nw = 0;
+        if (s != 0.f) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) nw |= f32_to_e4m3(__fdiv_rn(x[e], s)) << (8 * e);
+        }
+        reinterpret_cast<uint32_t*>(page + off * 128)[lane] = nw;
+    }
+    if (lane == 0) *scale_p = s;
+}
+
+// One warp per (token, kv_head).  Only the first token of each run of
+// consecutive tokens that land in the same block does work: it quantises the
+// whole run (at most bs tokens) for its head, K then V.
+__global__ void __launch_bounds__(256) kv_append_fp8_kernel(
+    uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
+    float* __restrict__ v_scale, const uint16_t* __restrict__ k_new,
+    const uint16_t* __restrict__ v_new, const int64_t* __restrict__ slots, int T, int Hkv, int bs,
+    int64_t cap_slots) {
+    const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    if (wid >= (int64_t)T * Hkv) return;
+    const int t = (int)(wid / Hkv), h = (int)(wid % Hkv);
+    const int64_t slot = slots[t];
+    if (slot < 0) return;
+    if (slot >= cap_slots) {
+        if (h == 0 && (threadIdx.x & 31) == 0) raise_error(PA_DEVERR_SLOT);
+        return;
+    }
+    const int64_t blk = slot / bs;
+    if (t > 0) {
+        const int64_t ps = slots[t - 1];
+        if (ps >= 0 && ps < cap_slots && ps / bs == blk) return;  // not the run's first token
+    }
+    int r = 1;
+    while (t + r < T && r < bs) {
+        const int64_t s2 = slots[t + r];
+        if (s2 < 0 || s2 >= cap_slots || s2 / bs != blk) break;
+        ++r;
+    }
+    const int first = (int)(slot - blk * bs);
+    const int64_t page = (blk * Hkv + h) * (int64_t)bs * 128;
+    fp8_run_one(k_cache + page, k_scale + blk * Hkv + h, k_new, slots, t, r, h, Hkv, bs, first);
+    fp8_run_one(v_cache + page, v_scale + blk * Hkv + h, v_new, slots, t, r, h, Hkv, bs, first);
+}
+
+cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {
+    const int64_t cap = (int64_t)L.num_blocks * L.bs;
+    if (L.fp8) {
+        const int64_t warps = (int64_t)L.T * L.Hkv;
+        const int blocks = (int)((warps * 32 + 255) / 256);
+        kv_append_fp8_kernel<<<blocks, 256, 0, stream>>>(
+            (uint8_t*)L.k_cache, (uint8_t*)L.v_cache, L.k_scale, L.v_scale,
+            (const uint16_t*)L.k_new, (const uint16_t*)L.v_new, L.slots, L.T, L.Hkv, L.bs, cap);
+    } else {
+        const int units = L.d / 8;
+        const int64_t total = (int64_t)L.T * L.Hkv * units;
+        int blocks = (int)std::min<int64_t>((total + 255) / 256, 1 << 20);
+        kv_append_bf16_kernel<<<blocks, 256, 0, stream>>>(
+            (uint4*)L.k_cache, (uint4*)L.v_cache, (const uint4*)L.k_new, (const uint4*)L.v_new,
+            L.slots, L.T, L.Hkv, units, L.bs, cap);
+    }
+    return cudaGetLastError();
+}
+
+// Self-test of the bounded wait: one warp waits on a barrier phase that no
+// thread or copy will ever complete.  The wait must give up on its own,
+// record PA_DEVERR_TIMEOUT and let the kernel finish.
+__global__ void bounded_wait_selftest_kernel() {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    mbar_wait(&bar, 0);
+}
+
+cudaError_t launch_wait_selftest(cudaStream_t stream) {
+    bounded_wait_selftest_kernel<<<1, 32, 0, stream>>>();
+    return cudaGetLastError();
+}
+
+cudaError_t append_unit_error(unsigned int* v, bool clear) { return read_unit_error(v, clear); }
+
+}  // namespace pa

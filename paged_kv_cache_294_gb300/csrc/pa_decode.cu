@@ -1,0 +1,506 @@
+// Paged decode attention for sm_103a, with split-K partitions and a
+// log-sum-exp merge.
+//
+// What it computes ("KV cache & continuous batching", sections "The core
+// insight" and "2. PagedAttention"; "LLM Serving - KV Cache, Batching,
+// Speculative Decoding", section "Hands-on"): for every sequence b and query
+// head i, out = softmax(scale * q . K^T) . V over the sequence's cached
+// tokens, K/V rows gathered through the block table; query head i reads KV
+// head i / G.  Scores, softmax and P.V stay on chip ("LLM Inference
+// Optimization", section "FlashAttention") with an fp32 online softmax.
+//
+// How (one CTA per (split, kv_head, sequence), 5 warps):
+//   * warp 4 is the producer: it reads the partition's block-table entries
+//     (32 at a time, coalesced) and, per page, issues TMA tile loads of the
+//     K and V pages of that (block, kv_head) into a ring of shared-memory
+//     stages with the 128-byte swizzle, completion counted on an mbarrier;
+//   * warps 0-3 consume pages round-robin; each keeps its own running max,
+//     sum and output accumulator for the G query heads of the group;
+//   * per page a consumer warp computes S^T = Q K^T with m16n8k16 MMAs (the G
+//     query heads are the M rows, the page's tokens the N columns, head_dim
+//     the K depth; q stays in registers for the whole CTA), updates the
+//     online softmax in registers, and accumulates O^T += V^T P^T with MMAs
+//     whose B operand is the probability tile straight from the score
+//     registers;
+//   * the four warps' states merge in shared memory; a single-partition
+//     sequence writes bf16 out directly, otherwise the CTA writes its
+//     normalised partial output and base-2 log-sum-exp to the workspace and
+//     the merge kernel combines them.
+// The fp8 cache path converts e4m3 codes to f16 exactly in registers (q and
+// probabilities are f16 there), folds the K scale into the scores and
+// applies the V scale per page to a fresh P.V accumulator.
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+struct DecodeArgs {
+    __nv_bfloat16* out;
+    const uint16_t* q;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* tables;
+    const int32_t* lens;
+    float* o_part;
+    float* lse;
+    int Hq, Hkv, G, M, num_blocks, part_blocks, S;
+    float scale_log2;
+};
+
+template <int D, int BS, bool FP8>
+struct Cfg {
+    static constexpr int ELT = FP8 ? 1 : 2;
+    static constexpr int ROWB = D * ELT;       // bytes of one token row of one head
+    static constexpr int NCH = ROWB / 128;      // 128-byte column chunks = TMA boxes per page
+    static constexpr int PAGEB = BS * ROWB;     // one (block, kv_head) page of K (or V)
+    static constexpr int STAGEB = 2 * PAGEB;    // K page + V page
+    static constexpr int NSTAGE = STAGEB >= 16384 ? 4 : (STAGEB >= 8192 ? 8 : 16);
+    static constexpr int NCW = 4;               // consumer warps
+    static constexpr int NTHREADS = (NCW + 1) * 32;
+    static constexpr int NT = BS / 8;           // 8-token column tiles per page (QK)
+    static constexpr int KS = D / 16;           // 16-deep steps over head_dim (QK)
+    static constexpr int MT = D / 16;           // 16-row tiles of head_dim (PV)
+    static constexpr int KT = BS / 16;          // 16-token steps (PV)
+    static constexpr int BAR_OFF = NSTAGE * STAGEB;
+    static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
+    static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
+    static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGEB, "combine area must fit in the stages");
+};
+
+template <int D, int BS, bool FP8>
+__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+    using C = Cfg<D, BS, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw_u32);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sgen + C::BAR_OFF);
+    uint64_t* empty = full + C::NSTAGE;
+
+    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    int len = a.lens[b];
+    const int cap = a.M * BS;
+    if (len < 0 || len > cap) {
+        if (threadIdx.x == 0 && split == 0 && h == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        len = len < 0 ? 0 : cap;
+    }
+    const int nblk = (len + BS - 1) / BS;
+    const int nsplit = (nblk + a.part_blocks - 1) / a.part_blocks;  // 0 when len == 0
+    if (split > 0 && split >= nsplit) return;
+    const int j0 = split * a.part_blocks;
+    const int npages = max(0, min(nblk, j0 + a.part_blocks) - j0);
+    const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const int g = lane >> 2;  // MMA row group: query head within the group (QK), token col (B)
+    const int c = lane & 3;
+    float m_run = -INFINITY, l_run = 0.f;
+    float o[C::MT][4];
+#pragma unroll
+    for (int i = 0; i < C::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+
+    if (warp == C::NCW) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        bool alive = true;
+        for (int base = 0; base < npages; base += 32) {
+            int myphys = 0;
+            if (base + lane < npages) {
+                myphys = trow[base + lane];
+                if (myphys < 0 || myphys >= a.num_blocks) {
+                    raise_error(PA_DEVERR_BLOCK_ID);
+                    myphys = 0;
+                }
+            }
+            const int cnt = min(32, npages - base);
+            for (int k = 0; k < cnt; ++k) {
+                const int phys = __shfl_sync(0xffffffffu, myphys, k);
+                if (lane == 0 && alive) {
+                    const int i = base + k;
+                    const int s = i % C::NSTAGE;
+                    if (i >= C::NSTAGE) alive = mbar_wait(&empty[s], ((i / C::NSTAGE) - 1) & 1);
+                    if (alive) {
+                        mbar_arrive_expect_tx(&full[s], C::STAGEB);
+                        const int y = (phys * a.Hkv + h) * BS;
+                        uint8_t* st = sgen + s * C::STAGEB;
+#pragma unroll
+                        for (int ch = 0; ch < C::NCH; ++ch)
+                            tma_load_2d(st + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
+#pragma unroll
+                        for (int ch = 0; ch < C::NCH; ++ch)
+                            tma_load_2d(st + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y,
+                                        &full[s]);
+                    }
+                }
+            }
+        }
+        // Every issued load must land before the CTA may reuse or release its
+        // shared memory: wait for the last use of each stage (already complete
+        // on the normal path).
+        if (lane == 0) {
+            for (int s = 0; s < C::NSTAGE && s < npages; ++s) {
+                const int last = s + ((npages - 1 - s) / C::NSTAGE) * C::NSTAGE;
+                mbar_wait(&full[s], (last / C::NSTAGE) & 1);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- consumers
+        // q of query head h*G + g as the A operand (rows g >= G stay zero).
+        uint32_t qa[C::KS][2];
+        if (g < a.G) {
+            const uint16_t* qrow = a.q + ((int64_t)b * a.Hq + h * a.G + g) * D;
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                if (FP8) {
+                    // k order inside a step matches the e4m3 byte order: 4c .. 4c+3
+                    const uint2 w = *reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * c);
+                    qa[ks][0] = pack_f16x2(__uint_as_float((w.x & 0xFFFF) << 16),
+                                           __uint_as_float(w.x & 0xFFFF0000u));
+                    qa[ks][1] = pack_f16x2(__uint_as_float((w.y & 0xFFFF) << 16),
+                                           __uint_as_float(w.y & 0xFFFF0000u));
+                } else {
+                    qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c);
+                    qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c + 8);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
+        }
+
+        for (int i = warp; i < npages; i += C::NCW) {
+            const int s = i % C::NSTAGE;
+            float ksc = 1.f, vsc = 1.f;
+            if (FP8) {
+                int phys = trow[i];
+                if (phys < 0 || phys >= a.num_blocks) phys = 0;
+                ksc = a.k_scale[(int64_t)phys * a.Hkv + h];
+                vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
+            }
+            if (!mbar_wait(&full[s], (i / C::NSTAGE) & 1)) break;
+            const uint32_t kt = sbase + s * C::STAGEB;
+            const uint32_t vt = kt + C::PAGEB;
+            const int valid = min(BS, len - (j0 + i) * BS);
+
+            // ------------------------------------------------ S^T = Q K^T
+            float acc[C::NT][4];
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < C::KS; ++ks) {
+                const uint32_t A[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+                if (FP8) {
+#pragma unroll
+                    for (int nt = 0; nt < C::NT; ++nt) {
+                        const int t = nt * 8 + g;
+                        const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
+                        mma_f16(acc[nt], A, e4m3x2_to_f16x2((uint16_t)(w & 0xFFFF)),
+                                e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+                    }
+                } else {
+                    const int mi = lane >> 3, r = lane & 7;
+                    const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
+                    const uint32_t ktile = kt + (jg >> 3) * (BS * 128);
+#pragma unroll
+                    for (int p = 0; p < C::NT / 2; ++p) {
+                        const int t = (2 * p + (mi >> 1)) * 8 + r;
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(swz128(ktile, t, (jg & 7) * 16), r0, r1, r2, r3);
+                        mma_bf16(acc[2 * p], A, r0, r1);
+                        mma_bf16(acc[2 * p + 1], A, r2, r3);
+                    }
+                }
+            }
+
+            // ------------------------------------------------ online softmax
+            const float sl2 = FP8 ? a.scale_log2 * ksc : a.scale_log2;
+            float sc[C::NT][2];
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tok = nt * 8 + 2 * c + e;
+                    const float v = tok < valid ? acc[nt][e] * sl2 : -INFINITY;
+                    sc[nt][e] = v;
+                    mx = fmaxf(mx, v);
+                }
+            }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m_run, mx);
+            const float m_use = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = exp2f(m_run - m_use);
+            float psum = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    sc[nt][e] = exp2f(sc[nt][e] - m_use);
+                    psum += sc[nt][e];
+                }
+            }
+            l_run = l_run * alpha + psum;
+            m_run = m_new;
+            // accumulator columns are query heads 2c and 2c+1
+            const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+            const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+
+            // rows past the sequence end hold stale bytes: zero them so that
+            // 0-probability x non-finite garbage cannot reach the accumulator
+            if (valid < BS) {
+                for (int idx = valid * C::ROWB / 16 + lane; idx < BS * C::ROWB / 16; idx += 32) {
+                    const int row = idx / (C::ROWB / 16), u = idx % (C::ROWB / 16);
+                    const uint32_t tile = vt + (u >> 3) * (BS * 128);
+                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
+                                     swz128(tile, row, (u & 7) * 16)),
+                                 "r"(0u)
+                                 : "memory");
+                }
+                __syncwarp();
+            }
+
+            // ------------------------------------------------ O^T += V^T P^T
+            if (FP8) {
+                uint32_t pb[C::KT][2];
+#pragma unroll
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                    pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                }
+                const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+                for (int mp = 0; mp < C::MT / 2; ++mp) {
+                    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < C::KT; ++kk) {
+                        const int t = kk * 16 + (mi & 1) * 8 + r;
+                        const int unit = 2 * mp + (mi >> 1);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4_t(swz128(vt, t, unit * 16), r0, r1, r2, r3);
+                        // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes
+                        const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
+                        const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
+                        const uint32_t A0[4] = {e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFF)),
+                                                e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
+                                                e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFF)),
+                                                e4m3x2_to_f16x2((uint16_t)(x1 >> 16))};
+                        const uint32_t A1[4] = {e4m3x2_to_f16x2((uint16_t)(x2 & 0xFFFF)),
+                                                e4m3x2_to_f16x2((uint16_t)(x2 >> 16)),
+                                                e4m3x2_to_f16x2((uint16_t)(x3 & 0xFFFF)),
+                                                e4m3x2_to_f16x2((uint16_t)(x3 >> 16))};
+                        mma_f16(t0, A0, pb[kk][0], pb[kk][1]);
+                        mma_f16(t1, A1, pb[kk][0], pb[kk][1]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        o[2 * mp][e] = fmaf(vsc, t0[e], o[2 * mp][e]);
+                        o[2 * mp + 1][e] = fmaf(vsc, t1[e], o[2 * mp + 1][e]);
+                    }
+                }
+            } else {
+                uint32_t pb[C::KT][2];
+#pragma unroll
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    pb[kk][0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                    pb[kk][1] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                }
+                const int mi = lane >> 3, r = lane & 7;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int jg = 2 * mt + (mi & 1);
+                    const uint32_t vtile = vt + (jg >> 3) * (BS * 128);
+#pragma unroll
+                    for (int kk = 0; kk < C::KT; ++kk) {
+                        const int t = kk * 16 + (mi >> 1) * 8 + r;
+                        uint32_t A[4];
+                        ldsm_x4_t(swz128(vtile, t, (jg & 7) * 16), A[0], A[1], A[2], A[3]);
+                        mma_bf16(o[mt], A, pb[kk][0], pb[kk][1]);
+                    }
+                }
+            }
+            if (valid < BS) fence_proxy_async_smem();  // generic writes before the next TMA fill
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+    }
+
+    __syncthreads();  // pipeline drained: the stage memory becomes the combine area
+    float* cm = reinterpret_cast<float*>(sgen);  // [NCW][8] running max (base 2)
+    float* cl = cm + C::NCW * 8;                 // [NCW][8] running sum
+    float* co = cl + C::NCW * 8;                 // [NCW][8][D] accumulators
+    if (warp < C::NCW) {
+        if (c == 0) {
+            cm[warp * 8 + g] = m_run;
+            cl[warp * 8 + g] = l_run;
+        }
+        const int n = lane >> 2;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int gq = 2 * c + (e & 1);
+                const int dim = FP8 ? mt * 16 + 2 * n + (e >> 1) : mt * 16 + n + 8 * (e >> 1);
+                co[(warp * 8 + gq) * D + dim] = o[mt][e];
+            }
+        }
+    }
+    __syncthreads();
+
+    const int G = a.G;
+    for (int idx = threadIdx.x; idx < G * D; idx += C::NTHREADS) {
+        const int gq = idx / D, dim = idx % D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, cm[w * 8 + gq]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < C::NCW; ++w) {
+                const float f = exp2f(cm[w * 8 + gq] - M);
+                L += cl[w * 8 + gq] * f;
+                O += co[(w * 8 + gq) * D + dim] * f;
+            }
+        }
+        const int64_t row = (int64_t)b * a.Hq + h * G + gq;
+        const float val = (M == -INFINITY) ? 0.f : O / L;
+        if (nsplit <= 1) {
+            a.out[row * D + dim] = __float2bfloat16_rn(val);
+        } else {
+            a.o_part[(row * a.S + split) * D + dim] = val;
+            if (dim == 0) a.lse[row * a.S + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
+        }
+    }
+}
+
+// One warp per (sequence, query head): combine the partitions of sequences
+// that used more than one.  out = sum_i 2^(lse_i - L) o_i / sum_i 2^(lse_i - L).
+template <int D>
+__global__ void __launch_bounds__(128) lse_merge_kernel(__nv_bfloat16* __restrict__ out,
+                                                        const float* __restrict__ o_part,
+                                                        const float* __restrict__ lse,
+                                                        const int32_t* __restrict__ lens, int B,
+                                                        int Hq, int M, int bs, int part_blocks,
+                                                        int S) {
+    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (gw >= B * Hq) return;
+    const int b = gw / Hq;
+    int len = lens[b];
+    len = len < 0 ? 0 : (len > M * bs ? M * bs : len);
+    const int nblk = (len + bs - 1) / bs;
+    const int nsplit = (nblk + part_blocks - 1) / part_blocks;
+    if (nsplit <= 1) return;
+    const float* L = lse + (int64_t)gw * S;
+    float mx = -INFINITY;
+    for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, L[k]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    constexpr int PER = D / 32;
+    float acc[PER];
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    float den = 0.f;
+    const float* op = o_part + (int64_t)gw * S * D + lane * PER;
+    for (int k = 0; k < nsplit; ++k) {
+        const float w = exp2f(L[k] - mx);
+        den += w;
+        if (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(op + (int64_t)k * D);
+            acc[0] = fmaf(w, v.x, acc[0]);
+            acc[1] = fmaf(w, v.y, acc[1]);
+            acc[2] = fmaf(w, v.z, acc[2]);
+            acc[3] = fmaf(w, v.w, acc[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, op[(int64_t)k * D + e], acc[e]);
+        }
+    }
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int e = 0; e < PER; ++e) out[(int64_t)gw * D + lane * PER + e] = __float2bfloat16_rn(acc[e] * inv);
+}
+
+template <int D, int BS, bool FP8>
+static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
+    using C = Cfg<D, BS, FP8>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {  // the attribute is per device; set it once per device used
+        e = cudaFuncSetAttribute(paged_decode_kernel<D, BS, FP8>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    DecodeArgs a;
+    a.out = (__nv_bfloat16*)L.out;
+    a.q = (const uint16_t*)L.q;
+    a.k_scale = L.k_scale;
+    a.v_scale = L.v_scale;
+    a.tables = L.tables;
+    a.lens = L.lens;
+    a.o_part = L.o_part;
+    a.lse = L.lse;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.G = L.Hq / L.Hkv;
+    a.M = L.M;
+    a.num_blocks = L.num_blocks;
+    a.part_blocks = L.part_blocks;
+    a.S = L.S;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    dim3 grid(L.S, L.Hkv, L.B);
+    paged_decode_kernel<D, BS, FP8><<<grid, C::NTHREADS, C::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || L.S <= 1) return e;
+    const int warps = L.B * L.Hq;
+    lse_merge_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(
+        (__nv_bfloat16*)L.out, L.o_part, L.lse, L.lens, L.B, L.Hq, L.M, L.bs, L.part_blocks, L.S);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
+    if (L.fp8) {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, true>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, true>(L, stream);
+    } else {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, false>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, false>(L, stream);
+        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, false>(L, stream);
+        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, false>(L, stream);
+    }
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t decode_unit_error(unsigned int* v, bool clear) { return read_unit_error(v, clear); }
+
+}  // namespace pa

@@ -1,0 +1,220 @@
+// Host-side parts of libpagedattn.so: the paged block allocator, KV
+// accounting, slot mapping and the iteration-level scheduler simulators.
+// No device access.
+#include <stdint.h>
+#include <stdlib.h>
+
+#include <algorithm>
+#include <deque>
+#include <new>
+#include <set>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pa.h"
+
+// Reference-counted pool of fixed-size KV blocks ("KV cache & continuous
+// batching", section "2. PagedAttention"; "LLM Serving - KV Cache, Batching,
+// Speculative Decoding", section "KV memory, paging and prefix identity").
+// The free set is ordered, so an allocation hands out the lowest free ids.
+struct pa_allocator {
+    int num_blocks;
+    int block_size;
+    std::vector<int32_t> refcnt;
+    std::set<int32_t> free_ids;
+};
+
+extern "C" {
+
+pa_allocator* pa_allocator_create(int num_blocks, int block_size) {
+    if (num_blocks < 0 || block_size <= 0) return nullptr;
+    pa_allocator* a = new (std::nothrow) pa_allocator;
+    if (!a) return nullptr;
+    try {
+        a->num_blocks = num_blocks;
+        a->block_size = block_size;
+        a->refcnt.assign((size_t)num_blocks, 0);
+        for (int i = 0; i < num_blocks; ++i) a->free_ids.insert(a->free_ids.end(), i);
+    } catch (...) {
+        delete a;
+        return nullptr;
+    }
+    return a;
+}
+
+void pa_allocator_destroy(pa_allocator* a) { delete a; }
+
+pa_status pa_block_alloc(pa_allocator* a, int n, int32_t* out_ids) {
+    if (!a || n < 0 || (n > 0 && !out_ids)) return PA_ERR_INVALID;
+    if ((size_t)n > a->free_ids.size()) return PA_ERR_OOM;
+    for (int k = 0; k < n; ++k) {
+        auto it = a->free_ids.begin();
+        out_ids[k] = *it;
+        a->refcnt[*it] = 1;
+        a->free_ids.erase(it);
+    }
+    return PA_OK;
+}
+
+pa_status pa_block_free(pa_allocator* a, const int32_t* ids, int n) {
+    if (!a || n < 0 || (n > 0 && !ids)) return PA_ERR_INVALID;
+    std::unordered_map<int32_t, int> drops;
+    for (int k = 0; k < n; ++k) {
+        if (ids[k] < 0 || ids[k] >= a->num_blocks) return PA_ERR_INVALID;
+        drops[ids[k]]++;
+    }
+    for (const auto& kv : drops)
+        if (a->refcnt[kv.first] < kv.second) return PA_ERR_INVALID;
+    for (const auto& kv : drops) {
+        a->refcnt[kv.first] -= kv.second;
+        if (a->refcnt[kv.first] == 0) a->free_ids.insert(kv.first);
+    }
+    return PA_OK;
+}
+
+pa_status pa_block_share(pa_allocator* a, const int32_t* ids, int n) {
+    if (!a || n < 0 || (n > 0 && !ids)) return PA_ERR_INVALID;
+    for (int k = 0; k < n; ++k)
+        if (ids[k] < 0 || ids[k] >= a->num_blocks || a->refcnt[ids[k]] == 0) return PA_ERR_INVALID;
+    for (int k = 0; k < n; ++k) a->refcnt[ids[k]]++;
+    return PA_OK;
+}
+
+int pa_allocator_num_free(const pa_allocator* a) { return a ? (int)a->free_ids.size() : -1; }
+
+int pa_allocator_num_blocks(const pa_allocator* a) { return a ? a->num_blocks : -1; }
+
+int pa_allocator_refcount(const pa_allocator* a, int32_t id) {
+    if (!a || id < 0 || id >= a->num_blocks) return -1;
+    return a->refcnt[id];
+}
+
+int64_t pa_blocks_for_tokens(int64_t tokens, int block_size) {
+    if (tokens <= 0 || block_size <= 0) return 0;
+    return (tokens + block_size - 1) / block_size;
+}
+
+uint64_t pa_kv_bytes(int layers, int kv_heads, int head_dim, int dtype_bits, int64_t tokens,
+                     int64_t batch) {
+    if (layers < 0 || kv_heads < 0 || head_dim < 0 || dtype_bits < 0 || tokens < 0 || batch < 0)
+        return 0;
+    // K and V, every layer, every KV head, every cached position of every sequence
+    const uint64_t elems = 2ull * (uint64_t)layers * (uint64_t)kv_heads * (uint64_t)head_dim *
+                           (uint64_t)tokens * (uint64_t)batch;
+    return elems * (uint64_t)dtype_bits / 8ull;
+}
+
+pa_status pa_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
+                          const int32_t* seq_ids, const int32_t* positions, int num_tokens,
+                          int block_size, int64_t* slots) {
+    if (num_tokens < 0 || block_size <= 0 || max_blocks_per_seq < 0) return PA_ERR_INVALID;
+    if (num_tokens == 0) return PA_OK;
+    if (!block_tables || !seq_ids || !positions || !slots) return PA_ERR_INVALID;
+    for (int t = 0; t < num_tokens; ++t) {
+        const int p = positions[t];
+        if (p < 0 || seq_ids[t] < 0 || p / block_size >= max_blocks_per_seq) return PA_ERR_INVALID;
+        const int32_t blk = block_tables[(int64_t)seq_ids[t] * max_blocks_per_seq + p / block_size];
+        slots[t] = (int64_t)blk * block_size + p % block_size;
+    }
+    return PA_OK;
+}
+
+pa_status pa_sched_simulate(const int64_t* out_lens, int n, int slots, int mode, int64_t* iters) {
+    if (n < 0 || slots <= 0 || (mode != 0 && mode != 1) || !iters || (n > 0 && !out_lens))
+        return PA_ERR_INVALID;
+    for (int i = 0; i < n; ++i)
+        if (out_lens[i] <= 0) return PA_ERR_INVALID;
+    int64_t total = 0;
+    if (mode == 0) {
+        for (int i = 0; i < n; i += slots) total += *std::max_element(out_lens + i, out_lens + std::min(n, i + slots));
+        *iters = total;
+        return PA_OK;
+    }
+    // Iteration-level: a min-heap of finishing times; a request admitted at
+    // tick t with length L occupies its slot for ticks t .. t+L-1.
+    std::multiset<int64_t> busy;  // finishing tick of each occupied slot
+    int64_t now = 0;
+    int next = 0;
+    while (next < n) {
+        while ((int)busy.size() < slots && next < n) busy.insert(now + out_lens[next++]);
+        if (next < n) {  // jump to the next tick at which a slot frees
+            now = *busy.begin();
+            while (!busy.empty() && *busy.begin() <= now) busy.erase(busy.begin());
+        }
+    }
+    for (int64_t f : busy) total = std::max(total, f);
+    *iters = n == 0 ? 0 : total;
+    return PA_OK;
+}
+
+pa_status pa_sched_continuous_kv(pa_allocator* a, const int64_t* prompt_lens,
+                                 const int64_t* out_lens, int n, int max_num_seqs,
+                                 int64_t stop_iter, int max_blocks_per_seq, int64_t* iters,
+                                 int64_t* admitted_at, int64_t* finished_at, int32_t* tables,
+                                 int32_t* lens) {
+    if (!a || n < 0 || max_num_seqs <= 0 || max_blocks_per_seq < 0 || (n > 0 && (!prompt_lens || !out_lens)))
+        return PA_ERR_INVALID;
+    for (int r = 0; r < n; ++r) {
+        if (prompt_lens[r] < 0 || out_lens[r] <= 0) return PA_ERR_INVALID;
+        const int64_t need = pa_blocks_for_tokens(prompt_lens[r] + out_lens[r], a->block_size);
+        if (need > a->num_blocks || (tables && need > max_blocks_per_seq)) return PA_ERR_INVALID;
+    }
+    struct Req {
+        int id;
+        int64_t generated;
+        std::vector<int32_t> blocks;
+    };
+    std::vector<Req> active;
+    std::deque<int> queue;
+    for (int r = 0; r < n; ++r) queue.push_back(r);
+    for (int r = 0; r < n; ++r) {
+        if (admitted_at) admitted_at[r] = -1;
+        if (finished_at) finished_at[r] = -1;
+    }
+    int64_t it = 0;
+    while ((!queue.empty() || !active.empty()) && (stop_iter < 0 || it < stop_iter)) {
+        // admission: in arrival order while a sequence slot and the reservation fit
+        while (!queue.empty() && (int)active.size() < max_num_seqs) {
+            const int r = queue.front();
+            const int64_t need = pa_blocks_for_tokens(prompt_lens[r] + out_lens[r], a->block_size);
+            if ((int64_t)a->free_ids.size() < need) break;
+            Req q{r, 0, std::vector<int32_t>((size_t)need)};
+            if (pa_block_alloc(a, (int)need, q.blocks.data()) != PA_OK) return PA_ERR_OOM;
+            active.push_back(std::move(q));
+            queue.pop_front();
+            if (admitted_at) admitted_at[r] = it;
+        }
+        if (active.empty()) return PA_ERR_INVALID;  // head of the queue can never fit
+        // one decode iteration: every active request produces one token
+        std::vector<Req> keep;
+        keep.reserve(active.size());
+        for (auto& q : active) {
+            q.generated++;
+            if (q.generated >= out_lens[q.id]) {
+                pa_block_free(a, q.blocks.data(), (int)q.blocks.size());
+                if (finished_at) finished_at[q.id] = it;
+            } else {
+                keep.push_back(std::move(q));
+            }
+        }
+        active.swap(keep);
+        ++it;
+    }
+    if (iters) *iters = it;
+    if (tables || lens) {
+        for (int r = 0; r < n; ++r) {
+            if (lens) lens[r] = 0;
+            if (tables)
+                for (int j = 0; j < max_blocks_per_seq; ++j) tables[(int64_t)r * max_blocks_per_seq + j] = -1;
+        }
+        for (const auto& q : active) {
+            if (lens) lens[q.id] = (int32_t)(prompt_lens[q.id] + q.generated);
+            if (tables)
+                for (size_t j = 0; j < q.blocks.size(); ++j)
+                    tables[(int64_t)q.id * max_blocks_per_seq + (int64_t)j] = q.blocks[j];
+        }
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// Launch descriptors shared between the C entry points (pa_api.cu) and the
+// kernel translation units.  Host-side only.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+namespace pa {
+
+struct AppendLaunch {
+    void* k_cache;
+    void* v_cache;
+    float* k_scale;
+    float* v_scale;
+    const void* k_new;
+    const void* v_new;
+    const int64_t* slots;
+    int T, num_blocks, Hkv, d, bs;
+    bool fp8;
+};
+
+struct DecodeLaunch {
+    void* out;
+    const void* q;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* tables;
+    const int32_t* lens;
+    float* o_part;      // workspace, [B][Hq][S][d] (S > 1 only)
+    float* lse;         // workspace, [B][Hq][S]
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    int B, Hq, Hkv, d, bs, M, num_blocks;
+    int part_blocks;    // blocks per split partition
+    int S;              // partitions per sequence at most (grid x)
+    float scale;
+    bool fp8;
+};
+
+cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
+
+cudaError_t launch_wait_selftest(cudaStream_t stream);
+cudaError_t append_unit_error(unsigned int* v, bool clear);
+cudaError_t decode_unit_error(unsigned int* v, bool clear);
+
+}  // namespace pa

@@ -1,0 +1,174 @@
+"""pa_decode_attention through the C ABI against the fp64 oracle.
+
+Tolerance: max |err| <= 1e-2 for the bf16 cache, <= 5e-2 for the fp8 cache
+(against the oracle evaluated on the stored fp8 cache).  Small cases compare
+every output; full-size cases (the benchmark's shapes and launch
+configuration) compare sampled sequences, each computed by the oracle from
+the same seeded inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_294_gb300 as pa
+import workloads
+from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
+from tests.gpu_util import BF16_TOL, FP8_TOL, gpu_out_f64, oracle_out, run_gpu, tol
+
+pytestmark = pytest.mark.gpu
+
+
+def check(w, num_splits=0, seqs=None):
+    layer = run_gpu(w, num_splits)
+    st, ref = oracle_out(w, seqs=seqs, tables=layer.tables_host)
+    got = gpu_out_f64(layer, seqs)
+    assert np.all(np.isfinite(got))
+    err = np.max(np.abs(got - ref))
+    assert err <= tol(w), (w.name, num_splits, err)
+    assert pa.pa_get_device_error() == 0
+    return layer, err
+
+
+SMALL = [("tiny", {}), ("8b", dict(B=8, seq_len=600)), ("70b", dict(B=12, seq_len=500)),
+         ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700))]
+
+
+@pytest.mark.parametrize("name,kw", SMALL)
+@pytest.mark.parametrize("splits", [0, 1, 3])
+def test_small_configs_all_outputs(name, kw, splits):
+    check(workloads.make(name, **kw), splits)
+
+
+@pytest.mark.parametrize("S", [1, 2, 4, 8, 16, 32, 64])
+def test_long_context_split_sweep(S):
+    w = workloads.make("long", B=2, seq_len=9000)
+    check(w, S)
+
+
+def _synthetic(B, Hq, Hkv, d, bs, lens, kv="bf16", seed=0, k_mult=1.0):
+    """A workload object with explicit lengths and a random block permutation."""
+    rng = np.random.default_rng(seed)
+    M = max(1, max(-(-L // bs) for L in lens))
+    nb = sum(-(-L // bs) for L in lens) + 7
+    perm = rng.permutation(nb).astype(np.int32)
+    tables = workloads._tables_from_perm(np.array(lens), bs, M, perm)
+    fs, fp = workloads._history(np.array(lens))
+    vals = workloads._values(seed, len(fs), B, Hq, Hkv, d, "cpu", k_mult)
+    return workloads.Workload(name="synthetic", Hq=Hq, Hkv=Hkv, d=d, bs=bs, kv=kv, B=B, num_blocks=nb,
+                              M=M, scale=1.0 / math.sqrt(d), seq_lens=np.array(lens, np.int32),
+                              block_tables=tables, trace=None, target_rids=None, fill_seq=fs,
+                              fill_pos=fp, **vals)
+
+
+SHAPES = [
+    # B, Hq, Hkv, d, bs, kv
+    (5, 8, 8, 128, 16, "bf16"),     # MHA
+    (5, 8, 1, 128, 16, "bf16"),     # MQA, G = 8
+    (5, 16, 8, 128, 16, "bf16"),    # G = 2
+    (5, 12, 3, 64, 16, "bf16"),     # G = 4, head_dim 64
+    (5, 8, 2, 64, 32, "bf16"),
+    (5, 16, 2, 128, 32, "bf16"),
+    (5, 4, 4, 128, 32, "fp8"),
+    (5, 8, 1, 128, 16, "fp8"),
+    (5, 6, 3, 128, 32, "fp8"),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES)
+def test_head_layouts_and_ragged_lengths(shape):
+    B, Hq, Hkv, d, bs, kv = shape
+    lens = [1, bs - 1, bs, bs + 1, 7 * bs + 3][:B]
+    w = _synthetic(B, Hq, Hkv, d, bs, lens, kv, seed=B + Hq + d + bs)
+    for S in (0, 2):
+        check(w, S)
+
+
+def test_one_token_returns_v_exactly():
+    w = _synthetic(3, 8, 2, 128, 16, [1, 1, 1], seed=4)
+    layer = run_gpu(w)
+    out = layer.out.view(torch.int16).cpu()
+    vn = w.v_new.view(torch.int16)
+    for b in range(3):
+        for i in range(8):
+            assert torch.equal(out[b, i], vn[b, i // 4])
+
+
+def test_zero_length_gives_zero_rows_and_others_unaffected():
+    w = _synthetic(3, 4, 2, 128, 16, [0, 20, 0], seed=5)
+    layer = run_gpu(w)
+    out = layer.out.float().cpu()
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    st, ref = oracle_out(w, tables=layer.tables_host)
+    assert np.max(np.abs(out[1].numpy() - ref[1])) <= BF16_TOL
+
+
+@pytest.mark.parametrize("S", [1, 3])
+def test_bit_identical_under_physical_permutation(S):
+    """For a fixed split count the accumulation order is logical, so moving blocks changes nothing."""
+    outs = []
+    for perm_seed in (1, 2):
+        w = _synthetic(4, 16, 2, 128, 16, [33, 200, 517, 64], seed=9)
+        rng = np.random.default_rng(perm_seed)
+        perm = rng.permutation(w.num_blocks).astype(np.int32)
+        w.block_tables = workloads._tables_from_perm(w.seq_lens, w.bs, w.M, perm)
+        layer = run_gpu(w, S)
+        outs.append(layer.out.view(torch.int16).cpu())
+    assert torch.equal(outs[0], outs[1])
+
+
+def test_stale_nan_bytes_past_the_end_do_not_leak():
+    """Rows of a partial last block beyond seq_len hold NaN bf16 patterns: output stays exact-ish."""
+    w = _synthetic(3, 8, 2, 128, 16, [5, 19, 40], seed=12)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    k = layer.k_cache.view(torch.int16)
+    v = layer.v_cache.view(torch.int16)
+    for b, L in enumerate(w.seq_lens):
+        blk = int(layer.tables_host[b, (L - 1) // 16])
+        k[blk, :, L % 16:, :] = 0x7FC0     # bf16 NaN
+        v[blk, :, L % 16:, :] = 0x7FC0
+    layer.step()
+    torch.cuda.synchronize()
+    got = layer.out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    st, ref = oracle_out(w, tables=layer.tables_host)
+    assert np.max(np.abs(got - ref)) <= BF16_TOL
+
+
+def test_fp8_stale_nan_codes_past_the_end_do_not_leak():
+    w = _synthetic(2, 4, 4, 128, 32, [7, 45], kv="fp8", seed=13)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    for b, L in enumerate(w.seq_lens):
+        blk = int(layer.tables_host[b, (L - 1) // 32])
+        layer.k_cache[blk, :, L % 32:, :] = 0x7F     # e4m3 NaN
+        layer.v_cache[blk, :, L % 32:, :] = 0x7F
+    layer.step()
+    torch.cuda.synchronize()
+    got = layer.out.float().cpu().numpy()
+    assert np.all(np.isfinite(got))
+    st, ref = oracle_out(w, tables=layer.tables_host)
+    assert np.max(np.abs(got - ref)) <= FP8_TOL
+
+
+# ------------------------------------------------------------ full sizes, sampled
+
+
+def _sample(B, k=6):
+    return sorted({0, B - 1} | set(np.random.default_rng(7).choice(B, size=k, replace=False).tolist()))
+
+
+@pytest.mark.parametrize("name", ["8b", "70b", "fp8prefix"])
+def test_full_size_sampled(name):
+    w = workloads.make(name, device="cuda")
+    seqs = _sample(w.B)
+    if name == "fp8prefix":
+        seqs = sorted(set(seqs) | {1, 50, 99, 100, 127})
+    check(w, 0, seqs)
+
+
+def test_full_size_long_sampled():
+    w = workloads.make("long", device="cuda")
+    check(w, 0, [1])
+    check(w, 64, [3])

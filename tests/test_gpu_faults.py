@@ -1,0 +1,86 @@
+"""Bad inputs return a status or set a device error bit; nothing faults or hangs."""
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_294_gb300 as pa
+import workloads
+from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
+
+pytestmark = pytest.mark.gpu
+
+
+def _layer():
+    w = workloads.make("tiny")
+    return PagedDecodeLayer.from_workload(w, "cuda")
+
+
+def test_out_of_range_block_id_is_flagged_and_clamped():
+    layer = _layer()
+    pa.pa_get_device_error(clear=True)
+    bad = layer.block_tables.clone()
+    bad[3, 2] = 10 ** 6
+    bad[2, 0] = -5
+    pa.pa_decode_attention(layer.out, layer.q, layer.k_cache, layer.v_cache, None, None, bad,
+                           layer.seq_lens, layer.scale, 0, layer.ensure_workspace())
+    flags = pa.pa_get_device_error()
+    assert flags & pa.PA_DEVERR_BLOCK_ID
+    assert torch.all(torch.isfinite(layer.out.float()))
+
+
+def test_seq_len_beyond_table_is_flagged():
+    layer = _layer()
+    pa.pa_get_device_error(clear=True)
+    lens = layer.seq_lens.clone()
+    lens[0] = 10 ** 6
+    pa.pa_decode_attention(layer.out, layer.q, layer.k_cache, layer.v_cache, None, None,
+                           layer.block_tables, lens, layer.scale, 0, layer.ensure_workspace())
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_SEQ_LEN
+
+
+def test_slot_beyond_pool_is_skipped_and_flagged():
+    layer = _layer()
+    pa.pa_get_device_error(clear=True)
+    before = layer.k_cache.clone()
+    slots = torch.tensor([64 * 16, 64 * 16 + 5, -1, 10 ** 9], dtype=torch.int64, device="cuda")
+    pa.pa_kv_append(layer.k_cache, layer.v_cache, None, None, layer.k_new, layer.v_new, slots)
+    assert pa.pa_get_device_error() & pa.PA_DEVERR_SLOT
+    assert torch.equal(before, layer.k_cache)
+
+
+def test_host_side_argument_errors():
+    layer = _layer()
+    lib = pa.load()
+    ws = layer.ensure_workspace(4)
+    need = pa.pa_decode_workspace_bytes(layer.B, layer.Hq, layer.Hkv, layer.d, layer.M, 4)
+    assert need > 0
+    args = dict(out=layer.out.data_ptr(), q=layer.q.data_ptr(), k=layer.k_cache.data_ptr(),
+                v=layer.v_cache.data_ptr(), t=layer.block_tables.data_ptr(), l=layer.seq_lens.data_ptr())
+
+    def call(ws_ptr, ws_bytes, splits=4, q=None, dtype=0):
+        return lib.pa_decode_attention(args["out"], args["q"] if q is None else q, args["k"], args["v"],
+                                       None, None, args["t"], args["l"], layer.B, layer.Hq, layer.Hkv,
+                                       layer.d, layer.bs, layer.M, layer.num_blocks, layer.scale, splits,
+                                       ws_ptr, ws_bytes, dtype, None)
+
+    assert call(ws.data_ptr(), need - 1) == pa.PA_ERR_INVALID          # workspace too small
+    assert call(None, 0) == pa.PA_ERR_INVALID                           # workspace missing
+    assert call(ws.data_ptr(), need, q=args["q"] + 2) == pa.PA_ERR_INVALID   # misaligned q
+    assert call(ws.data_ptr(), need, dtype=1) == pa.PA_ERR_INVALID      # fp8 without scales
+    assert call(ws.data_ptr(), need) == pa.PA_OK
+    torch.cuda.synchronize()
+    with pytest.raises(TypeError):
+        pa.pa_decode_attention(layer.out.float(), layer.q, layer.k_cache, layer.v_cache, None, None,
+                               layer.block_tables, layer.seq_lens, layer.scale)
+
+
+def test_bounded_wait_gives_up_and_reports():
+    """A barrier phase nobody completes: the wait ends by itself and reports a timeout."""
+    pa.pa_get_device_error(clear=True)
+    pa.pa_selftest_bounded_wait()
+    assert pa.pa_get_device_error() == pa.PA_DEVERR_TIMEOUT
+    # the context is still usable afterwards
+    layer = _layer()
+    layer.step()
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0

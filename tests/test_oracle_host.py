@@ -185,3 +185,38 @@ def test_bf16_append_is_an_exact_copy():
             assert np.all(c.k[blk, :, off] == 0)
     with pytest.raises(ValueError):
         c.append(k[:1], v[:1], np.array([24], np.int64))
+
+
+def test_continuous_kv_reduces_to_the_pages_scheduler():
+    lens = [5, 20, 10, 15, 10]
+    a = oracle.Allocator(1000)
+    r = oracle.sched_continuous_kv(a, 16, [0] * 5, lens, 3)
+    assert r["iters"] == 20 == oracle.sched_continuous(lens, 3)
+    assert a.num_free() == 1000                      # every block returned at the end
+    assert list(r["admitted_at"]) == [0, 0, 0, 5, 10]
+    assert list(r["finished_at"]) == [4, 19, 9, 19, 19]
+
+
+def test_continuous_kv_memory_bound_admission_acts_as_slots():
+    """Every request reserves 2 blocks of a 4-block pool: at most 2 run at once."""
+    rng = np.random.default_rng(3)
+    for _ in range(30):
+        n = int(rng.integers(1, 9))
+        outs = [int(x) for x in rng.integers(1, 17, size=n)]
+        prompts = [32 - o for o in outs]            # prompt + out = 32 tokens = 2 blocks of 16
+        a = oracle.Allocator(4)
+        r = oracle.sched_continuous_kv(a, 16, prompts, outs, 8)
+        assert r["iters"] == oracle.sched_continuous(outs, 2)
+
+
+def test_continuous_kv_snapshot_tables_and_lengths():
+    a = oracle.Allocator(10)
+    r = oracle.sched_continuous_kv(a, 4, [3, 6, 2], [4, 3, 5], 2, stop_iter=2, M=3)
+    # request 0 reserves ceil(7/4)=2 blocks [0,1]; request 1 ceil(9/4)=3 blocks [2,3,4];
+    # request 2 waits for a sequence slot
+    assert r["iters"] == 2
+    assert list(r["lens"]) == [3 + 2, 6 + 2, 0]
+    assert r["tables"].tolist() == [[0, 1, -1], [2, 3, 4], [-1, -1, -1]]
+    assert list(r["admitted_at"]) == [0, 0, -1]
+    with pytest.raises(ValueError):
+        oracle.sched_continuous_kv(oracle.Allocator(2), 4, [20], [1], 1)   # can never fit

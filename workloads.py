@@ -86,8 +86,8 @@ class TraceOp:
     """One allocator operation of a seeded admit/finish trace.
 
     kind: "alloc" (n blocks appended to request rid's table), "free" (release
-    every block of rid), "share" (rid's table starts with the blocks of `src`,
-    taking a reference on each).
+    every block of rid), "share" (the first n blocks of request `src`'s table
+    are appended to rid's table, taking a reference on each).
     """
     kind: str
     rid: int
@@ -245,9 +245,10 @@ def _trace_prefix(rng: np.random.Generator, n_shared: int, prefix_blocks: int,
     """Scramble the pool, then build 100 sequences over one shared prefix.
 
     Warm-up: allocate random-sized filler requests until ~70% full, finish a
-    random half, twice.  Then request P allocates the prefix blocks, each of
-    the n_shared sequences shares P's blocks and allocates its own blocks,
-    and the independent sequences allocate theirs.
+    random half, twice.  Then the first shared sequence allocates the prefix
+    blocks and its own, each later shared sequence takes a reference on the
+    first one's blocks (so the prefix blocks end with n_shared references) and
+    allocates its own, and the independent sequences allocate theirs.
     """
     ops: List[TraceOp] = []
     free = num_blocks
@@ -271,12 +272,14 @@ def _trace_prefix(rng: np.random.Generator, n_shared: int, prefix_blocks: int,
         r = rids[i]
         free += live.pop(r)
         ops.append(TraceOp("free", r))
+    # the first sequence computes the prefix; the others take references on its blocks
     prefix_rid = rid
-    rid += 1
-    ops.append(TraceOp("alloc", prefix_rid, prefix_blocks))
     targets = []
-    for _ in range(n_shared):
-        ops.append(TraceOp("share", rid, src=prefix_rid))
+    for i in range(n_shared):
+        if i == 0:
+            ops.append(TraceOp("alloc", rid, prefix_blocks))
+        else:
+            ops.append(TraceOp("share", rid, n=prefix_blocks, src=prefix_rid))
         ops.append(TraceOp("alloc", rid, own_blocks))
         targets.append(rid)
         rid += 1
