@@ -183,7 +183,7 @@ def cpu_oracle_baseline(w, tables, budget_s=10.0, threads=None):
             break
         n = min(w.B, n * 2)
     reps, total = 1, dt
-    while total < budget_s and reps < 50:
+    while total < budget_s and reps < 500:
         st = oracle.run.OracleStep(w, seqs=seqs, tables=tables)
         t0 = time.perf_counter()
         st.append()
@@ -205,7 +205,7 @@ def run_reference(args):
     dist, rank, world = dist_init()
     if rank != 0:
         return
-    w = workloads.make(args.workload, device="cpu")
+    w = workloads.make(args.workload, device="cpu", B=args.batch)
     import oracle.run
     tables = oracle.run.tables_of(w)
     threads = os.cpu_count() or 1
@@ -250,7 +250,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     pa.load()
 
-    w = workloads.make(args.workload, device=dev)
+    w = workloads.make(args.workload, device=dev, B=args.batch)
     layer = PagedDecodeLayer.from_workload(w, dev)
     S = layer.num_splits(args.splits)
     layer.ensure_workspace(args.splits)
@@ -366,14 +366,15 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_baseline(w, layer.tables_host, budget_s=args.cpu_seconds)
     clk = clocks.summary()
-    traffic = ncu_traffic(args.workload, S)
+    traffic = ncu_traffic(args.workload, S) if args.batch is None else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3-cache/f16-mma/f32-softmax" if w.kv == "fp8" else "bf16-cache/bf16-mma/f32-softmax",
         "data": "synthetic",
-        "config": {"workload": args.workload, "desc": w.desc, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
+        "config": {"workload": args.workload if args.batch is None else "%s-B%d" % (args.workload, w.B),
+                   "desc": w.desc, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv,
                    "head_dim": w.d, "block_size": w.bs, "kv": w.kv, "num_splits": S,
                    "tokens": int(np.sum(w.seq_lens)), "parallelism": "replicas" if world > 1 else "1 gpu",
                    "l2": "512 MiB memset between timed steps (untimed); step reads > L2"},
@@ -404,8 +405,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="8b", choices=sorted(workloads.CONFIGS))
     ap.add_argument("--splits", type=int, default=0, help="split-K partitions (0 = automatic)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="fewer sequences of the same workload recipe (profiling cases); default: full")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

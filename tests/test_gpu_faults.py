@@ -10,8 +10,8 @@ from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
 pytestmark = pytest.mark.gpu
 
 
-def _layer():
-    w = workloads.make("tiny")
+def _layer(name="tiny", **kw):
+    w = workloads.make(name, **kw)
     return PagedDecodeLayer.from_workload(w, "cuda")
 
 
@@ -49,7 +49,7 @@ def test_slot_beyond_pool_is_skipped_and_flagged():
 
 
 def test_host_side_argument_errors():
-    layer = _layer()
+    layer = _layer("8b", B=4, seq_len=300)
     lib = pa.load()
     ws = layer.ensure_workspace(4)
     need = pa.pa_decode_workspace_bytes(layer.B, layer.Hq, layer.Hkv, layer.d, layer.M, 4)
@@ -67,6 +67,7 @@ def test_host_side_argument_errors():
     assert call(None, 0) == pa.PA_ERR_INVALID                           # workspace missing
     assert call(ws.data_ptr(), need, q=args["q"] + 2) == pa.PA_ERR_INVALID   # misaligned q
     assert call(ws.data_ptr(), need, dtype=1) == pa.PA_ERR_INVALID      # fp8 without scales
+    assert call(ws.data_ptr(), need, dtype=5) == pa.PA_ERR_INVALID      # unknown cache dtype
     assert call(ws.data_ptr(), need) == pa.PA_OK
     torch.cuda.synchronize()
     with pytest.raises(TypeError):

@@ -322,6 +322,8 @@ def make(name: str, device="cpu", B: Optional[int] = None, seq_len: Optional[int
         hi = 4096 if seq_len is None else seq_len
         lens = rl.integers(128 if seq_len is None else 1, hi + 1, size=Bn).astype(np.int32)
         M = 256 if seq_len is None else -(-hi // bs)
+        if B is not None and B < Bfull:
+            num_blocks = max(-(-num_blocks * Bn // Bfull), int(np.sum(-(-lens // bs))))   # same pool density
         perm = rt.permutation(num_blocks).astype(np.int32)
         tables = _tables_from_perm(lens, bs, M, perm)
         fs, fp = _history(lens)
