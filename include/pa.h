@@ -110,19 +110,27 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
 /* ---------------------------------------------------------------------------
  * Split-K (flash-decoding) planning for pa_decode_attention.
  *
- * With S = num_splits the tokens of every sequence are cut into partitions
- * of P = ceil(max_blocks_per_seq / S) blocks; sequence b uses
- * ceil(ceil(seq_len_b / block_size) / P) partitions.  Each partition yields a
- * normalised partial output and its log-sum-exp, combined as
+ * With S = num_splits (at most 512, at most max_blocks_per_seq) the tokens of
+ * every sequence are cut into partitions of P = ceil(max_blocks_per_seq / S)
+ * blocks; sequence b uses ceil(ceil(seq_len_b / block_size) / P) partitions.
+ * Each partition yields a normalised partial output and its log-sum-exp,
+ * combined as
  *     out = sum_i exp(lse_i - L) o_i,  L = log sum_i exp(lse_i)
- * which equals the unsplit result in exact arithmetic.  num_splits == 0
- * picks S from the batch shape and the current device's SM count.
+ * which equals the unsplit result in exact arithmetic.  The combination runs
+ * inside pa_decode_attention: the last partition of a (sequence, kv head) to
+ * finish merges them.  num_splits == 0 picks S from the batch shape and the
+ * current device's SM count.
  *
  * pa_decode_resolve_splits returns the S that pa_decode_attention will use for
  * the request (0 asks for the automatic choice); the workspace must hold
  * pa_decode_workspace_bytes(...) bytes for that S (0 bytes when S == 1).
- * Workspace layout: o_part fp32 [batch][num_q_heads][S][head_dim], then
- * lse fp32 [batch][num_q_heads][S], 256-byte aligned.
+ * Workspace layout, each part 256-byte aligned: o_part fp32
+ * [batch][num_q_heads][S][head_dim], lse fp32 [batch][num_q_heads][S]
+ * (base-2 log-sum-exp of the scaled scores), counters int32
+ * [batch][num_kv_heads].  The workspace must be zero-filled before its first
+ * use; every call that completes leaves the counters at zero again (after a
+ * PA_DEVERR_TIMEOUT, zero it again).  Calls that share a workspace must not
+ * overlap on the device.
  * ------------------------------------------------------------------------- */
 int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits);
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,

@@ -117,6 +117,24 @@ int device_sms() {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+constexpr int kMaxSplits = 512;  // partitions per sequence
+
+struct WsLayout {
+    size_t o_off, lse_off, cnt_off, total;
+};
+
+// o_part fp32 [B][Hq][S][d] | lse fp32 [B][Hq][S] | counters int32 [B][Hkv], 256-byte aligned parts
+WsLayout ws_layout(int B, int Hq, int Hkv, int d, int S) {
+    const size_t rows = (size_t)B * Hq * S;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    WsLayout w;
+    w.o_off = 0;
+    w.lse_off = up(rows * d * sizeof(float));
+    w.cnt_off = w.lse_off + up(rows * sizeof(float));
+    w.total = w.cnt_off + up((size_t)B * Hkv * sizeof(int));
+    return w;
+}
+
 // Blocks per partition for a resolved split count.
 int part_blocks_for(int M, int S) { return (int)ceil_div(M, S < 1 ? 1 : S); }
 
@@ -159,7 +177,8 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
     if (batch <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return 1;
     const int M = max_blocks_per_seq;
     if (num_splits > 0) {
-        const int S = num_splits > M ? M : num_splits;
+        int S = num_splits > M ? M : num_splits;
+        if (S > kMaxSplits) S = kMaxSplits;
         return (int)ceil_div(M, part_blocks_for(M, S));
     }
     // Automatic: aim for ~12 CTAs per SM over the batch (several waves of the
@@ -171,17 +190,16 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
     if (P < 16) P = 16;
     if (P > 128) P = 128;
     if (P > M) P = M;
+    if (ceil_div(M, P) > kMaxSplits) P = ceil_div(M, kMaxSplits);
     return (int)ceil_div(M, P);
 }
 
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_blocks_per_seq, int num_splits) {
-    if (batch <= 0 || num_q_heads <= 0 || head_dim <= 0) return 0;
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
     if (S <= 1) return 0;
-    const size_t rows = (size_t)batch * num_q_heads * S;
-    const size_t o_bytes = (rows * head_dim * sizeof(float) + 255) & ~(size_t)255;
-    return o_bytes + rows * sizeof(float);
+    return ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S).total;
 }
 
 pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -229,11 +247,13 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
     L.lens = seq_lens;
     L.o_part = nullptr;
     L.lse = nullptr;
+    L.counters = nullptr;
     if (S > 1) {
-        const size_t o_rows = (size_t)batch * num_q_heads * S;
-        const size_t o_bytes = (o_rows * head_dim * sizeof(float) + 255) & ~(size_t)255;
-        L.o_part = static_cast<float*>(workspace);
-        L.lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + o_bytes);
+        const WsLayout wl = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S);
+        char* base = static_cast<char*>(workspace);
+        L.o_part = reinterpret_cast<float*>(base + wl.o_off);
+        L.lse = reinterpret_cast<float*>(base + wl.lse_off);
+        L.counters = reinterpret_cast<int*>(base + wl.cnt_off);
     }
     L.tm_k = &tm_k;
     L.tm_v = &tm_v;

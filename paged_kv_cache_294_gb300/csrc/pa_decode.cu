@@ -24,8 +24,9 @@
 //     registers;
 //   * the four warps' states merge in shared memory; a single-partition
 //     sequence writes bf16 out directly, otherwise the CTA writes its
-//     normalised partial output and base-2 log-sum-exp to the workspace and
-//     the merge kernel combines them.
+//     normalised partial output and base-2 log-sum-exp to the workspace, and
+//     the last CTA of the (sequence, kv head) group to finish merges the
+//     group's partials by log-sum-exp (an atomic counter per group).
 // The fp8 cache path converts e4m3 codes to f16 exactly in registers (q and
 // probabilities are f16 there), folds the K scale into the scores and
 // applies the V scale per page to a fresh P.V accumulator.
@@ -46,6 +47,7 @@ struct DecodeArgs {
     const int32_t* lens;
     float* o_part;
     float* lse;
+    int* counters;
     int Hq, Hkv, G, M, num_blocks, part_blocks, S;
     float scale_log2;
 };
@@ -398,54 +400,54 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             if (dim == 0) a.lse[row * a.S + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
         }
     }
-}
-
-// One warp per (sequence, query head): combine the partitions of sequences
-// that used more than one.  out = sum_i 2^(lse_i - L) o_i / sum_i 2^(lse_i - L).
-template <int D>
-__global__ void __launch_bounds__(128) lse_merge_kernel(__nv_bfloat16* __restrict__ out,
-                                                        const float* __restrict__ o_part,
-                                                        const float* __restrict__ lse,
-                                                        const int32_t* __restrict__ lens, int B,
-                                                        int Hq, int M, int bs, int part_blocks,
-                                                        int S) {
-    const int gw = blockIdx.x * 4 + (threadIdx.x >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= B * Hq) return;
-    const int b = gw / Hq;
-    int len = lens[b];
-    len = len < 0 ? 0 : (len > M * bs ? M * bs : len);
-    const int nblk = (len + bs - 1) / bs;
-    const int nsplit = (nblk + part_blocks - 1) / part_blocks;
     if (nsplit <= 1) return;
-    const float* L = lse + (int64_t)gw * S;
-    float mx = -INFINITY;
-    for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, L[k]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    constexpr int PER = D / 32;
-    float acc[PER];
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float den = 0.f;
-    const float* op = o_part + (int64_t)gw * S * D + lane * PER;
-    for (int k = 0; k < nsplit; ++k) {
-        const float w = exp2f(L[k] - mx);
-        den += w;
-        if (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(op + (int64_t)k * D);
-            acc[0] = fmaf(w, v.x, acc[0]);
-            acc[1] = fmaf(w, v.y, acc[1]);
-            acc[2] = fmaf(w, v.z, acc[2]);
-            acc[3] = fmaf(w, v.w, acc[3]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] = fmaf(w, op[(int64_t)k * D + e], acc[e]);
-        }
+
+    // ---------------------------------------------------------- split-K merge
+    // The CTA that finishes a (sequence, kv head) group last combines the
+    // group's partitions: out = sum_k 2^(lse_k - L) o_k, L = log2 sum_k 2^lse_k.
+    // Partials travel through L2 (stores, fence, counter); nothing waits on
+    // another CTA.  The last CTA resets the counter for the next call.
+    __shared__ int s_last;
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int old = atomicAdd(&a.counters[b * a.Hkv + h], 1);
+        s_last = (old == nsplit - 1);
     }
-    const float inv = 1.f / den;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    float* sw = cm;  // [G][nsplit] weights, reusing the combine area
+    const int64_t row0 = (int64_t)b * a.Hq + h * G;
+    for (int i = threadIdx.x; i < G * nsplit; i += C::NTHREADS) {
+        const int gq = i / nsplit, k = i - gq * nsplit;
+        sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
+    }
+    __syncthreads();
+    for (int gq = warp; gq < G; gq += C::NCW + 1) {
+        float* wr = sw + gq * nsplit;
+        float mx = -INFINITY;
+        for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, wr[k]);
 #pragma unroll
-    for (int e = 0; e < PER; ++e) out[(int64_t)gw * D + lane * PER + e] = __float2bfloat16_rn(acc[e] * inv);
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float den = 0.f;
+        for (int k = lane; k < nsplit; k += 32) den += exp2f(wr[k] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        __syncwarp();
+        for (int k = lane; k < nsplit; k += 32) wr[k] = exp2f(wr[k] - mx) * inv;
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * D; idx += C::NTHREADS) {
+        const int gq = idx / D, dim = idx - gq * D;
+        const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
+        const float* wr = sw + gq * nsplit;
+        float acc = 0.f;
+        for (int k = 0; k < nsplit; ++k) acc = fmaf(wr[k], __ldcg(op + (int64_t)k * D), acc);
+        a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc);
+    }
+    if (threadIdx.x == 0) a.counters[b * a.Hkv + h] = 0;
 }
 
 template <int D, int BS, bool FP8>
@@ -470,6 +472,7 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.lens = L.lens;
     a.o_part = L.o_part;
     a.lse = L.lse;
+    a.counters = L.counters;
     a.Hq = L.Hq;
     a.Hkv = L.Hkv;
     a.G = L.Hq / L.Hkv;
@@ -480,11 +483,6 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.scale_log2 = L.scale * 1.4426950408889634f;
     dim3 grid(L.S, L.Hkv, L.B);
     paged_decode_kernel<D, BS, FP8><<<grid, C::NTHREADS, C::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
-    e = cudaGetLastError();
-    if (e != cudaSuccess || L.S <= 1) return e;
-    const int warps = L.B * L.Hq;
-    lse_merge_kernel<D><<<(warps + 3) / 4, 128, 0, stream>>>(
-        (__nv_bfloat16*)L.out, L.o_part, L.lse, L.lens, L.B, L.Hq, L.M, L.bs, L.part_blocks, L.S);
     return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@ struct DecodeLaunch {
     const int32_t* lens;
     float* o_part;      // workspace, [B][Hq][S][d] (S > 1 only)
     float* lse;         // workspace, [B][Hq][S]
+    int* counters;      // workspace, [B][Hkv], zero between calls
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     int B, Hq, Hkv, d, bs, M, num_blocks;

@@ -74,7 +74,8 @@ class PagedDecodeLayer:
     def ensure_workspace(self, num_splits: int = 0) -> torch.Tensor:
         need = pa_decode_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits)
         if self.workspace is None or self.workspace.numel() < need:
-            self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            # zero-filled: the split-K counters must start at zero (calls keep them there)
+            self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
         return self.workspace
 
     def num_splits(self, num_splits: int = 0) -> int:

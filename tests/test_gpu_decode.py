@@ -172,3 +172,20 @@ def test_full_size_long_sampled():
     w = workloads.make("long", device="cuda")
     check(w, 0, [1])
     check(w, 64, [3])
+
+
+def test_split_counters_return_to_zero_and_calls_repeat_bit_exactly():
+    w = workloads.make("8b", B=6, seq_len=900)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    ws = layer.ensure_workspace(5)
+    assert layer.num_splits(5) > 1
+    outs = []
+    for _ in range(3):
+        layer.decode(num_splits=5)
+        torch.cuda.synchronize()
+        outs.append(layer.out.clone())
+        # counters: the last int32 words of the workspace, [B][Hkv]
+        need = pa.pa_decode_workspace_bytes(layer.B, layer.Hq, layer.Hkv, layer.d, layer.M, 5)
+        cnt = ws[:need].view(torch.int32)[-((layer.B * layer.Hkv + 63) // 64 * 64):]
+        assert int(cnt.abs().sum()) == 0
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
