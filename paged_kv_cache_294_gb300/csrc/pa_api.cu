@@ -120,18 +120,21 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int kMaxSplits = 512;  // partitions per sequence
 
 struct WsLayout {
-    size_t o_off, lse_off, cnt_off, total;
+    size_t o_off, lse_off, cnt_off, queue_off, total;
 };
 
-// o_part fp32 [B][Hq][S][d] | lse fp32 [B][Hq][S] | counters int32 [B][Hkv], 256-byte aligned parts
+// o_part fp32 [B][Hq][S][d] | lse fp32 [B][Hq][S]   (S > 1 only)
+// counters int32 [B][Hkv] | queue int32 [2]           (always)
+// each part 256-byte aligned
 WsLayout ws_layout(int B, int Hq, int Hkv, int d, int S) {
-    const size_t rows = (size_t)B * Hq * S;
+    const size_t rows = S > 1 ? (size_t)B * Hq * S : 0;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     WsLayout w;
     w.o_off = 0;
     w.lse_off = up(rows * d * sizeof(float));
     w.cnt_off = w.lse_off + up(rows * sizeof(float));
-    w.total = w.cnt_off + up((size_t)B * Hkv * sizeof(int));
+    w.queue_off = w.cnt_off + up((size_t)B * Hkv * sizeof(int));
+    w.total = w.queue_off + 256;
     return w;
 }
 
@@ -198,7 +201,6 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
                                  int max_blocks_per_seq, int num_splits) {
     if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
-    if (S <= 1) return 0;
     return ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S).total;
 }
 
@@ -229,8 +231,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
     const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
                                                   max_blocks_per_seq, num_splits);
-    if (need > 0 && (!workspace || workspace_bytes < need || !aligned16(workspace)))
-        return PA_ERR_INVALID;
+    if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_INVALID;
 
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
     CUtensorMap tm_k, tm_v;
@@ -247,14 +248,17 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
     L.lens = seq_lens;
     L.o_part = nullptr;
     L.lse = nullptr;
-    L.counters = nullptr;
-    if (S > 1) {
+    {
         const WsLayout wl = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S);
         char* base = static_cast<char*>(workspace);
-        L.o_part = reinterpret_cast<float*>(base + wl.o_off);
-        L.lse = reinterpret_cast<float*>(base + wl.lse_off);
+        if (S > 1) {
+            L.o_part = reinterpret_cast<float*>(base + wl.o_off);
+            L.lse = reinterpret_cast<float*>(base + wl.lse_off);
+        }
         L.counters = reinterpret_cast<int*>(base + wl.cnt_off);
+        L.queue = reinterpret_cast<int*>(base + wl.queue_off);
     }
+    L.persistent = pa::decode_persistent_ok(batch);
     L.tm_k = &tm_k;
     L.tm_v = &tm_v;
     L.B = batch;

@@ -1,5 +1,5 @@
-// Paged decode attention for sm_103a, with split-K partitions and a
-// log-sum-exp merge.
+// Paged decode attention for sm_103a, with split-K partitions merged by
+// log-sum-exp inside the same launch.
 //
 // What it computes ("KV cache & continuous batching", sections "The core
 // insight" and "2. PagedAttention"; "LLM Serving - KV Cache, Batching,
@@ -9,27 +9,31 @@
 // head i / G.  Scores, softmax and P.V stay on chip ("LLM Inference
 // Optimization", section "FlashAttention") with an fp32 online softmax.
 //
-// How (one CTA per (split, kv_head, sequence), 5 warps):
-//   * warp 4 is the producer: it reads the partition's block-table entries
-//     (32 at a time, coalesced) and, per page, issues TMA tile loads of the
-//     K and V pages of that (block, kv_head) into a ring of shared-memory
-//     stages with the 128-byte swizzle, completion counted on an mbarrier;
-//   * warps 0-3 consume pages round-robin; each keeps its own running max,
-//     sum and output accumulator for the G query heads of the group;
-//   * per page a consumer warp computes S^T = Q K^T with m16n8k16 MMAs (the G
-//     query heads are the M rows, the page's tokens the N columns, head_dim
-//     the K depth; q stays in registers for the whole CTA), updates the
-//     online softmax in registers, and accumulates O^T += V^T P^T with MMAs
-//     whose B operand is the probability tile straight from the score
-//     registers;
-//   * the four warps' states merge in shared memory; a single-partition
-//     sequence writes bf16 out directly, otherwise the CTA writes its
-//     normalised partial output and base-2 log-sum-exp to the workspace, and
-//     the last CTA of the (sequence, kv head) group to finish merges the
-//     group's partials by log-sum-exp (an atomic counter per group).
-// The fp8 cache path converts e4m3 codes to f16 exactly in registers (q and
-// probabilities are f16 there), folds the K scale into the scores and
-// applies the V scale per page to a fresh P.V accumulator.
+// Work unit ("item"): one partition of P blocks of one (sequence, kv head).
+// A CTA has 5 warps:
+//   * warp 4, the producer, issues TMA tile loads of each page's K and V
+//     (one (block, kv head) page = bs rows x head_dim) into a ring of shared
+//     memory stages written with the 128-byte swizzle; completion is counted
+//     in bytes on one mbarrier per stage;
+//   * warps 0-3 consume the item's pages round-robin.  Per page a warp forms
+//     S^T = Q K^T with m16n8k16 MMAs (the G query heads of the group are the
+//     M rows, the page's tokens the N columns, head_dim the K depth; q lives
+//     in registers), updates its fp32 online softmax in registers and
+//     accumulates O^T += V^T P^T with MMAs whose B operand is the probability
+//     tile taken straight from the score registers;
+//   * at the item's end the consumer warps merge their states in shared
+//     memory; a one-partition sequence writes bf16 out, otherwise the
+//     partition writes its normalised partial and base-2 log-sum-exp to the
+//     workspace and the group's last partition to finish merges them.
+// Two launch shapes share this code:
+//   * persistent (batch <= kPersistMaxB): one grid of (#SM x resident CTAs)
+//     CTAs pulls items from an atomic queue; the producer streams the next
+//     item's pages (and its q rows, by bulk copy) while the consumers finish
+//     the current one, so the ring never drains between items;
+//   * one CTA per item (grid = partitions x kv heads x sequences) otherwise.
+// fp8 cache: e4m3 codes convert exactly to f16 in registers (q and the
+// probabilities are f16 there), the K scale folds into the scores and the V
+// scale applies per page to a fresh P.V accumulator.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -47,8 +51,9 @@ struct DecodeArgs {
     const int32_t* lens;
     float* o_part;
     float* lse;
-    int* counters;
-    int Hq, Hkv, G, M, num_blocks, part_blocks, S;
+    int* counters;   // [B][Hkv] merge counters
+    int* queue;      // [2]: next item, finished CTAs (persistent launch)
+    int B, Hq, Hkv, G, M, num_blocks, part_blocks, S;
     float scale_log2;
 };
 
@@ -59,30 +64,310 @@ struct Cfg {
     static constexpr int NCH = ROWB / 128;      // 128-byte column chunks = TMA boxes per page
     static constexpr int PAGEB = BS * ROWB;     // one (block, kv_head) page of K (or V)
     static constexpr int STAGEB = 2 * PAGEB;    // K page + V page
-    static constexpr int NSTAGE = STAGEB >= 16384 ? 4 : (STAGEB >= 8192 ? 8 : 16);
     static constexpr int NCW = 4;               // consumer warps
     static constexpr int NTHREADS = (NCW + 1) * 32;
     static constexpr int NT = BS / 8;           // 8-token column tiles per page (QK)
     static constexpr int KS = D / 16;           // 16-deep steps over head_dim (QK)
     static constexpr int MT = D / 16;           // 16-row tiles of head_dim (PV)
     static constexpr int KT = BS / 16;          // 16-token steps (PV)
-    static constexpr int BAR_OFF = NSTAGE * STAGEB;
-    static constexpr int SMEM = BAR_OFF + 2 * NSTAGE * 8 + 1024;  // + alignment slack
+    static constexpr int COMBINE_FLOATS = NCW * (8 * D + 16);
+    static constexpr int QBYTES = 8 * D * 2;    // q rows of one group (G <= 8), bf16
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
-    static_assert(NCW * (8 * D + 16) * 4 <= NSTAGE * STAGEB, "combine area must fit in the stages");
 };
 
+constexpr int kPersistMaxB = 512;   // batch limit of the persistent launch (prefix table in smem)
+constexpr int kItemSlots = 4;       // item descriptors in flight (persistent launch)
+
+// ------------------------------------------------------------------ per warp
 template <int D, int BS, bool FP8>
+struct WarpAcc {
+    float m, l;
+    float o[D / 16][4];
+    uint32_t qa[D / 16][2];
+
+    __device__ __forceinline__ void reset() {
+        m = -INFINITY;
+        l = 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+
+    // q of query head h*G + g as the MMA A operand; rows g >= G stay zero.
+    // `qrow` is a generic pointer (global or shared) to that head's bf16 row.
+    __device__ __forceinline__ void load_q(const uint16_t* qrow, bool valid, int c) {
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            if (!valid) {
+                qa[ks][0] = qa[ks][1] = 0u;
+            } else if (FP8) {
+                // k order inside a 16-deep step matches the e4m3 byte order 4c .. 4c+3
+                const uint2 w = *reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * c);
+                qa[ks][0] = pack_f16x2(__uint_as_float((w.x & 0xFFFF) << 16), __uint_as_float(w.x & 0xFFFF0000u));
+                qa[ks][1] = pack_f16x2(__uint_as_float((w.y & 0xFFFF) << 16), __uint_as_float(w.y & 0xFFFF0000u));
+            } else {
+                qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c);
+                qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c + 8);
+            }
+        }
+    }
+
+    // One page: kt / vt are the shared addresses of its K and V tiles, `valid`
+    // the number of its tokens inside the sequence, sl2 = scale * log2(e)
+    // (times the K scale for fp8), vsc the V scale (fp8).
+    __device__ __forceinline__ void page(uint32_t kt, uint32_t vt, int valid, float sl2, float vsc, int lane) {
+        using C = Cfg<D, BS, FP8>;
+        const int g = lane >> 2, c = lane & 3;
+        const int mi = lane >> 3, r = lane & 7;
+
+        // ------------------------------------------------ S^T = Q K^T
+        float acc[C::NT][4];
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < C::KS; ++ks) {
+            const uint32_t A[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+            if (FP8) {
+#pragma unroll
+                for (int nt = 0; nt < C::NT; ++nt) {
+                    const int t = nt * 8 + g;
+                    const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
+                    mma_f16(acc[nt], A, e4m3x2_to_f16x2((uint16_t)(w & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+                }
+            } else {
+                const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
+                const uint32_t ktile = kt + (jg >> 3) * (BS * 128);
+#pragma unroll
+                for (int p = 0; p < C::NT / 2; ++p) {
+                    const int t = (2 * p + (mi >> 1)) * 8 + r;
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(swz128(ktile, t, (jg & 7) * 16), r0, r1, r2, r3);
+                    mma_bf16(acc[2 * p], A, r0, r1);
+                    mma_bf16(acc[2 * p + 1], A, r2, r3);
+                }
+            }
+        }
+
+        // ------------------------------------------------ online softmax
+        float sc[C::NT][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tok = nt * 8 + 2 * c + e;
+                const float v = tok < valid ? acc[nt][e] * sl2 : -INFINITY;
+                sc[nt][e] = v;
+                mx = fmaxf(mx, v);
+            }
+        }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = exp2f(m - m_use);
+        float psum = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < C::NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                sc[nt][e] = exp2f(sc[nt][e] - m_use);
+                psum += sc[nt][e];
+            }
+        }
+        l = l * alpha + psum;
+        m = m_new;
+        // accumulator columns are query heads 2c and 2c+1
+        const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+        const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            o[mt][0] *= al0;
+            o[mt][1] *= al1;
+            o[mt][2] *= al0;
+            o[mt][3] *= al1;
+        }
+
+        // rows past the sequence end hold stale bytes: zero them so that
+        // 0-probability x non-finite garbage cannot reach the accumulator
+        if (valid < BS) {
+            for (int idx = valid * C::ROWB / 16 + lane; idx < BS * C::ROWB / 16; idx += 32) {
+                const int row = idx / (C::ROWB / 16), u = idx % (C::ROWB / 16);
+                const uint32_t tile = vt + (u >> 3) * (BS * 128);
+                asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz128(tile, row, (u & 7) * 16)), "r"(0u)
+                             : "memory");
+            }
+            __syncwarp();
+        }
+
+        // ------------------------------------------------ O^T += V^T P^T
+        if (FP8) {
+            uint32_t pb[C::KT][2];
+#pragma unroll
+            for (int kk = 0; kk < C::KT; ++kk) {
+                pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+            }
+#pragma unroll
+            for (int mp = 0; mp < C::MT / 2; ++mp) {
+                float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    const int t = kk * 16 + (mi & 1) * 8 + r;
+                    const int unit = 2 * mp + (mi >> 1);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(swz128(vt, t, unit * 16), r0, r1, r2, r3);
+                    // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes
+                    const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
+                    const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
+                    const uint32_t A0[4] = {e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
+                                            e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x1 >> 16))};
+                    const uint32_t A1[4] = {e4m3x2_to_f16x2((uint16_t)(x2 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x2 >> 16)),
+                                            e4m3x2_to_f16x2((uint16_t)(x3 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x3 >> 16))};
+                    mma_f16(t0, A0, pb[kk][0], pb[kk][1]);
+                    mma_f16(t1, A1, pb[kk][0], pb[kk][1]);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    o[2 * mp][e] = fmaf(vsc, t0[e], o[2 * mp][e]);
+                    o[2 * mp + 1][e] = fmaf(vsc, t1[e], o[2 * mp + 1][e]);
+                }
+            }
+        } else {
+            uint32_t pb[C::KT][2];
+#pragma unroll
+            for (int kk = 0; kk < C::KT; ++kk) {
+                pb[kk][0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                pb[kk][1] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+            }
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const int jg = 2 * mt + (mi & 1);
+                const uint32_t vtile = vt + (jg >> 3) * (BS * 128);
+#pragma unroll
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    const int t = kk * 16 + (mi >> 1) * 8 + r;
+                    uint32_t A[4];
+                    ldsm_x4_t(swz128(vtile, t, (jg & 7) * 16), A[0], A[1], A[2], A[3]);
+                    mma_bf16(o[mt], A, pb[kk][0], pb[kk][1]);
+                }
+            }
+        }
+        if (valid < BS) fence_proxy_async_smem();  // generic writes before the next TMA fill
+    }
+
+    // Publish this warp's state for the item-level combine.
+    __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int warp, int lane) {
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        const int g = lane >> 2, c = lane & 3, n = lane >> 2;
+        if (c == 0) {
+            cm[warp * 8 + g] = m;
+            cl[warp * 8 + g] = l;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int gq = 2 * c + (e & 1);
+                const int dim = FP8 ? mt * 16 + 2 * n + (e >> 1) : mt * 16 + n + 8 * (e >> 1);
+                co[(warp * 8 + gq) * D + dim] = o[mt][e];
+            }
+        }
+    }
+};
+
+// Item-level combine of the consumer warps' states, then the output: bf16 out
+// for a one-partition sequence, else the partition's normalised partial and
+// base-2 log-sum-exp.  Threads tid < nthr take part.
+template <int D, int NCW>
+__device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* cm, const float* cl, const float* co,
+                                              int b, int h, int split, int nsplit, int tid, int nthr) {
+    const int G = a.G;
+    for (int idx = tid; idx < G * D; idx += nthr) {
+        const int gq = idx / D, dim = idx - gq * D;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) M = fmaxf(M, cm[w * 8 + gq]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) {
+                const float f = exp2f(cm[w * 8 + gq] - M);
+                L += cl[w * 8 + gq] * f;
+                O += co[(w * 8 + gq) * D + dim] * f;
+            }
+        }
+        const int64_t row = (int64_t)b * a.Hq + h * G + gq;
+        const float val = (M == -INFINITY) ? 0.f : O / L;
+        if (nsplit <= 1) {
+            a.out[row * D + dim] = __float2bfloat16_rn(val);
+        } else {
+            a.o_part[(row * a.S + split) * D + dim] = val;
+            if (dim == 0) a.lse[row * a.S + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
+        }
+    }
+}
+
+// Log-sum-exp merge of a (sequence, kv head) group's nsplit partials, by the
+// group's last partition to finish:  out = sum_k 2^(lse_k - L) o_k.
+// `sw` holds G * nsplit floats of shared memory.
+template <int D>
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int b, int h, int nsplit, int tid,
+                                           int nthr, int warp, int nwarps, int lane, void (*sync)()) {
+    const int G = a.G;
+    const int64_t row0 = (int64_t)b * a.Hq + h * G;
+    for (int i = tid; i < G * nsplit; i += nthr) {
+        const int gq = i / nsplit, k = i - gq * nsplit;
+        sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
+    }
+    sync();
+    for (int gq = warp; gq < G; gq += nwarps) {
+        float* wr = sw + gq * nsplit;
+        float mx = -INFINITY;
+        for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, wr[k]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float den = 0.f;
+        for (int k = lane; k < nsplit; k += 32) den += exp2f(wr[k] - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        __syncwarp();
+        for (int k = lane; k < nsplit; k += 32) wr[k] = exp2f(wr[k] - mx) * inv;
+    }
+    sync();
+    for (int idx = tid; idx < G * D; idx += nthr) {
+        const int gq = idx / D, dim = idx - gq * D;
+        const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
+        const float* wr = sw + gq * nsplit;
+        float acc = 0.f;
+        for (int k = 0; k < nsplit; ++k) acc = fmaf(wr[k], __ldcg(op + (int64_t)k * D), acc);
+        a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc);
+    }
+}
+
+__device__ __forceinline__ void sync_cta() { __syncthreads(); }
+// named barrier 1 over the 4 consumer warps only (the producer keeps streaming)
+__device__ __forceinline__ void sync_consumers() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
+
+// ========================================================================
+// One CTA per item: grid (partitions, kv heads, sequences).
+// ========================================================================
+template <int D, int BS, bool FP8, int NSTAGE>
 __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v, const DecodeArgs a) {
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeArgs a) {
     using C = Cfg<D, BS, FP8>;
+    constexpr int BAR_OFF = NSTAGE * C::STAGEB;
+    static_assert(C::COMBINE_FLOATS * 4 <= NSTAGE * C::STAGEB, "combine area must fit in the stages");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - raw_u32);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sgen + C::BAR_OFF);
-    uint64_t* empty = full + C::NSTAGE;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sgen + BAR_OFF);
+    uint64_t* empty = full + NSTAGE;
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -91,7 +376,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
         if (threadIdx.x == 0 && split == 0 && h == 0) raise_error(PA_DEVERR_SEQ_LEN);
-        len = len < 0 ? 0 : cap;
+        len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
     const int nsplit = (nblk + a.part_blocks - 1) / a.part_blocks;  // 0 when len == 0
@@ -101,7 +386,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::NSTAGE; ++s) {
+        for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
@@ -109,15 +394,9 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     }
     __syncthreads();
 
-    const int g = lane >> 2;  // MMA row group: query head within the group (QK), token col (B)
-    const int c = lane & 3;
-    float m_run = -INFINITY, l_run = 0.f;
-    float o[C::MT][4];
-#pragma unroll
-    for (int i = 0; i < C::MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-
+    WarpAcc<D, BS, FP8> st;
+    st.reset();
     if (warp == C::NCW) {
-        // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
             prefetch_tensormap(&tm_v);
@@ -137,59 +416,34 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 const int phys = __shfl_sync(0xffffffffu, myphys, k);
                 if (lane == 0 && alive) {
                     const int i = base + k;
-                    const int s = i % C::NSTAGE;
-                    if (i >= C::NSTAGE) alive = mbar_wait(&empty[s], ((i / C::NSTAGE) - 1) & 1);
+                    const int s = i % NSTAGE;
+                    if (i >= NSTAGE) alive = mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1);
                     if (alive) {
                         mbar_arrive_expect_tx(&full[s], C::STAGEB);
                         const int y = (phys * a.Hkv + h) * BS;
-                        uint8_t* st = sgen + s * C::STAGEB;
+                        uint8_t* stg = sgen + s * C::STAGEB;
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
-                            tma_load_2d(st + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
+                            tma_load_2d(stg + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
-                            tma_load_2d(st + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y,
-                                        &full[s]);
+                            tma_load_2d(stg + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y, &full[s]);
                     }
                 }
             }
         }
-        // Every issued load must land before the CTA may reuse or release its
-        // shared memory: wait for the last use of each stage (already complete
-        // on the normal path).
+        // every issued load lands before the shared memory is reused or released
         if (lane == 0) {
-            for (int s = 0; s < C::NSTAGE && s < npages; ++s) {
-                const int last = s + ((npages - 1 - s) / C::NSTAGE) * C::NSTAGE;
-                mbar_wait(&full[s], (last / C::NSTAGE) & 1);
+            for (int s = 0; s < NSTAGE && s < npages; ++s) {
+                const int last = s + ((npages - 1 - s) / NSTAGE) * NSTAGE;
+                mbar_wait(&full[s], (last / NSTAGE) & 1);
             }
         }
     } else {
-        // ---------------------------------------------------------- consumers
-        // q of query head h*G + g as the A operand (rows g >= G stay zero).
-        uint32_t qa[C::KS][2];
-        if (g < a.G) {
-            const uint16_t* qrow = a.q + ((int64_t)b * a.Hq + h * a.G + g) * D;
-#pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) {
-                if (FP8) {
-                    // k order inside a step matches the e4m3 byte order: 4c .. 4c+3
-                    const uint2 w = *reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * c);
-                    qa[ks][0] = pack_f16x2(__uint_as_float((w.x & 0xFFFF) << 16),
-                                           __uint_as_float(w.x & 0xFFFF0000u));
-                    qa[ks][1] = pack_f16x2(__uint_as_float((w.y & 0xFFFF) << 16),
-                                           __uint_as_float(w.y & 0xFFFF0000u));
-                } else {
-                    qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c);
-                    qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c + 8);
-                }
-            }
-        } else {
-#pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) qa[ks][0] = qa[ks][1] = 0u;
-        }
-
+        const int g = lane >> 2;
+        st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
         for (int i = warp; i < npages; i += C::NCW) {
-            const int s = i % C::NSTAGE;
+            const int s = i % NSTAGE;
             float ksc = 1.f, vsc = 1.f;
             if (FP8) {
                 int phys = trow[i];
@@ -197,216 +451,24 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 ksc = a.k_scale[(int64_t)phys * a.Hkv + h];
                 vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
             }
-            if (!mbar_wait(&full[s], (i / C::NSTAGE) & 1)) break;
+            if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
             const uint32_t kt = sbase + s * C::STAGEB;
-            const uint32_t vt = kt + C::PAGEB;
-            const int valid = min(BS, len - (j0 + i) * BS);
-
-            // ------------------------------------------------ S^T = Q K^T
-            float acc[C::NT][4];
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < C::KS; ++ks) {
-                const uint32_t A[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-                if (FP8) {
-#pragma unroll
-                    for (int nt = 0; nt < C::NT; ++nt) {
-                        const int t = nt * 8 + g;
-                        const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
-                        mma_f16(acc[nt], A, e4m3x2_to_f16x2((uint16_t)(w & 0xFFFF)),
-                                e4m3x2_to_f16x2((uint16_t)(w >> 16)));
-                    }
-                } else {
-                    const int mi = lane >> 3, r = lane & 7;
-                    const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
-                    const uint32_t ktile = kt + (jg >> 3) * (BS * 128);
-#pragma unroll
-                    for (int p = 0; p < C::NT / 2; ++p) {
-                        const int t = (2 * p + (mi >> 1)) * 8 + r;
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4(swz128(ktile, t, (jg & 7) * 16), r0, r1, r2, r3);
-                        mma_bf16(acc[2 * p], A, r0, r1);
-                        mma_bf16(acc[2 * p + 1], A, r2, r3);
-                    }
-                }
-            }
-
-            // ------------------------------------------------ online softmax
-            const float sl2 = FP8 ? a.scale_log2 * ksc : a.scale_log2;
-            float sc[C::NT][2];
-            float mx = -INFINITY;
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tok = nt * 8 + 2 * c + e;
-                    const float v = tok < valid ? acc[nt][e] * sl2 : -INFINITY;
-                    sc[nt][e] = v;
-                    mx = fmaxf(mx, v);
-                }
-            }
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m_run, mx);
-            const float m_use = m_new == -INFINITY ? 0.f : m_new;
-            const float alpha = exp2f(m_run - m_use);
-            float psum = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < C::NT; ++nt) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    sc[nt][e] = exp2f(sc[nt][e] - m_use);
-                    psum += sc[nt][e];
-                }
-            }
-            l_run = l_run * alpha + psum;
-            m_run = m_new;
-            // accumulator columns are query heads 2c and 2c+1
-            const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
-            const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
-#pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
-            }
-
-            // rows past the sequence end hold stale bytes: zero them so that
-            // 0-probability x non-finite garbage cannot reach the accumulator
-            if (valid < BS) {
-                for (int idx = valid * C::ROWB / 16 + lane; idx < BS * C::ROWB / 16; idx += 32) {
-                    const int row = idx / (C::ROWB / 16), u = idx % (C::ROWB / 16);
-                    const uint32_t tile = vt + (u >> 3) * (BS * 128);
-                    asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(
-                                     swz128(tile, row, (u & 7) * 16)),
-                                 "r"(0u)
-                                 : "memory");
-                }
-                __syncwarp();
-            }
-
-            // ------------------------------------------------ O^T += V^T P^T
-            if (FP8) {
-                uint32_t pb[C::KT][2];
-#pragma unroll
-                for (int kk = 0; kk < C::KT; ++kk) {
-                    pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                    pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                }
-                const int mi = lane >> 3, r = lane & 7;
-#pragma unroll
-                for (int mp = 0; mp < C::MT / 2; ++mp) {
-                    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < C::KT; ++kk) {
-                        const int t = kk * 16 + (mi & 1) * 8 + r;
-                        const int unit = 2 * mp + (mi >> 1);
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4_t(swz128(vt, t, unit * 16), r0, r1, r2, r3);
-                        // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes
-                        const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
-                        const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
-                        const uint32_t A0[4] = {e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFF)),
-                                                e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
-                                                e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFF)),
-                                                e4m3x2_to_f16x2((uint16_t)(x1 >> 16))};
-                        const uint32_t A1[4] = {e4m3x2_to_f16x2((uint16_t)(x2 & 0xFFFF)),
-                                                e4m3x2_to_f16x2((uint16_t)(x2 >> 16)),
-                                                e4m3x2_to_f16x2((uint16_t)(x3 & 0xFFFF)),
-                                                e4m3x2_to_f16x2((uint16_t)(x3 >> 16))};
-                        mma_f16(t0, A0, pb[kk][0], pb[kk][1]);
-                        mma_f16(t1, A1, pb[kk][0], pb[kk][1]);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        o[2 * mp][e] = fmaf(vsc, t0[e], o[2 * mp][e]);
-                        o[2 * mp + 1][e] = fmaf(vsc, t1[e], o[2 * mp + 1][e]);
-                    }
-                }
-            } else {
-                uint32_t pb[C::KT][2];
-#pragma unroll
-                for (int kk = 0; kk < C::KT; ++kk) {
-                    pb[kk][0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                    pb[kk][1] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-                }
-                const int mi = lane >> 3, r = lane & 7;
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                    const int jg = 2 * mt + (mi & 1);
-                    const uint32_t vtile = vt + (jg >> 3) * (BS * 128);
-#pragma unroll
-                    for (int kk = 0; kk < C::KT; ++kk) {
-                        const int t = kk * 16 + (mi >> 1) * 8 + r;
-                        uint32_t A[4];
-                        ldsm_x4_t(swz128(vtile, t, (jg & 7) * 16), A[0], A[1], A[2], A[3]);
-                        mma_bf16(o[mt], A, pb[kk][0], pb[kk][1]);
-                    }
-                }
-            }
-            if (valid < BS) fence_proxy_async_smem();  // generic writes before the next TMA fill
+            st.page(kt, kt + C::PAGEB, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc,
+                    lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-        l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
     }
 
     __syncthreads();  // pipeline drained: the stage memory becomes the combine area
-    float* cm = reinterpret_cast<float*>(sgen);  // [NCW][8] running max (base 2)
-    float* cl = cm + C::NCW * 8;                 // [NCW][8] running sum
-    float* co = cl + C::NCW * 8;                 // [NCW][8][D] accumulators
-    if (warp < C::NCW) {
-        if (c == 0) {
-            cm[warp * 8 + g] = m_run;
-            cl[warp * 8 + g] = l_run;
-        }
-        const int n = lane >> 2;
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int gq = 2 * c + (e & 1);
-                const int dim = FP8 ? mt * 16 + 2 * n + (e >> 1) : mt * 16 + n + 8 * (e >> 1);
-                co[(warp * 8 + gq) * D + dim] = o[mt][e];
-            }
-        }
-    }
+    float* cm = reinterpret_cast<float*>(sgen);
+    float* cl = cm + C::NCW * 8;
+    float* co = cl + C::NCW * 8;
+    if (warp < C::NCW) st.publish(cm, cl, co, warp, lane);
     __syncthreads();
-
-    const int G = a.G;
-    for (int idx = threadIdx.x; idx < G * D; idx += C::NTHREADS) {
-        const int gq = idx / D, dim = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < C::NCW; ++w) M = fmaxf(M, cm[w * 8 + gq]);
-        float L = 0.f, O = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < C::NCW; ++w) {
-                const float f = exp2f(cm[w * 8 + gq] - M);
-                L += cl[w * 8 + gq] * f;
-                O += co[(w * 8 + gq) * D + dim] * f;
-            }
-        }
-        const int64_t row = (int64_t)b * a.Hq + h * G + gq;
-        const float val = (M == -INFINITY) ? 0.f : O / L;
-        if (nsplit <= 1) {
-            a.out[row * D + dim] = __float2bfloat16_rn(val);
-        } else {
-            a.o_part[(row * a.S + split) * D + dim] = val;
-            if (dim == 0) a.lse[row * a.S + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
-        }
-    }
+    combine_store<D, C::NCW>(a, cm, cl, co, b, h, split, nsplit, threadIdx.x, C::NTHREADS);
     if (nsplit <= 1) return;
 
-    // ---------------------------------------------------------- split-K merge
-    // The CTA that finishes a (sequence, kv head) group last combines the
-    // group's partitions: out = sum_k 2^(lse_k - L) o_k, L = log2 sum_k 2^lse_k.
-    // Partials travel through L2 (stores, fence, counter); nothing waits on
-    // another CTA.  The last CTA resets the counter for the next call.
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
@@ -417,52 +479,282 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    float* sw = cm;  // [G][nsplit] weights, reusing the combine area
-    const int64_t row0 = (int64_t)b * a.Hq + h * G;
-    for (int i = threadIdx.x; i < G * nsplit; i += C::NTHREADS) {
-        const int gq = i / nsplit, k = i - gq * nsplit;
-        sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
-    }
-    __syncthreads();
-    for (int gq = warp; gq < G; gq += C::NCW + 1) {
-        float* wr = sw + gq * nsplit;
-        float mx = -INFINITY;
-        for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, wr[k]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float den = 0.f;
-        for (int k = lane; k < nsplit; k += 32) den += exp2f(wr[k] - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        const float inv = 1.f / den;
-        __syncwarp();
-        for (int k = lane; k < nsplit; k += 32) wr[k] = exp2f(wr[k] - mx) * inv;
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += C::NTHREADS) {
-        const int gq = idx / D, dim = idx - gq * D;
-        const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
-        const float* wr = sw + gq * nsplit;
-        float acc = 0.f;
-        for (int k = 0; k < nsplit; ++k) acc = fmaf(wr[k], __ldcg(op + (int64_t)k * D), acc);
-        a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc);
-    }
+    merge_group<D>(a, cm, b, h, nsplit, threadIdx.x, C::NTHREADS, warp, C::NCW + 1, lane, sync_cta);
     if (threadIdx.x == 0) a.counters[b * a.Hkv + h] = 0;
+}
+
+// ========================================================================
+// Persistent: items from an atomic queue, pages streamed across items.
+// ========================================================================
+struct ItemDesc {
+    int b, h, split, nsplit, j0, npages, len, gp0;  // gp0 = global page index of the item's first page
+    int end;                                        // 1: no more items
+    float pad[7];
+};
+
+template <int D, int BS, bool FP8, int NSTAGE>
+struct PersistLayout {
+    using C = Cfg<D, BS, FP8>;
+    static constexpr int RING = 0;
+    static constexpr int COMBINE = RING + NSTAGE * C::STAGEB;
+    // combine area: the warps' states, later the merge weights (8 x kMaxSplits floats)
+    static constexpr int COMBINE_BYTES = (C::COMBINE_FLOATS > 8 * 512 ? C::COMBINE_FLOATS : 8 * 512) * 4;
+    static constexpr int QBUF = COMBINE + ((COMBINE_BYTES + 127) & ~127);
+    static constexpr int DESC = QBUF + kItemSlots * C::QBYTES;
+    static constexpr int PREFIX = DESC + kItemSlots * (int)sizeof(ItemDesc);
+    static constexpr int BARS = (PREFIX + (kPersistMaxB + 1) * 4 + 15) & ~15;
+    static constexpr int NBARS = 2 * NSTAGE + 2 * kItemSlots;
+    static constexpr int SMEM = BARS + NBARS * 8 + 1024;  // + alignment slack
+};
+
+template <int D, int BS, bool FP8, int NSTAGE>
+__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
+    paged_decode_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                            const DecodeArgs a) {
+    using C = Cfg<D, BS, FP8>;
+    using Lay = PersistLayout<D, BS, FP8, NSTAGE>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw_u32);
+    float* cm = reinterpret_cast<float*>(sgen + Lay::COMBINE);
+    float* cl = cm + C::NCW * 8;
+    float* co = cl + C::NCW * 8;
+    ItemDesc* desc = reinterpret_cast<ItemDesc*>(sgen + Lay::DESC);
+    int* prefix = reinterpret_cast<int*>(sgen + Lay::PREFIX);
+    uint64_t* full = reinterpret_cast<uint64_t*>(sgen + Lay::BARS);
+    uint64_t* empty = full + NSTAGE;
+    uint64_t* ifull = empty + NSTAGE;
+    uint64_t* iempty = ifull + kItemSlots;
+    __shared__ int s_last;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int cap = a.M * BS;
+    const int P = a.part_blocks;
+
+    if (warp == C::NCW) {
+        // item prefix over sequences: sequence b owns items [prefix[b], prefix[b+1]),
+        // max(1, partitions) x Hkv of them (a zero-length sequence still needs its
+        // zero output written)
+        int running = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            int n = 0;
+            if (b < a.B) {
+                const int raw = a.lens[b];
+                if ((raw < 0 || raw > cap) && blockIdx.x == 0) raise_error(PA_DEVERR_SEQ_LEN);
+                const int len = clamp_len(raw, cap);
+                const int nsplit = ((len + BS - 1) / BS + P - 1) / P;
+                n = max(1, nsplit) * a.Hkv;
+            }
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (b < a.B) prefix[b + 1] = running + incl;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kItemSlots; ++s) {
+            mbar_init(&ifull[s], 1);
+            mbar_init(&iempty[s], C::NCW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int total = prefix[a.B];
+
+    if (warp == C::NCW) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+        }
+        bool alive = true;
+        int gp = 0;
+        for (int k = 0; alive; ++k) {
+            int it = 0;
+            if (lane == 0) it = atomicAdd(&a.queue[0], 1);
+            it = __shfl_sync(0xffffffffu, it, 0);
+            const int slot = k % kItemSlots;
+            if (lane == 0 && k >= kItemSlots) alive = mbar_wait(&iempty[slot], ((k / kItemSlots) - 1) & 1);
+            alive = __shfl_sync(0xffffffffu, alive, 0);
+            if (!alive) break;
+            if (it >= total) {
+                if (lane == 0) {
+                    desc[slot].end = 1;
+                    mbar_arrive(&ifull[slot]);
+                }
+                break;
+            }
+            // item -> sequence: last b with prefix[b] <= it (binary search)
+            int lo = 0, hi = a.B - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (prefix[mid] <= it) lo = mid; else hi = mid - 1;
+            }
+            const int b = lo;
+            const int rem = it - prefix[b];
+            const int split = rem / a.Hkv, h = rem - split * a.Hkv;
+            const int len = clamp_len(a.lens[b], cap);
+            const int nblk = (len + BS - 1) / BS;
+            const int nsplit = (nblk + P - 1) / P;
+            const int j0 = split * P;
+            const int npages = max(0, min(nblk, j0 + P) - j0);
+            if (lane == 0) {
+                ItemDesc& d = desc[slot];
+                d.b = b;
+                d.h = h;
+                d.split = split;
+                d.nsplit = nsplit;
+                d.j0 = j0;
+                d.npages = npages;
+                d.len = len;
+                d.gp0 = gp;
+                d.end = 0;
+                // q rows of the group ride on the descriptor barrier
+                const int qb = a.G * D * 2;
+                mbar_arrive_expect_tx(&ifull[slot], qb);
+                bulk_g2s(sgen + Lay::QBUF + slot * C::QBYTES, a.q + ((int64_t)b * a.Hq + h * a.G) * D, qb, &ifull[slot]);
+            }
+            const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
+            for (int base = 0; base < npages && alive; base += 32) {
+                int myphys = 0;
+                if (base + lane < npages) {
+                    myphys = trow[base + lane];
+                    if (myphys < 0 || myphys >= a.num_blocks) {
+                        raise_error(PA_DEVERR_BLOCK_ID);
+                        myphys = 0;
+                    }
+                }
+                const int cnt = min(32, npages - base);
+                for (int kk = 0; kk < cnt; ++kk) {
+                    const int phys = __shfl_sync(0xffffffffu, myphys, kk);
+                    if (lane == 0 && alive) {
+                        const int s = gp % NSTAGE;
+                        if (gp >= NSTAGE) alive = mbar_wait(&empty[s], ((gp / NSTAGE) - 1) & 1);
+                        if (alive) {
+                            mbar_arrive_expect_tx(&full[s], C::STAGEB);
+                            const int y = (phys * a.Hkv + h) * BS;
+                            uint8_t* stg = sgen + Lay::RING + s * C::STAGEB;
+#pragma unroll
+                            for (int ch = 0; ch < C::NCH; ++ch)
+                                tma_load_2d(stg + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
+#pragma unroll
+                            for (int ch = 0; ch < C::NCH; ++ch)
+                                tma_load_2d(stg + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y, &full[s]);
+                        }
+                    }
+                    ++gp;
+                }
+                alive = __shfl_sync(0xffffffffu, alive, 0);
+            }
+        }
+        // every issued load lands before the CTA exits
+        if (lane == 0) {
+            for (int s = 0; s < NSTAGE && s < gp; ++s) {
+                const int last = s + ((gp - 1 - s) / NSTAGE) * NSTAGE;
+                mbar_wait(&full[s], (last / NSTAGE) & 1);
+            }
+        }
+    } else {
+        // ---------------------------------------------------------- consumers
+        WarpAcc<D, BS, FP8> st;
+        const int tid = threadIdx.x;  // 0 .. 127
+        for (int k = 0;; ++k) {
+            const int slot = k % kItemSlots;
+            if (!mbar_wait(&ifull[slot], (k / kItemSlots) & 1)) break;
+            const ItemDesc d = desc[slot];
+            if (d.end) break;
+            const int g = lane >> 2;
+            st.reset();
+            st.load_q(reinterpret_cast<const uint16_t*>(sgen + Lay::QBUF + slot * C::QBYTES) + g * D, g < a.G,
+                      lane & 3);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&iempty[slot]);
+            const int32_t* trow = a.tables + (int64_t)d.b * a.M + d.j0;
+            bool ok = true;
+            for (int i = warp; i < d.npages; i += C::NCW) {
+                const int gp = d.gp0 + i;
+                const int s = gp % NSTAGE;
+                float ksc = 1.f, vsc = 1.f;
+                if (FP8) {
+                    int phys = trow[i];
+                    if (phys < 0 || phys >= a.num_blocks) phys = 0;
+                    ksc = a.k_scale[(int64_t)phys * a.Hkv + d.h];
+                    vsc = a.v_scale[(int64_t)phys * a.Hkv + d.h];
+                }
+                if (!mbar_wait(&full[s], (gp / NSTAGE) & 1)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t kt = sbase + Lay::RING + s * C::STAGEB;
+                st.page(kt, kt + C::PAGEB, min(BS, d.len - (d.j0 + i) * BS),
+                        FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if (!ok) break;
+            st.publish(cm, cl, co, warp, lane);
+            sync_consumers();
+            combine_store<D, C::NCW>(a, cm, cl, co, d.b, d.h, d.split, d.nsplit, tid, C::NCW * 32);
+            if (d.nsplit > 1) {
+                __threadfence();
+                sync_consumers();
+                if (tid == 0) {
+                    const int old = atomicAdd(&a.counters[d.b * a.Hkv + d.h], 1);
+                    s_last = (old == d.nsplit - 1);
+                }
+                sync_consumers();
+                if (s_last) {
+                    __threadfence();
+                    merge_group<D>(a, cm, d.b, d.h, d.nsplit, tid, C::NCW * 32, warp, C::NCW, lane,
+                                   sync_consumers);
+                    if (tid == 0) a.counters[d.b * a.Hkv + d.h] = 0;
+                }
+            }
+            sync_consumers();  // combine area free for the next item
+        }
+    }
+
+    // the last CTA to finish resets the queue for the next call
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        const int done = atomicAdd(&a.queue[1], 1);
+        if (done == (int)gridDim.x - 1) {
+            a.queue[0] = 0;
+            a.queue[1] = 0;
+            __threadfence();
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launch
+template <typename K>
+static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (configured_device != dev) {  // the attribute is per device
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        configured_device = dev;
+    }
+    return cudaSuccess;
 }
 
 template <int D, int BS, bool FP8>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     using C = Cfg<D, BS, FP8>;
-    static int configured_device = -1;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (configured_device != dev) {  // the attribute is per device; set it once per device used
-        e = cudaFuncSetAttribute(paged_decode_kernel<D, BS, FP8>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
     DecodeArgs a;
     a.out = (__nv_bfloat16*)L.out;
     a.q = (const uint16_t*)L.q;
@@ -473,6 +765,8 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.o_part = L.o_part;
     a.lse = L.lse;
     a.counters = L.counters;
+    a.queue = L.queue;
+    a.B = L.B;
     a.Hq = L.Hq;
     a.Hkv = L.Hkv;
     a.G = L.Hq / L.Hkv;
@@ -481,10 +775,35 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.part_blocks = L.part_blocks;
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
+    if (L.persistent) {
+        // ring depth chosen so that three CTAs fit on an SM
+        constexpr int NST = (C::STAGEB >= 16384) ? 3 : (C::STAGEB >= 8192 ? 5 : 10);
+        using Lay = PersistLayout<D, BS, FP8, NST>;
+        static int configured = -1;
+        cudaError_t e = set_smem_once(paged_decode_persistent<D, BS, FP8, NST>, Lay::SMEM, configured);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_decode_persistent<D, BS, FP8, NST>,
+                                                          C::NTHREADS, Lay::SMEM);
+        if (e != cudaSuccess) return e;
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int grid = max(1, per_sm) * max(1, sms);
+        paged_decode_persistent<D, BS, FP8, NST><<<grid, C::NTHREADS, Lay::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
+        return cudaGetLastError();
+    }
+    constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
+    constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
+    static int configured = -1;
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, FP8, NST>, SMEM, configured);
+    if (e != cudaSuccess) return e;
     dim3 grid(L.S, L.Hkv, L.B);
-    paged_decode_kernel<D, BS, FP8><<<grid, C::NTHREADS, C::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
+    paged_decode_kernel<D, BS, FP8, NST><<<grid, C::NTHREADS, SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
     return cudaGetLastError();
 }
+
+bool decode_persistent_ok(int B) { return B <= kPersistMaxB; }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
     if (L.fp8) {

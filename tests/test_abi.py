@@ -77,10 +77,10 @@ def test_split_planning():
     assert pa.pa_decode_resolve_splits(4, 8, 7, 5) == 4
     assert pa.pa_decode_resolve_splits(4, 8, 7, 100) == 7
     assert pa.pa_decode_resolve_splits(4, 8, 7, 1) == 1
-    assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 1) == 0
-    ws = pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 64)
     up = lambda x: -(-x // 256) * 256
-    assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4)
+    assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 1) == up(4 * 8 * 4) + 256
+    ws = pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 64)
+    assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4) + 256
     assert pa.pa_decode_resolve_splits(4, 8, 8192, 4096) == 512      # at most 512 partitions
     # automatic choice keeps partitions between 16 and 128 blocks
     for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (4, 8, 8192), (128, 32, 256), (4, 2, 7)]:

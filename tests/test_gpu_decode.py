@@ -184,8 +184,25 @@ def test_split_counters_return_to_zero_and_calls_repeat_bit_exactly():
         layer.decode(num_splits=5)
         torch.cuda.synchronize()
         outs.append(layer.out.clone())
-        # counters: the last int32 words of the workspace, [B][Hkv]
+        # merge counters and the work queue: the last 256-byte-aligned parts of the workspace
         need = pa.pa_decode_workspace_bytes(layer.B, layer.Hq, layer.Hkv, layer.d, layer.M, 5)
-        cnt = ws[:need].view(torch.int32)[-((layer.B * layer.Hkv + 63) // 64 * 64):]
-        assert int(cnt.abs().sum()) == 0
+        tail = ws[:need].view(torch.int32)[-((layer.B * layer.Hkv + 63) // 64 * 64 + 64):]
+        assert int(tail.abs().sum()) == 0
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+
+
+@pytest.mark.parametrize("S", [0, 2])
+def test_large_batch_uses_the_per_item_grid(S):
+    """Batches above 512 sequences launch one CTA per item instead of the persistent grid."""
+    rng = np.random.default_rng(21)
+    lens = [int(x) for x in rng.integers(0, 70, size=600)]
+    w = _synthetic(600, 8, 2, 128, 16, lens, seed=21)
+    check(w, S)
+
+
+def test_persistent_queue_returns_to_zero_across_shapes():
+    """Consecutive calls with different batch shapes on one workspace stay correct."""
+    for B, lens in ((7, [5, 300, 17, 1, 0, 64, 900]), (3, [2000, 3, 40])):
+        w = _synthetic(B, 16, 4, 128, 16, lens, seed=B)
+        for S in (0, 1, 4):
+            check(w, S)
