@@ -26,8 +26,8 @@
 //     partition writes its normalised partial and base-2 log-sum-exp to the
 //     workspace and the group's last partition to finish merges them.
 // Two launch shapes share this code:
-//   * persistent (batch <= kPersistMaxB): one grid of (#SM x resident CTAs)
-//     CTAs pulls items from an atomic queue; the producer streams the next
+//   * persistent (batch <= kPersistMaxB): one grid of (#SM x 2) CTAs that
+//     pull items from an atomic queue; the producer streams the next
 //     item's pages (and its q rows, by bulk copy) while the consumers finish
 //     the current one, so the ring never drains between items;
 //   * one CTA per item (grid = partitions x kv heads x sequences) otherwise.
@@ -75,7 +75,7 @@ struct Cfg {
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
 };
 
-constexpr int kPersistMaxB = 512;   // batch limit of the persistent launch (prefix table in smem)
+constexpr int kPersistMaxB = 4096;  // batch limit of the persistent launch (prefix table in smem)
 constexpr int kItemSlots = 4;       // item descriptors in flight (persistent launch)
 
 // ------------------------------------------------------------------ per warp
@@ -362,6 +362,9 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     using C = Cfg<D, BS, FP8>;
     constexpr int BAR_OFF = NSTAGE * C::STAGEB;
     static_assert(C::COMBINE_FLOATS * 4 <= NSTAGE * C::STAGEB, "combine area must fit in the stages");
+    // stage s is always consumed by warp s % NCW, so no waiter can run two
+    // phases ahead of a stage's oldest unconsumed fill (parity waits alias)
+    static_assert(NSTAGE % Cfg<D, BS, FP8>::NCW == 0, "ring depth must be a multiple of the consumer warps");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -508,11 +511,16 @@ struct PersistLayout {
 };
 
 template <int D, int BS, bool FP8, int NSTAGE>
-__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
+__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
     paged_decode_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a) {
     using C = Cfg<D, BS, FP8>;
     using Lay = PersistLayout<D, BS, FP8, NSTAGE>;
+    // Page gp (global index over the CTA's items) sits in stage gp % NSTAGE and
+    // is consumed by warp gp % NCW; with NSTAGE a multiple of NCW each stage
+    // has a single consumer warp, which waits for its fills strictly in order,
+    // so a parity wait can never match a stale phase.
+    static_assert(NSTAGE % C::NCW == 0, "ring depth must be a multiple of the consumer warps");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -682,8 +690,8 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             if (lane == 0) mbar_arrive(&iempty[slot]);
             const int32_t* trow = a.tables + (int64_t)d.b * a.M + d.j0;
             bool ok = true;
-            for (int i = warp; i < d.npages; i += C::NCW) {
-                const int gp = d.gp0 + i;
+            for (int i = (warp - d.gp0 % C::NCW + C::NCW) % C::NCW; i < d.npages; i += C::NCW) {
+                const int gp = d.gp0 + i;  // gp % NCW == warp
                 const int s = gp % NSTAGE;
                 float ksc = 1.f, vsc = 1.f;
                 if (FP8) {
@@ -776,8 +784,8 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     if (L.persistent) {
-        // ring depth chosen so that three CTAs fit on an SM
-        constexpr int NST = (C::STAGEB >= 16384) ? 3 : (C::STAGEB >= 8192 ? 5 : 10);
+        // a 64 KiB ring; two CTAs fit on an SM
+        constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
         using Lay = PersistLayout<D, BS, FP8, NST>;
         static int configured = -1;
         cudaError_t e = set_smem_once(paged_decode_persistent<D, BS, FP8, NST>, Lay::SMEM, configured);
