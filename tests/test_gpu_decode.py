@@ -1,7 +1,9 @@
 """pa_decode_attention through the C ABI against the fp64 oracle.
 
 Tolerance: max |err| <= 1e-2 for the bf16 cache, <= 5e-2 for the fp8 cache
-(against the oracle evaluated on the stored fp8 cache).  Small cases compare
+(against the oracle evaluated on the stored fp8 cache); where the bf16
+output grid is coarser than that bound (|ref| >= 2, resp. >= 8) one bf16 ulp
+of the reference.  Small cases compare
 every output; full-size cases (the benchmark's shapes and launch
 configuration) compare sampled sequences, each computed by the oracle from
 the same seeded inputs.
@@ -16,7 +18,7 @@ import oracle
 import paged_kv_cache_294_gb300 as pa
 import workloads
 from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
-from tests.gpu_util import BF16_TOL, FP8_TOL, gpu_out_f64, oracle_out, run_gpu, tol
+from tests.gpu_util import BF16_TOL, FP8_TOL, excess, gpu_out_f64, oracle_out, run_gpu, tol
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +29,7 @@ def check(w, num_splits=0, seqs=None):
     got = gpu_out_f64(layer, seqs)
     assert np.all(np.isfinite(got))
     err = np.max(np.abs(got - ref))
-    assert err <= tol(w), (w.name, num_splits, err)
+    assert excess(got, ref, tol(w)) <= 1.0, (w.name, num_splits, err)
     assert pa.pa_get_device_error() == 0
     return layer, err
 
@@ -102,7 +104,7 @@ def test_zero_length_gives_zero_rows_and_others_unaffected():
     out = layer.out.float().cpu()
     assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
     st, ref = oracle_out(w, tables=layer.tables_host)
-    assert np.max(np.abs(out[1].numpy() - ref[1])) <= BF16_TOL
+    assert excess(out[1].numpy(), ref[1], BF16_TOL) <= 1.0
 
 
 @pytest.mark.parametrize("S", [1, 3])
@@ -134,7 +136,7 @@ def test_stale_nan_bytes_past_the_end_do_not_leak():
     got = layer.out.float().cpu().numpy()
     assert np.all(np.isfinite(got))
     st, ref = oracle_out(w, tables=layer.tables_host)
-    assert np.max(np.abs(got - ref)) <= BF16_TOL
+    assert excess(got, ref, BF16_TOL) <= 1.0
 
 
 def test_fp8_stale_nan_codes_past_the_end_do_not_leak():
@@ -149,7 +151,7 @@ def test_fp8_stale_nan_codes_past_the_end_do_not_leak():
     got = layer.out.float().cpu().numpy()
     assert np.all(np.isfinite(got))
     st, ref = oracle_out(w, tables=layer.tables_host)
-    assert np.max(np.abs(got - ref)) <= FP8_TOL
+    assert excess(got, ref, FP8_TOL) <= 1.0
 
 
 # ------------------------------------------------------------ full sizes, sampled
