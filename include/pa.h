@@ -165,6 +165,42 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
                               int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
                               void* workspace, size_t workspace_bytes, int kv_dtype, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * pa_decode_attention_static_ws - pa_decode_attention for callers that cannot
+ * allocate device memory.  (The pages have no counterpart to this entry
+ * point: it is a convenience of this library.)
+ *
+ * Some callers only ever receive their input and output buffers and may not
+ * call cudaMalloc themselves: plugins of inference runtimes that plan every
+ * byte of device memory ahead of time, or code that runs while another
+ * component owns the allocator, where an allocation would fail, upset the
+ * memory plan or implicitly synchronise the device.  This entry point takes
+ * the same arguments as pa_decode_attention minus the workspace and uses a
+ * workspace owned by the library instead: a device array of
+ * PA_STATIC_WORKSPACE_BYTES that every GPU which loads the library keeps
+ * until the process exits.  It allocates nothing (no cudaMalloc, no
+ * cudaFree) and gives the same outputs as pa_decode_attention.
+ *   - Requests whose workspace (pa_decode_workspace_bytes) exceeds
+ *     PA_STATIC_WORKSPACE_BYTES return PA_ERR_INVALID and launch nothing;
+ *     use pa_decode_attention with a caller workspace for those.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, which may load the library's device code); make
+ *     that first call on each device before any stream capture.
+ *   - Every call uses the same array: each call zeroes its counter words with
+ *     cudaMemsetAsync on `stream` before the kernel, and calls whose work
+ *     overlaps on the GPU (other streams, other threads) race on the array
+ *     and must be serialised by the caller.
+ * ------------------------------------------------------------------------- */
+#define PA_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+
+pa_status pa_decode_attention_static_ws(void* out, const void* q, const void* k_cache,
+                                        const void* v_cache, const float* k_scale,
+                                        const float* v_scale, const int32_t* block_tables,
+                                        const int32_t* seq_lens, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int max_blocks_per_seq, int num_blocks, float scale,
+                                        int num_splits, int kv_dtype, void* stream);
+
 /* Read (and optionally clear) the current device's error word; synchronises
  * the device.  *flags receives an OR of PA_DEVERR_* bits set since the last
  * clear. */

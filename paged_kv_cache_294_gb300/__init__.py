@@ -189,6 +189,38 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tenso
            "pa_decode_attention")
 
 
+PA_STATIC_WORKSPACE_BYTES = 16 << 20
+
+
+def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor,
+                                  v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
+                                  v_scale: Optional[torch.Tensor], block_tables: torch.Tensor,
+                                  seq_lens: torch.Tensor, scale: float, num_splits: int = 0,
+                                  stream=None) -> None:
+    """pa_decode_attention without a caller workspace, for callers that may not
+    allocate device memory (the library's own PA_STATIC_WORKSPACE_BYTES array
+    is used; calls sharing it must not overlap on the GPU)."""
+    lib = load()
+    f = lib.pa_decode_attention_static_ws
+    P, i32 = ctypes.c_void_p, ctypes.c_int
+    f.restype = i32
+    f.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, P]
+    kvd = _kv_dtype(k_cache)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, dc = k_cache.shape
+    M = block_tables.shape[1]
+    if dc != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch")
+    _check(f(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+             _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M, nb, float(scale), int(num_splits),
+             kvd, _stream(stream)),
+           "pa_decode_attention_static_ws")
+
+
 def pa_get_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(load().pa_get_device_error(ctypes.byref(v), 1 if clear else 0), "pa_get_device_error")
