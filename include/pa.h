@@ -131,7 +131,7 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
  * zero-filled before its first use; every call that completes leaves the
  * counters and the queue at zero again (after a PA_DEVERR_TIMEOUT, zero it
  * again).  Calls that share a workspace must not overlap on the device.
- * Batches of up to 4096 sequences run as one persistent grid that pulls
+ * Batches of up to 2048 sequences run as one persistent grid that pulls
  * (sequence, kv head, partition) items from the queue; larger batches launch
  * one CTA per item.
  * ------------------------------------------------------------------------- */

@@ -75,7 +75,7 @@ struct Cfg {
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
 };
 
-constexpr int kPersistMaxB = 4096;  // batch limit of the persistent launch (prefix table in smem)
+constexpr int kPersistMaxB = 2048;  // batch limit of the persistent launch (prefix table in smem)
 constexpr int kItemSlots = 4;       // item descriptors in flight (persistent launch)
 
 // ------------------------------------------------------------------ per warp
@@ -492,26 +492,77 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
 struct ItemDesc {
     int b, h, split, nsplit, j0, npages, len, gp0;  // gp0 = global page index of the item's first page
     int end;                                        // 1: no more items
-    float pad[7];
+    int pad[7];
 };
+
+constexpr int kPersistWarps = 6;   // warps 0-3 consumers, 4 producer, 5 epilogue
+constexpr int kProducerWarp = 4;
+constexpr int kEpilogueWarp = 5;
 
 template <int D, int BS, bool FP8, int NSTAGE>
 struct PersistLayout {
     using C = Cfg<D, BS, FP8>;
     static constexpr int RING = 0;
-    static constexpr int COMBINE = RING + NSTAGE * C::STAGEB;
-    // combine area: the warps' states, later the merge weights (8 x kMaxSplits floats)
-    static constexpr int COMBINE_BYTES = (C::COMBINE_FLOATS > 8 * 512 ? C::COMBINE_FLOATS : 8 * 512) * 4;
-    static constexpr int QBUF = COMBINE + ((COMBINE_BYTES + 127) & ~127);
+    static constexpr int COMBINE = RING + NSTAGE * C::STAGEB;  // the consumer warps' states of one item
+    static constexpr int CDESC = COMBINE + ((C::COMBINE_FLOATS * 4 + 127) & ~127);
+    static constexpr int QBUF = CDESC + 128;
     static constexpr int DESC = QBUF + kItemSlots * C::QBYTES;
     static constexpr int PREFIX = DESC + kItemSlots * (int)sizeof(ItemDesc);
     static constexpr int BARS = (PREFIX + (kPersistMaxB + 1) * 4 + 15) & ~15;
-    static constexpr int NBARS = 2 * NSTAGE + 2 * kItemSlots;
+    static constexpr int NBARS = 2 * NSTAGE + 2 * kItemSlots + 2;
     static constexpr int SMEM = BARS + NBARS * 8 + 1024;  // + alignment slack
 };
 
+// Log-sum-exp merge of a (sequence, kv head) group's nsplit partials by one
+// warp, without shared memory: per query head, the weights of 32 partitions
+// at a time live in the lanes' registers and are broadcast by shuffles.
+template <int D>
+__device__ __forceinline__ void merge_group_warp(const DecodeArgs& a, int b, int h, int nsplit, int lane) {
+    constexpr int PER = D / 32;
+    for (int gq = 0; gq < a.G; ++gq) {
+        const int64_t row = (int64_t)b * a.Hq + h * a.G + gq;
+        const float* L = a.lse + row * a.S;
+        float mx = -INFINITY;
+        for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, __ldcg(L + k));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        float den = 0.f;
+        for (int k = lane; k < nsplit; k += 32) den += exp2f(__ldcg(L + k) - mx);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float inv = 1.f / den;
+        float acc[PER];
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+        const float* op = a.o_part + row * a.S * D + lane * PER;
+        for (int kb = 0; kb < nsplit; kb += 32) {
+            const int kl = kb + lane;
+            const float wl = kl < nsplit ? exp2f(__ldcg(L + kl) - mx) * inv : 0.f;
+            const int cnt = min(32, nsplit - kb);
+#pragma unroll 4
+            for (int j = 0; j < cnt; ++j) {
+                const float w = __shfl_sync(0xffffffffu, wl, j);
+                const float* src = op + (int64_t)(kb + j) * D;
+                if (PER == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]);
+                    acc[3] = fmaf(w, v.w, acc[3]);
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
+                    acc[0] = fmaf(w, v.x, acc[0]);
+                    acc[1] = fmaf(w, v.y, acc[1]);
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < PER; ++e) a.out[row * D + lane * PER + e] = __float2bfloat16_rn(acc[e]);
+    }
+}
+
 template <int D, int BS, bool FP8, int NSTAGE>
-__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
+__global__ void __launch_bounds__(kPersistWarps * 32, 2)
     paged_decode_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a) {
     using C = Cfg<D, BS, FP8>;
@@ -528,43 +579,29 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
     float* cm = reinterpret_cast<float*>(sgen + Lay::COMBINE);
     float* cl = cm + C::NCW * 8;
     float* co = cl + C::NCW * 8;
+    ItemDesc* cdesc = reinterpret_cast<ItemDesc*>(sgen + Lay::CDESC);
     ItemDesc* desc = reinterpret_cast<ItemDesc*>(sgen + Lay::DESC);
     int* prefix = reinterpret_cast<int*>(sgen + Lay::PREFIX);
     uint64_t* full = reinterpret_cast<uint64_t*>(sgen + Lay::BARS);
     uint64_t* empty = full + NSTAGE;
     uint64_t* ifull = empty + NSTAGE;
     uint64_t* iempty = ifull + kItemSlots;
-    __shared__ int s_last;
+    uint64_t* cfull = iempty + kItemSlots;   // consumers -> epilogue: an item's states are published
+    uint64_t* cempty = cfull + 1;            // epilogue -> consumers: the combine area is free again
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cap = a.M * BS;
     const int P = a.part_blocks;
 
-    if (warp == C::NCW) {
-        // item prefix over sequences: sequence b owns items [prefix[b], prefix[b+1]),
-        // max(1, partitions) x Hkv of them (a zero-length sequence still needs its
-        // zero output written)
-        int running = 0;
-        for (int base = 0; base < a.B; base += 32) {
-            const int b = base + lane;
-            int n = 0;
-            if (b < a.B) {
-                const int raw = a.lens[b];
-                if ((raw < 0 || raw > cap) && blockIdx.x == 0) raise_error(PA_DEVERR_SEQ_LEN);
-                const int len = clamp_len(raw, cap);
-                const int nsplit = ((len + BS - 1) / BS + P - 1) / P;
-                n = max(1, nsplit) * a.Hkv;
-            }
-            int incl = n;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (b < a.B) prefix[b + 1] = running + incl;
-            running += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
+    // Items of sequence b: max(1, partitions) x Hkv (a zero-length sequence still
+    // has its zero output written).  Counts are read in parallel, then one warp
+    // turns them into prefix sums: sequence b owns items [prefix[b], prefix[b+1]).
+    for (int b = threadIdx.x; b < a.B; b += kPersistWarps * 32) {
+        const int raw = a.lens[b];
+        if ((raw < 0 || raw > cap) && blockIdx.x == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        const int len = clamp_len(raw, cap);
+        const int nsplit = ((len + BS - 1) / BS + P - 1) / P;
+        prefix[b + 1] = max(1, nsplit) * a.Hkv;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -575,12 +612,30 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
             mbar_init(&ifull[s], 1);
             mbar_init(&iempty[s], C::NCW);
         }
+        mbar_init(cfull, C::NCW * 32);
+        mbar_init(cempty, 1);
         fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int running = 0;
+        for (int base = 0; base < a.B; base += 32) {
+            const int b = base + lane;
+            int incl = b < a.B ? prefix[b + 1] : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (b < a.B) prefix[b + 1] = running + incl;
+            running += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) prefix[0] = 0;
     }
     __syncthreads();
     const int total = prefix[a.B];
 
-    if (warp == C::NCW) {
+    if (warp == kProducerWarp) {
         // ---------------------------------------------------------- producer
         if (lane == 0) {
             prefetch_tensormap(&tm_k);
@@ -628,7 +683,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
                 d.len = len;
                 d.gp0 = gp;
                 d.end = 0;
-                // q rows of the group ride on the descriptor barrier
+                // the group's q rows ride on the descriptor barrier
                 const int qb = a.G * D * 2;
                 mbar_arrive_expect_tx(&ifull[slot], qb);
                 bulk_g2s(sgen + Lay::QBUF + slot * C::QBYTES, a.q + ((int64_t)b * a.Hq + h * a.G) * D, qb, &ifull[slot]);
@@ -673,23 +728,52 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
                 mbar_wait(&full[s], (last / NSTAGE) & 1);
             }
         }
+    } else if (warp == kEpilogueWarp) {
+        // ---------------------------------------------------------- epilogue
+        // Combines each item's four warp states, writes out or the partition's
+        // partial, and for split sequences lets the group's last partition merge.
+        for (int k = 0;; ++k) {
+            if (!mbar_wait(cfull, k & 1)) break;
+            const ItemDesc d = *cdesc;
+            if (d.end) break;
+            combine_store<D, C::NCW>(a, cm, cl, co, d.b, d.h, d.split, d.nsplit, lane, 32);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cempty);  // the combine area may be overwritten now
+            if (d.nsplit > 1) {
+                __threadfence();
+                __syncwarp();
+                int last = 0;
+                if (lane == 0) last = atomicAdd(&a.counters[d.b * a.Hkv + d.h], 1) == d.nsplit - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    merge_group_warp<D>(a, d.b, d.h, d.nsplit, lane);
+                    if (lane == 0) a.counters[d.b * a.Hkv + d.h] = 0;
+                }
+            }
+        }
     } else {
         // ---------------------------------------------------------- consumers
         WarpAcc<D, BS, FP8> st;
-        const int tid = threadIdx.x;  // 0 .. 127
-        for (int k = 0;; ++k) {
+        int k = 0;
+        bool ok = true;
+        for (;; ++k) {
             const int slot = k % kItemSlots;
-            if (!mbar_wait(&ifull[slot], (k / kItemSlots) & 1)) break;
+            if (!mbar_wait(&ifull[slot], (k / kItemSlots) & 1)) {
+                ok = false;
+                break;
+            }
             const ItemDesc d = desc[slot];
-            if (d.end) break;
-            const int g = lane >> 2;
-            st.reset();
-            st.load_q(reinterpret_cast<const uint16_t*>(sgen + Lay::QBUF + slot * C::QBYTES) + g * D, g < a.G,
-                      lane & 3);
+            if (!d.end) {
+                const int g = lane >> 2;
+                st.reset();
+                st.load_q(reinterpret_cast<const uint16_t*>(sgen + Lay::QBUF + slot * C::QBYTES) + g * D, g < a.G,
+                          lane & 3);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&iempty[slot]);
+            if (d.end) break;
             const int32_t* trow = a.tables + (int64_t)d.b * a.M + d.j0;
-            bool ok = true;
             for (int i = (warp - d.gp0 % C::NCW + C::NCW) % C::NCW; i < d.npages; i += C::NCW) {
                 const int gp = d.gp0 + i;  // gp % NCW == warp
                 const int s = gp % NSTAGE;
@@ -711,25 +795,20 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 2)
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
             if (!ok) break;
-            st.publish(cm, cl, co, warp, lane);
-            sync_consumers();
-            combine_store<D, C::NCW>(a, cm, cl, co, d.b, d.h, d.split, d.nsplit, tid, C::NCW * 32);
-            if (d.nsplit > 1) {
-                __threadfence();
-                sync_consumers();
-                if (tid == 0) {
-                    const int old = atomicAdd(&a.counters[d.b * a.Hkv + d.h], 1);
-                    s_last = (old == d.nsplit - 1);
-                }
-                sync_consumers();
-                if (s_last) {
-                    __threadfence();
-                    merge_group<D>(a, cm, d.b, d.h, d.nsplit, tid, C::NCW * 32, warp, C::NCW, lane,
-                                   sync_consumers);
-                    if (tid == 0) a.counters[d.b * a.Hkv + d.h] = 0;
-                }
+            // hand this warp's state to the epilogue warp once it is done with the previous item
+            if (k > 0 && !mbar_wait(cempty, (k - 1) & 1)) {
+                ok = false;
+                break;
             }
-            sync_consumers();  // combine area free for the next item
+            st.publish(cm, cl, co, warp, lane);
+            if (warp == 0 && lane == 0) *cdesc = d;
+            mbar_arrive(cfull);  // every consumer thread: each releases its own writes
+        }
+        if (ok) {
+            // no more items: publish an end marker once the last item's area is free
+            if (k > 0) mbar_wait(cempty, (k - 1) & 1);
+            if (warp == 0 && lane == 0) cdesc->end = 1;
+            mbar_arrive(cfull);
         }
     }
 
@@ -792,13 +871,13 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         int per_sm = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_decode_persistent<D, BS, FP8, NST>,
-                                                          C::NTHREADS, Lay::SMEM);
+                                                          kPersistWarps * 32, Lay::SMEM);
         if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         const int grid = max(1, per_sm) * max(1, sms);
-        paged_decode_persistent<D, BS, FP8, NST><<<grid, C::NTHREADS, Lay::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
+        paged_decode_persistent<D, BS, FP8, NST><<<grid, kPersistWarps * 32, Lay::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
         return cudaGetLastError();
     }
     constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);

@@ -33,7 +33,7 @@ struct DecodeLaunch {
     float* lse;         // workspace, [B][Hq][S]
     int* counters;      // workspace, [B][Hkv], zero between calls
     int* queue;         // workspace, [2] item queue of the persistent launch, zero between calls
-    bool persistent;    // persistent launch (batch <= 4096)
+    bool persistent;    // persistent launch (batch <= 2048)
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     int B, Hq, Hkv, d, bs, M, num_blocks;

@@ -195,7 +195,7 @@ def test_split_counters_return_to_zero_and_calls_repeat_bit_exactly():
 
 @pytest.mark.parametrize("S", [0, 2])
 def test_large_batch_uses_the_per_item_grid(S):
-    """Batches above 4096 sequences launch one CTA per item instead of the persistent grid."""
+    """Batches above 2048 sequences launch one CTA per item instead of the persistent grid."""
     rng = np.random.default_rng(21)
     lens = [int(x) for x in rng.integers(0, 40, size=4200)]
     w = _synthetic(4200, 4, 2, 64, 16, lens, seed=21)
