@@ -324,28 +324,34 @@ def run_ours(args):
     dec_gbs = alg * K / t_dec / 1e9
     peak, peak_kind = hbm_peak()
 
-    # end to end through the public API with host buffers: H2D of the step's inputs from
-    # pinned memory, append + decode, D2H of the output, all inside the timed region
-    h_q = w.q.cpu().pin_memory()
-    h_kn = w.k_new.cpu().pin_memory()
-    h_vn = w.v_new.cpu().pin_memory()
-    h_slots = torch.from_numpy(layer.step_slots_host).pin_memory()
-    h_tab = torch.from_numpy(layer.tables_host).pin_memory()
-    h_len = torch.from_numpy(layer.lens_host).pin_memory()
+    # end to end through the public API with host buffers: the step's inputs (q,
+    # new K/V, slots, tables, lengths) packed in one pinned buffer and copied
+    # host->device in one transfer, append + decode, the output copied back,
+    # all inside the timed region
+    parts = [layer.q, layer.k_new, layer.v_new, layer.step_slots, layer.block_tables, layer.seq_lens]
+    offs, total = [], 0
+    for t in parts:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+    d_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+
+    def view(buf, i):
+        t = parts[i]
+        n = t.numel() * t.element_size()
+        return buf[offs[i]:offs[i] + n].view(t.dtype).view(t.shape)
+
+    for i, t in enumerate(parts):
+        view(h_buf, i).copy_(t.cpu())
+    d_q, d_kn, d_vn, d_slots, d_tab, d_len = (view(d_buf, i) for i in range(len(parts)))
     h_out = torch.empty(tuple(layer.out.shape), dtype=torch.bfloat16).pin_memory()
-    d_q, d_kn, d_vn = torch.empty_like(layer.q), torch.empty_like(layer.k_new), torch.empty_like(layer.v_new)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_slots, h_tab, h_len))
+    h2d = total
     d2h = h_out.numel() * h_out.element_size()
 
     def e2e_step():
-        d_q.copy_(h_q, non_blocking=True)
-        d_kn.copy_(h_kn, non_blocking=True)
-        d_vn.copy_(h_vn, non_blocking=True)
-        layer.step_slots.copy_(h_slots, non_blocking=True)
-        layer.block_tables.copy_(h_tab, non_blocking=True)
-        layer.seq_lens.copy_(h_len, non_blocking=True)
-        layer.append_step(d_kn, d_vn)
-        layer.decode(q=d_q, num_splits=args.splits)
+        d_buf.copy_(h_buf, non_blocking=True)
+        layer.append_step(d_kn, d_vn, slots=d_slots)
+        layer.decode(q=d_q, num_splits=args.splits, tables=d_tab, lens=d_len)
         h_out.copy_(layer.out, non_blocking=True)
 
     for _ in range(args.warmup):

@@ -127,13 +127,10 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
  * Workspace layout, each part 256-byte aligned: when S > 1, o_part fp32
  * [batch][num_q_heads][S][head_dim] and lse fp32 [batch][num_q_heads][S]
  * (base-2 log-sum-exp of the scaled scores); then merge counters int32
- * [batch][num_kv_heads] and a 2-word work queue.  The workspace must be
- * zero-filled before its first use; every call that completes leaves the
- * counters and the queue at zero again (after a PA_DEVERR_TIMEOUT, zero it
- * again).  Calls that share a workspace must not overlap on the device.
- * Batches of up to 2048 sequences run as one persistent grid that pulls
- * (sequence, kv head, partition) items from the queue; larger batches launch
- * one CTA per item.
+ * [batch][num_kv_heads].  The workspace must be zero-filled before its
+ * first use; every call that completes leaves the counters at zero again
+ * (after a PA_DEVERR_TIMEOUT, zero it again).  Calls that share a workspace
+ * must not overlap on the device.
  * ------------------------------------------------------------------------- */
 int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits);
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,

@@ -120,11 +120,11 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 constexpr int kMaxSplits = 512;  // partitions per sequence
 
 struct WsLayout {
-    size_t o_off, lse_off, cnt_off, queue_off, total;
+    size_t o_off, lse_off, cnt_off, total;
 };
 
 // o_part fp32 [B][Hq][S][d] | lse fp32 [B][Hq][S]   (S > 1 only)
-// counters int32 [B][Hkv] | queue int32 [2]           (always)
+// counters int32 [B][Hkv]                            (always)
 // each part 256-byte aligned
 WsLayout ws_layout(int B, int Hq, int Hkv, int d, int S) {
     const size_t rows = S > 1 ? (size_t)B * Hq * S : 0;
@@ -133,8 +133,7 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int d, int S) {
     w.o_off = 0;
     w.lse_off = up(rows * d * sizeof(float));
     w.cnt_off = w.lse_off + up(rows * sizeof(float));
-    w.queue_off = w.cnt_off + up((size_t)B * Hkv * sizeof(int));
-    w.total = w.queue_off + 256;
+    w.total = w.cnt_off + up((size_t)B * Hkv * sizeof(int));
     return w;
 }
 
@@ -184,13 +183,14 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
         if (S > kMaxSplits) S = kMaxSplits;
         return (int)ceil_div(M, part_blocks_for(M, S));
     }
-    // Automatic: aim for ~12 CTAs per SM over the batch (several waves of the
-    // three CTAs an SM holds) assuming tables half full on average; a
-    // partition holds 16 .. 128 blocks.
+    // Automatic: about two waves of the three CTAs an SM holds, assuming the
+    // tables are half full on average; a partition holds 32 .. 128 blocks
+    // (enough pages per CTA to amortise its start-up, few enough to keep the
+    // last wave short).
     const int64_t pages = (int64_t)batch * num_kv_heads * M / 2;
-    const int64_t target = (int64_t)device_sms() * 12;
+    const int64_t target = (int64_t)device_sms() * 6;
     int64_t P = ceil_div(pages, target);
-    if (P < 16) P = 16;
+    if (P < 32) P = 32;
     if (P > 128) P = 128;
     if (P > M) P = M;
     if (ceil_div(M, P) > kMaxSplits) P = ceil_div(M, kMaxSplits);
@@ -216,7 +216,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
         return PA_ERR_INVALID;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
     if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
-    if (batch > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;  // grid y / z
+    if (batch > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;  // grid z / y
     if ((int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31) return PA_ERR_INVALID;
     const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
     if (ks != PA_OK) return ks;
@@ -256,9 +256,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
             L.lse = reinterpret_cast<float*>(base + wl.lse_off);
         }
         L.counters = reinterpret_cast<int*>(base + wl.cnt_off);
-        L.queue = reinterpret_cast<int*>(base + wl.queue_off);
     }
-    L.persistent = pa::decode_persistent_ok(batch);
     L.tm_k = &tm_k;
     L.tm_v = &tm_v;
     L.B = batch;

@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(256) kv_append_bf16_kernel(
     uint4* __restrict__ k_cache, uint4* __restrict__ v_cache, const uint4* __restrict__ k_new,
     const uint4* __restrict__ v_new, const int64_t* __restrict__ slots, int T, int Hkv, int units,
     int bs, int64_t cap_slots) {
+    griddep_launch_dependents();  // the decode that follows may start its prologue
     const int64_t total = (int64_t)T * Hkv * units;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
@@ -115,6 +116,7 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(
     float* __restrict__ v_scale, const uint16_t* __restrict__ k_new,
     const uint16_t* __restrict__ v_new, const int64_t* __restrict__ slots, int T, int Hkv, int bs,
     int64_t cap_slots) {
+    griddep_launch_dependents();  // the decode that follows may start its prologue
     const int64_t wid = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (wid >= (int64_t)T * Hkv) return;
     const int t = (int)(wid / Hkv), h = (int)(wid % Hkv);

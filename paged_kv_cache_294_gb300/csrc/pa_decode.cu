@@ -9,28 +9,22 @@
 // head i / G.  Scores, softmax and P.V stay on chip ("LLM Inference
 // Optimization", section "FlashAttention") with an fp32 online softmax.
 //
-// Work unit ("item"): one partition of P blocks of one (sequence, kv head).
-// A CTA has 5 warps:
+// One CTA per (partition of P blocks, kv head, sequence).  A CTA has 5 warps:
 //   * warp 4, the producer, issues TMA tile loads of each page's K and V
 //     (one (block, kv head) page = bs rows x head_dim) into a ring of shared
 //     memory stages written with the 128-byte swizzle; completion is counted
 //     in bytes on one mbarrier per stage;
-//   * warps 0-3 consume the item's pages round-robin.  Per page a warp forms
+//   * warps 0-3 consume the pages round-robin.  Per page a warp forms
 //     S^T = Q K^T with m16n8k16 MMAs (the G query heads of the group are the
 //     M rows, the page's tokens the N columns, head_dim the K depth; q lives
 //     in registers), updates its fp32 online softmax in registers and
 //     accumulates O^T += V^T P^T with MMAs whose B operand is the probability
 //     tile taken straight from the score registers;
-//   * at the item's end the consumer warps merge their states in shared
-//     memory; a one-partition sequence writes bf16 out, otherwise the
-//     partition writes its normalised partial and base-2 log-sum-exp to the
-//     workspace and the group's last partition to finish merges them.
-// Two launch shapes share this code:
-//   * persistent (batch <= kPersistMaxB): one grid of (#SM x 2) CTAs that
-//     pull items from an atomic queue; the producer streams the next
-//     item's pages (and its q rows, by bulk copy) while the consumers finish
-//     the current one, so the ring never drains between items;
-//   * one CTA per item (grid = partitions x kv heads x sequences) otherwise.
+//   * the consumer warps' states merge in shared memory; a one-partition
+//     sequence writes bf16 out, otherwise the partition writes its normalised
+//     partial and base-2 log-sum-exp to the workspace and the group's last
+//     partition to finish merges them (an atomic counter per group; nothing
+//     waits on another CTA).
 // fp8 cache: e4m3 codes convert exactly to f16 in registers (q and the
 // probabilities are f16 there), the K scale folds into the scores and the V
 // scale applies per page to a fresh P.V accumulator.
@@ -52,7 +46,6 @@ struct DecodeArgs {
     float* o_part;
     float* lse;
     int* counters;   // [B][Hkv] merge counters
-    int* queue;      // [2]: next item, finished CTAs (persistent launch)
     int B, Hq, Hkv, G, M, num_blocks, part_blocks, S;
     float scale_log2;
 };
@@ -71,12 +64,9 @@ struct Cfg {
     static constexpr int MT = D / 16;           // 16-row tiles of head_dim (PV)
     static constexpr int KT = BS / 16;          // 16-token steps (PV)
     static constexpr int COMBINE_FLOATS = NCW * (8 * D + 16);
-    static constexpr int QBYTES = 8 * D * 2;    // q rows of one group (G <= 8), bf16
     static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
 };
 
-constexpr int kPersistMaxB = 2048;  // batch limit of the persistent launch (prefix table in smem)
-constexpr int kItemSlots = 4;       // item descriptors in flight (persistent launch)
 
 // ------------------------------------------------------------------ per warp
 template <int D, int BS, bool FP8>
@@ -347,13 +337,11 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int 
 }
 
 __device__ __forceinline__ void sync_cta() { __syncthreads(); }
-// named barrier 1 over the 4 consumer warps only (the producer keeps streaming)
-__device__ __forceinline__ void sync_consumers() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
 
 // ========================================================================
-// One CTA per item: grid (partitions, kv heads, sequences).
+// grid (partitions, kv heads, sequences)
 // ========================================================================
 template <int D, int BS, bool FP8, int NSTAGE>
 __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
@@ -375,6 +363,22 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NSTAGE; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        fence_mbar_init();
+    }
+    // Inputs may come from the preceding kernel in the stream (this step's
+    // append): wait for it before the first global read.
+    griddep_wait();
+
+    // The producer's first 32 table entries load alongside the length.
+    const int j0 = split * a.part_blocks;
+    const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
+    int phys0 = 0;
+    if (warp == C::NCW && lane < a.part_blocks && j0 + lane < a.M) phys0 = trow[lane];
     int len = a.lens[b];
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
@@ -384,17 +388,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int nblk = (len + BS - 1) / BS;
     const int nsplit = (nblk + a.part_blocks - 1) / a.part_blocks;  // 0 when len == 0
     if (split > 0 && split >= nsplit) return;
-    const int j0 = split * a.part_blocks;
     const int npages = max(0, min(nblk, j0 + a.part_blocks) - j0);
-    const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        fence_mbar_init();
-    }
     __syncthreads();
 
     WarpAcc<D, BS, FP8> st;
@@ -408,7 +402,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
         for (int base = 0; base < npages; base += 32) {
             int myphys = 0;
             if (base + lane < npages) {
-                myphys = trow[base + lane];
+                myphys = base == 0 ? phys0 : trow[base + lane];
                 if (myphys < 0 || myphys >= a.num_blocks) {
                     raise_error(PA_DEVERR_BLOCK_ID);
                     myphys = 0;
@@ -486,345 +480,6 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     if (threadIdx.x == 0) a.counters[b * a.Hkv + h] = 0;
 }
 
-// ========================================================================
-// Persistent: items from an atomic queue, pages streamed across items.
-// ========================================================================
-struct ItemDesc {
-    int b, h, split, nsplit, j0, npages, len, gp0;  // gp0 = global page index of the item's first page
-    int end;                                        // 1: no more items
-    int pad[7];
-};
-
-constexpr int kPersistWarps = 6;   // warps 0-3 consumers, 4 producer, 5 epilogue
-constexpr int kProducerWarp = 4;
-constexpr int kEpilogueWarp = 5;
-
-template <int D, int BS, bool FP8, int NSTAGE>
-struct PersistLayout {
-    using C = Cfg<D, BS, FP8>;
-    static constexpr int RING = 0;
-    static constexpr int COMBINE = RING + NSTAGE * C::STAGEB;  // the consumer warps' states of one item
-    static constexpr int CDESC = COMBINE + ((C::COMBINE_FLOATS * 4 + 127) & ~127);
-    static constexpr int QBUF = CDESC + 128;
-    static constexpr int DESC = QBUF + kItemSlots * C::QBYTES;
-    static constexpr int PREFIX = DESC + kItemSlots * (int)sizeof(ItemDesc);
-    static constexpr int BARS = (PREFIX + (kPersistMaxB + 1) * 4 + 15) & ~15;
-    static constexpr int NBARS = 2 * NSTAGE + 2 * kItemSlots + 2;
-    static constexpr int SMEM = BARS + NBARS * 8 + 1024;  // + alignment slack
-};
-
-// Log-sum-exp merge of a (sequence, kv head) group's nsplit partials by one
-// warp, without shared memory: per query head, the weights of 32 partitions
-// at a time live in the lanes' registers and are broadcast by shuffles.
-template <int D>
-__device__ __forceinline__ void merge_group_warp(const DecodeArgs& a, int b, int h, int nsplit, int lane) {
-    constexpr int PER = D / 32;
-    for (int gq = 0; gq < a.G; ++gq) {
-        const int64_t row = (int64_t)b * a.Hq + h * a.G + gq;
-        const float* L = a.lse + row * a.S;
-        float mx = -INFINITY;
-        for (int k = lane; k < nsplit; k += 32) mx = fmaxf(mx, __ldcg(L + k));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        float den = 0.f;
-        for (int k = lane; k < nsplit; k += 32) den += exp2f(__ldcg(L + k) - mx);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-        const float inv = 1.f / den;
-        float acc[PER];
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-        const float* op = a.o_part + row * a.S * D + lane * PER;
-        for (int kb = 0; kb < nsplit; kb += 32) {
-            const int kl = kb + lane;
-            const float wl = kl < nsplit ? exp2f(__ldcg(L + kl) - mx) * inv : 0.f;
-            const int cnt = min(32, nsplit - kb);
-#pragma unroll 4
-            for (int j = 0; j < cnt; ++j) {
-                const float w = __shfl_sync(0xffffffffu, wl, j);
-                const float* src = op + (int64_t)(kb + j) * D;
-                if (PER == 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src));
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                    acc[2] = fmaf(w, v.z, acc[2]);
-                    acc[3] = fmaf(w, v.w, acc[3]);
-                } else {
-                    const float2 v = __ldcg(reinterpret_cast<const float2*>(src));
-                    acc[0] = fmaf(w, v.x, acc[0]);
-                    acc[1] = fmaf(w, v.y, acc[1]);
-                }
-            }
-        }
-#pragma unroll
-        for (int e = 0; e < PER; ++e) a.out[row * D + lane * PER + e] = __float2bfloat16_rn(acc[e]);
-    }
-}
-
-template <int D, int BS, bool FP8, int NSTAGE>
-__global__ void __launch_bounds__(kPersistWarps * 32, 2)
-    paged_decode_persistent(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                            const DecodeArgs a) {
-    using C = Cfg<D, BS, FP8>;
-    using Lay = PersistLayout<D, BS, FP8, NSTAGE>;
-    // Page gp (global index over the CTA's items) sits in stage gp % NSTAGE and
-    // is consumed by warp gp % NCW; with NSTAGE a multiple of NCW each stage
-    // has a single consumer warp, which waits for its fills strictly in order,
-    // so a parity wait can never match a stale phase.
-    static_assert(NSTAGE % C::NCW == 0, "ring depth must be a multiple of the consumer warps");
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw_u32 = smem_u32(smem_raw);
-    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
-    uint8_t* sgen = smem_raw + (sbase - raw_u32);
-    float* cm = reinterpret_cast<float*>(sgen + Lay::COMBINE);
-    float* cl = cm + C::NCW * 8;
-    float* co = cl + C::NCW * 8;
-    ItemDesc* cdesc = reinterpret_cast<ItemDesc*>(sgen + Lay::CDESC);
-    ItemDesc* desc = reinterpret_cast<ItemDesc*>(sgen + Lay::DESC);
-    int* prefix = reinterpret_cast<int*>(sgen + Lay::PREFIX);
-    uint64_t* full = reinterpret_cast<uint64_t*>(sgen + Lay::BARS);
-    uint64_t* empty = full + NSTAGE;
-    uint64_t* ifull = empty + NSTAGE;
-    uint64_t* iempty = ifull + kItemSlots;
-    uint64_t* cfull = iempty + kItemSlots;   // consumers -> epilogue: an item's states are published
-    uint64_t* cempty = cfull + 1;            // epilogue -> consumers: the combine area is free again
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int cap = a.M * BS;
-    const int P = a.part_blocks;
-
-    // Items of sequence b: max(1, partitions) x Hkv (a zero-length sequence still
-    // has its zero output written).  Counts are read in parallel, then one warp
-    // turns them into prefix sums: sequence b owns items [prefix[b], prefix[b+1]).
-    for (int b = threadIdx.x; b < a.B; b += kPersistWarps * 32) {
-        const int raw = a.lens[b];
-        if ((raw < 0 || raw > cap) && blockIdx.x == 0) raise_error(PA_DEVERR_SEQ_LEN);
-        const int len = clamp_len(raw, cap);
-        const int nsplit = ((len + BS - 1) / BS + P - 1) / P;
-        prefix[b + 1] = max(1, nsplit) * a.Hkv;
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NSTAGE; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        for (int s = 0; s < kItemSlots; ++s) {
-            mbar_init(&ifull[s], 1);
-            mbar_init(&iempty[s], C::NCW);
-        }
-        mbar_init(cfull, C::NCW * 32);
-        mbar_init(cempty, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int running = 0;
-        for (int base = 0; base < a.B; base += 32) {
-            const int b = base + lane;
-            int incl = b < a.B ? prefix[b + 1] : 0;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int v = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += v;
-            }
-            if (b < a.B) prefix[b + 1] = running + incl;
-            running += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) prefix[0] = 0;
-    }
-    __syncthreads();
-    const int total = prefix[a.B];
-
-    if (warp == kProducerWarp) {
-        // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-        }
-        bool alive = true;
-        int gp = 0;
-        for (int k = 0; alive; ++k) {
-            int it = 0;
-            if (lane == 0) it = atomicAdd(&a.queue[0], 1);
-            it = __shfl_sync(0xffffffffu, it, 0);
-            const int slot = k % kItemSlots;
-            if (lane == 0 && k >= kItemSlots) alive = mbar_wait(&iempty[slot], ((k / kItemSlots) - 1) & 1);
-            alive = __shfl_sync(0xffffffffu, alive, 0);
-            if (!alive) break;
-            if (it >= total) {
-                if (lane == 0) {
-                    desc[slot].end = 1;
-                    mbar_arrive(&ifull[slot]);
-                }
-                break;
-            }
-            // item -> sequence: last b with prefix[b] <= it (binary search)
-            int lo = 0, hi = a.B - 1;
-            while (lo < hi) {
-                const int mid = (lo + hi + 1) >> 1;
-                if (prefix[mid] <= it) lo = mid; else hi = mid - 1;
-            }
-            const int b = lo;
-            const int rem = it - prefix[b];
-            const int split = rem / a.Hkv, h = rem - split * a.Hkv;
-            const int len = clamp_len(a.lens[b], cap);
-            const int nblk = (len + BS - 1) / BS;
-            const int nsplit = (nblk + P - 1) / P;
-            const int j0 = split * P;
-            const int npages = max(0, min(nblk, j0 + P) - j0);
-            if (lane == 0) {
-                ItemDesc& d = desc[slot];
-                d.b = b;
-                d.h = h;
-                d.split = split;
-                d.nsplit = nsplit;
-                d.j0 = j0;
-                d.npages = npages;
-                d.len = len;
-                d.gp0 = gp;
-                d.end = 0;
-                // the group's q rows ride on the descriptor barrier
-                const int qb = a.G * D * 2;
-                mbar_arrive_expect_tx(&ifull[slot], qb);
-                bulk_g2s(sgen + Lay::QBUF + slot * C::QBYTES, a.q + ((int64_t)b * a.Hq + h * a.G) * D, qb, &ifull[slot]);
-            }
-            const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
-            for (int base = 0; base < npages && alive; base += 32) {
-                int myphys = 0;
-                if (base + lane < npages) {
-                    myphys = trow[base + lane];
-                    if (myphys < 0 || myphys >= a.num_blocks) {
-                        raise_error(PA_DEVERR_BLOCK_ID);
-                        myphys = 0;
-                    }
-                }
-                const int cnt = min(32, npages - base);
-                for (int kk = 0; kk < cnt; ++kk) {
-                    const int phys = __shfl_sync(0xffffffffu, myphys, kk);
-                    if (lane == 0 && alive) {
-                        const int s = gp % NSTAGE;
-                        if (gp >= NSTAGE) alive = mbar_wait(&empty[s], ((gp / NSTAGE) - 1) & 1);
-                        if (alive) {
-                            mbar_arrive_expect_tx(&full[s], C::STAGEB);
-                            const int y = (phys * a.Hkv + h) * BS;
-                            uint8_t* stg = sgen + Lay::RING + s * C::STAGEB;
-#pragma unroll
-                            for (int ch = 0; ch < C::NCH; ++ch)
-                                tma_load_2d(stg + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
-#pragma unroll
-                            for (int ch = 0; ch < C::NCH; ++ch)
-                                tma_load_2d(stg + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y, &full[s]);
-                        }
-                    }
-                    ++gp;
-                }
-                alive = __shfl_sync(0xffffffffu, alive, 0);
-            }
-        }
-        // every issued load lands before the CTA exits
-        if (lane == 0) {
-            for (int s = 0; s < NSTAGE && s < gp; ++s) {
-                const int last = s + ((gp - 1 - s) / NSTAGE) * NSTAGE;
-                mbar_wait(&full[s], (last / NSTAGE) & 1);
-            }
-        }
-    } else if (warp == kEpilogueWarp) {
-        // ---------------------------------------------------------- epilogue
-        // Combines each item's four warp states, writes out or the partition's
-        // partial, and for split sequences lets the group's last partition merge.
-        for (int k = 0;; ++k) {
-            if (!mbar_wait(cfull, k & 1)) break;
-            const ItemDesc d = *cdesc;
-            if (d.end) break;
-            combine_store<D, C::NCW>(a, cm, cl, co, d.b, d.h, d.split, d.nsplit, lane, 32);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(cempty);  // the combine area may be overwritten now
-            if (d.nsplit > 1) {
-                __threadfence();
-                __syncwarp();
-                int last = 0;
-                if (lane == 0) last = atomicAdd(&a.counters[d.b * a.Hkv + d.h], 1) == d.nsplit - 1;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    __threadfence();
-                    merge_group_warp<D>(a, d.b, d.h, d.nsplit, lane);
-                    if (lane == 0) a.counters[d.b * a.Hkv + d.h] = 0;
-                }
-            }
-        }
-    } else {
-        // ---------------------------------------------------------- consumers
-        WarpAcc<D, BS, FP8> st;
-        int k = 0;
-        bool ok = true;
-        for (;; ++k) {
-            const int slot = k % kItemSlots;
-            if (!mbar_wait(&ifull[slot], (k / kItemSlots) & 1)) {
-                ok = false;
-                break;
-            }
-            const ItemDesc d = desc[slot];
-            if (!d.end) {
-                const int g = lane >> 2;
-                st.reset();
-                st.load_q(reinterpret_cast<const uint16_t*>(sgen + Lay::QBUF + slot * C::QBYTES) + g * D, g < a.G,
-                          lane & 3);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&iempty[slot]);
-            if (d.end) break;
-            const int32_t* trow = a.tables + (int64_t)d.b * a.M + d.j0;
-            for (int i = (warp - d.gp0 % C::NCW + C::NCW) % C::NCW; i < d.npages; i += C::NCW) {
-                const int gp = d.gp0 + i;  // gp % NCW == warp
-                const int s = gp % NSTAGE;
-                float ksc = 1.f, vsc = 1.f;
-                if (FP8) {
-                    int phys = trow[i];
-                    if (phys < 0 || phys >= a.num_blocks) phys = 0;
-                    ksc = a.k_scale[(int64_t)phys * a.Hkv + d.h];
-                    vsc = a.v_scale[(int64_t)phys * a.Hkv + d.h];
-                }
-                if (!mbar_wait(&full[s], (gp / NSTAGE) & 1)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t kt = sbase + Lay::RING + s * C::STAGEB;
-                st.page(kt, kt + C::PAGEB, min(BS, d.len - (d.j0 + i) * BS),
-                        FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc, lane);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[s]);
-            }
-            if (!ok) break;
-            // hand this warp's state to the epilogue warp once it is done with the previous item
-            if (k > 0 && !mbar_wait(cempty, (k - 1) & 1)) {
-                ok = false;
-                break;
-            }
-            st.publish(cm, cl, co, warp, lane);
-            if (warp == 0 && lane == 0) *cdesc = d;
-            mbar_arrive(cfull);  // every consumer thread: each releases its own writes
-        }
-        if (ok) {
-            // no more items: publish an end marker once the last item's area is free
-            if (k > 0) mbar_wait(cempty, (k - 1) & 1);
-            if (warp == 0 && lane == 0) cdesc->end = 1;
-            mbar_arrive(cfull);
-        }
-    }
-
-    // the last CTA to finish resets the queue for the next call
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        const int done = atomicAdd(&a.queue[1], 1);
-        if (done == (int)gridDim.x - 1) {
-            a.queue[0] = 0;
-            a.queue[1] = 0;
-            __threadfence();
-        }
-    }
-}
-
 // ------------------------------------------------------------------ launch
 template <typename K>
 static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
@@ -852,7 +507,6 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.o_part = L.o_part;
     a.lse = L.lse;
     a.counters = L.counters;
-    a.queue = L.queue;
     a.B = L.B;
     a.Hq = L.Hq;
     a.Hkv = L.Hkv;
@@ -862,35 +516,26 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.part_blocks = L.part_blocks;
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
-    if (L.persistent) {
-        // a 64 KiB ring; two CTAs fit on an SM
-        constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
-        using Lay = PersistLayout<D, BS, FP8, NST>;
-        static int configured = -1;
-        cudaError_t e = set_smem_once(paged_decode_persistent<D, BS, FP8, NST>, Lay::SMEM, configured);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, paged_decode_persistent<D, BS, FP8, NST>,
-                                                          kPersistWarps * 32, Lay::SMEM);
-        if (e != cudaSuccess) return e;
-        int dev = 0, sms = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int grid = max(1, per_sm) * max(1, sms);
-        paged_decode_persistent<D, BS, FP8, NST><<<grid, kPersistWarps * 32, Lay::SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
-        return cudaGetLastError();
-    }
     constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
     static int configured = -1;
     cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, FP8, NST>, SMEM, configured);
     if (e != cudaSuccess) return e;
-    dim3 grid(L.S, L.Hkv, L.B);
-    paged_decode_kernel<D, BS, FP8, NST><<<grid, C::NTHREADS, SMEM, stream>>>(*L.tm_k, *L.tm_v, a);
-    return cudaGetLastError();
+    // programmatic stream serialisation: the CTAs may be scheduled while the
+    // previous kernel (typically this step's append) finishes; they wait for it
+    // in griddep_wait() before reading any input
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.S, L.Hkv, L.B);
+    cfg.blockDim = dim3(C::NTHREADS);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, FP8, NST>, *L.tm_k, *L.tm_v, a);
 }
-
-bool decode_persistent_ok(int B) { return B <= kPersistMaxB; }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
     if (L.fp8) {

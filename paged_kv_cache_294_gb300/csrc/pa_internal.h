@@ -32,8 +32,6 @@ struct DecodeLaunch {
     float* o_part;      // workspace, [B][Hq][S][d] (S > 1 only)
     float* lse;         // workspace, [B][Hq][S]
     int* counters;      // workspace, [B][Hkv], zero between calls
-    int* queue;         // workspace, [2] item queue of the persistent launch, zero between calls
-    bool persistent;    // persistent launch (batch <= 2048)
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
     int B, Hq, Hkv, d, bs, M, num_blocks;
@@ -45,7 +43,6 @@ struct DecodeLaunch {
 
 cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
-bool decode_persistent_ok(int B);
 
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 cudaError_t append_unit_error(unsigned int* v, bool clear);

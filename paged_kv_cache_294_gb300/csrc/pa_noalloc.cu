@@ -1,7 +1,7 @@
 // pa_decode_attention_static_ws: decode attention for callers that cannot
-// allocate device memory.  The split-K partials, merge counters and work
-// queue live in a workspace owned by this library (a file-scope device array)
-// instead of one the caller allocates.
+// allocate device memory.  The split-K partials and merge counters live in a
+// workspace owned by this library (a file-scope device array) instead of one
+// the caller allocates.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -57,10 +57,9 @@ extern "C" pa_status pa_decode_attention_static_ws(
     void* ws = nullptr;
     const pa_status st = static_ws_address(&ws);
     if (st != PA_OK) return st;
-    // The merge counters and the work queue are the workspace's last parts and
-    // must start at zero; the array keeps whatever the previous call left.
-    const size_t counters = (((size_t)batch * num_kv_heads * sizeof(int)) + 255) & ~(size_t)255;
-    const size_t zero_bytes = counters + 256;
+    // The merge counters are the workspace's last part and must start at zero;
+    // the array keeps whatever the previous call left.
+    const size_t zero_bytes = (((size_t)batch * num_kv_heads * sizeof(int)) + 255) & ~(size_t)255;
     if (cudaMemsetAsync(static_cast<char*>(ws) + (need - zero_bytes), 0, zero_bytes,
                         static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;

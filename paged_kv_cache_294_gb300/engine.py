@@ -116,16 +116,17 @@ class PagedDecodeLayer:
         return layer
 
     # ---------------------------------------------------------------- step
-    def append_step(self, k_new=None, v_new=None, stream=None):
+    def append_step(self, k_new=None, v_new=None, slots=None, stream=None):
         pa_kv_append(self.k_cache, self.v_cache, self.k_scale, self.v_scale,
                      self.k_new if k_new is None else k_new, self.v_new if v_new is None else v_new,
-                     self.step_slots, stream=stream)
+                     self.step_slots if slots is None else slots, stream=stream)
 
-    def decode(self, q=None, out=None, num_splits: int = 0, stream=None):
+    def decode(self, q=None, out=None, num_splits: int = 0, tables=None, lens=None, stream=None):
         ws = self.ensure_workspace(num_splits)
         out = self.out if out is None else out
         pa_decode_attention(out, self.q if q is None else q, self.k_cache, self.v_cache, self.k_scale,
-                            self.v_scale, self.block_tables, self.seq_lens, self.scale, num_splits,
+                            self.v_scale, self.block_tables if tables is None else tables,
+                            self.seq_lens if lens is None else lens, self.scale, num_splits,
                             ws, stream=stream)
         return out
 

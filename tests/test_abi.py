@@ -78,12 +78,12 @@ def test_split_planning():
     assert pa.pa_decode_resolve_splits(4, 8, 7, 100) == 7
     assert pa.pa_decode_resolve_splits(4, 8, 7, 1) == 1
     up = lambda x: -(-x // 256) * 256
-    assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 1) == up(4 * 8 * 4) + 256
+    assert pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 1) == up(4 * 8 * 4)
     ws = pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 64)
-    assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4) + 256
+    assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4)
     assert pa.pa_decode_resolve_splits(4, 8, 8192, 4096) == 512      # at most 512 partitions
-    # automatic choice keeps partitions between 16 and 128 blocks
+    # automatic choice keeps partitions between 32 and 128 blocks
     for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (4, 8, 8192), (128, 32, 256), (4, 2, 7)]:
         S = pa.pa_decode_resolve_splits(B, Hkv, M, 0)
         P = -(-M // S)
-        assert 1 <= S <= M and (P >= min(16, M)) and P <= 128
+        assert 1 <= S <= M and (P >= min(32, M)) and P <= 128
