@@ -58,13 +58,17 @@ def algorithmic_bytes(w):
 
 
 def unique_kv_bytes(w, tables):
+    """K/V bytes of distinct cached tokens: a physical block shared by several
+    sequences (a common prefix) counts once, with as many tokens as its longest
+    user fills.  Equals the logical count when no block is shared."""
     elt = 1 if w.kv == "fp8" else 2
-    blocks = set()
+    used = {}
     for b, L in enumerate(w.seq_lens):
-        nb = -(-int(L) // w.bs)
-        blocks.update(int(x) for x in tables[b, :nb])
-    # a block holds full pages; count tokens actually cached in each distinct block
-    return len(blocks) * w.bs * 2 * w.Hkv * w.d * elt
+        L = int(L)
+        for j in range(-(-L // w.bs)):
+            p = int(tables[b, j])
+            used[p] = max(used.get(p, 0), min(w.bs, L - j * w.bs))
+    return sum(used.values()) * 2 * w.Hkv * w.d * elt
 
 
 class ClockSampler:
@@ -278,11 +282,7 @@ def run_ours(args):
     # fp8, keeps the block scale (max(old, same absmax)) -- every step does identical work.
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)   # > 2 x L2
     stream = torch.cuda.current_stream(dev)
-    launches_per_step = 2   # pa_kv_append + pa_decode_attention (merge fused)
-
-    def one_step():
-        layer.append_step()
-        layer.decode(num_splits=args.splits)
+    launches_per_step = 1   # pa_decode_step: append, attention and split-K merge in one kernel
 
     def flush_l2():
         # write then read 512 MiB: evicts the previous step's lines and leaves no dirty
@@ -290,38 +290,42 @@ def run_ours(args):
         flush.fill_(1)
         flush.sum(dtype=torch.int32)
 
-    for _ in range(args.warmup):
-        flush_l2()
-        one_step()
-    torch.cuda.synchronize()
+    def timed(fn, K, sampler=None):
+        """Per-step CUDA-event time (s, summed over K steps), L2 flushed before each (untimed)."""
+        for _ in range(args.warmup):
+            flush_l2()
+            fn()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t = sum(x.elapsed_time(y) for x, y in ev) / 1e3
+        if dist:
+            tt = torch.tensor([t], dtype=torch.float64, device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t = float(tt[0])
+        return t
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    K = args.steps
+    # the step: pa_decode_step (append of every new token + attention, one launch)
     wall0 = time.perf_counter()
     with ClockSampler(local) as clocks:
-        for i in range(args.steps):
-            flush_l2()                          # untimed
-            ev[i][0].record(stream)
-            layer.append_step()
-            ev[i][1].record(stream)
-            layer.decode(num_splits=args.splits)
-            ev[i][2].record(stream)
-        torch.cuda.synchronize()
+        t_step = timed(lambda: layer.fused_step(num_splits=args.splits), K)
     wall = time.perf_counter() - wall0
-    step_ms = [a.elapsed_time(c) for a, b, c in ev]
-    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
-    t_step = sum(step_ms) / 1e3
-    t_dec = sum(dec_ms) / 1e3
-    if dist:
-        t = torch.tensor([t_step, t_dec], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_step, t_dec = float(t[0]), float(t[1])
-    K = args.steps
+    # the same step as two launches (pa_kv_append, then pa_decode_attention)
+    t_two = timed(lambda: (layer.append_step(), layer.decode(num_splits=args.splits)), K)
+    # pa_decode_attention alone
+    t_attn = timed(lambda: layer.decode(num_splits=args.splits), K)
     value = world * alg * K / t_step / 1e9
-    dec_gbs = alg * K / t_dec / 1e9
+    # roofline of the step's only kernel: distinct KV bytes (a shared prefix once) + q + out
+    dec_gbs = (uniq + qo_bytes) * K / t_step / 1e9
     peak, peak_kind = hbm_peak()
 
     # end to end through the public API with host buffers: the step's inputs (q,
@@ -350,26 +354,10 @@ def run_ours(args):
 
     def e2e_step():
         d_buf.copy_(h_buf, non_blocking=True)
-        layer.append_step(d_kn, d_vn, slots=d_slots)
-        layer.decode(q=d_q, num_splits=args.splits, tables=d_tab, lens=d_len)
+        layer.fused_step(q=d_q, k_new=d_kn, v_new=d_vn, num_splits=args.splits, tables=d_tab, lens=d_len)
         h_out.copy_(layer.out, non_blocking=True)
 
-    for _ in range(args.warmup):
-        flush_l2()
-        e2e_step()
-    torch.cuda.synchronize()
-    ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for i in range(K):
-        flush_l2()
-        ee[i][0].record(stream)
-        e2e_step()
-        ee[i][1].record(stream)
-    torch.cuda.synchronize()
-    t_e2e = sum(a.elapsed_time(b) for a, b in ee) / 1e3
-    if dist:
-        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t[0])
+    t_e2e = timed(e2e_step, K)
     e2e_value = world * alg * K / t_e2e / 1e9
 
     if rank != 0:
@@ -392,12 +380,16 @@ def run_ours(args):
                    "l2": "512 MiB write+read between timed steps (untimed); step reads > L2"},
         "seq_steps_per_s": world * w.B * K / t_step,
         "hbm_frac_of_%s" % peak_kind: (value / world) / peak,
-        "decode_only": {"GBps": dec_gbs, "us_per_call": 1e6 * t_dec / K},
-        "bytes_per_step": {"algorithmic": alg, "kv_logical": kv_bytes, "q_out": qo_bytes,
-                           "kv_unique_physical": uniq},
+        "us_per_step": 1e6 * t_step / K,
+        "two_launch_step": {"GBps": alg * K / t_two / 1e9, "us": 1e6 * t_two / K,
+                            "calls": "pa_kv_append + pa_decode_attention"},
+        "attention_only": {"GBps": alg * K / t_attn / 1e9, "us": 1e6 * t_attn / K,
+                           "calls": "pa_decode_attention"},
+        "bytes_per_step": {"algorithmic_logical": alg, "kv_logical": kv_bytes, "q_out": qo_bytes,
+                           "kv_distinct": uniq},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(dec_gbs / peak, 4), "traffic": traffic,
-                     "peak_source": peak_kind, "kernel": "pa_decode_attention (one launch, split-K merge fused)"},
+                     "peak_source": peak_kind, "kernel": "paged_decode_kernel via pa_decode_step (append + attention + split-K merge, one launch)"},
         "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * K,

@@ -163,6 +163,29 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
                               void* workspace, size_t workspace_bytes, int kv_dtype, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * pa_decode_step - one whole decode step of a layer in one launch: the append
+ * of every sequence's new token followed by decode attention.
+ *
+ * Equivalent to pa_kv_append(k_new, v_new, slot_mapping) with slot_mapping[b]
+ * = block_tables[b][(seq_lens[b]-1) / block_size] * block_size +
+ * (seq_lens[b]-1) % block_size (the new token is position seq_lens[b]-1,
+ * [P1] "The core insight"; [P2] "Recall and stretch" 3), followed by
+ * pa_decode_attention with the same arguments: the cache bytes, fp8 scales
+ * and outputs are the same as those two calls give.  Sequences with
+ * seq_len 0 append nothing.  The block receiving a sequence's new token must
+ * belong to that sequence alone (a shared block must be copied first).
+ *   k_new, v_new  bf16 [batch][num_kv_heads][head_dim], 16-byte aligned
+ * Everything else as pa_decode_attention; k_cache / v_cache (and the fp8
+ * scales) are written.
+ * ------------------------------------------------------------------------- */
+pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                         const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                         int num_splits, void* workspace, size_t workspace_bytes, int kv_dtype,
+                         void* stream);
+
+/* ---------------------------------------------------------------------------
  * pa_decode_attention_static_ws - pa_decode_attention for callers that cannot
  * allocate device memory.  (The pages have no counterpart to this entry
  * point: it is a convenience of this library.)

@@ -60,6 +60,8 @@ def load(build_if_missing: bool = True):
         "pa_decode_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32]),
         "pa_decode_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                       ctypes.c_float, i32, P, sz, i32, P]),
+        "pa_decode_step": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                 ctypes.c_float, i32, P, sz, i32, P]),
         "pa_get_device_error": (i32, [P, i32]),
         "pa_selftest_bounded_wait": (i32, [P]),
         "pa_allocator_create": (P, [i32, i32]),
@@ -187,6 +189,34 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tenso
                                    bs, M, nb, float(scale), int(num_splits), _ptr(workspace), ws,
                                    kvd, _stream(stream)),
            "pa_decode_attention")
+
+
+def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
+                   v_scale: Optional[torch.Tensor], block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                   scale: float, num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                   stream=None) -> None:
+    """Append each sequence's new token (position seq_len-1) and attend, in one launch."""
+    lib = load()
+    kvd = _kv_dtype(k_cache)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, dc = k_cache.shape
+    M = block_tables.shape[1]
+    if (dc != d or tuple(out.shape) != (B, hq, d) or tuple(k_new.shape) != (B, hkv, d)
+            or tuple(v_new.shape) != (B, hkv, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B):
+        raise ValueError("shape mismatch")
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.pa_decode_step(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv,
+                              d, bs, M, nb, float(scale), int(num_splits), _ptr(workspace), ws, kvd,
+                              _stream(stream)),
+           "pa_decode_step")
 
 
 PA_STATIC_WORKSPACE_BYTES = 16 << 20

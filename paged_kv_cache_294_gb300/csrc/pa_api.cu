@@ -204,13 +204,17 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
     return ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S).total;
 }
 
-pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
-                              const float* k_scale, const float* v_scale,
-                              const int32_t* block_tables, const int32_t* seq_lens, int batch,
-                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                              int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
-                              void* workspace, size_t workspace_bytes, int kv_dtype,
-                              void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by pa_decode_attention (k_new == NULL) and pa_decode_step.
+pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                      const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                      void* workspace, size_t workspace_bytes, int kv_dtype, void* stream, const void* k_new,
+                      const void* v_new) {
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_splits < 0 ||
         !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
         return PA_ERR_INVALID;
@@ -228,6 +232,8 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
         return PA_ERR_INVALID;
     const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
     if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+    if ((k_new != nullptr) != (v_new != nullptr)) return PA_ERR_INVALID;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
     const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
                                                   max_blocks_per_seq, num_splits);
@@ -270,7 +276,40 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
     L.S = S;
     L.scale = scale;
     L.fp8 = fp8;
+    L.k_new = k_new;
+    L.v_new = v_new;
+    L.k_cache_w = const_cast<void*>(k_cache);
+    L.v_cache_w = const_cast<void*>(v_cache);
+    L.k_scale_w = const_cast<float*>(k_scale);
+    L.v_scale_w = const_cast<float*>(v_scale);
     return cuda_status(pa::launch_decode(L, static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                              void* workspace, size_t workspace_bytes, int kv_dtype,
+                              void* stream) {
+    return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       scale, num_splits, workspace, workspace_bytes, kv_dtype, stream, nullptr, nullptr);
+}
+
+pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                         const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                         int num_splits, void* workspace, size_t workspace_bytes, int kv_dtype, void* stream) {
+    if (batch > 0 && (!k_new || !v_new)) return PA_ERR_INVALID;
+    return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
+                       num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
+                       scale, num_splits, workspace, workspace_bytes, kv_dtype, stream, k_new, v_new);
 }
 
 pa_status pa_selftest_bounded_wait(void* stream) {

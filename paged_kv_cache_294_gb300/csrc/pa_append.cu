@@ -10,6 +10,7 @@
 #include <cuda_fp8.h>
 
 #include "pa_device.cuh"
+#include "pa_fp8.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -39,73 +40,6 @@ __global__ void __launch_bounds__(256) kv_append_bf16_kernel(
         k_cache[dst] = k_new[src];
         v_cache[dst] = v_new[src];
     }
-}
-
-// e4m3 code -> fp32, exact (the e4m3 -> f16 conversion is exact).
-__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
-    const uint32_t h2 = e4m3x2_to_f16x2((uint16_t)(code & 0xFF));
-    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFF)));
-}
-
-__device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
-    return (uint32_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) {
-    return __uint_as_float(bits16 << 16);
-}
-
-// Quantise one run of tokens that land in one block, for one kv head, into
-// `page` (bs rows of 128 codes) with its scale.  One warp; lane owns bytes
-// 4*lane .. 4*lane+3 of every row.
-__device__ void fp8_run_one(uint8_t* __restrict__ page, float* __restrict__ scale_p,
-                            const uint16_t* __restrict__ src, const int64_t* __restrict__ slots,
-                            int t0, int r, int h, int Hkv, int bs, int first) {
-    const int lane = threadIdx.x & 31;
-    float a = 0.f;
-#pragma unroll 1
-    for (int j = 0; j < r; ++j) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src + ((int64_t)(t0 + j) * Hkv + h) * 128 +
-                                                        lane * 4);
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x & 0xFFFF)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x >> 16)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y & 0xFFFF)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y >> 16)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const float old = (first == 0) ? 0.f : *scale_p;
-    float s = __fdiv_rn(a, 448.0f);
-    if (old > s) s = old;
-    if (s > old && old > 0.f) {
-#pragma unroll 1
-        for (int o = 0; o < first; ++o) {
-            uint32_t* row = reinterpret_cast<uint32_t*>(page + o * 128) + lane;
-            const uint32_t w = *row;
-            uint32_t nw = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float v = e4m3_to_f32((w >> (8 * e)) & 0xFF);
-                nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
-            }
-            *row = nw;
-        }
-    }
-#pragma unroll 1
-    for (int j = 0; j < r; ++j) {
-        const int off = (int)(slots[t0 + j] % bs);
-        const uint2 w = *reinterpret_cast<const uint2*>(src + ((int64_t)(t0 + j) * Hkv + h) * 128 +
-                                                        lane * 4);
-        const float x[4] = {bf16_bits_to_f32(w.x & 0xFFFF), bf16_bits_to_f32(w.x >> 16),
-                            bf16_bits_to_f32(w.y & 0xFFFF), bf16_bits_to_f32(w.y >> 16)};
-        uint32_t nw = 0;
-        if (s != 0.f) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) nw |= f32_to_e4m3(__fdiv_rn(x[e], s)) << (8 * e);
-        }
-        reinterpret_cast<uint32_t*>(page + off * 128)[lane] = nw;
-    }
-    if (lane == 0) *scale_p = s;
 }
 
 // One warp per (token, kv_head).  Only the first token of each run of
@@ -139,8 +73,10 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(
     }
     const int first = (int)(slot - blk * bs);
     const int64_t page = (blk * Hkv + h) * (int64_t)bs * 128;
-    fp8_run_one(k_cache + page, k_scale + blk * Hkv + h, k_new, slots, t, r, h, Hkv, bs, first);
-    fp8_run_one(v_cache + page, v_scale + blk * Hkv + h, v_new, slots, t, r, h, Hkv, bs, first);
+    const int64_t row0 = ((int64_t)t * Hkv + h) * 128;
+    auto off_of = [&](int j) { return (int)(slots[t + j] % bs); };
+    fp8_quantise_run(k_cache + page, k_scale + blk * Hkv + h, k_new + row0, (int64_t)Hkv * 128, r, first, off_of);
+    fp8_quantise_run(v_cache + page, v_scale + blk * Hkv + h, v_new + row0, (int64_t)Hkv * 128, r, first, off_of);
 }
 
 cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {

@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include "pa_device.cuh"
+#include "pa_fp8.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -46,6 +47,13 @@ struct DecodeArgs {
     float* o_part;
     float* lse;
     int* counters;   // [B][Hkv] merge counters
+    // fused step (APPEND): new K/V rows written before their page is loaded
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint8_t* k_cache_w;
+    uint8_t* v_cache_w;
+    float* k_scale_w;
+    float* v_scale_w;
     int B, Hq, Hkv, G, M, num_blocks, part_blocks, S;
     float scale_log2;
 };
@@ -343,7 +351,33 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 // ========================================================================
 // grid (partitions, kv heads, sequences)
 // ========================================================================
-template <int D, int BS, bool FP8, int NSTAGE>
+// Writes sequence b's new token (position len-1, at offset `off` of physical
+// block `phys`) for kv head h, exactly as pa_kv_append would, then fences the
+// writes for the TMA load of that page.  One full warp.  Returns the block's
+// scales (fp8) so that the page's consumer need not re-read global memory.
+template <int D, int BS, bool FP8>
+__device__ __forceinline__ float2 append_new_row(const DecodeArgs& a, int b, int h, int phys, int off, int lane) {
+    const int64_t src = ((int64_t)b * a.Hkv + h) * D;
+    const int64_t prow = ((int64_t)phys * a.Hkv + h) * BS;  // first row of the page
+    float2 sc = make_float2(1.f, 1.f);
+    if (FP8) {
+        auto off_of = [&](int) { return off; };
+        sc.x = fp8_quantise_run(a.k_cache_w + prow * 128, a.k_scale_w + (int64_t)phys * a.Hkv + h, a.k_new + src,
+                                0, 1, off, off_of);
+        sc.y = fp8_quantise_run(a.v_cache_w + prow * 128, a.v_scale_w + (int64_t)phys * a.Hkv + h, a.v_new + src,
+                                0, 1, off, off_of);
+    } else if (lane < D / 4) {
+        const uint2 kv = *reinterpret_cast<const uint2*>(a.k_new + src + lane * 4);
+        const uint2 vv = *reinterpret_cast<const uint2*>(a.v_new + src + lane * 4);
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = kv;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.v_cache_w) + (prow + off) * D + lane * 4) = vv;
+    }
+    fence_proxy_async_global();
+    __syncwarp();
+    return sc;
+}
+
+template <int D, int BS, bool FP8, int NSTAGE, bool APPEND>
 __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeArgs a) {
@@ -362,6 +396,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __shared__ float s_new_scale[2];  // fused fp8 step: scales of the page holding the new token
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -405,12 +440,21 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 myphys = base == 0 ? phys0 : trow[base + lane];
                 if (myphys < 0 || myphys >= a.num_blocks) {
                     raise_error(PA_DEVERR_BLOCK_ID);
-                    myphys = 0;
+                    myphys = -1;  // loads read block 0; nothing is written through it
                 }
             }
             const int cnt = min(32, npages - base);
             for (int k = 0; k < cnt; ++k) {
-                const int phys = __shfl_sync(0xffffffffu, myphys, k);
+                const int phys_raw = __shfl_sync(0xffffffffu, myphys, k);
+                const int phys = phys_raw < 0 ? 0 : phys_raw;
+                if (APPEND && base + k == npages - 1 && split == nsplit - 1 && phys_raw >= 0) {
+                    // this page holds position len-1: write the new row before loading it
+                    const float2 sc = append_new_row<D, BS, FP8>(a, b, h, phys_raw, (len - 1) % BS, lane);
+                    if (FP8 && lane == 0) {
+                        s_new_scale[0] = sc.x;
+                        s_new_scale[1] = sc.y;
+                    }
+                }
                 if (lane == 0 && alive) {
                     const int i = base + k;
                     const int s = i % NSTAGE;
@@ -449,6 +493,11 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
             }
             if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
+            if (FP8 && APPEND && i == npages - 1 && split == nsplit - 1) {
+                // the producer re-scaled this block just before loading it
+                ksc = s_new_scale[0];
+                vsc = s_new_scale[1];
+            }
             const uint32_t kt = sbase + s * C::STAGEB;
             st.page(kt, kt + C::PAGEB, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc,
                     lane);
@@ -494,7 +543,7 @@ static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
     return cudaSuccess;
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, bool APPEND>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     using C = Cfg<D, BS, FP8>;
     DecodeArgs a;
@@ -507,6 +556,12 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.o_part = L.o_part;
     a.lse = L.lse;
     a.counters = L.counters;
+    a.k_new = (const uint16_t*)L.k_new;
+    a.v_new = (const uint16_t*)L.v_new;
+    a.k_cache_w = (uint8_t*)L.k_cache_w;
+    a.v_cache_w = (uint8_t*)L.v_cache_w;
+    a.k_scale_w = L.k_scale_w;
+    a.v_scale_w = L.v_scale_w;
     a.B = L.B;
     a.Hq = L.Hq;
     a.Hkv = L.Hkv;
@@ -519,7 +574,7 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
     static int configured = -1;
-    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, FP8, NST>, SMEM, configured);
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, FP8, NST, APPEND>, SMEM, configured);
     if (e != cudaSuccess) return e;
     // programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel (typically this step's append) finishes; they wait for it
@@ -534,20 +589,25 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, FP8, NST>, *L.tm_k, *L.tm_v, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, FP8, NST, APPEND>, *L.tm_k, *L.tm_v, a);
+}
+
+template <bool APPEND>
+static cudaError_t launch_shape(const DecodeLaunch& L, cudaStream_t stream) {
+    if (L.fp8) {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, true, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, true, APPEND>(L, stream);
+    } else {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, false, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, false, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, false, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, false, APPEND>(L, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream) {
-    if (L.fp8) {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, true>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, true>(L, stream);
-    } else {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, false>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, false>(L, stream);
-        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, false>(L, stream);
-        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, false>(L, stream);
-    }
-    return cudaErrorInvalidValue;
+    return L.k_new ? launch_shape<true>(L, stream) : launch_shape<false>(L, stream);
 }
 
 cudaError_t decode_unit_error(unsigned int* v, bool clear) { return read_unit_error(v, clear); }

@@ -34,6 +34,13 @@ struct DecodeLaunch {
     int* counters;      // workspace, [B][Hkv], zero between calls
     const CUtensorMap* tm_k;
     const CUtensorMap* tm_v;
+    // fused step: each sequence's new token (position len-1) is written first
+    const void* k_new;  // bf16 [B][Hkv][d], NULL: attention only
+    const void* v_new;
+    void* k_cache_w;
+    void* v_cache_w;
+    float* k_scale_w;
+    float* v_scale_w;
     int B, Hq, Hkv, d, bs, M, num_blocks;
     int part_blocks;    // blocks per split partition
     int S;              // partitions per sequence at most (grid x)

@@ -15,7 +15,7 @@ import numpy as np
 import torch
 
 from . import (PA_KV_FP8_E4M3, pa_allocator, pa_decode_attention, pa_decode_resolve_splits,
-               pa_decode_workspace_bytes, pa_kv_append, pa_slot_mapping)
+               pa_decode_step, pa_decode_workspace_bytes, pa_kv_append, pa_slot_mapping)
 
 
 def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[int], M: int):
@@ -131,5 +131,17 @@ class PagedDecodeLayer:
         return out
 
     def step(self, num_splits: int = 0, stream=None):
+        """pa_kv_append of the new tokens, then pa_decode_attention (two launches)."""
         self.append_step(stream=stream)
         return self.decode(num_splits=num_splits, stream=stream)
+
+    def fused_step(self, q=None, k_new=None, v_new=None, out=None, num_splits: int = 0, tables=None,
+                   lens=None, stream=None):
+        """The same step through pa_decode_step (one launch)."""
+        ws = self.ensure_workspace(num_splits)
+        out = self.out if out is None else out
+        pa_decode_step(out, self.q if q is None else q, self.k_new if k_new is None else k_new,
+                       self.v_new if v_new is None else v_new, self.k_cache, self.v_cache, self.k_scale,
+                       self.v_scale, self.block_tables if tables is None else tables,
+                       self.seq_lens if lens is None else lens, self.scale, num_splits, ws, stream=stream)
+        return out
