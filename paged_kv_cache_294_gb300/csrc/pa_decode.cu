@@ -397,12 +397,15 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     __shared__ float s_new_scale[2];  // fused fp8 step: scales of the page holding the new token
+    __shared__ __align__(8) uint64_t s_app_bar;  // fused step: the new row is in global memory
+    uint64_t* app_bar = &s_app_bar;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
+        mbar_init(app_bar, 1);
         fence_mbar_init();
     }
     // Inputs may come from the preceding kernel in the stream (this step's
@@ -447,17 +450,11 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             for (int k = 0; k < cnt; ++k) {
                 const int phys_raw = __shfl_sync(0xffffffffu, myphys, k);
                 const int phys = phys_raw < 0 ? 0 : phys_raw;
-                if (APPEND && base + k == npages - 1 && split == nsplit - 1 && phys_raw >= 0) {
-                    // this page holds position len-1: write the new row before loading it
-                    const float2 sc = append_new_row<D, BS, FP8>(a, b, h, phys_raw, (len - 1) % BS, lane);
-                    if (FP8 && lane == 0) {
-                        s_new_scale[0] = sc.x;
-                        s_new_scale[1] = sc.y;
-                    }
-                }
                 if (lane == 0 && alive) {
                     const int i = base + k;
                     const int s = i % NSTAGE;
+                    // the page holding position len-1 loads only after its new row is written
+                    if (APPEND && i == npages - 1 && split == nsplit - 1) alive = mbar_wait(app_bar, 0);
                     if (i >= NSTAGE) alive = mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1);
                     if (alive) {
                         mbar_arrive_expect_tx(&full[s], C::STAGEB);
@@ -483,6 +480,23 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     } else {
         const int g = lane >> 2;
         st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
+        if (APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW) {
+            // fused step: the warp that will consume the last page first writes this
+            // head's new row (position len-1) into it, then lets the producer load it
+            int phys = trow[npages - 1];
+            if (phys >= 0 && phys < a.num_blocks) {
+                const float2 sc = append_new_row<D, BS, FP8>(a, b, h, phys, (len - 1) % BS, lane);
+                if (FP8 && lane == 0) {
+                    s_new_scale[0] = sc.x;
+                    s_new_scale[1] = sc.y;
+                }
+            } else if (FP8 && lane == 0) {  // nothing written; the page loads block 0
+                s_new_scale[0] = a.k_scale[h];
+                s_new_scale[1] = a.v_scale[h];
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(app_bar);
+        }
         for (int i = warp; i < npages; i += C::NCW) {
             const int s = i % NSTAGE;
             float ksc = 1.f, vsc = 1.f;
@@ -494,7 +508,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             }
             if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
             if (FP8 && APPEND && i == npages - 1 && split == nsplit - 1) {
-                // the producer re-scaled this block just before loading it
+                // this warp re-scaled the block before it was loaded
                 ksc = s_new_scale[0];
                 vsc = s_new_scale[1];
             }
