@@ -351,30 +351,54 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 // ========================================================================
 // grid (partitions, kv heads, sequences)
 // ========================================================================
-// Writes sequence b's new token (position len-1, at offset `off` of physical
-// block `phys`) for kv head h, exactly as pa_kv_append would, then fences the
-// writes for the TMA load of that page.  One full warp.  Returns the block's
-// scales (fp8) so that the page's consumer need not re-read global memory.
+// Fused step: put sequence b's new token (position len-1, offset `off` of
+// the page just loaded into shared memory at kt / vt) into that page both in
+// shared memory, so that this page's attention sees it, and in the cache in
+// global memory, exactly as pa_kv_append would (no other CTA reads this page
+// in this launch).  kraw / vraw: this lane's 4 new values of K / V; kold /
+// vold: the block's scales before the call (fp8).  Returns the scales the
+// page must be read with.  One full warp.
 template <int D, int BS, bool FP8>
-__device__ __forceinline__ float2 append_new_row(const DecodeArgs& a, int b, int h, int phys, int off, int lane) {
-    const int64_t src = ((int64_t)b * a.Hkv + h) * D;
+__device__ __forceinline__ float2 patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt,
+                                               uint32_t vt, uint2 kraw, uint2 vraw, float kold, float vold,
+                                               int lane) {
     const int64_t prow = ((int64_t)phys * a.Hkv + h) * BS;  // first row of the page
-    float2 sc = make_float2(1.f, 1.f);
     if (FP8) {
-        auto off_of = [&](int) { return off; };
-        sc.x = fp8_quantise_run(a.k_cache_w + prow * 128, a.k_scale_w + (int64_t)phys * a.Hkv + h, a.k_new + src,
-                                0, 1, off, off_of);
-        sc.y = fp8_quantise_run(a.v_cache_w + prow * 128, a.v_scale_w + (int64_t)phys * a.Hkv + h, a.v_new + src,
-                                0, 1, off, off_of);
-    } else if (lane < D / 4) {
-        const uint2 kv = *reinterpret_cast<const uint2*>(a.k_new + src + lane * 4);
-        const uint2 vv = *reinterpret_cast<const uint2*>(a.v_new + src + lane * 4);
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = kv;
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.v_cache_w) + (prow + off) * D + lane * 4) = vv;
+        float2 sc;
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t tile = kv == 0 ? kt : vt;
+            uint32_t* grow = reinterpret_cast<uint32_t*>((kv == 0 ? a.k_cache_w : a.v_cache_w) + prow * 128);
+            const uint2 raw = kv == 0 ? kraw : vraw;
+            const float old = off == 0 ? 0.f : (kv == 0 ? kold : vold);
+            const float s = fp8_rescale(
+                old, warp_max(absmax4(raw)), off, [&](int o) { return ld_shared_u32(swz128(tile, o, lane * 4)); },
+                [&](int o, uint32_t nw) {
+                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, o, lane * 4)), "r"(nw) : "memory");
+                    grow[o * 32 + lane] = nw;
+                });
+            const uint32_t nw = fp8_encode4(raw, s);
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, off, lane * 4)), "r"(nw) : "memory");
+            grow[off * 32 + lane] = nw;
+            if (lane == 0) (kv == 0 ? a.k_scale_w : a.v_scale_w)[(int64_t)phys * a.Hkv + h] = s;
+            if (kv == 0) sc.x = s; else sc.y = s;
+        }
+        __syncwarp();
+        return sc;
     }
-    fence_proxy_async_global();
+    if (lane < D / 4) {
+        const int ct = (lane * 4) / 64, byte = (lane * 4 % 64) * 2;
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(kt + ct * BS * 128, off, byte)), "r"(kraw.x),
+                     "r"(kraw.y)
+                     : "memory");
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(vt + ct * BS * 128, off, byte)), "r"(vraw.x),
+                     "r"(vraw.y)
+                     : "memory");
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = kraw;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.v_cache_w) + (prow + off) * D + lane * 4) = vraw;
+    }
     __syncwarp();
-    return sc;
+    return make_float2(1.f, 1.f);
 }
 
 template <int D, int BS, bool FP8, int NSTAGE, bool APPEND>
@@ -396,16 +420,12 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
 
     const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    __shared__ float s_new_scale[2];  // fused fp8 step: scales of the page holding the new token
-    __shared__ __align__(8) uint64_t s_app_bar;  // fused step: the new row is in global memory
-    uint64_t* app_bar = &s_app_bar;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
-        mbar_init(app_bar, 1);
         fence_mbar_init();
     }
     // Inputs may come from the preceding kernel in the stream (this step's
@@ -453,8 +473,6 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 if (lane == 0 && alive) {
                     const int i = base + k;
                     const int s = i % NSTAGE;
-                    // the page holding position len-1 loads only after its new row is written
-                    if (APPEND && i == npages - 1 && split == nsplit - 1) alive = mbar_wait(app_bar, 0);
                     if (i >= NSTAGE) alive = mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1);
                     if (alive) {
                         mbar_arrive_expect_tx(&full[s], C::STAGEB);
@@ -480,22 +498,24 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     } else {
         const int g = lane >> 2;
         st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
-        if (APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW) {
-            // fused step: the warp that will consume the last page first writes this
-            // head's new row (position len-1) into it, then lets the producer load it
-            int phys = trow[npages - 1];
-            if (phys >= 0 && phys < a.num_blocks) {
-                const float2 sc = append_new_row<D, BS, FP8>(a, b, h, phys, (len - 1) % BS, lane);
-                if (FP8 && lane == 0) {
-                    s_new_scale[0] = sc.x;
-                    s_new_scale[1] = sc.y;
-                }
-            } else if (FP8 && lane == 0) {  // nothing written; the page loads block 0
-                s_new_scale[0] = a.k_scale[h];
-                s_new_scale[1] = a.v_scale[h];
+        // fused step: the warp that consumes the page holding position len-1 fetches
+        // this head's new K/V row (and the block's scales) up front
+        const bool appends = APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW;
+        int app_phys = -1;
+        uint2 kraw = make_uint2(0u, 0u), vraw = make_uint2(0u, 0u);
+        float kold = 0.f, vold = 0.f;
+        if (appends) {
+            app_phys = trow[npages - 1];
+            if (app_phys < 0 || app_phys >= a.num_blocks) app_phys = -1;
+            const int64_t src = ((int64_t)b * a.Hkv + h) * D;
+            if (lane < D / 4) {
+                kraw = *reinterpret_cast<const uint2*>(a.k_new + src + lane * 4);
+                vraw = *reinterpret_cast<const uint2*>(a.v_new + src + lane * 4);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(app_bar);
+            if (FP8 && app_phys >= 0) {
+                kold = a.k_scale_w[(int64_t)app_phys * a.Hkv + h];
+                vold = a.v_scale_w[(int64_t)app_phys * a.Hkv + h];
+            }
         }
         for (int i = warp; i < npages; i += C::NCW) {
             const int s = i % NSTAGE;
@@ -507,14 +527,19 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
                 vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
             }
             if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
-            if (FP8 && APPEND && i == npages - 1 && split == nsplit - 1) {
-                // this warp re-scaled the block before it was loaded
-                ksc = s_new_scale[0];
-                vsc = s_new_scale[1];
-            }
             const uint32_t kt = sbase + s * C::STAGEB;
+            const bool patched = appends && i == npages - 1 && app_phys >= 0;
+            if (patched) {
+                const float2 sc = patch_new_row<D, BS, FP8>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, kraw,
+                                                            vraw, kold, vold, lane);
+                if (FP8) {
+                    ksc = sc.x;
+                    vsc = sc.y;
+                }
+            }
             st.page(kt, kt + C::PAGEB, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc,
                     lane);
+            if (patched) fence_proxy_async_smem();  // generic writes before the next TMA fill
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
         }

@@ -29,6 +29,55 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// The block's new scale from its current one (`old`, already 0 when the call
+// starts the block at offset 0) and the absmax `a` of the new values; when it
+// grows, the older rows (offsets < first) are re-encoded through
+// load_old(o) / store_old(o, codes), 4 codes per lane.  One full warp.
+template <typename LoadOld, typename StoreOld>
+__device__ __forceinline__ float fp8_rescale(float old, float a, int first, LoadOld load_old, StoreOld store_old) {
+    float s = __fdiv_rn(a, 448.0f);
+    if (old > s) s = old;
+    if (s > old && old > 0.f) {
+#pragma unroll 1
+        for (int o = 0; o < first; ++o) {
+            const uint32_t w = load_old(o);
+            uint32_t nw = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float v = e4m3_to_f32((w >> (8 * e)) & 0xFF);
+                nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
+            }
+            store_old(o, nw);
+        }
+    }
+    return s;
+}
+
+// 4 bf16 values (packed in w) -> 4 codes E4M3(x / s); all +0 when s == 0.
+__device__ __forceinline__ uint32_t fp8_encode4(uint2 w, float s) {
+    const float x[4] = {bf16_bits_to_f32(w.x & 0xFFFF), bf16_bits_to_f32(w.x >> 16), bf16_bits_to_f32(w.y & 0xFFFF),
+                        bf16_bits_to_f32(w.y >> 16)};
+    uint32_t nw = 0;
+    if (s != 0.f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) nw |= f32_to_e4m3(__fdiv_rn(x[e], s)) << (8 * e);
+    }
+    return nw;
+}
+
+__device__ __forceinline__ float absmax4(uint2 w) {
+    float a = fabsf(bf16_bits_to_f32(w.x & 0xFFFF));
+    a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x >> 16)));
+    a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y & 0xFFFF)));
+    return fmaxf(a, fabsf(bf16_bits_to_f32(w.y >> 16)));
+}
+
+__device__ __forceinline__ float warp_max(float a) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    return a;
+}
+
 // Quantise r bf16 rows of 128 values (row j at src + j * src_stride) into
 // `page` (rows of 128 codes) at offsets off_of(j), for one (block, kv head)
 // with scale *scale_p; `first` is the smallest offset written.  One full warp;
@@ -40,45 +89,16 @@ __device__ __forceinline__ float fp8_quantise_run(uint8_t* __restrict__ page, fl
     const int lane = threadIdx.x & 31;
     float a = 0.f;
 #pragma unroll 1
-    for (int j = 0; j < r; ++j) {
-        const uint2 w = *reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4);
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x & 0xFFFF)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.x >> 16)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y & 0xFFFF)));
-        a = fmaxf(a, fabsf(bf16_bits_to_f32(w.y >> 16)));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    for (int j = 0; j < r; ++j) a = fmaxf(a, absmax4(*reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4)));
+    a = warp_max(a);
     const float old = (first == 0) ? 0.f : *scale_p;
-    float s = __fdiv_rn(a, 448.0f);
-    if (old > s) s = old;
-    if (s > old && old > 0.f) {
+    uint32_t* rows = reinterpret_cast<uint32_t*>(page);
+    const float s = fp8_rescale(
+        old, a, first, [&](int o) { return rows[o * 32 + lane]; },
+        [&](int o, uint32_t nw) { rows[o * 32 + lane] = nw; });
 #pragma unroll 1
-        for (int o = 0; o < first; ++o) {
-            uint32_t* row = reinterpret_cast<uint32_t*>(page + o * 128) + lane;
-            const uint32_t w = *row;
-            uint32_t nw = 0;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float v = e4m3_to_f32((w >> (8 * e)) & 0xFF);
-                nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
-            }
-            *row = nw;
-        }
-    }
-#pragma unroll 1
-    for (int j = 0; j < r; ++j) {
-        const int off = off_of(j);
-        const uint2 w = *reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4);
-        const float x[4] = {bf16_bits_to_f32(w.x & 0xFFFF), bf16_bits_to_f32(w.x >> 16),
-                            bf16_bits_to_f32(w.y & 0xFFFF), bf16_bits_to_f32(w.y >> 16)};
-        uint32_t nw = 0;
-        if (s != 0.f) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) nw |= f32_to_e4m3(__fdiv_rn(x[e], s)) << (8 * e);
-        }
-        reinterpret_cast<uint32_t*>(page + off * 128)[lane] = nw;
-    }
+    for (int j = 0; j < r; ++j)
+        rows[off_of(j) * 32 + lane] = fp8_encode4(*reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4), s);
     __syncwarp();
     if (lane == 0) *scale_p = s;
     return s;
