@@ -351,54 +351,80 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 // ========================================================================
 // grid (partitions, kv heads, sequences)
 // ========================================================================
-// Fused step: put sequence b's new token (position len-1, offset `off` of
-// the page just loaded into shared memory at kt / vt) into that page both in
-// shared memory, so that this page's attention sees it, and in the cache in
-// global memory, exactly as pa_kv_append would (no other CTA reads this page
-// in this launch).  kraw / vraw: this lane's 4 new values of K / V; kold /
-// vold: the block's scales before the call (fp8).  Returns the scales the
-// page must be read with.  One full warp.
+// Fused step.  The warp that consumes the page holding sequence b's position
+// len-1 prepares this head's new row when the CTA starts (fp8: the block's new
+// scale and the row's codes, computed while the first pages are in flight),
+// then, once that page is in shared memory, writes the row into the page so
+// that this page's attention sees it, and into the cache in global memory
+// exactly as pa_kv_append would (no other CTA reads this page in this launch).
+struct NewRow {
+    uint2 kraw, vraw;    // this lane's 4 new bf16 values of K / V
+    uint32_t kc, vc;     // fp8: their codes under the new scales
+    float kold, vold;    // fp8: scales the older rows were encoded with (0 when the block restarts)
+    float ks, vs;        // fp8: the block's new scales
+};
+
+template <int D, bool FP8>
+__device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, int h, int phys, int off, int lane) {
+    NewRow r;
+    const int64_t src = ((int64_t)b * a.Hkv + h) * D;
+    r.kraw = r.vraw = make_uint2(0u, 0u);
+    if (lane < D / 4) {
+        r.kraw = *reinterpret_cast<const uint2*>(a.k_new + src + lane * 4);
+        r.vraw = *reinterpret_cast<const uint2*>(a.v_new + src + lane * 4);
+    }
+    r.kc = r.vc = 0u;
+    r.kold = r.vold = r.ks = r.vs = 1.f;
+    if (FP8) {
+        r.kold = off == 0 ? 0.f : a.k_scale_w[(int64_t)phys * a.Hkv + h];
+        r.vold = off == 0 ? 0.f : a.v_scale_w[(int64_t)phys * a.Hkv + h];
+        r.ks = fmaxf(r.kold, __fdiv_rn(warp_max(absmax4(r.kraw)), 448.0f));
+        r.vs = fmaxf(r.vold, __fdiv_rn(warp_max(absmax4(r.vraw)), 448.0f));
+        r.kc = fp8_encode4(r.kraw, r.ks);
+        r.vc = fp8_encode4(r.vraw, r.vs);
+    }
+    return r;
+}
+
 template <int D, int BS, bool FP8>
-__device__ __forceinline__ float2 patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt,
-                                               uint32_t vt, uint2 kraw, uint2 vraw, float kold, float vold,
-                                               int lane) {
+__device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
+                                              const NewRow& r, int lane) {
     const int64_t prow = ((int64_t)phys * a.Hkv + h) * BS;  // first row of the page
     if (FP8) {
-        float2 sc;
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
             const uint32_t tile = kv == 0 ? kt : vt;
             uint32_t* grow = reinterpret_cast<uint32_t*>((kv == 0 ? a.k_cache_w : a.v_cache_w) + prow * 128);
-            const uint2 raw = kv == 0 ? kraw : vraw;
-            const float old = off == 0 ? 0.f : (kv == 0 ? kold : vold);
-            const float s = fp8_rescale(
-                old, warp_max(absmax4(raw)), off, [&](int o) { return ld_shared_u32(swz128(tile, o, lane * 4)); },
-                [&](int o, uint32_t nw) {
+            const float old = kv == 0 ? r.kold : r.vold, sn = kv == 0 ? r.ks : r.vs;
+            if (sn > old && old > 0.f) {  // the scale grew: re-encode the older rows (same rule as the append)
+#pragma unroll 1
+                for (int o = 0; o < off; ++o) {
+                    const uint32_t w = ld_shared_u32(swz128(tile, o, lane * 4));
+                    uint32_t nw = 0;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(e4m3_to_f32((w >> (8 * e)) & 0xFF), old), sn)) << (8 * e);
                     asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, o, lane * 4)), "r"(nw) : "memory");
                     grow[o * 32 + lane] = nw;
-                });
-            const uint32_t nw = fp8_encode4(raw, s);
+                }
+            }
+            const uint32_t nw = kv == 0 ? r.kc : r.vc;
             asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, off, lane * 4)), "r"(nw) : "memory");
             grow[off * 32 + lane] = nw;
-            if (lane == 0) (kv == 0 ? a.k_scale_w : a.v_scale_w)[(int64_t)phys * a.Hkv + h] = s;
-            if (kv == 0) sc.x = s; else sc.y = s;
+            if (lane == 0) (kv == 0 ? a.k_scale_w : a.v_scale_w)[(int64_t)phys * a.Hkv + h] = sn;
         }
-        __syncwarp();
-        return sc;
-    }
-    if (lane < D / 4) {
+    } else if (lane < D / 4) {
         const int ct = (lane * 4) / 64, byte = (lane * 4 % 64) * 2;
-        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(kt + ct * BS * 128, off, byte)), "r"(kraw.x),
-                     "r"(kraw.y)
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(kt + ct * BS * 128, off, byte)), "r"(r.kraw.x),
+                     "r"(r.kraw.y)
                      : "memory");
-        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(vt + ct * BS * 128, off, byte)), "r"(vraw.x),
-                     "r"(vraw.y)
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(vt + ct * BS * 128, off, byte)), "r"(r.vraw.x),
+                     "r"(r.vraw.y)
                      : "memory");
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = kraw;
-        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.v_cache_w) + (prow + off) * D + lane * 4) = vraw;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = r.kraw;
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.v_cache_w) + (prow + off) * D + lane * 4) = r.vraw;
     }
     __syncwarp();
-    return make_float2(1.f, 1.f);
 }
 
 template <int D, int BS, bool FP8, int NSTAGE, bool APPEND>
@@ -502,20 +528,11 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
         // this head's new K/V row (and the block's scales) up front
         const bool appends = APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW;
         int app_phys = -1;
-        uint2 kraw = make_uint2(0u, 0u), vraw = make_uint2(0u, 0u);
-        float kold = 0.f, vold = 0.f;
+        NewRow nr;
         if (appends) {
             app_phys = trow[npages - 1];
             if (app_phys < 0 || app_phys >= a.num_blocks) app_phys = -1;
-            const int64_t src = ((int64_t)b * a.Hkv + h) * D;
-            if (lane < D / 4) {
-                kraw = *reinterpret_cast<const uint2*>(a.k_new + src + lane * 4);
-                vraw = *reinterpret_cast<const uint2*>(a.v_new + src + lane * 4);
-            }
-            if (FP8 && app_phys >= 0) {
-                kold = a.k_scale_w[(int64_t)app_phys * a.Hkv + h];
-                vold = a.v_scale_w[(int64_t)app_phys * a.Hkv + h];
-            }
+            if (app_phys >= 0) nr = prepare_new_row<D, FP8>(a, b, h, app_phys, (len - 1) % BS, lane);
         }
         for (int i = warp; i < npages; i += C::NCW) {
             const int s = i % NSTAGE;
@@ -530,11 +547,10 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             const uint32_t kt = sbase + s * C::STAGEB;
             const bool patched = appends && i == npages - 1 && app_phys >= 0;
             if (patched) {
-                const float2 sc = patch_new_row<D, BS, FP8>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, kraw,
-                                                            vraw, kold, vold, lane);
+                patch_new_row<D, BS, FP8>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, nr, lane);
                 if (FP8) {
-                    ksc = sc.x;
-                    vsc = sc.y;
+                    ksc = nr.ks;
+                    vsc = nr.vs;
                 }
             }
             st.page(kt, kt + C::PAGEB, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc,
