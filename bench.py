@@ -136,7 +136,7 @@ class ClockSampler:
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("pa_decode.cu", "pa_device.cuh"):
+    for f in ("pa_decode.cu", "pa_device.cuh", "pa_fp8.cuh"):
         with open(os.path.join(ROOT, "paged_kv_cache_294_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
