@@ -110,9 +110,10 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
 /* ---------------------------------------------------------------------------
  * Split-K (flash-decoding) planning for pa_decode_attention.
  *
- * With S = num_splits (at most 512, at most max_blocks_per_seq) the tokens of
- * every sequence are cut into partitions of P = ceil(max_blocks_per_seq / S)
- * blocks; sequence b uses ceil(ceil(seq_len_b / block_size) / P) partitions.
+ * With S = num_splits (at most 512, at most max_blocks_per_seq) and
+ * P = ceil(max_blocks_per_seq / S), sequence b with n = ceil(seq_len_b /
+ * block_size) blocks uses k = ceil(n / P) partitions of ceil(n / k) blocks
+ * each (the last one possibly shorter).
  * Each partition yields a normalised partial output and its log-sum-exp,
  * combined as
  *     out = sum_i exp(lse_i - L) o_i,  L = log sum_i exp(lse_i)

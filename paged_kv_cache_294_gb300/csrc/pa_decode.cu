@@ -458,11 +458,6 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     // append): wait for it before the first global read.
     griddep_wait();
 
-    // The producer's first 32 table entries load alongside the length.
-    const int j0 = split * a.part_blocks;
-    const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
-    int phys0 = 0;
-    if (warp == C::NCW && lane < a.part_blocks && j0 + lane < a.M) phys0 = trow[lane];
     int len = a.lens[b];
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
@@ -472,7 +467,13 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int nblk = (len + BS - 1) / BS;
     const int nsplit = (nblk + a.part_blocks - 1) / a.part_blocks;  // 0 when len == 0
     if (split > 0 && split >= nsplit) return;
-    const int npages = max(0, min(nblk, j0 + a.part_blocks) - j0);
+    // the sequence's blocks split evenly over its partitions (at most P each)
+    const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
+    const int j0 = split * pb;
+    const int npages = max(0, min(nblk, j0 + pb) - j0);
+    const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
+    int phys0 = 0;
+    if (warp == C::NCW && lane < npages) phys0 = trow[lane];
     __syncthreads();
 
     WarpAcc<D, BS, FP8> st;
