@@ -458,6 +458,10 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     // append): wait for it before the first global read.
     griddep_wait();
 
+    // partition 0 starts at block 0: its producer fetches the first table
+    // entries alongside the length (entries past the sequence are not used)
+    int phys0 = 0;
+    if (split == 0 && warp == C::NCW && lane < a.M) phys0 = a.tables[(int64_t)b * a.M + lane];
     int len = a.lens[b];
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
@@ -472,8 +476,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     const int j0 = split * pb;
     const int npages = max(0, min(nblk, j0 + pb) - j0);
     const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
-    int phys0 = 0;
-    if (warp == C::NCW && lane < npages) phys0 = trow[lane];
+    if (split > 0 && warp == C::NCW && lane < npages) phys0 = trow[lane];
     __syncthreads();
 
     WarpAcc<D, BS, FP8> st;
