@@ -261,8 +261,65 @@ pa_status pa_block_free(pa_allocator* a, const int32_t* ids, int n);
 pa_status pa_block_share(pa_allocator* a, const int32_t* ids, int n);
 int pa_allocator_num_free(const pa_allocator* a);
 int pa_allocator_num_blocks(const pa_allocator* a);
+int pa_allocator_block_size(const pa_allocator* a);
 /* References held on block id (0 = free); -1 if id is out of range. */
 int pa_allocator_refcount(const pa_allocator* a, int32_t id);
+
+/* ---------------------------------------------------------------------------
+ * Prefix cache and copy-on-write ([P1] "4. Prefix caching": a shared prefix's
+ * KV is computed once and reused, vLLM hashing prefix blocks, a radix tree
+ * sharing any common prefix; [P3] "KV Cache Management": 100 requests with
+ * one system prompt share its KV; [P2] "KV memory, paging and prefix
+ * identity": reuse requires the exact token prefix).
+ *
+ * Block j of a sequence (tokens [j*bs, (j+1)*bs)) is cached under the whole
+ * token prefix [0, (j+1)*bs): two sequences share it exactly when those
+ * tokens agree.  Only full blocks are cached; the cache holds one reference
+ * on each block it lists (on the allocator it was created with).
+ * The cache keeps a clock that every match and insert call advances by one;
+ * an entry's last use is the clock of the last call that matched or
+ * inserted it.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_prefix_cache pa_prefix_cache;
+
+pa_prefix_cache* pa_prefix_cache_create(pa_allocator* a);
+/* Drops the cache's references. */
+void pa_prefix_cache_destroy(pa_prefix_cache* c);
+int pa_prefix_cache_size(const pa_prefix_cache* c);
+/* The longest cached prefix of tokens[0..n_tokens): the physical blocks of
+ * its first *n_blocks full blocks (at most max_out) are written to out_blocks
+ * and the caller receives one reference on each. */
+pa_status pa_prefix_match(pa_prefix_cache* c, const int32_t* tokens, int64_t n_tokens, int32_t* out_blocks,
+                          int max_out, int* n_blocks);
+/* Registers the full blocks of a sequence: blocks[j] holds tokens
+ * [j*bs, (j+1)*bs) of tokens[0..n_tokens).  A prefix already cached keeps its
+ * existing block; each new entry takes one reference.  Every listed block
+ * must be allocated (PA_ERR_INVALID otherwise, nothing changed). */
+pa_status pa_prefix_insert(pa_prefix_cache* c, const int32_t* tokens, int64_t n_tokens, const int32_t* blocks,
+                           int n_blocks);
+/* Frees up to `want` cached blocks, one at a time, each time taking among
+ * the entries that end a chain (no cached entry continues them) and that no
+ * sequence references any more (refcount 1: only the cache holds them) the
+ * least recently used, then the deepest, then the lowest block id.  Freeing
+ * a chain's end can make its parent eligible.  *freed = count. */
+pa_status pa_prefix_evict(pa_prefix_cache* c, int want, int* freed);
+
+/* Copy-on-write of one block the caller holds a reference on, before the
+ * caller writes into it: if the caller is its only user (refcount 1) the
+ * block is returned as it is (*needs_copy = 0); otherwise a fresh block is
+ * allocated (lowest free id), the caller's reference moves from `block` to
+ * it and *needs_copy = 1: the caller then copies the data with
+ * pa_copy_blocks.  PA_ERR_OOM if no block is free (nothing changed). */
+pa_status pa_block_cow(pa_allocator* a, int32_t block, int32_t* out_block, int* needs_copy);
+
+/* Device copy of whole blocks: for i < n, block dst[i] (every kv head's K and
+ * V page, and for the fp8 cache both scales) becomes a copy of block src[i].
+ * src / dst are device int32 arrays; no dst may appear as a src of the same
+ * call.  Ids out of range are skipped (PA_DEVERR_BLOCK_ID).  Same layout
+ * rules as pa_kv_append. */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
+                         const int32_t* dst, int n, int num_blocks, int num_kv_heads, int head_dim,
+                         int block_size, int kv_dtype, void* stream);
 
 /* Blocks needed for `tokens` tokens: ceil(tokens / block_size) ([P1] "Visual:
  * the lifecycle of a request": 50 tokens use 4 blocks, 5000 use 313).

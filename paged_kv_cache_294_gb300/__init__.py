@@ -72,6 +72,15 @@ def load(build_if_missing: bool = True):
         "pa_allocator_num_free": (i32, [P]),
         "pa_allocator_num_blocks": (i32, [P]),
         "pa_allocator_refcount": (i32, [P, i32]),
+        "pa_allocator_block_size": (i32, [P]),
+        "pa_prefix_cache_create": (P, [P]),
+        "pa_prefix_cache_destroy": (None, [P]),
+        "pa_prefix_cache_size": (i32, [P]),
+        "pa_prefix_match": (i32, [P, P, i64, P, i32, P]),
+        "pa_prefix_insert": (i32, [P, P, i64, P, i32]),
+        "pa_prefix_evict": (i32, [P, i32, P]),
+        "pa_block_cow": (i32, [P, i32, P, P]),
+        "pa_copy_blocks": (i32, [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, P]),
         "pa_blocks_for_tokens": (i64, [i64, i32]),
         "pa_kv_bytes": (u64, [i32, i32, i32, i32, i64, i64]),
         "pa_slot_mapping": (i32, [P, i32, P, P, i32, i32, P]),
@@ -251,6 +260,20 @@ def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: t
            "pa_decode_attention_static_ws")
 
 
+def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
+                   v_scale: Optional[torch.Tensor], src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
+    """Block dst[i] becomes a copy of block src[i] (K and V pages, fp8 scales)."""
+    lib = load()
+    kvd = _kv_dtype(k_cache)
+    _need(src, torch.int32, "src", 1)
+    _need(dst, torch.int32, "dst", 1)
+    if src.shape != dst.shape or v_cache.shape != k_cache.shape:
+        raise ValueError("src/dst or cache shapes differ")
+    nb, hkv, bs, d = k_cache.shape
+    _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(src), _ptr(dst),
+                              int(src.shape[0]), nb, hkv, d, bs, kvd, _stream(stream)), "pa_copy_blocks")
+
+
 def pa_get_device_error(clear: bool = True) -> int:
     v = ctypes.c_uint32(0)
     _check(load().pa_get_device_error(ctypes.byref(v), 1 if clear else 0), "pa_get_device_error")
@@ -295,6 +318,71 @@ class pa_allocator:
 
     def refcount(self, i: int) -> int:
         return int(self._lib.pa_allocator_refcount(self._h, int(i)))
+
+
+class pa_prefix_cache:
+    """Cache of full KV blocks keyed by their whole token prefix."""
+
+    def __init__(self, a: pa_allocator):
+        self._lib = load()
+        self._alloc = a            # the cache holds references on a's blocks: keep a alive
+        self._h = self._lib.pa_prefix_cache_create(a.handle)
+        if not self._h:
+            raise ValueError("invalid allocator")
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.pa_prefix_cache_destroy(h)
+
+    @property
+    def handle(self):
+        return self._h
+
+    def size(self) -> int:
+        return int(self._lib.pa_prefix_cache_size(self._h))
+
+    def match(self, tokens, max_out: Optional[int] = None) -> np.ndarray:
+        return pa_prefix_match(self, tokens, max_out)
+
+    def insert(self, tokens, blocks) -> None:
+        pa_prefix_insert(self, tokens, blocks)
+
+    def evict(self, want: int) -> int:
+        return pa_prefix_evict(self, want)
+
+
+def pa_prefix_match(c: pa_prefix_cache, tokens, max_out: Optional[int] = None) -> np.ndarray:
+    """Blocks of the longest cached prefix of tokens; the caller gets a reference on each."""
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    bs = c._alloc.block_size
+    cap = len(t) // bs if max_out is None else int(max_out)
+    out = np.zeros(max(cap, 1), np.int32)
+    n = ctypes.c_int(0)
+    _check(load().pa_prefix_match(c.handle, _np_ptr(t) if t.size else None, int(t.size), _np_ptr(out), cap,
+                                  ctypes.byref(n)), "pa_prefix_match")
+    return out[: n.value]
+
+
+def pa_prefix_insert(c: pa_prefix_cache, tokens, blocks) -> None:
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+    b = np.ascontiguousarray(np.asarray(blocks, dtype=np.int32))
+    _check(load().pa_prefix_insert(c.handle, _np_ptr(t) if t.size else None, int(t.size),
+                                   _np_ptr(b) if b.size else None, int(b.size)), "pa_prefix_insert")
+
+
+def pa_prefix_evict(c: pa_prefix_cache, want: int) -> int:
+    n = ctypes.c_int(0)
+    _check(load().pa_prefix_evict(c.handle, int(want), ctypes.byref(n)), "pa_prefix_evict")
+    return int(n.value)
+
+
+def pa_block_cow(a: pa_allocator, block: int):
+    """(block to write, needs_copy) for a block the caller holds a reference on."""
+    out = ctypes.c_int32(0)
+    nc = ctypes.c_int(0)
+    _check(load().pa_block_cow(a.handle, int(block), ctypes.byref(out), ctypes.byref(nc)), "pa_block_cow")
+    return int(out.value), bool(nc.value)
 
 
 def pa_block_alloc(a: pa_allocator, n: int) -> np.ndarray:

@@ -312,6 +312,21 @@ pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void
                        scale, num_splits, workspace, workspace_bytes, kv_dtype, stream, k_new, v_new);
 }
 
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
+                         const int32_t* dst, int n, int num_blocks, int num_kv_heads, int head_dim, int block_size,
+                         int kv_dtype, void* stream) {
+    if (n < 0 || !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)) return PA_ERR_INVALID;
+    const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
+    if (ks != PA_OK) return ks;
+    if (n == 0) return PA_OK;
+    if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
+    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return PA_ERR_INVALID;
+    return cuda_status(pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, n, num_blocks,
+                                              num_kv_heads, head_dim, block_size, fp8,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_selftest_bounded_wait(void* stream) {
     return cuda_status(pa::launch_wait_selftest(static_cast<cudaStream_t>(stream)));
 }

@@ -98,6 +98,44 @@ cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Whole-block copies (copy-on-write): for each pair i, every kv head's K and
+// V page of block dst[i] becomes a copy of block src[i] (and the fp8 scales).
+// One thread per 16-byte unit of a block's K (and V) data.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                          float* __restrict__ k_scale, float* __restrict__ v_scale,
+                                                          const int32_t* __restrict__ src,
+                                                          const int32_t* __restrict__ dst, int n,
+                                                          int64_t units, int Hkv, int num_blocks) {
+    const int64_t total = (int64_t)n * units;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int p = (int)(i / units);
+        const int64_t u = i - (int64_t)p * units;
+        const int s = src[p], d = dst[p];
+        if (s < 0 || s >= num_blocks || d < 0 || d >= num_blocks) {
+            if (u == 0) raise_error(PA_DEVERR_BLOCK_ID);
+            continue;
+        }
+        k_cache[(int64_t)d * units + u] = k_cache[(int64_t)s * units + u];
+        v_cache[(int64_t)d * units + u] = v_cache[(int64_t)s * units + u];
+        if (k_scale && u < Hkv) {
+            k_scale[(int64_t)d * Hkv + u] = k_scale[(int64_t)s * Hkv + u];
+            v_scale[(int64_t)d * Hkv + u] = v_scale[(int64_t)s * Hkv + u];
+        }
+    }
+}
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
+                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool fp8,
+                               cudaStream_t stream) {
+    const int64_t units = (int64_t)Hkv * bs * d * (fp8 ? 1 : 2) / 16;
+    const int64_t total = (int64_t)n * units;
+    const int blocks = (int)std::min<int64_t>((total + 255) / 256, 1 << 20);
+    copy_blocks_kernel<<<blocks, 256, 0, stream>>>((uint4*)k_cache, (uint4*)v_cache, k_scale, v_scale, src, dst, n,
+                                                   units, Hkv, num_blocks);
+    return cudaGetLastError();
+}
+
 // Self-test of the bounded wait: one warp waits on a barrier phase that no
 // thread or copy will ever complete.  The wait must give up on its own,
 // record PA_DEVERR_TIMEOUT and let the kernel finish.

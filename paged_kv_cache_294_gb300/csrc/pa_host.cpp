@@ -84,6 +84,8 @@ int pa_allocator_num_free(const pa_allocator* a) { return a ? (int)a->free_ids.s
 
 int pa_allocator_num_blocks(const pa_allocator* a) { return a ? a->num_blocks : -1; }
 
+int pa_allocator_block_size(const pa_allocator* a) { return a ? a->block_size : -1; }
+
 int pa_allocator_refcount(const pa_allocator* a, int32_t id) {
     if (!a || id < 0 || id >= a->num_blocks) return -1;
     return a->refcnt[id];

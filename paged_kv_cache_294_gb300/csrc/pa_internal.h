@@ -52,6 +52,9 @@ cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(cudaStream_t stream);
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
+                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool fp8,
+                               cudaStream_t stream);
 cudaError_t append_unit_error(unsigned int* v, bool clear);
 cudaError_t decode_unit_error(unsigned int* v, bool clear);
 

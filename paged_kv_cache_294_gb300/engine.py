@@ -14,8 +14,9 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import (PA_KV_FP8_E4M3, pa_allocator, pa_decode_attention, pa_decode_resolve_splits,
-               pa_decode_step, pa_decode_workspace_bytes, pa_kv_append, pa_slot_mapping)
+from . import (PA_ERR_OOM, PA_KV_FP8_E4M3, PagedAttnError, pa_allocator, pa_block_cow, pa_copy_blocks,
+               pa_decode_attention, pa_decode_resolve_splits, pa_decode_step, pa_decode_workspace_bytes,
+               pa_kv_append, pa_prefix_cache, pa_slot_mapping)
 
 
 def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[int], M: int):
@@ -41,6 +42,102 @@ def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[
             raise ValueError("table wider than M")
         tables[b, : len(ids)] = ids
     return tables, alloc
+
+
+class BlockManager:
+    """Block tables of live sequences over a pa_allocator, with prefix caching
+    and copy-on-write ("KV cache & continuous batching", sections
+    "2. PagedAttention" and "4. Prefix caching").
+
+    add(sid, tokens)     reuses the longest cached prefix, allocates blocks for
+                         the rest and returns the first position whose KV the
+                         caller must still write;
+    commit(sid)          caches the sequence's full blocks (after their KV is
+                         written);
+    fork(child, parent)  the child shares every block of the parent;
+    append(sid, token)   reserves the next token's slot: a fresh block at a
+                         block boundary, else the block it lands in after
+                         pa_block_cow; returns (slot, (src, dst) or None), the
+                         pair naming a block copy the caller must run (with
+                         pa_copy_blocks) before writing;
+    free(sid)            drops the sequence's references.
+    When the pool runs dry, blocks only the prefix cache holds are evicted.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, prefix_caching: bool = True):
+        self.bs = int(block_size)
+        self.alloc = pa_allocator(num_blocks, block_size)
+        self.cache = pa_prefix_cache(self.alloc) if prefix_caching else None
+        self.tokens: Dict[int, List[int]] = {}
+        self.blocks: Dict[int, List[int]] = {}
+
+    def _alloc(self, n: int) -> List[int]:
+        if n <= 0:
+            return []
+        short = n - self.alloc.num_free()
+        if short > 0 and self.cache is not None:
+            self.cache.evict(short)
+        return [int(x) for x in self.alloc.alloc(n)]
+
+    def add(self, sid: int, tokens: Sequence[int]) -> int:
+        if sid in self.blocks:
+            raise ValueError("sequence %d exists" % sid)
+        toks = [int(t) for t in tokens]
+        shared = [int(x) for x in self.cache.match(toks)] if self.cache is not None else []
+        try:
+            own = self._alloc(-(-len(toks) // self.bs) - len(shared))
+        except PagedAttnError:
+            self.alloc.free(shared)
+            raise
+        self.tokens[sid], self.blocks[sid] = toks, shared + own
+        return len(shared) * self.bs
+
+    def commit(self, sid: int) -> None:
+        if self.cache is not None:
+            self.cache.insert(self.tokens[sid], self.blocks[sid])
+
+    def fork(self, child: int, parent: int) -> None:
+        if child in self.blocks:
+            raise ValueError("sequence %d exists" % child)
+        self.alloc.share(self.blocks[parent])
+        self.tokens[child] = list(self.tokens[parent])
+        self.blocks[child] = list(self.blocks[parent])
+
+    def append(self, sid: int, token: int):
+        toks, blocks = self.tokens[sid], self.blocks[sid]
+        n = len(toks)
+        j = n // self.bs
+        copy = None
+        if j == len(blocks):
+            blocks.append(self._alloc(1)[0])
+        else:
+            try:
+                dst, needs_copy = pa_block_cow(self.alloc, blocks[j])
+            except PagedAttnError as e:
+                if e.status != PA_ERR_OOM or self.cache is None or self.cache.evict(1) == 0:
+                    raise
+                dst, needs_copy = pa_block_cow(self.alloc, blocks[j])
+            if needs_copy:
+                copy = (blocks[j], dst)
+            blocks[j] = dst
+        toks.append(int(token))
+        return blocks[j] * self.bs + n % self.bs, copy
+
+    def free(self, sid: int) -> None:
+        self.alloc.free(self.blocks.pop(sid))
+        del self.tokens[sid]
+
+    def table(self, sids: Sequence[int], M: int) -> np.ndarray:
+        t = np.full((len(sids), M), -1, dtype=np.int32)
+        for i, sid in enumerate(sids):
+            b = self.blocks[sid]
+            if len(b) > M:
+                raise ValueError("table wider than M")
+            t[i, : len(b)] = b
+        return t
+
+    def lens(self, sids: Sequence[int]) -> np.ndarray:
+        return np.asarray([len(self.tokens[s]) for s in sids], dtype=np.int32)
 
 
 class PagedDecodeLayer:
@@ -134,6 +231,14 @@ class PagedDecodeLayer:
         """pa_kv_append of the new tokens, then pa_decode_attention (two launches)."""
         self.append_step(stream=stream)
         return self.decode(num_splits=num_splits, stream=stream)
+
+    def copy_blocks(self, pairs, stream=None):
+        """Run the block copies BlockManager.append asked for (copy-on-write)."""
+        if not pairs:
+            return
+        src = torch.tensor([p[0] for p in pairs], dtype=torch.int32).to(self.device)
+        dst = torch.tensor([p[1] for p in pairs], dtype=torch.int32).to(self.device)
+        pa_copy_blocks(self.k_cache, self.v_cache, self.k_scale, self.v_scale, src, dst, stream=stream)
 
     def fused_step(self, q=None, k_new=None, v_new=None, out=None, num_splits: int = 0, tables=None,
                    lens=None, stream=None):

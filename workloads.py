@@ -390,6 +390,70 @@ def make(name: str, device="cpu", B: Optional[int] = None, seq_len: Optional[int
                     **vals)
 
 
+@dataclasses.dataclass
+class ServingScenario:
+    """Requests with one shared system prompt, forks, then decode steps.
+
+    Request r's tokens are prompt + suffix[r]; its KV for every position is
+    k_pre[r] / v_pre[r] (a request that reuses a cached prefix writes only the
+    positions after it).  After all requests are admitted, forks[i] =
+    (parent) makes sequence R + i a copy of sequence `parent`.  Each step
+    appends one token to every live sequence (ids 0 .. R + len(forks) - 1, in
+    order): tokens[s][i], with new K/V k_new[s][i] / v_new[s][i] and query
+    q[s][i].
+    """
+    Hq: int
+    Hkv: int
+    d: int
+    bs: int
+    kv: str
+    num_blocks: int
+    M: int
+    scale: float
+    prompt: List[int]
+    requests: List[List[int]]
+    k_pre: List[torch.Tensor]           # bf16 [len_r, Hkv, d]
+    v_pre: List[torch.Tensor]
+    forks: List[int]
+    tokens: List[List[int]]             # [steps][n_seq]
+    q: List[torch.Tensor]               # [steps] bf16 [n_seq, Hq, d]
+    k_new: List[torch.Tensor]           # [steps] bf16 [n_seq, Hkv, d]
+    v_new: List[torch.Tensor]
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.requests) + len(self.forks)
+
+
+def serving_scenario(layer: str = "8b", R: int = 6, n_forks: int = 2, steps: int = 20, seed: int = 7,
+                     device="cpu") -> ServingScenario:
+    """A small prefix-sharing trace on one layer's shape (the system prompt ends
+    mid-block, so its last block is recomputed per request; suffixes span 0 to
+    2 blocks; forks share a parent's partly filled last block)."""
+    cfg = CONFIGS[layer]
+    Hq, Hkv, d, bs, kv = cfg["Hq"], cfg["Hkv"], cfg["d"], cfg["bs"], cfg["kv"]
+    rng = _np_rng(seed, 50)
+    P = 5 * bs + 7
+    prompt = [int(x) for x in rng.integers(0, 32000, P)]
+    requests = [prompt + [int(x) for x in rng.integers(32000, 64000, int(rng.integers(0, 2 * bs + 1)))]
+                for _ in range(R)]
+    forks = [int(x) for x in rng.integers(0, R, n_forks)]
+    n_seq = R + n_forks
+    k_pre = [randn_bf16((len(t), Hkv, d), seed, 100 + r, device) for r, t in enumerate(requests)]
+    v_pre = [randn_bf16((len(t), Hkv, d), seed, 200 + r, device) for r, t in enumerate(requests)]
+    tokens = [[int(x) for x in rng.integers(0, 64000, n_seq)] for _ in range(steps)]
+    q = [randn_bf16((n_seq, Hq, d), seed, 300 + s, device) for s in range(steps)]
+    # the new values grow over the steps so that fp8 block scales grow and re-encode
+    k_new = [randn_bf16((n_seq, Hkv, d), seed, 400 + s, device, mult=1.0 + 0.2 * s) for s in range(steps)]
+    v_new = [randn_bf16((n_seq, Hkv, d), seed, 500 + s, device, mult=1.0 + 0.1 * s) for s in range(steps)]
+    longest = max(len(t) for t in requests) + steps
+    M = -(-longest // bs) + 1
+    num_blocks = 4 * n_seq * M
+    return ServingScenario(Hq=Hq, Hkv=Hkv, d=d, bs=bs, kv=kv, num_blocks=num_blocks, M=M,
+                           scale=1.0 / math.sqrt(d), prompt=prompt, requests=requests, k_pre=k_pre,
+                           v_pre=v_pre, forks=forks, tokens=tokens, q=q, k_new=k_new, v_new=v_new)
+
+
 def roofline_bytes(w: Workload) -> dict:
     """Bytes the step must move at minimum: K/V history read once, q read, out written.
 
