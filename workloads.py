@@ -443,9 +443,10 @@ def serving_scenario(layer: str = "8b", R: int = 6, n_forks: int = 2, steps: int
     v_pre = [randn_bf16((len(t), Hkv, d), seed, 200 + r, device) for r, t in enumerate(requests)]
     tokens = [[int(x) for x in rng.integers(0, 64000, n_seq)] for _ in range(steps)]
     q = [randn_bf16((n_seq, Hq, d), seed, 300 + s, device) for s in range(steps)]
-    # the new values grow over the steps so that fp8 block scales grow and re-encode
-    k_new = [randn_bf16((n_seq, Hkv, d), seed, 400 + s, device, mult=1.0 + 0.2 * s) for s in range(steps)]
-    v_new = [randn_bf16((n_seq, Hkv, d), seed, 500 + s, device, mult=1.0 + 0.1 * s) for s in range(steps)]
+    # unit-variance values like the history: a block filled one token at a time
+    # still grows its fp8 scale whenever a new row sets a new absmax
+    k_new = [randn_bf16((n_seq, Hkv, d), seed, 400 + s, device) for s in range(steps)]
+    v_new = [randn_bf16((n_seq, Hkv, d), seed, 500 + s, device) for s in range(steps)]
     longest = max(len(t) for t in requests) + steps
     M = -(-longest // bs) + 1
     num_blocks = 4 * n_seq * M
