@@ -12,6 +12,9 @@ Each wrapper names the page section its definition follows; see the C file.
 Parity status of each function (what pins it, in tests/test_oracle_*.py):
   decode_attention        brute-force dense attention, cached == causal, closed forms
   decode_attention_split  equals decode_attention for every partition size
+  prefill_attention       whole-sequence chunks equal a library causal attention
+                          (torch, fp64); one-token chunks equal decode_attention;
+                          a verify chunk equals the sequential decode steps
   kv_append (bf16)        exact copy: checked against direct indexing
   kv_append (fp8)         scale == absmax/448, round-trip bounds, brute-force encode
   e4m3_encode/value       nearest-value brute force over the 256-code table, format facts
@@ -83,6 +86,8 @@ def _load():
                                           i64, dbl, i32]),
             "or_decode_attention_split": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
                                                 i32, i64, dbl, i32, i32]),
+            "or_prefill_attention": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
+                                           i64, dbl, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -303,4 +308,42 @@ def decode_attention(cache: Cache, q, block_tables: np.ndarray, seq_lens: np.nda
             rcs = list(ex.map(lambda b: run(b, b + 1), order))
     if any(rc != 0 for rc in rcs):
         raise ValueError("invalid decode arguments (block id or length out of range)")
+    return out
+
+
+def prefill_attention(cache: Cache, q, block_tables: np.ndarray, seq_lens: np.ndarray,
+                      q_start: np.ndarray, Hq: int, scale: float, threads: int = 1) -> np.ndarray:
+    """fp64 multi-query (chunked-prefill / verify) attention; out [total_q, Hq, d].
+
+    Sequence b's queries are rows q_start[b] .. q_start[b+1]-1 of q: the last
+    C_b positions of its seq_lens[b] cached tokens, each attending causally.
+    """
+    qb = _u16(q)
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(q_start, dtype=np.int32)
+    B = int(len(lens))
+    M = int(tables.shape[1]) if tables.ndim == 2 else 0
+    d = cache.d
+    out = np.zeros((int(qs[-1]) if len(qs) else 0, Hq, d), dtype=np.float64)
+    lib = _load()
+    fp8 = 1 if cache.kv == "fp8" else 0
+
+    def run(b):
+        qsb = np.ascontiguousarray(qs[b:b + 2] - qs[b])
+        r0 = int(qs[b])
+        if int(qs[b + 1]) == r0:
+            return 0
+        return lib.or_prefill_attention(out[r0:].ctypes.data, qb[r0:].ctypes.data, _p(cache.k), _p(cache.v),
+                                        _p(cache.k_scale), _p(cache.v_scale), tables[b:b + 1].ctypes.data,
+                                        lens[b:b + 1].ctypes.data, qsb.ctypes.data, 1, Hq, cache.Hkv, d,
+                                        cache.bs, M, cache.num_blocks, float(scale), fp8)
+
+    if threads <= 1 or B <= 1:
+        rcs = [run(b) for b in range(B)]
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            rcs = list(ex.map(run, range(B)))
+    if any(rc != 0 for rc in rcs):
+        raise ValueError("invalid prefill arguments (block id, length or query count out of range)")
     return out

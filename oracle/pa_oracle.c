@@ -413,7 +413,7 @@ static double kv_elem(const void* cache, const float* sc, int fp8, int64_t blk, 
 }
 
 /* Attention of one query head over tokens [t0, t1) of one sequence.
- * Writes the un-normalised weighted sum into acc[d] and returns its
+ * Writes the softmax-weighted sum of the values into acc[d] and returns the
  * log-sum-exp (natural log) of the scaled scores; -INFINITY when empty. */
 static double attend_range(double* acc, const uint16_t* qrow, const void* k_cache,
                            const void* v_cache, const float* k_scale, const float* v_scale,
@@ -463,6 +463,40 @@ int or_decode_attention(double* out, const uint16_t* q, const void* k_cache, con
                          block_tables + (int64_t)b * M, i / G, Hkv, d, bs, scale, fp8, 0, len,
                          num_blocks, &bad);
             if (bad) return -1;
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Multi-query attention over the paged cache: [P1] "3. Chunked prefill" (a  */
+/* long prompt is processed a chunk at a time; the chunk's queries attend to */
+/* the cache holding the earlier chunks and the chunk itself) and [P2]       */
+/* "Speculative decoding" (the target model scores the K proposed tokens in  */
+/* one pass).  Sequence b has C_b = q_start[b+1] - q_start[b] query tokens:  */
+/* the last C_b of its seq_lens[b] cached positions.  Query token i of the   */
+/* sequence sits at position p = seq_lens[b] - C_b + i and attends causally  */
+/* to positions 0..p; head mapping and the fp8 value rule as above.  q and   */
+/* out are [total queries][Hq][d], sequence b's rows starting at q_start[b]. */
+/* ------------------------------------------------------------------------ */
+int or_prefill_attention(double* out, const uint16_t* q, const void* k_cache, const void* v_cache,
+                         const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                         const int32_t* seq_lens, const int32_t* q_start, int B, int Hq, int Hkv, int d,
+                         int bs, int M, int64_t num_blocks, double scale, int fp8) {
+    int b, i, c, G, bad = 0;
+    if (Hkv <= 0 || Hq % Hkv != 0 || d <= 0 || bs <= 0) return -1;
+    G = Hq / Hkv;
+    for (b = 0; b < B; b++) {
+        int len = seq_lens[b], C = q_start[b + 1] - q_start[b];
+        if (len > M * bs || C < 0 || C > len) return -1;
+        for (c = 0; c < C; c++) {
+            int64_t row = (int64_t)q_start[b] + c;
+            for (i = 0; i < Hq; i++) {
+                attend_range(out + (row * Hq + i) * d, q + (row * Hq + i) * d, k_cache, v_cache, k_scale,
+                             v_scale, block_tables + (int64_t)b * M, i / G, Hkv, d, bs, scale, fp8, 0,
+                             len - C + c + 1, num_blocks, &bad);
+                if (bad) return -1;
+            }
         }
     }
     return 0;
