@@ -360,6 +360,23 @@ def run_ours(args):
     t_e2e = timed(e2e_step, K)
     e2e_value = world * alg * K / t_e2e / 1e9
 
+    # copy-on-write block copies (pa_copy_blocks) on this layer's page shape:
+    # 4096 random source blocks into 4096 others of a separate pool
+    nb_copy = 4096
+    ck = torch.empty((2 * nb_copy,) + tuple(layer.k_cache.shape[1:]), dtype=layer.k_cache.dtype, device=dev)
+    cv = torch.empty_like(ck)
+    ck.view(torch.uint8).fill_(3)
+    cv.view(torch.uint8).fill_(5)
+    cks = torch.ones((2 * nb_copy, w.Hkv), dtype=torch.float32, device=dev) if w.kv == "fp8" else None
+    cvs = torch.ones_like(cks) if cks is not None else None
+    perm = torch.from_numpy(np.random.default_rng(1).permutation(2 * nb_copy).astype(np.int32)).to(dev)
+    c_src, c_dst = perm[:nb_copy].contiguous(), perm[nb_copy:].contiguous()
+    t_copy = timed(lambda: pa.pa_copy_blocks(ck, cv, cks, cvs, c_src, c_dst), K)
+    page = ck[0].numel() * ck.element_size()
+    copy_bytes = 2 * 2 * nb_copy * (page + (4 * w.Hkv if cks is not None else 0))   # K and V, read + write
+    copy_gbs = copy_bytes * K / t_copy / 1e9
+    del ck, cv, cks, cvs
+
     if rank != 0:
         return
     cpu = None
@@ -385,6 +402,9 @@ def run_ours(args):
                             "calls": "pa_kv_append + pa_decode_attention"},
         "attention_only": {"GBps": alg * K / t_attn / 1e9, "us": 1e6 * t_attn / K,
                            "calls": "pa_decode_attention"},
+        "copy_blocks": {"GBps": round(copy_gbs, 1), "frac": round(copy_gbs / hbm_peak()[0], 4),
+                        "us": 1e6 * t_copy / K, "blocks": nb_copy, "bytes": copy_bytes,
+                        "calls": "pa_copy_blocks (copy-on-write of whole K/V pages)"},
         "bytes_per_step": {"algorithmic_logical": alg, "kv_logical": kv_bytes, "q_out": qo_bytes,
                            "kv_distinct": uniq},
         "roofline": {"bound": "hbm", "achieved": round(dec_gbs, 1), "peak": peak, "unit": "GB/s",

@@ -265,6 +265,36 @@ int pa_allocator_block_size(const pa_allocator* a);
 /* References held on block id (0 = free); -1 if id is out of range. */
 int pa_allocator_refcount(const pa_allocator* a, int32_t id);
 
+/* Multi-query attention over the paged cache: a prefill chunk ([P1] "3.
+ * Chunked prefill": a long prompt is processed a chunk at a time, each chunk
+ * attending to the cache that holds the earlier chunks) or a speculative
+ * verification pass ([P2] "Speculative decoding": the target model scores
+ * the K proposed tokens in one pass).
+ *
+ * Sequence b has C_b = q_start[b+1] - q_start[b] query tokens, which are the
+ * last C_b of its seq_lens[b] cached positions: query token i of the
+ * sequence sits at position seq_lens[b] - C_b + i and attends to positions
+ * 0 .. that position.  The chunk's own K/V must already be in the cache
+ * (pa_kv_append with its slots).  Query head i uses kv head i / G.
+ *
+ *   out, q        bf16 [total_q][num_q_heads][head_dim], total_q = q_start[batch];
+ *                 sequence b's rows start at q_start[b]
+ *   q_start       device int32 [batch + 1], non-decreasing, q_start[0] = 0
+ *   max_q_len     host bound on every C_b (sizes the grid)
+ *   other arguments as for pa_decode_attention (no workspace).
+ *
+ * Supported: bf16 cache, head_dim 128, block_size 16 or 32, G dividing 128
+ * (PA_ERR_UNSUPPORTED otherwise).  A sequence with C_b < 0, C_b > seq_lens[b],
+ * seq_lens[b] > max_blocks_per_seq * block_size or C_b > max_q_len is
+ * skipped (PA_DEVERR_SEQ_LEN); out-of-range block ids raise
+ * PA_DEVERR_BLOCK_ID and leave that sequence's outputs unspecified (finite).
+ * Enqueued on `stream`; no allocation, no synchronisation. */
+pa_status pa_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                               const int32_t* seq_lens, const int32_t* q_start, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                               int num_blocks, int max_q_len, float scale, int kv_dtype, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Prefix cache and copy-on-write ([P1] "4. Prefix caching": a shared prefix's
  * KV is computed once and reused, vLLM hashing prefix blocks, a radix tree

@@ -62,6 +62,8 @@ def load(build_if_missing: bool = True):
                                       ctypes.c_float, i32, P, sz, i32, P]),
         "pa_decode_step": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                  ctypes.c_float, i32, P, sz, i32, P]),
+        "pa_prefill_attention": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       ctypes.c_float, i32, P]),
         "pa_get_device_error": (i32, [P, i32]),
         "pa_selftest_bounded_wait": (i32, [P]),
         "pa_allocator_create": (P, [i32, i32]),
@@ -258,6 +260,29 @@ def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: t
              _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M, nb, float(scale), int(num_splits),
              kvd, _stream(stream)),
            "pa_decode_attention_static_ws")
+
+
+def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                         k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor],
+                         block_tables: torch.Tensor, seq_lens: torch.Tensor, q_start: torch.Tensor,
+                         max_q_len: int, scale: float, stream=None) -> None:
+    """Chunked-prefill / verify attention: sequence b's queries (rows q_start[b] ..
+    q_start[b+1]-1 of q) are the last positions of its seq_lens[b] cached tokens."""
+    lib = load()
+    kvd = _kv_dtype(k_cache)
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(q_start, torch.int32, "q_start", 1)
+    nb, hkv, bs, d = k_cache.shape
+    B, M = block_tables.shape
+    if out.shape != q.shape or q.shape[2] != d or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
+        raise ValueError("shape mismatch between q, out, caches, tables, lengths and q_start")
+    _check(lib.pa_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                    _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _ptr(q_start), B,
+                                    q.shape[1], hkv, d, bs, M, nb, int(max_q_len), float(scale), kvd,
+                                    _stream(stream)), "pa_prefill_attention")
 
 
 def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],

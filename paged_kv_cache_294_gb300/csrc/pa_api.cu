@@ -327,18 +327,66 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
                                               static_cast<cudaStream_t>(stream)));
 }
 
+pa_status pa_prefill_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                               const int32_t* seq_lens, const int32_t* q_start, int batch, int num_q_heads,
+                               int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                               int num_blocks, int max_q_len, float scale, int kv_dtype, void* stream) {
+    if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_q_len < 0 ||
+        !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
+        return PA_ERR_INVALID;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
+    if ((int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31) return PA_ERR_INVALID;
+    if (!(scale == scale)) return PA_ERR_INVALID;
+    const int G = num_q_heads / num_kv_heads;
+    if (kv_dtype != PA_KV_BF16 || head_dim != 128 || (block_size != 16 && block_size != 32) || 128 % G != 0)
+        return PA_ERR_UNSUPPORTED;
+    if (batch > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;  // grid z / y
+    if (batch == 0 || max_q_len == 0) return PA_OK;
+    if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens || !q_start) return PA_ERR_INVALID;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(q_start) & 3u))
+        return PA_ERR_INVALID;
+    (void)k_scale;
+    (void)v_scale;
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
+    CUtensorMap tm_k, tm_v;
+    if (!encode_cache_map(k_cache, rows, head_dim, block_size, kv_dtype, &tm_k) ||
+        !encode_cache_map(v_cache, rows, head_dim, block_size, kv_dtype, &tm_v))
+        return PA_ERR_CUDA;
+    pa::PrefillLaunch L;
+    L.out = out;
+    L.q = q;
+    L.tables = block_tables;
+    L.lens = seq_lens;
+    L.q_start = q_start;
+    L.tm_k = &tm_k;
+    L.tm_v = &tm_v;
+    L.B = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.bs = block_size;
+    L.M = max_blocks_per_seq;
+    L.num_blocks = num_blocks;
+    L.max_q = max_q_len;
+    L.scale = scale;
+    return cuda_status(pa::launch_prefill(L, static_cast<cudaStream_t>(stream)));
+}
+
 pa_status pa_selftest_bounded_wait(void* stream) {
     return cuda_status(pa::launch_wait_selftest(static_cast<cudaStream_t>(stream)));
 }
 
 pa_status pa_get_device_error(uint32_t* flags, int clear) {
     if (!flags) return PA_ERR_INVALID;
-    unsigned int a = 0, d = 0;
+    unsigned int a = 0, d = 0, p = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = pa::append_unit_error(&a, clear != 0);
     if (e == cudaSuccess) e = pa::decode_unit_error(&d, clear != 0);
+    if (e == cudaSuccess) e = pa::prefill_unit_error(&p, clear != 0);
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    *flags = a | d;
+    *flags = a | d | p;
     return PA_OK;
 }
 

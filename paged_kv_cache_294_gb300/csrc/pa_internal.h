@@ -48,7 +48,21 @@ struct DecodeLaunch {
     bool fp8;
 };
 
+struct PrefillLaunch {
+    void* out;          // bf16 [total_q][Hq][d]
+    const void* q;      // bf16 [total_q][Hq][d]
+    const int32_t* tables;
+    const int32_t* lens;
+    const int32_t* q_start;   // [B + 1]
+    const CUtensorMap* tm_k;
+    const CUtensorMap* tm_v;
+    int B, Hq, Hkv, bs, M, num_blocks, max_q;
+    float scale;
+};
+
 cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream);
+cudaError_t prefill_unit_error(unsigned int* v, bool clear);
 cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(cudaStream_t stream);

@@ -1,0 +1,494 @@
+// Multi-query attention over the paged KV cache on the 5th-generation tensor
+// cores: the queries of a prefill chunk ("KV cache & continuous batching",
+// section "3. Chunked prefill") or of a speculative-verification pass ("LLM
+// Serving - KV Cache, Batching, Speculative Decoding", section "Speculative
+// decoding") attend causally to the cache, which already holds the chunk's
+// own keys and values.
+//
+// One CTA computes one tile of 128 query rows of one (sequence, kv head):
+// with G query heads per kv head a row is a (token, head) pair, row =
+// token * G + head, so the G heads share every K/V tile.  KV is walked in
+// tiles of 128 tokens (128 / block_size pages, each page fetched by TMA from
+// its physical block with the 128-byte swizzle).
+//
+//   warp 0      TMA producer: K tile ring (2) and V tile ring (2)
+//   warp 1      owns the tensor memory; one lane issues tcgen05.mma:
+//                 S[j%2] = Q K_j^T  (A = Q, K-major; B = K tile, K-major)
+//                 O     += P_j V_j  (A = P, K-major; B = V tile, MN-major)
+//   warps 2-5   softmax: thread = query row = tensor-memory lane; reads S,
+//               keeps the running max m and sum l in fp32 (log2 domain),
+//               writes P (bf16) to shared memory, rescales O in tensor
+//               memory only when the max grows by more than 2^8, and
+//               finally writes out = O / l.
+//
+// Tensor memory: S0 columns [0,128), S1 [128,256), O [256,384) (fp32).
+// Every wait is bounded; on a timeout the CTA records PA_DEVERR_TIMEOUT,
+// drains its own copies and MMAs, frees the tensor memory and ends.
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int D = 128;                 // head_dim
+constexpr int TN = 128;                // KV tokens per tile
+constexpr int TM = 128;                // query rows per CTA
+constexpr int HALF = TN * 128;         // one 64-column half of a 128-row tile (bytes)
+constexpr int TILEB = 2 * HALF;        // a 128 x 128 bf16 tile (32 KB)
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + TILEB;   // 2 K tiles
+constexpr int OFF_V = OFF_K + 2 * TILEB;
+constexpr int OFF_P = OFF_V + 2 * TILEB;
+constexpr int SMEM_TILES = OFF_P + TILEB;   // 192 KB
+constexpr int SMEM_BYTES = SMEM_TILES + 1024;
+constexpr int NTHREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t COL_O = 256;
+constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 256)
+
+struct PrefillArgs {
+    __nv_bfloat16* out;
+    const __nv_bfloat16* q;
+    const int32_t* tables;
+    const int32_t* lens;
+    const int32_t* q_start;
+    int Hq, Hkv, G, M, num_blocks, max_q;
+    float scale_log2;
+};
+
+struct Bars {
+    uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+    uint64_t q_full, s_full[2], s_free[2], p_full, o_done, drain;
+    uint32_t kbad[2], vbad[2];   // pages of the stage whose block id was out of range
+    uint32_t tmem_base;
+    int abort;
+};
+
+// ------------------------------------------------------------------ tcgen05
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    // shared-memory matrix descriptor: start >> 4, leading / stride byte
+    // offsets >> 4, descriptor version 1, 128-byte swizzle
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator,
+// A K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), M x N
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+           ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
+// Bounded wait that also gives up once another role of the CTA has aborted.
+__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t polls = 1; polls < (1u << 30); ++polls) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((polls & 63u) == 0) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+        }
+    }
+    raise_error(PA_DEVERR_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+
+// Rows [r0, TN) of both 64-column halves of a tile, and every row of the
+// pages flagged in `bad`, set to zero (generic stores; one warp).
+__device__ __forceinline__ void zero_tile_rows(uint32_t tile, int r0, uint32_t bad, int bs, int lane) {
+    for (int row = r0 + (lane >> 3); row < TN; row += 4)
+        for (int hh = 0; hh < 2; ++hh) st_shared_v4(tile + hh * HALF + row * 128 + (lane & 7) * 16, 0, 0, 0, 0);
+    while (bad) {
+        const int pg = __ffs(bad) - 1;
+        bad &= bad - 1;
+        for (int row = pg * bs + (lane >> 3); row < (pg + 1) * bs; row += 4)
+            for (int hh = 0; hh < 2; ++hh)
+                st_shared_v4(tile + hh * HALF + row * 128 + (lane & 7) * 16, 0, 0, 0, 0);
+    }
+}
+
+template <int BS>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                         const PrefillArgs a) {
+    constexpr int PPT = TN / BS;  // pages per KV tile
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ Bars bars;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // later (longer) query tiles first
+    const int G = a.G, T = TM / G;
+
+    // ---- this tile's work (uniform over the CTA)
+    const int qs0 = a.q_start[b];
+    const int C = a.q_start[b + 1] - qs0;
+    const int L = a.lens[b];
+    if (C < 0 || C > L || L > a.M * BS || C > a.max_q) {
+        if (tid == 0 && h == 0 && qt == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        return;
+    }
+    const int t0 = qt * T;
+    if (t0 >= C) return;
+    const int tv = min(T, C - t0);              // valid query tokens in the tile
+    const int nkv = L - C + t0 + tv;            // KV positions needed: 0 .. nkv-1
+    const int nT = (nkv + TN - 1) / TN;
+    const int npages = (nkv + BS - 1) / BS;
+    const int32_t* table = a.tables + (int64_t)b * a.M;
+    volatile int* abort = &bars.abort;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.kfull[i], 1);
+            mbar_init(&bars.kempty[i], 1);
+            mbar_init(&bars.vfull[i], 1);
+            mbar_init(&bars.vempty[i], 1);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.s_free[i], 128);
+        }
+        mbar_init(&bars.q_full, 128);
+        mbar_init(&bars.p_full, 128);
+        mbar_init(&bars.o_done, 1);
+        mbar_init(&bars.drain, 1);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
+            int issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};   // last tile loaded per stage
+            for (int j = 0; j < nT; ++j) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                const int p0 = j * PPT, pn = min(PPT, npages - p0);
+                int ids[PPT];
+                uint32_t bad = 0;
+                int nvalid = 0;
+#pragma unroll
+                for (int i = 0; i < PPT; ++i) {
+                    ids[i] = -1;
+                    if (i < pn) {
+                        const int id = table[p0 + i];
+                        if (id >= 0 && id < a.num_blocks) {
+                            ids[i] = id;
+                            ++nvalid;
+                        } else {
+                            bad |= 1u << i;
+                        }
+                    }
+                }
+                if (bad) raise_error(PA_DEVERR_BLOCK_ID);
+                const uint32_t bytes = (uint32_t)nvalid * 2u * BS * 128u;
+                // K tile
+                if (!cta_wait(&bars.kempty[s], ph ^ 1, abort)) break;
+                bars.kbad[s] = bad;
+                mbar_arrive_expect_tx(&bars.kfull[s], bytes);
+                const uint32_t kt = sbase + OFF_K + s * TILEB;
+#pragma unroll
+                for (int i = 0; i < PPT; ++i)
+                    if (ids[i] >= 0) {
+                        const int y = (ids[i] * a.Hkv + h) * BS;
+                        tma_load_2d_at(kt + i * BS * 128, &tm_k, 0, y, &bars.kfull[s]);
+                        tma_load_2d_at(kt + HALF + i * BS * 128, &tm_k, 64, y, &bars.kfull[s]);
+                    }
+                issued_k[s] = j;
+                // V tile
+                if (!cta_wait(&bars.vempty[s], ph ^ 1, abort)) break;
+                bars.vbad[s] = bad;
+                mbar_arrive_expect_tx(&bars.vfull[s], bytes);
+                const uint32_t vt = sbase + OFF_V + s * TILEB;
+#pragma unroll
+                for (int i = 0; i < PPT; ++i)
+                    if (ids[i] >= 0) {
+                        const int y = (ids[i] * a.Hkv + h) * BS;
+                        tma_load_2d_at(vt + i * BS * 128, &tm_v, 0, y, &bars.vfull[s]);
+                        tma_load_2d_at(vt + HALF + i * BS * 128, &tm_v, 64, y, &bars.vfull[s]);
+                    }
+                issued_v[s] = j;
+            }
+            if (*abort) {
+                // let this CTA's own copies land before it ends
+                for (int s = 0; s < 2; ++s) {
+                    if (issued_k[s] >= 0) mbar_wait(&bars.kfull[s], (issued_k[s] >> 1) & 1);
+                    if (issued_v[s] >= 0) mbar_wait(&bars.vfull[s], (issued_v[s] >> 1) & 1);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
+        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
+        const uint32_t sq = sbase + OFF_Q, sp = sbase + OFF_P;
+        bool ok = cta_wait(&bars.q_full, 0, abort);
+        tc_fence_after();
+        for (int j = 0; ok && j <= nT; ++j) {
+            if (j < nT) {
+                const int s = j & 1;
+                const uint32_t ph = (j >> 1) & 1;
+                if (!(ok = cta_wait(&bars.kfull[s], ph, abort))) break;
+                const uint32_t kt = sbase + OFF_K + s * TILEB;
+                const uint32_t kbad = bars.kbad[s];
+                if (kbad) {
+                    zero_tile_rows(kt, TN, kbad, BS, lane);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (!(ok = cta_wait(&bars.s_free[s], ph ^ 1, abort))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t d_tmem = tmem + (uint32_t)s * TN;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
+                        umma(d_tmem, smem_desc(sq + off, 16, 1024), smem_desc(kt + off, 16, 1024), ID_S, kk > 0);
+                    }
+                    umma_commit(&bars.s_full[s]);
+                    umma_commit(&bars.kempty[s]);
+                }
+                __syncwarp();
+            }
+            if (j > 0) {
+                const int jj = j - 1, s = jj & 1;
+                if (!(ok = cta_wait(&bars.vfull[s], (jj >> 1) & 1, abort))) break;
+                const uint32_t vt = sbase + OFF_V + s * TILEB;
+                const int rz = (jj == nT - 1) ? nkv - jj * TN : TN;   // rows past the last needed position
+                const uint32_t vbad = bars.vbad[s];
+                if (rz < TN || vbad) {
+                    zero_tile_rows(vt, rz, vbad, BS, lane);
+                    fence_proxy_async_smem();
+                }
+                __syncwarp();
+                if (!(ok = cta_wait(&bars.p_full, jj & 1, abort))) break;
+                tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < TN / 16; ++kk) {
+                        const uint32_t pa_off = (kk >> 2) * HALF + (kk & 3) * 32;
+                        umma(tmem + COL_O, smem_desc(sp + pa_off, 16, 1024), smem_desc(vt + kk * 2048, HALF, 1024),
+                             ID_O, (jj > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    umma_commit(&bars.o_done);
+                    umma_commit(&bars.vempty[s]);
+                }
+                __syncwarp();
+            }
+        }
+        // every MMA this thread issued has completed before the CTA frees the tensor memory
+        if (lane == 0) {
+            umma_commit(&bars.drain);
+            mbar_wait(&bars.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;             // query row = tensor-memory lane
+        const int tok = t0 + r / G, g = r % G;
+        const bool valid_row = tok < C;
+        const int qpos = valid_row ? L - C + tok : -1;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        {
+            // Q row -> shared memory, 128-byte swizzled
+            const uint32_t sq = sbase + OFF_Q;
+            const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D);
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid_row) v = __ldg(src + u);
+                st_shared_v4(sq + (u >> 3) * HALF + r * 128 + (((u & 7) ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars.q_full);
+        }
+        const uint32_t sp = sbase + OFF_P;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nT; ++j) {
+            const int s = j & 1;
+            if (!(ok = cta_wait(&bars.s_full[s], (j >> 1) & 1, abort))) break;
+            tc_fence_after();
+            float x[TN];
+#pragma unroll
+            for (int c = 0; c < TN; c += 32) tmem_ld32(tmem + lane_off + s * TN + c, &x[c]);
+            tc_fence_before();
+            mbar_arrive(&bars.s_free[s]);
+            const int kb = j * TN;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < TN; ++c) {
+                x[c] = (kb + c <= qpos) ? x[c] * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, x[c]);
+            }
+            const float m_new = fmaxf(m, mx);
+            if (j > 0) {
+                if (!(ok = cta_wait(&bars.o_done, (j - 1) & 1, abort))) break;
+                tc_fence_after();
+            }
+            if (m_new > m + RESCALE_LOG2) {
+                if (j > 0 && m != -INFINITY) {
+                    const float alpha = exp2f(m - m_new);
+                    l *= alpha;
+#pragma unroll 1
+                    for (int c = 0; c < D; c += 32) {
+                        float o[32];
+                        tmem_ld32(tmem + lane_off + COL_O + c, o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tmem_st32(tmem + lane_off + COL_O + c, o);
+                    }
+                }
+                m = m_new;
+            }
+#pragma unroll
+            for (int c = 0; c < TN; c += 8) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float p0 = (x[c + 2 * e] == -INFINITY) ? 0.f : exp2f(x[c + 2 * e] - m);
+                    const float p1 = (x[c + 2 * e + 1] == -INFINITY) ? 0.f : exp2f(x[c + 2 * e + 1] - m);
+                    l += p0 + p1;
+                    w[e] = pack_bf16x2(p0, p1);
+                }
+                const int u = (c & 63) >> 3;
+                st_shared_v4(sp + (c >> 6) * HALF + r * 128 + ((u ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars.p_full);
+        }
+        if (ok && cta_wait(&bars.o_done, (nT - 1) & 1, abort)) {
+            tc_fence_after();
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D);
+#pragma unroll 1
+            for (int c = 0; c < D; c += 32) {
+                float o[32];
+                tmem_ld32(tmem + lane_off + COL_O + c, o);
+                if (valid_row) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[c / 8 + v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                                    pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                                    pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                                    pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+template <int BS>
+cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
+    static bool attr_set[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(paged_prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    PrefillArgs a;
+    a.out = static_cast<__nv_bfloat16*>(L.out);
+    a.q = static_cast<const __nv_bfloat16*>(L.q);
+    a.tables = L.tables;
+    a.lens = L.lens;
+    a.q_start = L.q_start;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.G = L.Hq / L.Hkv;
+    a.M = L.M;
+    a.num_blocks = L.num_blocks;
+    a.max_q = L.max_q;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    const int T = TM / a.G;
+    dim3 grid((unsigned)((L.max_q + T - 1) / T), (unsigned)L.Hkv, (unsigned)L.B);
+    paged_prefill_kernel<BS><<<grid, NTHREADS, SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
+    if (L.bs == 16) return launch_typed<16>(L, stream);
+    if (L.bs == 32) return launch_typed<32>(L, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t prefill_unit_error(unsigned int* v, bool clear) { return read_unit_error(v, clear); }
+
+}  // namespace pa

@@ -455,6 +455,45 @@ def serving_scenario(layer: str = "8b", R: int = 6, n_forks: int = 2, steps: int
                            v_pre=v_pre, forks=forks, tokens=tokens, q=q, k_new=k_new, v_new=v_new)
 
 
+@dataclasses.dataclass
+class PrefillWorkload(Workload):
+    """A decode-shaped workload whose last C_b tokens per sequence are a query
+    chunk: q_chunk [q_start[-1], Hq, d], sequence b's rows from q_start[b].
+    The history (fill_*) covers every position, the chunk's included."""
+    q_chunk: Optional[torch.Tensor] = None
+    q_start: Optional[np.ndarray] = None
+    max_q: int = 0
+
+
+def make_prefill(layer: str, ctx: List[int], chunk: List[int], seed: int = 11, device="cpu",
+                 Hq: Optional[int] = None, Hkv: Optional[int] = None, bs: Optional[int] = None) -> PrefillWorkload:
+    """Sequences with ctx[b] earlier tokens and a chunk of chunk[b] query tokens
+    (seq_len = ctx + chunk) on one layer's shape (bf16 cache), tables from a
+    seeded permutation of the pool."""
+    cfg = dict(CONFIGS[layer])
+    Hq = cfg["Hq"] if Hq is None else Hq
+    Hkv = cfg["Hkv"] if Hkv is None else Hkv
+    bs = cfg["bs"] if bs is None else bs
+    d = cfg["d"]
+    lens = (np.asarray(ctx, dtype=np.int64) + np.asarray(chunk, dtype=np.int64)).astype(np.int32)
+    B = len(lens)
+    M = max(1, int(max(-(-int(n) // bs) for n in lens)))
+    blocks = int(sum(-(-int(n) // bs) for n in lens))
+    num_blocks = max(blocks + 8, 64)
+    rng = _np_rng(seed, _S_TABLES)
+    tables = _tables_from_perm(lens, bs, M, rng.permutation(num_blocks).astype(np.int32))
+    fs, fp = _history(lens + 1)          # every position 0 .. len-1, the chunk's too
+    vals = _values(seed, len(fs), B, Hq, Hkv, d, device)
+    q_start = np.concatenate([[0], np.cumsum(np.asarray(chunk, dtype=np.int64))]).astype(np.int32)
+    q_chunk = randn_bf16((int(q_start[-1]), Hq, d), seed, 40, device)
+    return PrefillWorkload(name="prefill-" + layer, Hq=Hq, Hkv=Hkv, d=d, bs=bs, kv="bf16", B=B,
+                           num_blocks=num_blocks, M=M, scale=1.0 / math.sqrt(d), seq_lens=lens,
+                           block_tables=tables, trace=None, target_rids=None, fill_seq=fs, fill_pos=fp,
+                           desc="prefill chunks %s over contexts %s" % (list(chunk)[:4], list(ctx)[:4]),
+                           q_chunk=q_chunk, q_start=q_start, max_q=int(max(chunk) if len(chunk) else 0),
+                           **vals)
+
+
 def roofline_bytes(w: Workload) -> dict:
     """Bytes the step must move at minimum: K/V history read once, q read, out written.
 
