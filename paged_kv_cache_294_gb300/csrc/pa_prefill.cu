@@ -15,11 +15,11 @@
 //   warp 1      owns the tensor memory; one lane issues tcgen05.mma:
 //                 S[j%2] = Q K_j^T  (A = Q, K-major; B = K tile, K-major)
 //                 O     += P_j V_j  (A = P, K-major; B = V tile, MN-major)
-//   warps 2-5   softmax: thread = query row = tensor-memory lane; reads S,
-//               keeps the running max m and sum l in fp32 (log2 domain),
-//               writes P (bf16) to shared memory, rescales O in tensor
-//               memory only when the max grows by more than 2^8, and
-//               finally writes out = O / l.
+//   warps 2-9   softmax: a thread holds one query row (its tensor-memory
+//               lane) and one 64-column half of it; keeps the running max
+//               m and sum l in fp32 (log2 domain), writes P (bf16) to shared
+//               memory, rescales O in tensor memory only when the max grows
+//               by more than 2^8, and finally writes out = O / l.
 //
 // Tensor memory: S0 columns [0,128), S1 [128,256), O [256,384) (fp32).
 // Every wait is bounded; on a timeout the CTA records PA_DEVERR_TIMEOUT,
@@ -41,7 +41,8 @@ constexpr int OFF_V = OFF_K + 2 * TILEB;
 constexpr int OFF_P = OFF_V + 2 * TILEB;
 constexpr int SMEM_TILES = OFF_P + TILEB;   // 192 KB
 constexpr int SMEM_BYTES = SMEM_TILES + 1024;
-constexpr int NTHREADS = 192;
+constexpr int NTHREADS = 320;             // producer, MMA, 8 softmax warps
+constexpr int NSOFT = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 256)
@@ -59,6 +60,9 @@ struct PrefillArgs {
 struct Bars {
     uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
     uint64_t q_full, s_full[2], s_free[2], p_full, o_done, drain;
+    uint64_t pair[4];            // the two softmax warps of a lane quadrant
+    float red[2][2][128];        // partial row maxima [tile parity][half][row]
+    float red_l[2][128];         // partial row sums [half][row]
     uint32_t kbad[2], vbad[2];   // pages of the stage whose block id was out of range
     uint32_t tmem_base;
     int abort;
@@ -122,6 +126,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
         "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 2^x on the special-function unit (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
@@ -196,10 +207,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bars.vfull[i], 1);
             mbar_init(&bars.vempty[i], 1);
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.s_free[i], 128);
+            mbar_init(&bars.s_free[i], NSOFT);
         }
-        mbar_init(&bars.q_full, 128);
-        mbar_init(&bars.p_full, 128);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 64);
+        mbar_init(&bars.q_full, NSOFT);
+        mbar_init(&bars.p_full, NSOFT);
         mbar_init(&bars.o_done, 1);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
@@ -347,96 +359,117 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        const int quad = warp & 3;
-        const int r = quad * 32 + lane;             // query row = tensor-memory lane
+        // warps 2..9: quad = warp % 4 selects the tensor-memory lanes (query
+        // rows) the warp may access; hf selects the 64-column half of S, P
+        // and O it handles.  The two warps of a quad exchange their partial
+        // row maxima (and, at the end, row sums) through shared memory.
+        const int quad = warp & 3, hf = (warp - 2) >> 2;
+        const int r = quad * 32 + lane;
         const int tok = t0 + r / G, g = r % G;
         const bool valid_row = tok < C;
         const int qpos = valid_row ? L - C + tok : -1;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         {
-            // Q row -> shared memory, 128-byte swizzled
-            const uint32_t sq = sbase + OFF_Q;
-            const uint4* src = reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D);
+            // this half of the Q row -> shared memory, 128-byte swizzled
+            const uint32_t sq = sbase + OFF_Q + hf * HALF;
+            const uint4* src =
+                reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + hf * 8;
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
+            for (int u = 0; u < 8; ++u) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid_row) v = __ldg(src + u);
-                st_shared_v4(sq + (u >> 3) * HALF + r * 128 + (((u & 7) ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+                st_shared_v4(sq + r * 128 + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars.q_full);
         }
-        const uint32_t sp = sbase + OFF_P;
-        float m = -INFINITY, l = 0.f;
+        const uint32_t sp = sbase + OFF_P + hf * HALF;
+        const float sl2 = a.scale_log2;
+        float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this half's sum
         bool ok = true;
         for (int j = 0; j < nT; ++j) {
             const int s = j & 1;
             if (!(ok = cta_wait(&bars.s_full[s], (j >> 1) & 1, abort))) break;
             tc_fence_after();
-            float x[TN];
-#pragma unroll
-            for (int c = 0; c < TN; c += 32) tmem_ld32(tmem + lane_off + s * TN + c, &x[c]);
+            float x[64];
+            tmem_ld32(tmem + lane_off + s * TN + hf * 64, &x[0]);
+            tmem_ld32(tmem + lane_off + s * TN + hf * 64 + 32, &x[32]);
             tc_fence_before();
             mbar_arrive(&bars.s_free[s]);
-            const int kb = j * TN;
-            float mx = -INFINITY;
+            const int lim = qpos - j * TN - hf * 64;   // columns c <= lim are visible to this row
+            if (lim < 63) {
 #pragma unroll
-            for (int c = 0; c < TN; ++c) {
-                x[c] = (kb + c <= qpos) ? x[c] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, x[c]);
+                for (int c = 0; c < 64; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
             }
-            const float m_new = fmaxf(m, mx);
+            float mx8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            const float mxs = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+            bars.red[j & 1][hf][r] = mxs;
+            mbar_arrive(&bars.pair[quad]);
+            if (!(ok = cta_wait(&bars.pair[quad], j & 1, abort))) break;
+            const float m_new = fmaxf(m, fmaxf(mxs, bars.red[j & 1][hf ^ 1][r]));
+            const bool rescale = m_new > m + RESCALE_LOG2;
+            const float m_next = rescale ? m_new : m;
+            const float mb = (m_next == -INFINITY) ? 0.f : m_next;
+            uint32_t w[32];
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                const float p0 = ex2(fmaf(x[c], sl2, -mb));
+                const float p1 = ex2(fmaf(x[c + 1], sl2, -mb));
+                ls[(c >> 1) & 3] += p0 + p1;
+                w[c >> 1] = pack_bf16x2(p0, p1);
+            }
             if (j > 0) {
+                // P_{j-1} V_{j-1} has finished: O is stable and the P buffer is free
                 if (!(ok = cta_wait(&bars.o_done, (j - 1) & 1, abort))) break;
                 tc_fence_after();
             }
-            if (m_new > m + RESCALE_LOG2) {
-                if (j > 0 && m != -INFINITY) {
-                    const float alpha = exp2f(m - m_new);
-                    l *= alpha;
-#pragma unroll 1
-                    for (int c = 0; c < D; c += 32) {
-                        float o[32];
-                        tmem_ld32(tmem + lane_off + COL_O + c, o);
+            if (rescale && m != -INFINITY) {
+                const float alpha = ex2(m - m_new);
+                l *= alpha;
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tmem_st32(tmem + lane_off + COL_O + c, o);
-                    }
+                for (int c = 0; c < 64; c += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_off + COL_O + hf * 64 + c, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(tmem + lane_off + COL_O + hf * 64 + c, o);
                 }
-                m = m_new;
             }
+            m = m_next;
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
 #pragma unroll
-            for (int c = 0; c < TN; c += 8) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = (x[c + 2 * e] == -INFINITY) ? 0.f : exp2f(x[c + 2 * e] - m);
-                    const float p1 = (x[c + 2 * e + 1] == -INFINITY) ? 0.f : exp2f(x[c + 2 * e + 1] - m);
-                    l += p0 + p1;
-                    w[e] = pack_bf16x2(p0, p1);
-                }
-                const int u = (c & 63) >> 3;
-                st_shared_v4(sp + (c >> 6) * HALF + r * 128 + ((u ^ (r & 7)) << 4), w[0], w[1], w[2], w[3]);
-            }
+            for (int u = 0; u < 8; ++u)
+                st_shared_v4(sp + r * 128 + ((u ^ (r & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bars.p_full);
         }
         if (ok && cta_wait(&bars.o_done, (nT - 1) & 1, abort)) {
             tc_fence_after();
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D);
-#pragma unroll 1
-            for (int c = 0; c < D; c += 32) {
-                float o[32];
-                tmem_ld32(tmem + lane_off + COL_O + c, o);
-                if (valid_row) {
+            bars.red_l[hf][r] = l;
+            mbar_arrive(&bars.pair[quad]);
+            if (cta_wait(&bars.pair[quad], nT & 1, abort)) {
+                const float lt = l + bars.red_l[hf ^ 1][r];
+                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + hf * 8;
 #pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[c / 8 + v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                                    pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                                    pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                                    pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                for (int c = 0; c < 64; c += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_off + COL_O + hf * 64 + c, o);
+                    if (valid_row) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            dst[c / 8 + v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                    }
                 }
             }
         }
