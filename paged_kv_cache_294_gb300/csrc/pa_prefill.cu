@@ -11,19 +11,23 @@
 // tiles of 128 tokens (128 / block_size pages, each page fetched by TMA from
 // its physical block with the 128-byte swizzle).
 //
-//   warp 0      TMA producer: K tile ring (2) and V tile ring (2)
+//   warp 0      TMA producer of the K tile ring (3 stages)
+//   warp 10     TMA producer of the V tile ring (2 stages)
 //   warp 1      owns the tensor memory; one lane issues tcgen05.mma:
-//                 S[j%2] = Q K_j^T  (A = Q, K-major; B = K tile, K-major)
-//                 O     += P_j V_j  (A = P, K-major; B = V tile, MN-major)
+//                 S[j%2] = Q K_j^T  (A = Q in shared memory, K-major;
+//                                    B = K tile, K-major)
+//                 O     += P_j V_j  (A = P[j%2] in tensor memory;
+//                                    B = V tile, MN-major)
 //   warps 2-9   softmax: a thread holds one query row (its tensor-memory
 //               lane) and one 64-column half of it; keeps the running max
-//               m and sum l in fp32 (log2 domain), writes P (bf16) to shared
-//               memory, rescales O in tensor memory only when the max grows
-//               by more than 2^8, and finally writes out = O / l.
+//               m and sum l in fp32 (log2 domain), writes P (bf16) into
+//               tensor memory, rescales O only when the max grows by more
+//               than 2^8, and finally writes out = O / l.
 //
-// Tensor memory: S0 columns [0,128), S1 [128,256), O [256,384) (fp32).
-// Every wait is bounded; on a timeout the CTA records PA_DEVERR_TIMEOUT,
-// drains its own copies and MMAs, frees the tensor memory and ends.
+// Tensor memory (fp32 columns): S0 [0,128), S1 [128,256), O [256,384),
+// P0 [384,448), P1 [448,512) (P as bf16 pairs).  Every wait is bounded; on a
+// timeout the CTA records PA_DEVERR_TIMEOUT, drains its own copies and MMAs,
+// frees the tensor memory and ends.
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -35,16 +39,18 @@ constexpr int TN = 128;                // KV tokens per tile
 constexpr int TM = 128;                // query rows per CTA
 constexpr int HALF = TN * 128;         // one 64-column half of a 128-row tile (bytes)
 constexpr int TILEB = 2 * HALF;        // a 128 x 128 bf16 tile (32 KB)
+constexpr int KST = 3;                 // K tile stages
+constexpr int VST = 2;                 // V tile stages
 constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILEB;   // 2 K tiles
-constexpr int OFF_V = OFF_K + 2 * TILEB;
-constexpr int OFF_P = OFF_V + 2 * TILEB;
-constexpr int SMEM_TILES = OFF_P + TILEB;   // 192 KB
+constexpr int OFF_K = OFF_Q + TILEB;
+constexpr int OFF_V = OFF_K + KST * TILEB;
+constexpr int SMEM_TILES = OFF_V + VST * TILEB;   // 192 KB
 constexpr int SMEM_BYTES = SMEM_TILES + 1024;
-constexpr int NTHREADS = 320;             // producer, MMA, 8 softmax warps
+constexpr int NTHREADS = 352;          // K producer, MMA, 8 softmax warps, V producer
 constexpr int NSOFT = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
+constexpr uint32_t COL_P = 384;        // two 64-column P buffers
 constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 256)
 
 struct PrefillArgs {
@@ -58,12 +64,12 @@ struct PrefillArgs {
 };
 
 struct Bars {
-    uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
-    uint64_t q_full, s_full[2], s_free[2], p_full, o_done, drain;
+    uint64_t kfull[KST], kempty[KST], vfull[VST], vempty[VST];
+    uint64_t q_full, s_full[2], s_free[2], p_full[2], o_done[2], drain;
     uint64_t pair[4];            // the two softmax warps of a lane quadrant
     float red[2][2][128];        // partial row maxima [tile parity][half][row]
     float red_l[2][128];         // partial row sums [half][row]
-    uint32_t kbad[2], vbad[2];   // pages of the stage whose block id was out of range
+    uint32_t kbad[KST], vbad[VST];   // pages of the stage whose block id was out of range
     uint32_t tmem_base;
     int abort;
 };
@@ -91,6 +97,15 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         : "memory");
 }
 
+// the same with the A operand (M x K, bf16 pairs along the columns) in tensor memory
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
@@ -114,6 +129,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
@@ -201,18 +228,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     volatile int* abort = &bars.abort;
 
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < KST; ++i) {
             mbar_init(&bars.kfull[i], 1);
             mbar_init(&bars.kempty[i], 1);
+        }
+        for (int i = 0; i < VST; ++i) {
             mbar_init(&bars.vfull[i], 1);
             mbar_init(&bars.vempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
             mbar_init(&bars.s_free[i], NSOFT);
+            mbar_init(&bars.p_full[i], NSOFT);
+            mbar_init(&bars.o_done[i], 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 64);
         mbar_init(&bars.q_full, NSOFT);
-        mbar_init(&bars.p_full, NSOFT);
-        mbar_init(&bars.o_done, 1);
         mbar_init(&bars.drain, 1);
         bars.abort = 0;
         fence_mbar_init();
@@ -229,124 +260,128 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == 10) {
+        // ------------------------------------------------------------ producers
+        // warp 0 fills the K ring, warp 10 the V ring; each reads the block
+        // ids of its next tile one tile ahead
         if (lane == 0) {
-            prefetch_tensormap(&tm_k);
-            prefetch_tensormap(&tm_v);
-            int issued_k[2] = {-1, -1}, issued_v[2] = {-1, -1};   // last tile loaded per stage
+            const bool is_k = warp == 0;
+            const int NS = is_k ? KST : VST;
+            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+            uint64_t* full = is_k ? bars.kfull : bars.vfull;
+            uint64_t* empty = is_k ? bars.kempty : bars.vempty;
+            uint32_t* badw = is_k ? bars.kbad : bars.vbad;
+            const uint32_t ring = sbase + (is_k ? OFF_K : OFF_V);
+            prefetch_tensormap(map);
+            int issued[KST] = {-1, -1, -1};   // last tile loaded into each stage
+            int nxt[PPT];
+#pragma unroll
+            for (int i = 0; i < PPT; ++i) nxt[i] = (i < npages) ? table[i] : -1;
+            int st = 0, use = 0;              // stage of tile j, and how often it was used before
             for (int j = 0; j < nT; ++j) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                const int p0 = j * PPT, pn = min(PPT, npages - p0);
+                const int pn = min(PPT, npages - j * PPT);
                 int ids[PPT];
+#pragma unroll
+                for (int i = 0; i < PPT; ++i) ids[i] = nxt[i];
+                if (j + 1 < nT) {
+                    const int p1 = (j + 1) * PPT;
+#pragma unroll
+                    for (int i = 0; i < PPT; ++i) nxt[i] = (p1 + i < npages) ? table[p1 + i] : -1;
+                }
                 uint32_t bad = 0;
                 int nvalid = 0;
 #pragma unroll
                 for (int i = 0; i < PPT; ++i) {
-                    ids[i] = -1;
-                    if (i < pn) {
-                        const int id = table[p0 + i];
-                        if (id >= 0 && id < a.num_blocks) {
-                            ids[i] = id;
-                            ++nvalid;
-                        } else {
-                            bad |= 1u << i;
-                        }
+                    if (i >= pn) {
+                        ids[i] = -1;
+                    } else if (ids[i] >= 0 && ids[i] < a.num_blocks) {
+                        ++nvalid;
+                    } else {
+                        ids[i] = -1;
+                        bad |= 1u << i;
                     }
                 }
-                if (bad) raise_error(PA_DEVERR_BLOCK_ID);
-                const uint32_t bytes = (uint32_t)nvalid * 2u * BS * 128u;
-                // K tile
-                if (!cta_wait(&bars.kempty[s], ph ^ 1, abort)) break;
-                bars.kbad[s] = bad;
-                mbar_arrive_expect_tx(&bars.kfull[s], bytes);
-                const uint32_t kt = sbase + OFF_K + s * TILEB;
+                if (bad && is_k) raise_error(PA_DEVERR_BLOCK_ID);
+                if (!cta_wait(&empty[st], (use & 1) ^ 1, abort)) break;
+                badw[st] = bad;
+                mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
+                const uint32_t dst = ring + st * TILEB;
 #pragma unroll
                 for (int i = 0; i < PPT; ++i)
                     if (ids[i] >= 0) {
                         const int y = (ids[i] * a.Hkv + h) * BS;
-                        tma_load_2d_at(kt + i * BS * 128, &tm_k, 0, y, &bars.kfull[s]);
-                        tma_load_2d_at(kt + HALF + i * BS * 128, &tm_k, 64, y, &bars.kfull[s]);
+                        tma_load_2d_at(dst + i * BS * 128, map, 0, y, &full[st]);
+                        tma_load_2d_at(dst + HALF + i * BS * 128, map, 64, y, &full[st]);
                     }
-                issued_k[s] = j;
-                // V tile
-                if (!cta_wait(&bars.vempty[s], ph ^ 1, abort)) break;
-                bars.vbad[s] = bad;
-                mbar_arrive_expect_tx(&bars.vfull[s], bytes);
-                const uint32_t vt = sbase + OFF_V + s * TILEB;
-#pragma unroll
-                for (int i = 0; i < PPT; ++i)
-                    if (ids[i] >= 0) {
-                        const int y = (ids[i] * a.Hkv + h) * BS;
-                        tma_load_2d_at(vt + i * BS * 128, &tm_v, 0, y, &bars.vfull[s]);
-                        tma_load_2d_at(vt + HALF + i * BS * 128, &tm_v, 64, y, &bars.vfull[s]);
-                    }
-                issued_v[s] = j;
+                issued[st] = use;
+                if (++st == NS) {
+                    st = 0;
+                    ++use;
+                }
             }
             if (*abort) {
                 // let this CTA's own copies land before it ends
-                for (int s = 0; s < 2; ++s) {
-                    if (issued_k[s] >= 0) mbar_wait(&bars.kfull[s], (issued_k[s] >> 1) & 1);
-                    if (issued_v[s] >= 0) mbar_wait(&bars.vfull[s], (issued_v[s] >> 1) & 1);
-                }
+                for (int i = 0; i < NS; ++i)
+                    if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
         constexpr uint32_t ID_O = instr_desc(TM, D, 1);
-        const uint32_t sq = sbase + OFF_Q, sp = sbase + OFF_P;
+        const uint32_t sq = sbase + OFF_Q;
         bool ok = cta_wait(&bars.q_full, 0, abort);
         tc_fence_after();
+        int ks = 0, kuse = 0;   // K stage of tile j and its use count
         for (int j = 0; ok && j <= nT; ++j) {
             if (j < nT) {
-                const int s = j & 1;
-                const uint32_t ph = (j >> 1) & 1;
-                if (!(ok = cta_wait(&bars.kfull[s], ph, abort))) break;
-                const uint32_t kt = sbase + OFF_K + s * TILEB;
-                const uint32_t kbad = bars.kbad[s];
+                const int sb = j & 1;
+                if (!(ok = cta_wait(&bars.kfull[ks], kuse & 1, abort))) break;
+                const uint32_t kt = sbase + OFF_K + ks * TILEB;
+                const uint32_t kbad = bars.kbad[ks];
                 if (kbad) {
                     zero_tile_rows(kt, TN, kbad, BS, lane);
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (!(ok = cta_wait(&bars.s_free[s], ph ^ 1, abort))) break;
+                if (!(ok = cta_wait(&bars.s_free[sb], ((j >> 1) & 1) ^ 1, abort))) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t d_tmem = tmem + (uint32_t)s * TN;
+                    const uint32_t d_tmem = tmem + (uint32_t)sb * TN;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
                         umma(d_tmem, smem_desc(sq + off, 16, 1024), smem_desc(kt + off, 16, 1024), ID_S, kk > 0);
                     }
-                    umma_commit(&bars.s_full[s]);
-                    umma_commit(&bars.kempty[s]);
+                    umma_commit(&bars.s_full[sb]);
+                    umma_commit(&bars.kempty[ks]);
                 }
                 __syncwarp();
+                if (++ks == KST) {
+                    ks = 0;
+                    ++kuse;
+                }
             }
             if (j > 0) {
-                const int jj = j - 1, s = jj & 1;
-                if (!(ok = cta_wait(&bars.vfull[s], (jj >> 1) & 1, abort))) break;
-                const uint32_t vt = sbase + OFF_V + s * TILEB;
+                const int jj = j - 1, pb = jj & 1, vs = jj & 1;
+                if (!(ok = cta_wait(&bars.vfull[vs], (jj >> 1) & 1, abort))) break;
+                const uint32_t vt = sbase + OFF_V + vs * TILEB;
                 const int rz = (jj == nT - 1) ? nkv - jj * TN : TN;   // rows past the last needed position
-                const uint32_t vbad = bars.vbad[s];
+                const uint32_t vbad = bars.vbad[vs];
                 if (rz < TN || vbad) {
                     zero_tile_rows(vt, rz, vbad, BS, lane);
                     fence_proxy_async_smem();
                 }
                 __syncwarp();
-                if (!(ok = cta_wait(&bars.p_full, jj & 1, abort))) break;
+                if (!(ok = cta_wait(&bars.p_full[pb], (jj >> 1) & 1, abort))) break;
                 tc_fence_after();
                 if (lane == 0) {
 #pragma unroll
-                    for (int kk = 0; kk < TN / 16; ++kk) {
-                        const uint32_t pa_off = (kk >> 2) * HALF + (kk & 3) * 32;
-                        umma(tmem + COL_O, smem_desc(sp + pa_off, 16, 1024), smem_desc(vt + kk * 2048, HALF, 1024),
-                             ID_O, (jj > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    umma_commit(&bars.o_done);
-                    umma_commit(&bars.vempty[s]);
+                    for (int kk = 0; kk < TN / 16; ++kk)
+                        umma_ts(tmem + COL_O, tmem + COL_P + pb * 64 + kk * 8, smem_desc(vt + kk * 2048, HALF, 1024),
+                                ID_O, (jj > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars.o_done[pb]);
+                    umma_commit(&bars.vempty[vs]);
                 }
                 __syncwarp();
             }
@@ -383,7 +418,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(&bars.q_full);
         }
-        const uint32_t sp = sbase + OFF_P + hf * HALF;
         const float sl2 = a.scale_log2;
         float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this half's sum
         bool ok = true;
@@ -424,12 +458,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ls[(c >> 1) & 3] += p0 + p1;
                 w[c >> 1] = pack_bf16x2(p0, p1);
             }
-            if (j > 0) {
-                // P_{j-1} V_{j-1} has finished: O is stable and the P buffer is free
-                if (!(ok = cta_wait(&bars.o_done, (j - 1) & 1, abort))) break;
-                tc_fence_after();
-            }
             if (rescale && m != -INFINITY) {
+                // O must be stable: P_{j-1} V_{j-1} has finished
+                if (!(ok = cta_wait(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) break;
+                tc_fence_after();
                 const float alpha = ex2(m - m_new);
                 l *= alpha;
 #pragma unroll
@@ -443,14 +475,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             m = m_next;
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                st_shared_v4(sp + r * 128 + ((u ^ (r & 7)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-            fence_proxy_async_smem();
+            if (j >= 2) {
+                // P buffer j%2 is free once P_{j-2} V_{j-2} has finished
+                if (!(ok = cta_wait(&bars.o_done[s], ((j >> 1) & 1) ^ 1, abort))) break;
+                tc_fence_after();
+            }
+            tmem_st32u(tmem + lane_off + COL_P + s * 64 + hf * 32, w);
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            mbar_arrive(&bars.p_full[s]);
         }
-        if (ok && cta_wait(&bars.o_done, (nT - 1) & 1, abort)) {
+        if (ok && cta_wait(&bars.o_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, abort)) {
             tc_fence_after();
             bars.red_l[hf][r] = l;
             mbar_arrive(&bars.pair[quad]);
