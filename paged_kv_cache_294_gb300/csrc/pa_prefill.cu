@@ -12,20 +12,24 @@
 // its physical block with the 128-byte swizzle).
 //
 //   warp 0      TMA producer of the K tile ring (3 stages)
-//   warp 10     TMA producer of the V tile ring (2 stages)
-//   warp 1      owns the tensor memory; one lane issues tcgen05.mma:
-//                 S[j%2] = Q K_j^T  (A = Q in shared memory, K-major;
-//                                    B = K tile, K-major)
-//                 O     += P_j V_j  (A = P[j%2] in tensor memory;
-//                                    B = V tile, MN-major)
+//   warp 10     TMA producer of the V tile ring (3 stages)
+//   warp 1      owns the tensor memory; one lane issues S[j%2] = Q K_j^T
+//   warp 11     one lane issues O += P_j V_j
+//               (tcgen05.mma, A operand in tensor memory, B in shared
+//               memory: K tile K-major, V tile MN-major; two issuing
+//               threads because one cannot keep the tensor core busy with
+//               M=128 x N=128 instructions)
 //   warps 2-9   softmax: a thread holds one query row (its tensor-memory
 //               lane) and one 64-column half of it; keeps the running max
 //               m and sum l in fp32 (log2 domain), writes P (bf16) into
 //               tensor memory, rescales O only when the max grows by more
-//               than 2^8, and finally writes out = O / l.
+//               than 2^8, and finally writes out = O / l.  These warps
+//               also place Q in tensor memory at the start.
 //
-// Tensor memory (fp32 columns): S0 [0,128), S1 [128,256), O [256,384),
-// P0 [384,448), P1 [448,512) (P as bf16 pairs).  Every wait is bounded; on a
+// Tensor memory (32-bit columns): S0 [0,128), S1 [128,256), O [256,384)
+// in fp32; Q [384,448) and P [448,512) as bf16 pairs.  Shared memory holds
+// only the K and V rings, so the tensor core reads one operand per MMA from
+// it.  Every wait is bounded; on a
 // timeout the CTA records PA_DEVERR_TIMEOUT, drains its own copies and MMAs,
 // frees the tensor memory and ends.
 #include "pa_device.cuh"
@@ -40,17 +44,17 @@ constexpr int TM = 128;                // query rows per CTA
 constexpr int HALF = TN * 128;         // one 64-column half of a 128-row tile (bytes)
 constexpr int TILEB = 2 * HALF;        // a 128 x 128 bf16 tile (32 KB)
 constexpr int KST = 3;                 // K tile stages
-constexpr int VST = 2;                 // V tile stages
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + TILEB;
+constexpr int VST = 3;                 // V tile stages
+constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KST * TILEB;
 constexpr int SMEM_TILES = OFF_V + VST * TILEB;   // 192 KB
 constexpr int SMEM_BYTES = SMEM_TILES + 1024;
-constexpr int NTHREADS = 352;          // K producer, MMA, 8 softmax warps, V producer
+constexpr int NTHREADS = 384;          // K producer, QK issuer, 8 softmax warps, V producer, PV issuer
 constexpr int NSOFT = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
-constexpr uint32_t COL_P = 384;        // two 64-column P buffers
+constexpr uint32_t COL_Q = 384;
+constexpr uint32_t COL_P = 448;
 constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 256)
 
 struct PrefillArgs {
@@ -65,7 +69,7 @@ struct PrefillArgs {
 
 struct Bars {
     uint64_t kfull[KST], kempty[KST], vfull[VST], vempty[VST];
-    uint64_t q_full, s_full[2], s_free[2], p_full[2], o_done[2], drain;
+    uint64_t q_full, s_full[2], s_free[2], p_full, o_done, drain[2];
     uint64_t pair[4];            // the two softmax warps of a lane quadrant
     float red[2][2][128];        // partial row maxima [tile parity][half][row]
     float red_l[2][128];         // partial row sums [half][row]
@@ -89,15 +93,8 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// the same with the A operand (M x K, bf16 pairs along the columns) in tensor memory
+// D (+)= A B with the A operand (M x K, bf16 pairs along the columns) in tensor memory
+// and B described by a shared-memory matrix descriptor
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
@@ -239,12 +236,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
             mbar_init(&bars.s_free[i], NSOFT);
-            mbar_init(&bars.p_full[i], NSOFT);
-            mbar_init(&bars.o_done[i], 1);
         }
+        mbar_init(&bars.p_full, NSOFT);
+        mbar_init(&bars.o_done, 1);
         for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 64);
         mbar_init(&bars.q_full, NSOFT);
-        mbar_init(&bars.drain, 1);
+        mbar_init(&bars.drain[0], 1);
+        mbar_init(&bars.drain[1], 1);
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -326,70 +324,82 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S = Q K^T issuer
         constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
-        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
-        const uint32_t sq = sbase + OFF_Q;
+        const uint64_t kd0 = smem_desc(sbase + OFF_K, 16, 1024);   // + (byte offset >> 4) per MMA
         bool ok = cta_wait(&bars.q_full, 0, abort);
         tc_fence_after();
         int ks = 0, kuse = 0;   // K stage of tile j and its use count
-        for (int j = 0; ok && j <= nT; ++j) {
-            if (j < nT) {
-                const int sb = j & 1;
-                if (!(ok = cta_wait(&bars.kfull[ks], kuse & 1, abort))) break;
-                const uint32_t kt = sbase + OFF_K + ks * TILEB;
-                const uint32_t kbad = bars.kbad[ks];
-                if (kbad) {
-                    zero_tile_rows(kt, TN, kbad, BS, lane);
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (!(ok = cta_wait(&bars.s_free[sb], ((j >> 1) & 1) ^ 1, abort))) break;
-                tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t d_tmem = tmem + (uint32_t)sb * TN;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-                        umma(d_tmem, smem_desc(sq + off, 16, 1024), smem_desc(kt + off, 16, 1024), ID_S, kk > 0);
-                    }
-                    umma_commit(&bars.s_full[sb]);
-                    umma_commit(&bars.kempty[ks]);
-                }
-                __syncwarp();
-                if (++ks == KST) {
-                    ks = 0;
-                    ++kuse;
-                }
+        for (int j = 0; ok && j < nT; ++j) {
+            const int sb = j & 1;
+            if (!(ok = cta_wait(&bars.kfull[ks], kuse & 1, abort))) break;
+            const uint32_t kbad = bars.kbad[ks];
+            if (kbad) {
+                zero_tile_rows(sbase + OFF_K + ks * TILEB, TN, kbad, BS, lane);
+                fence_proxy_async_smem();
             }
-            if (j > 0) {
-                const int jj = j - 1, pb = jj & 1, vs = jj & 1;
-                if (!(ok = cta_wait(&bars.vfull[vs], (jj >> 1) & 1, abort))) break;
-                const uint32_t vt = sbase + OFF_V + vs * TILEB;
-                const int rz = (jj == nT - 1) ? nkv - jj * TN : TN;   // rows past the last needed position
-                const uint32_t vbad = bars.vbad[vs];
-                if (rz < TN || vbad) {
-                    zero_tile_rows(vt, rz, vbad, BS, lane);
-                    fence_proxy_async_smem();
-                }
-                __syncwarp();
-                if (!(ok = cta_wait(&bars.p_full[pb], (jj >> 1) & 1, abort))) break;
-                tc_fence_after();
-                if (lane == 0) {
+            __syncwarp();
+            if (!(ok = cta_wait(&bars.s_free[sb], ((j >> 1) & 1) ^ 1, abort))) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t d_tmem = tmem + (uint32_t)sb * TN;
+                const uint64_t kd = kd0 + (uint64_t)((ks * TILEB) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < TN / 16; ++kk)
-                        umma_ts(tmem + COL_O, tmem + COL_P + pb * 64 + kk * 8, smem_desc(vt + kk * 2048, HALF, 1024),
-                                ID_O, (jj > 0 || kk > 0) ? 1u : 0u);
-                    umma_commit(&bars.o_done[pb]);
-                    umma_commit(&bars.vempty[vs]);
-                }
-                __syncwarp();
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ts(d_tmem, tmem + COL_Q + kk * 8, kd + (uint64_t)((((kk >> 2) * HALF) + (kk & 3) * 32) >> 4),
+                            ID_S, kk > 0);
+                umma_commit(&bars.s_full[sb]);
+                umma_commit(&bars.kempty[ks]);
+            }
+            __syncwarp();
+            if (++ks == KST) {
+                ks = 0;
+                ++kuse;
             }
         }
         // every MMA this thread issued has completed before the CTA frees the tensor memory
         if (lane == 0) {
-            umma_commit(&bars.drain);
-            mbar_wait(&bars.drain, 0);
+            umma_commit(&bars.drain[0]);
+            mbar_wait(&bars.drain[0], 0);
+        }
+        __syncwarp();
+    } else if (warp == 11) {
+        // ------------------------------------------------------------ O += P V issuer
+        // (a second issuing thread: one thread alone cannot issue MMAs of this
+        // size as fast as the tensor core retires them)
+        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
+        const uint64_t vd0 = smem_desc(sbase + OFF_V, HALF, 1024);
+        bool ok = true;
+        int vs = 0, vuse = 0;   // V stage of tile j and its use count
+        for (int j = 0; ok && j < nT; ++j) {
+            if (!(ok = cta_wait(&bars.vfull[vs], vuse & 1, abort))) break;
+            const int rz = (j == nT - 1) ? nkv - j * TN : TN;   // rows past the last needed position
+            const uint32_t vbad = bars.vbad[vs];
+            if (rz < TN || vbad) {
+                zero_tile_rows(sbase + OFF_V + vs * TILEB, rz, vbad, BS, lane);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            if (!(ok = cta_wait(&bars.p_full, j & 1, abort))) break;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t vd = vd0 + (uint64_t)((vs * TILEB) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < TN / 16; ++kk)
+                    umma_ts(tmem + COL_O, tmem + COL_P + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), ID_O,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars.o_done);
+                umma_commit(&bars.vempty[vs]);
+            }
+            __syncwarp();
+            if (++vs == VST) {
+                vs = 0;
+                ++vuse;
+            }
+        }
+        if (lane == 0) {
+            umma_commit(&bars.drain[1]);
+            mbar_wait(&bars.drain[1], 0);
         }
         __syncwarp();
     } else {
@@ -405,17 +415,22 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const int qpos = valid_row ? L - C + tok : -1;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         {
-            // this half of the Q row -> shared memory, 128-byte swizzled
-            const uint32_t sq = sbase + OFF_Q + hf * HALF;
+            // this half of the Q row -> tensor memory (bf16 pairs, element
+            // 2i in the low half of column i)
             const uint4* src =
                 reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + hf * 8;
+            uint32_t qv[32];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid_row) v = __ldg(src + u);
-                st_shared_v4(sq + r * 128 + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+                qv[4 * u] = v.x;
+                qv[4 * u + 1] = v.y;
+                qv[4 * u + 2] = v.z;
+                qv[4 * u + 3] = v.w;
             }
-            fence_proxy_async_smem();
+            tmem_st32u(tmem + lane_off + COL_Q + hf * 32, qv);
+            tc_fence_before();
             mbar_arrive(&bars.q_full);
         }
         const float sl2 = a.scale_log2;
@@ -458,10 +473,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 ls[(c >> 1) & 3] += p0 + p1;
                 w[c >> 1] = pack_bf16x2(p0, p1);
             }
-            if (rescale && m != -INFINITY) {
-                // O must be stable: P_{j-1} V_{j-1} has finished
-                if (!(ok = cta_wait(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) break;
+            if (j > 0) {
+                // P_{j-1} V_{j-1} has finished: O is stable and the P buffer free
+                if (!(ok = cta_wait(&bars.o_done, (j - 1) & 1, abort))) break;
                 tc_fence_after();
+            }
+            if (rescale && m != -INFINITY) {
                 const float alpha = ex2(m - m_new);
                 l *= alpha;
 #pragma unroll
@@ -475,16 +492,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             m = m_next;
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            if (j >= 2) {
-                // P buffer j%2 is free once P_{j-2} V_{j-2} has finished
-                if (!(ok = cta_wait(&bars.o_done[s], ((j >> 1) & 1) ^ 1, abort))) break;
-                tc_fence_after();
-            }
-            tmem_st32u(tmem + lane_off + COL_P + s * 64 + hf * 32, w);
+            tmem_st32u(tmem + lane_off + COL_P + hf * 32, w);
             tc_fence_before();
-            mbar_arrive(&bars.p_full[s]);
+            mbar_arrive(&bars.p_full);
         }
-        if (ok && cta_wait(&bars.o_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, abort)) {
+        if (ok && cta_wait(&bars.o_done, (nT - 1) & 1, abort)) {
             tc_fence_after();
             bars.red_l[hf][r] = l;
             mbar_arrive(&bars.pair[quad]);
