@@ -36,6 +36,7 @@ import workloads  # noqa: E402
 
 METRIC = "paged decode attention KV-read GB/s (% of GB300 HBM peak), seq-steps/sec"
 UNIT = "GB/s"
+FALLBACK_BF16 = 1900.0
 FALLBACK_HBM = 6800.0
 
 
@@ -55,6 +56,25 @@ def algorithmic_bytes(w):
     lens = np.asarray(w.seq_lens, dtype=np.int64)
     qo = 2 * w.B * w.Hq * w.d * 2
     return int(lens.sum()) * tok + qo, int(lens.sum()) * tok, qo
+
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16, "fallback"
+
+
+def prefill_flops(w):
+    """Causal multi-query attention FLOPs: query i of a C-token chunk over L cached
+    positions scores L - C + i + 1 keys; 2 d FLOPs per score for Q K^T, 2 d for P V."""
+    tot = 0
+    for b in range(w.B):
+        C = int(w.q_start[b + 1] - w.q_start[b])
+        L = int(w.seq_lens[b])
+        tot += C * (L - C) + C * (C + 1) // 2
+    return 4 * w.d * w.Hq * tot
 
 
 def unique_kv_bytes(w, tables):
@@ -377,6 +397,41 @@ def run_ours(args):
     copy_gbs = copy_bytes * K / t_copy / 1e9
     del ck, cv, cks, cvs
 
+    # multi-query attention (pa_prefill_attention) on this workload's layer shape:
+    # a chunked-prefill batch (16 sequences, 2048 cached + a 2048-token chunk) and
+    # a speculative-verify batch (64 sequences, 4 proposals + 1, U[128, 4096] cached)
+    extras = {}
+    if not args.no_extras and w.kv == "bf16" and w.d == 128:
+        base = args.workload if args.workload in ("8b", "70b", "long") else "8b"
+        rng = np.random.default_rng(7)
+        cases = {"prefill": ([2048] * 16, [2048] * 16),
+                 "verify": ([int(x) for x in rng.integers(128, 4097, 64)], [5] * 64)}
+        for name, (ctx, chunk) in cases.items():
+            pw = workloads.make_prefill(base, ctx, chunk, seed=31, device=dev)
+            pl = PagedDecodeLayer.from_workload(pw, dev)
+            pq = pw.q_chunk.to(dev)
+            po = torch.empty_like(pq)
+            pqs = torch.from_numpy(pw.q_start).to(dev)
+            fn = lambda: pa.pa_prefill_attention(po, pq, pl.k_cache, pl.v_cache, None, None, pl.block_tables,
+                                                 pl.seq_lens, pqs, pw.max_q, pw.scale)
+            pa.pa_get_device_error(clear=True)
+            t_p = timed(fn, K)
+            flops = prefill_flops(pw)
+            kvb = int(np.sum(pw.seq_lens.astype(np.int64))) * 2 * pw.Hkv * pw.d * 2 + 2 * pq.numel() * 2
+            e = {"layer": base, "sequences": pw.B, "cached": "%s" % ("2048" if name == "prefill" else "U[128,4096]"),
+                 "chunk": chunk[0], "us": 1e6 * t_p / K, "TFLOPs": flops * K / t_p / 1e12,
+                 "kv_GBps": kvb * K / t_p / 1e9, "flops": flops, "kv_bytes": kvb,
+                 "device_error": pa.pa_get_device_error()}
+            if name == "prefill":
+                pk, pk_kind = bf16_peak()
+                e["bound"], e["frac"] = "tensor", round(e["TFLOPs"] / pk, 4)
+                e["peak"] = "%s bf16 %.1f TFLOP/s" % (pk_kind, pk)
+            else:
+                e["bound"], e["frac"] = "hbm", round(e["kv_GBps"] / hbm_peak()[0], 4)
+                e["peak"] = "%s HBM %.1f GB/s" % hbm_peak()[::-1]
+            extras[name] = e
+            del pl, pq, po
+
     if rank != 0:
         return
     cpu = None
@@ -402,6 +457,7 @@ def run_ours(args):
                             "calls": "pa_kv_append + pa_decode_attention"},
         "attention_only": {"GBps": alg * K / t_attn / 1e9, "us": 1e6 * t_attn / K,
                            "calls": "pa_decode_attention"},
+        "multi_query_attention": extras,
         "copy_blocks": {"GBps": round(copy_gbs, 1), "frac": round(copy_gbs / hbm_peak()[0], 4),
                         "us": 1e6 * t_copy / K, "blocks": nb_copy, "bytes": copy_bytes,
                         "calls": "pa_copy_blocks (copy-on-write of whole K/V pages)"},
@@ -434,6 +490,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the secondary measurements (block copy, prefill / verify attention)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
