@@ -1,6 +1,8 @@
 /*
- * pa.h - C ABI of libpagedattn.so: single-token decode attention over a
- * paged KV cache, for NVIDIA GB300 (sm_103a).
+ * pa.h - C ABI of libpagedattn.so: attention over a paged KV cache for
+ * NVIDIA GB300 (sm_103a): single-token decode, multi-query (chunked-prefill /
+ * speculative-verify) attention, the cache append, and the host-side block
+ * allocator, prefix cache and schedulers.
  *
  * Pages this interface follows (cited by title and section):
  *   [P1] "KV cache & continuous batching" (docs.masst.dev/ai/inference/kv-cache-batching)
