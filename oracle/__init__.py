@@ -17,6 +17,8 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
                           a verify chunk equals the sequential decode steps
   kv_append (bf16)        exact copy: checked against direct indexing
   kv_append (fp8)         scale == absmax/448, round-trip bounds, brute-force encode
+  int8 codec / append     numpy rint + clip on fp32 quotients, the growth / restart /
+                          zero cases; attention on the int8 cache against torch
   e4m3_encode/value       nearest-value brute force over the 256-code table, format facts
   kv_bytes/blocks_for     the pages' printed per-token sizes and block counts
   sched_*                 the pages' printed iteration counts
@@ -82,6 +84,9 @@ def _load():
             "or_sched_continuous_kv": (i32, [P, i32, P, P, i32, i32, i64, i32, P, P, P, P, P]),
             "or_kv_append_bf16": (i32, [P, P, P, P, P, i32, i64, i32, i32, i32]),
             "or_kv_append_fp8": (i32, [P, P, P, P, P, P, P, i32, i64, i32, i32, i32]),
+            "or_kv_append_int8": (i32, [P, P, P, P, P, P, P, i32, i64, i32, i32, i32]),
+            "or_int8_value": (dbl, [ctypes.c_uint8]),
+            "or_int8_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "or_decode_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                           i64, dbl, i32]),
             "or_decode_attention_split": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
@@ -127,6 +132,18 @@ def e4m3_value(code: int) -> float:
 
 def e4m3_encode(x: float) -> int:
     return int(_load().or_e4m3_encode(float(x)))
+
+
+def int8_value(code: int) -> float:
+    return float(_load().or_int8_value(int(code) & 0xFF))
+
+
+def int8_encode(x: float) -> int:
+    """Code byte (two's complement) of clamp(rint(x), -127, 127)."""
+    return int(_load().or_int8_encode(float(x)))
+
+
+_KV_CODE = {"bf16": 0, "fp8": 1, "int8": 2}
 
 
 def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
@@ -244,11 +261,13 @@ class Cache:
 
     def __init__(self, num_blocks, Hkv, d, bs, kv="bf16"):
         self.num_blocks, self.Hkv, self.d, self.bs, self.kv = num_blocks, Hkv, d, bs, kv
-        dt = np.uint8 if kv == "fp8" else np.uint16
+        if kv not in _KV_CODE:
+            raise ValueError("kv must be bf16, fp8 or int8")
+        dt = np.uint8 if kv != "bf16" else np.uint16
         # np.zeros maps lazily: only pages the appends touch take memory
         self.k = np.zeros((num_blocks, Hkv, bs, d), dtype=dt)
         self.v = np.zeros((num_blocks, Hkv, bs, d), dtype=dt)
-        if kv == "fp8":
+        if kv != "bf16":
             self.k_scale = np.zeros((num_blocks, Hkv), dtype=np.float32)
             self.v_scale = np.zeros((num_blocks, Hkv), dtype=np.float32)
         else:
@@ -259,10 +278,10 @@ class Cache:
         slots = np.ascontiguousarray(slots, dtype=np.int64)
         T = len(slots)
         lib = _load()
-        if self.kv == "fp8":
-            rc = lib.or_kv_append_fp8(_p(self.k), _p(self.v), _p(self.k_scale), _p(self.v_scale),
-                                      _p(kn), _p(vn), _p(slots), T, self.num_blocks, self.Hkv,
-                                      self.d, self.bs)
+        if self.kv != "bf16":
+            fn = lib.or_kv_append_fp8 if self.kv == "fp8" else lib.or_kv_append_int8
+            rc = fn(_p(self.k), _p(self.v), _p(self.k_scale), _p(self.v_scale), _p(kn), _p(vn), _p(slots), T,
+                    self.num_blocks, self.Hkv, self.d, self.bs)
         else:
             rc = lib.or_kv_append_bf16(_p(self.k), _p(self.v), _p(kn), _p(vn), _p(slots), T,
                                        self.num_blocks, self.Hkv, self.d, self.bs)
@@ -286,7 +305,7 @@ def decode_attention(cache: Cache, q, block_tables: np.ndarray, seq_lens: np.nda
     M = int(tables.shape[1]) if tables.ndim == 2 else 0
     out = np.zeros((B, Hq, d), dtype=np.float64)
     lib = _load()
-    fp8 = 1 if cache.kv == "fp8" else 0
+    fp8 = _KV_CODE[cache.kv]
 
     def run(b0, b1):
         if b1 <= b0:
@@ -327,7 +346,7 @@ def prefill_attention(cache: Cache, q, block_tables: np.ndarray, seq_lens: np.nd
     d = cache.d
     out = np.zeros((int(qs[-1]) if len(qs) else 0, Hq, d), dtype=np.float64)
     lib = _load()
-    fp8 = 1 if cache.kv == "fp8" else 0
+    fp8 = _KV_CODE[cache.kv]
 
     def run(b):
         qsb = np.ascontiguousarray(qs[b:b + 2] - qs[b])

@@ -101,6 +101,27 @@ uint8_t or_e4m3_encode(float x) {
     return (uint8_t)((s << 7) | code);
 }
 
+/* int8 cache ([P3] "Memory Bandwidth Optimization": INT8 KV quantization):
+ * a code c in [-127, 127] stands for c * scale.  Encoding rounds a binary32
+ * quotient to the nearest integer, ties to even (rint under the default
+ * rounding mode), and clamps to +-127; NaN maps to 0.  Codes are stored as
+ * two's-complement bytes. */
+double or_int8_value(uint8_t code) { return (double)(int8_t)code; }
+
+uint8_t or_int8_encode(float x) {
+    double q;
+    if (isnan(x)) return 0;
+    q = rint((double)x);
+    if (q > 127.0) q = 127.0;
+    if (q < -127.0) q = -127.0;
+    return (uint8_t)(int8_t)q;
+}
+
+/* The two one-byte codecs: 1 = e4m3 (largest code value 448), 2 = int8 (127). */
+static double q8_value(int codec, uint8_t c) { return codec == 2 ? or_int8_value(c) : or_e4m3_value(c); }
+static uint8_t q8_encode(int codec, float x) { return codec == 2 ? or_int8_encode(x) : or_e4m3_encode(x); }
+static float q8_max(int codec) { return codec == 2 ? 127.0f : 448.0f; }
+
 /* ------------------------------------------------------------------------ */
 /* Accounting: [P1] "KV cache memory math" and [P2] "KV memory, paging and   */
 /* prefix identity": bytes = 2 x layers x kv_heads x head_dim x tokens x     */
@@ -324,9 +345,9 @@ int or_kv_append_bf16(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_ne
  *   scale[p][h] = s
  * so that the block's scale is always its absmax / 448 and no stored code
  * saturates by more than rounding.  448 is the largest finite E4M3 value. */
-static void fp8_block_head(uint8_t* cache, float* scale, const uint16_t* src, const int64_t* slots,
-                           const int* toks, int ntok, int64_t p, int h, int Hkv, int d, int bs,
-                           int first) {
+static void q8_block_head(int codec, uint8_t* cache, float* scale, const uint16_t* src,
+                          const int64_t* slots, const int* toks, int ntok, int64_t p, int h, int Hkv,
+                          int d, int bs, int first) {
     float old, a = 0.0f, s;
     int k, i, o;
     int64_t sidx = p * Hkv + h;
@@ -339,26 +360,26 @@ static void fp8_block_head(uint8_t* cache, float* scale, const uint16_t* src, co
             if (v > a) a = v;
         }
     }
-    s = a / 448.0f;
+    s = a / q8_max(codec);
     if (old > s) s = old;
     if (s > old && old > 0.0f) {
         for (o = 0; o < first; o++)
             for (i = 0; i < d; i++) {
                 uint8_t* e = page + (int64_t)o * d + i;
-                float prod = (float)or_e4m3_value(*e) * old;
-                *e = or_e4m3_encode(prod / s);
+                float prod = (float)q8_value(codec, *e) * old;
+                *e = q8_encode(codec, prod / s);
             }
     }
     for (k = 0; k < ntok; k++) {
         const uint16_t* x = src + ((int64_t)toks[k] * Hkv + h) * d;
         int64_t off = slots[toks[k]] % bs;
         for (i = 0; i < d; i++)
-            page[off * d + i] = (s == 0.0f) ? (uint8_t)0 : or_e4m3_encode(bf16_to_float(x[i]) / s);
+            page[off * d + i] = (s == 0.0f) ? (uint8_t)0 : q8_encode(codec, bf16_to_float(x[i]) / s);
     }
     scale[sidx] = s;
 }
 
-int or_kv_append_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+static int q8_append(int codec, uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
                      const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int T,
                      int64_t num_blocks, int Hkv, int d, int bs) {
     int t, u, h;
@@ -382,13 +403,28 @@ int or_kv_append_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* 
             }
         }
         for (h = 0; h < Hkv; h++) {
-            fp8_block_head(k_cache, k_scale, k_new, slots, toks, n, p, h, Hkv, d, bs, first);
-            fp8_block_head(v_cache, v_scale, v_new, slots, toks, n, p, h, Hkv, d, bs, first);
+            q8_block_head(codec, k_cache, k_scale, k_new, slots, toks, n, p, h, Hkv, d, bs, first);
+            q8_block_head(codec, v_cache, v_scale, v_new, slots, toks, n, p, h, Hkv, d, bs, first);
         }
     }
     free(toks);
     free(done);
     return 0;
+}
+
+int or_kv_append_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                     const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int T,
+                     int64_t num_blocks, int Hkv, int d, int bs) {
+    return q8_append(1, k_cache, v_cache, k_scale, v_scale, k_new, v_new, slots, T, num_blocks, Hkv, d, bs);
+}
+
+/* The same rule for the int8 cache: s = max(old, fp32(absmax) / 127), codes
+ * clamp(rint(x / s), -127, 127), older codes re-encoded as
+ * clamp(rint(fp32(c * old) / s)) when s grows. */
+int or_kv_append_int8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                      const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int T,
+                      int64_t num_blocks, int Hkv, int d, int bs) {
+    return q8_append(2, k_cache, v_cache, k_scale, v_scale, k_new, v_new, slots, T, num_blocks, Hkv, d, bs);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -402,13 +438,15 @@ int or_kv_append_fp8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* 
 /* Query head i of a sequence uses KV head i / G, G = Hq / Hkv (consecutive  */
 /* query heads share a KV head; the pages do not fix the mapping).  Token t  */
 /* of sequence b is row t mod bs of physical block table[b][t / bs].  For    */
-/* the fp8 cache an element's value is value(code) * scale[block][head].     */
+/* the fp8 / int8 cache an element's value is value(code) * scale[block]     */
+/* [head]; the attention functions' `fp8` argument is the cache type:        */
+/* 0 bf16, 1 e4m3, 2 int8.                                                   */
 /* A sequence of length 0 yields a zero output row.                          */
 /* ------------------------------------------------------------------------ */
 static double kv_elem(const void* cache, const float* sc, int fp8, int64_t blk, int h, int off,
                       int i, int Hkv, int d, int bs) {
     int64_t idx = ((blk * Hkv + h) * bs + off) * (int64_t)d + i;
-    if (fp8) return or_e4m3_value(((const uint8_t*)cache)[idx]) * (double)sc[blk * Hkv + h];
+    if (fp8) return q8_value(fp8, ((const uint8_t*)cache)[idx]) * (double)sc[blk * Hkv + h];
     return or_bf16_value(((const uint16_t*)cache)[idx]);
 }
 
