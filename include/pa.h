@@ -28,9 +28,10 @@
  *
  * Memory layout (all row-major, innermost last)
  *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
- *                     bf16 (PA_KV_BF16) or e4m3 bytes (PA_KV_FP8_E4M3).
+ *                     bf16 (PA_KV_BF16), e4m3 bytes (PA_KV_FP8_E4M3) or
+ *                     two's-complement int8 codes (PA_KV_INT8).
  *                     One (block, kv_head) page is contiguous.
- *   k_scale, v_scale  [num_blocks][num_kv_heads] fp32 (fp8 cache only)
+ *   k_scale, v_scale  [num_blocks][num_kv_heads] fp32 (one-byte caches only)
  *   q, out            [batch][num_q_heads][head_dim] bf16
  *   k_new, v_new      [num_tokens][num_kv_heads][head_dim] bf16
  *   block_tables      [batch][max_blocks_per_seq] int32: physical block of
@@ -63,7 +64,9 @@ typedef enum {
 
 typedef enum {
     PA_KV_BF16 = 0,
-    PA_KV_FP8_E4M3 = 1
+    PA_KV_FP8_E4M3 = 1,
+    PA_KV_INT8 = 2      /* int8 codes c in [-127, 127], value c * scale ([P3] "Memory
+                           Bandwidth Optimization": INT8 KV quantization) */
 } pa_kv_dtype;
 
 /* Bits of the per-device error word (pa_get_device_error). */
@@ -96,13 +99,17 @@ const char* pa_status_string(pa_status s);
  *         E4M3(fp32(value(e) * old) / s)
  *     each new value x is stored as E4M3(x / s) (round to nearest even,
  *     saturating at +-448); all codes are +0 when s == 0;  scale[p][h] = s.
- * Precondition (fp8 only): the tokens a call writes into one block form one
+ * PA_KV_INT8 ([P3] "Memory Bandwidth Optimization": INT8 KV quantization
+ * halves the cache reads): the same rule with 127 in place of 448 and the
+ * code Q(y) = clamp(round-half-to-even(y), -127, 127) in place of E4M3; an
+ * element's value is code * scale.
+ * Precondition (one-byte caches only): the tokens a call writes into one block form one
  * run of consecutive entries of slot_mapping with increasing offsets (true for
  * one decode token per sequence and for a prefill of one sequence).  A
  * violation gives unspecified cache contents but no out-of-bounds access.
  *
  * num_blocks * num_kv_heads * block_size must be below 2^31.  head_dim in
- * {64, 128} (fp8: 128), block_size in {16, 32}.  num_tokens == 0 is a no-op.
+ * {64, 128} (one-byte caches: 128), block_size in {16, 32}.  num_tokens == 0 is a no-op.
  * ------------------------------------------------------------------------- */
 pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                        const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -151,11 +158,11 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
  *
  *   out[b][i][:] = sum_t softmax_t(scale * q[b][i] . K_t) V_t,
  *   t = 0 .. seq_lens[b]-1,  K_t = k_cache[block_tables[b][t / bs]][i / G][t % bs]
- * fp8: K_t and V_t elements are value(code) * scale[block][kv_head].
+ * fp8 / int8: K_t and V_t elements are value(code) * scale[block][kv_head].
  * A sequence with seq_len 0 gives a zero row.  The outputs are bf16.
  *
  * num_blocks * num_kv_heads * block_size must be below 2^31; head_dim in
- * {64, 128} (fp8: 128); block_size in {16, 32}; num_q_heads a multiple of
+ * {64, 128} (one-byte caches: 128); block_size in {16, 32}; num_q_heads a multiple of
  * num_kv_heads with a group size of at most 8.  batch == 0 is a no-op.
  * ------------------------------------------------------------------------- */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,

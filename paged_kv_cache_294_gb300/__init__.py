@@ -25,7 +25,7 @@ import torch
 from . import _build
 
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = range(5)
-PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_INT8 = 0, 1, 2
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _lib = None
@@ -134,7 +134,9 @@ def _kv_dtype(cache: torch.Tensor) -> int:
         return PA_KV_BF16
     if cache.dtype == torch.uint8:
         return PA_KV_FP8_E4M3
-    raise TypeError("cache dtype must be bfloat16 or uint8 (e4m3 codes)")
+    if cache.dtype == torch.int8:
+        return PA_KV_INT8
+    raise TypeError("cache dtype must be bfloat16, uint8 (e4m3 codes) or int8")
 
 
 def _need(t: torch.Tensor, dtype, name: str, dim: Optional[int] = None):
@@ -155,7 +157,7 @@ def pa_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional
     _need(k_new, torch.bfloat16, "k_new", 3)
     _need(v_new, torch.bfloat16, "v_new", 3)
     _need(slot_mapping, torch.int64, "slot_mapping", 1)
-    if kvd == PA_KV_FP8_E4M3:
+    if kvd != PA_KV_BF16:
         _need(k_scale, torch.float32, "k_scale", 2)
         _need(v_scale, torch.float32, "v_scale", 2)
     nb, hkv, bs, d = k_cache.shape

@@ -19,7 +19,7 @@ pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_
 
 bool shape_ok(int num_blocks, int Hkv, int d, int bs, int kv_dtype) {
     if (num_blocks <= 0 || Hkv <= 0 || bs <= 0 || d <= 0) return false;
-    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return false;
+    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_INT8) return false;
     if ((int64_t)num_blocks * Hkv * bs >= (int64_t)1 << 31) return false;  // TMA row coordinate
     return true;
 }
@@ -27,7 +27,7 @@ bool shape_ok(int num_blocks, int Hkv, int d, int bs, int kv_dtype) {
 // PA_OK, PA_ERR_INVALID or PA_ERR_UNSUPPORTED for head_dim / block_size / dtype.
 pa_status kernel_shape(int d, int bs, int kv_dtype) {
     if (bs != 16 && bs != 32) return PA_ERR_UNSUPPORTED;
-    if (kv_dtype == PA_KV_FP8_E4M3) return d == 128 ? PA_OK : PA_ERR_UNSUPPORTED;
+    if (kv_dtype != PA_KV_BF16) return d == 128 ? PA_OK : PA_ERR_UNSUPPORTED;   // one-byte codes: a 128-byte row
     return (d == 64 || d == 128) ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
@@ -86,14 +86,14 @@ bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, 
             *out = c.map[i];
             return true;
         }
-    const bool fp8 = dtype == PA_KV_FP8_E4M3;
-    const int elt = fp8 ? 1 : 2;
+    const bool q8 = dtype != PA_KV_BF16;   // one-byte codes (e4m3 or int8)
+    const int elt = q8 ? 1 : 2;
     cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t gstride[1] = {(cuuint64_t)d * elt};
     cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)bs};
     cuuint32_t estride[2] = {1, 1};
     CUtensorMap m;
-    CUresult r = enc(&m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    CUresult r = enc(&m, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                      const_cast<void*>(base), gdim, gstride, box, estride,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -168,10 +168,10 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
     if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_new) || !aligned16(v_new) ||
         (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
         return PA_ERR_INVALID;
-    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
-    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return PA_ERR_INVALID;
+    const bool q8 = kv_dtype != PA_KV_BF16;   // one-byte codes with scales
+    if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr)) return PA_ERR_INVALID;
     pa::AppendLaunch L{k_cache, v_cache, k_scale, v_scale, k_new, v_new, slot_mapping,
-                       num_tokens, num_blocks, num_kv_heads, head_dim, block_size, fp8};
+                       num_tokens, num_blocks, num_kv_heads, head_dim, block_size, kv_dtype};
     return cuda_status(pa::launch_kv_append(L, static_cast<cudaStream_t>(stream)));
 }
 
@@ -230,8 +230,8 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
         return PA_ERR_INVALID;
-    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
-    if (fp8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
+    const bool q8 = kv_dtype != PA_KV_BF16;
+    if (q8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
     if ((k_new != nullptr) != (v_new != nullptr)) return PA_ERR_INVALID;
     if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
@@ -275,7 +275,7 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     L.part_blocks = part_blocks_for(max_blocks_per_seq, S);
     L.S = S;
     L.scale = scale;
-    L.fp8 = fp8;
+    L.kvt = kv_dtype;
     L.k_new = k_new;
     L.v_new = v_new;
     L.k_cache_w = const_cast<void*>(k_cache);
@@ -320,10 +320,10 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
     if (ks != PA_OK) return ks;
     if (n == 0) return PA_OK;
     if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
-    const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
-    if (fp8 != (k_scale != nullptr) || fp8 != (v_scale != nullptr)) return PA_ERR_INVALID;
+    const bool q8 = kv_dtype != PA_KV_BF16;   // one-byte codes with scales
+    if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr)) return PA_ERR_INVALID;
     return cuda_status(pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, n, num_blocks,
-                                              num_kv_heads, head_dim, block_size, fp8,
+                                              num_kv_heads, head_dim, block_size, q8,
                                               static_cast<cudaStream_t>(stream)));
 }
 

@@ -42,10 +42,12 @@ __global__ void __launch_bounds__(256) kv_append_bf16_kernel(
     }
 }
 
-// One warp per (token, kv_head).  Only the first token of each run of
-// consecutive tokens that land in the same block does work: it quantises the
-// whole run (at most bs tokens) for its head, K then V.
-__global__ void __launch_bounds__(256) kv_append_fp8_kernel(
+// One-byte caches (e4m3 or int8 codes, KVT).  One warp per (token, kv_head).
+// Only the first token of each run of consecutive tokens that land in the
+// same block does work: it quantises the whole run (at most bs tokens) for its
+// head, K then V.
+template <int KVT>
+__global__ void __launch_bounds__(256) kv_append_q8_kernel(
     uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache, float* __restrict__ k_scale,
     float* __restrict__ v_scale, const uint16_t* __restrict__ k_new,
     const uint16_t* __restrict__ v_new, const int64_t* __restrict__ slots, int T, int Hkv, int bs,
@@ -75,18 +77,21 @@ __global__ void __launch_bounds__(256) kv_append_fp8_kernel(
     const int64_t page = (blk * Hkv + h) * (int64_t)bs * 128;
     const int64_t row0 = ((int64_t)t * Hkv + h) * 128;
     auto off_of = [&](int j) { return (int)(slots[t + j] % bs); };
-    fp8_quantise_run(k_cache + page, k_scale + blk * Hkv + h, k_new + row0, (int64_t)Hkv * 128, r, first, off_of);
-    fp8_quantise_run(v_cache + page, v_scale + blk * Hkv + h, v_new + row0, (int64_t)Hkv * 128, r, first, off_of);
+    q8_quantise_run<KVT>(k_cache + page, k_scale + blk * Hkv + h, k_new + row0, (int64_t)Hkv * 128, r, first,
+                         off_of);
+    q8_quantise_run<KVT>(v_cache + page, v_scale + blk * Hkv + h, v_new + row0, (int64_t)Hkv * 128, r, first,
+                         off_of);
 }
 
 cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {
     const int64_t cap = (int64_t)L.num_blocks * L.bs;
-    if (L.fp8) {
+    if (L.kvt != PA_KV_BF16) {
         const int64_t warps = (int64_t)L.T * L.Hkv;
         const int blocks = (int)((warps * 32 + 255) / 256);
-        kv_append_fp8_kernel<<<blocks, 256, 0, stream>>>(
-            (uint8_t*)L.k_cache, (uint8_t*)L.v_cache, L.k_scale, L.v_scale,
-            (const uint16_t*)L.k_new, (const uint16_t*)L.v_new, L.slots, L.T, L.Hkv, L.bs, cap);
+        auto kern = (L.kvt == PA_KV_INT8) ? kv_append_q8_kernel<KV_INT8> : kv_append_q8_kernel<KV_FP8>;
+        kern<<<blocks, 256, 0, stream>>>((uint8_t*)L.k_cache, (uint8_t*)L.v_cache, L.k_scale, L.v_scale,
+                                         (const uint16_t*)L.k_new, (const uint16_t*)L.v_new, L.slots, L.T, L.Hkv,
+                                         L.bs, cap);
     } else {
         const int units = L.d / 8;
         const int64_t total = (int64_t)L.T * L.Hkv * units;
@@ -126,9 +131,9 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
-                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool fp8,
+                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool q8,
                                cudaStream_t stream) {
-    const int64_t units = (int64_t)Hkv * bs * d * (fp8 ? 1 : 2) / 16;
+    const int64_t units = (int64_t)Hkv * bs * d * (q8 ? 1 : 2) / 16;
     const int64_t total = (int64_t)n * units;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 1 << 20);
     copy_blocks_kernel<<<blocks, 256, 0, stream>>>((uint4*)k_cache, (uint4*)v_cache, k_scale, v_scale, src, dst, n,

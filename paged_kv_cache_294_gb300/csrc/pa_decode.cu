@@ -58,8 +58,9 @@ struct DecodeArgs {
     float scale_log2;
 };
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KVT>
 struct Cfg {
+    static constexpr bool FP8 = KVT != KV_BF16;   // one-byte codes (e4m3 or int8)
     static constexpr int ELT = FP8 ? 1 : 2;
     static constexpr int ROWB = D * ELT;       // bytes of one token row of one head
     static constexpr int NCH = ROWB / 128;      // 128-byte column chunks = TMA boxes per page
@@ -77,8 +78,9 @@ struct Cfg {
 
 
 // ------------------------------------------------------------------ per warp
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KVT>
 struct WarpAcc {
+    static constexpr bool FP8 = KVT != KV_BF16;
     float m, l;
     float o[D / 16][4];
     uint32_t qa[D / 16][2];
@@ -113,7 +115,7 @@ struct WarpAcc {
     // the number of its tokens inside the sequence, sl2 = scale * log2(e)
     // (times the K scale for fp8), vsc the V scale (fp8).
     __device__ __forceinline__ void page(uint32_t kt, uint32_t vt, int valid, float sl2, float vsc, int lane) {
-        using C = Cfg<D, BS, FP8>;
+        using C = Cfg<D, BS, KVT>;
         const int g = lane >> 2, c = lane & 3;
         const int mi = lane >> 3, r = lane & 7;
 
@@ -129,7 +131,9 @@ struct WarpAcc {
                 for (int nt = 0; nt < C::NT; ++nt) {
                     const int t = nt * 8 + g;
                     const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
-                    mma_f16(acc[nt], A, e4m3x2_to_f16x2((uint16_t)(w & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+                    uint32_t b0, b1;
+                    code4_to_f16x2<KVT>(w, b0, b1);
+                    mma_f16(acc[nt], A, b0, b1);
                 }
             } else {
                 const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
@@ -217,10 +221,11 @@ struct WarpAcc {
                     // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes
                     const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
                     const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
-                    const uint32_t A0[4] = {e4m3x2_to_f16x2((uint16_t)(x0 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x0 >> 16)),
-                                            e4m3x2_to_f16x2((uint16_t)(x1 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x1 >> 16))};
-                    const uint32_t A1[4] = {e4m3x2_to_f16x2((uint16_t)(x2 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x2 >> 16)),
-                                            e4m3x2_to_f16x2((uint16_t)(x3 & 0xFFFF)), e4m3x2_to_f16x2((uint16_t)(x3 >> 16))};
+                    uint32_t A0[4], A1[4];
+                    code4_to_f16x2<KVT>(x0, A0[0], A0[1]);
+                    code4_to_f16x2<KVT>(x1, A0[2], A0[3]);
+                    code4_to_f16x2<KVT>(x2, A1[0], A1[1]);
+                    code4_to_f16x2<KVT>(x3, A1[2], A1[3]);
                     mma_f16(t0, A0, pb[kk][0], pb[kk][1]);
                     mma_f16(t1, A1, pb[kk][0], pb[kk][1]);
                 }
@@ -364,8 +369,10 @@ struct NewRow {
     float ks, vs;        // fp8: the block's new scales
 };
 
-template <int D, bool FP8>
+template <int D, int KVT>
 __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, int h, int phys, int off, int lane) {
+    constexpr bool FP8 = KVT != KV_BF16;
+    using QC = Codec<KVT == KV_INT8 ? KV_INT8 : KV_FP8>;
     NewRow r;
     const int64_t src = ((int64_t)b * a.Hkv + h) * D;
     r.kraw = r.vraw = make_uint2(0u, 0u);
@@ -378,17 +385,19 @@ __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, in
     if (FP8) {
         r.kold = off == 0 ? 0.f : a.k_scale_w[(int64_t)phys * a.Hkv + h];
         r.vold = off == 0 ? 0.f : a.v_scale_w[(int64_t)phys * a.Hkv + h];
-        r.ks = fmaxf(r.kold, __fdiv_rn(warp_max(absmax4(r.kraw)), 448.0f));
-        r.vs = fmaxf(r.vold, __fdiv_rn(warp_max(absmax4(r.vraw)), 448.0f));
-        r.kc = fp8_encode4(r.kraw, r.ks);
-        r.vc = fp8_encode4(r.vraw, r.vs);
+        r.ks = fmaxf(r.kold, __fdiv_rn(warp_max(absmax4(r.kraw)), QC::QMAX));
+        r.vs = fmaxf(r.vold, __fdiv_rn(warp_max(absmax4(r.vraw)), QC::QMAX));
+        r.kc = q8_encode4<KVT == KV_INT8 ? KV_INT8 : KV_FP8>(r.kraw, r.ks);
+        r.vc = q8_encode4<KVT == KV_INT8 ? KV_INT8 : KV_FP8>(r.vraw, r.vs);
     }
     return r;
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KVT>
 __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
                                               const NewRow& r, int lane) {
+    constexpr bool FP8 = KVT != KV_BF16;
+    using QC = Codec<KVT == KV_INT8 ? KV_INT8 : KV_FP8>;
     const int64_t prow = ((int64_t)phys * a.Hkv + h) * BS;  // first row of the page
     if (FP8) {
 #pragma unroll
@@ -403,7 +412,7 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
                     uint32_t nw = 0;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(e4m3_to_f32((w >> (8 * e)) & 0xFF), old), sn)) << (8 * e);
+                        nw |= QC::encode(__fdiv_rn(__fmul_rn(QC::value((w >> (8 * e)) & 0xFF), old), sn)) << (8 * e);
                     asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, o, lane * 4)), "r"(nw) : "memory");
                     grow[o * 32 + lane] = nw;
                 }
@@ -427,16 +436,17 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
     __syncwarp();
 }
 
-template <int D, int BS, bool FP8, int NSTAGE, bool APPEND>
-__global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
+template <int D, int BS, int KVT, int NSTAGE, bool APPEND>
+__global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeArgs a) {
-    using C = Cfg<D, BS, FP8>;
+    using C = Cfg<D, BS, KVT>;
+    constexpr bool FP8 = C::FP8;
     constexpr int BAR_OFF = NSTAGE * C::STAGEB;
     static_assert(C::COMBINE_FLOATS * 4 <= NSTAGE * C::STAGEB, "combine area must fit in the stages");
     // stage s is always consumed by warp s % NCW, so no waiter can run two
     // phases ahead of a stage's oldest unconsumed fill (parity waits alias)
-    static_assert(NSTAGE % Cfg<D, BS, FP8>::NCW == 0, "ring depth must be a multiple of the consumer warps");
+    static_assert(NSTAGE % Cfg<D, BS, KVT>::NCW == 0, "ring depth must be a multiple of the consumer warps");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -479,7 +489,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
     if (split > 0 && warp == C::NCW && lane < npages) phys0 = trow[lane];
     __syncthreads();
 
-    WarpAcc<D, BS, FP8> st;
+    WarpAcc<D, BS, KVT> st;
     st.reset();
     if (warp == C::NCW) {
         if (lane == 0) {
@@ -536,7 +546,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
         if (appends) {
             app_phys = trow[npages - 1];
             if (app_phys < 0 || app_phys >= a.num_blocks) app_phys = -1;
-            if (app_phys >= 0) nr = prepare_new_row<D, FP8>(a, b, h, app_phys, (len - 1) % BS, lane);
+            if (app_phys >= 0) nr = prepare_new_row<D, KVT>(a, b, h, app_phys, (len - 1) % BS, lane);
         }
         for (int i = warp; i < npages; i += C::NCW) {
             const int s = i % NSTAGE;
@@ -551,7 +561,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, FP8>::NTHREADS, 3)
             const uint32_t kt = sbase + s * C::STAGEB;
             const bool patched = appends && i == npages - 1 && app_phys >= 0;
             if (patched) {
-                patch_new_row<D, BS, FP8>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, nr, lane);
+                patch_new_row<D, BS, KVT>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, nr, lane);
                 if (FP8) {
                     ksc = nr.ks;
                     vsc = nr.vs;
@@ -602,9 +612,9 @@ static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
     return cudaSuccess;
 }
 
-template <int D, int BS, bool FP8, bool APPEND>
+template <int D, int BS, int KVT, bool APPEND>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
-    using C = Cfg<D, BS, FP8>;
+    using C = Cfg<D, BS, KVT>;
     DecodeArgs a;
     a.out = (__nv_bfloat16*)L.out;
     a.q = (const uint16_t*)L.q;
@@ -633,7 +643,7 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
     static int configured = -1;
-    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, FP8, NST, APPEND>, SMEM, configured);
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND>, SMEM, configured);
     if (e != cudaSuccess) return e;
     // programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel (typically this step's append) finishes; they wait for it
@@ -648,19 +658,22 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, FP8, NST, APPEND>, *L.tm_k, *L.tm_v, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND>, *L.tm_k, *L.tm_v, a);
 }
 
 template <bool APPEND>
 static cudaError_t launch_shape(const DecodeLaunch& L, cudaStream_t stream) {
-    if (L.fp8) {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, true, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, true, APPEND>(L, stream);
+    if (L.kvt == PA_KV_FP8_E4M3) {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_FP8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_FP8, APPEND>(L, stream);
+    } else if (L.kvt == PA_KV_INT8) {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_INT8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_INT8, APPEND>(L, stream);
     } else {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, false, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, false, APPEND>(L, stream);
-        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, false, APPEND>(L, stream);
-        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, false, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_BF16, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_BF16, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, KV_BF16, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, KV_BF16, APPEND>(L, stream);
     }
     return cudaErrorInvalidValue;
 }

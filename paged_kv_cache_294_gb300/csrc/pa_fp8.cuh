@@ -1,14 +1,16 @@
-// fp8 (e4m3) cache append arithmetic, shared by the append kernel and the
-// fused decode step so that both write identical bytes.
+// One-byte cache append arithmetic (e4m3 and int8 codes), shared by the
+// append kernel and the fused decode step so that both write identical bytes.
 //
 // The rule ("KV cache & continuous batching", section "KV cache memory math":
 // fp8 = 1 byte per element; "LLM Inference Optimization", section "Memory
-// Bandwidth Optimization": KV-cache quantization): one fp32 scale per (block,
-// kv head).  When a call writes tokens into a block starting at offset
-// `first`:  old = first == 0 ? 0 : scale;  s = max(old, fp32(absmax) / 448);
-// if s > old > 0 every older row (offset < first) is re-encoded as
-// E4M3(fp32(value * old) / s);  each new value x becomes E4M3(x / s) (all +0
-// when s == 0);  scale = s.  E4M3 rounds to nearest even and saturates at 448.
+// Bandwidth Optimization": KV-cache quantization, INT8 halving the reads):
+// one fp32 scale per (block, kv head).  When a call writes tokens into a
+// block starting at offset `first`:  old = first == 0 ? 0 : scale;
+// s = max(old, fp32(absmax) / QMAX);  if s > old > 0 every older row
+// (offset < first) is re-encoded as Q(fp32(value * old) / s);  each new value
+// x becomes Q(x / s) (all codes 0 when s == 0);  scale = s.
+//   e4m3 (KV_FP8):  QMAX = 448, Q = E4M3 round to nearest even, saturating;
+//   int8 (KV_INT8): QMAX = 127, Q = clamp(round half to even, -127, 127).
 #pragma once
 
 #include <cuda_fp8.h>
@@ -16,6 +18,8 @@
 #include "pa_device.cuh"
 
 namespace pa {
+
+enum KvType { KV_BF16 = 0, KV_FP8 = 1, KV_INT8 = 2 };
 
 // e4m3 code -> fp32, exact (the e4m3 -> f16 conversion is exact).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
@@ -29,13 +33,60 @@ __device__ __forceinline__ uint32_t f32_to_e4m3(float x) {
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
 
+// int8 code (two's-complement byte) -> fp32, exact.
+__device__ __forceinline__ float s8_to_f32(uint32_t code) { return (float)(int8_t)(code & 0xFF); }
+
+__device__ __forceinline__ uint32_t f32_to_s8(float x) {
+    const int q = max(-127, min(127, __float2int_rn(x)));   // NaN converts to 0
+    return (uint32_t)q & 0xFF;
+}
+
+// four one-byte codes of the cache type KVT (bytes 0..3 of w) -> two f16x2:
+// lo = {byte 0, byte 1}, hi = {byte 2, byte 3}; exact for both code types.
+// int8: with its sign bit flipped a code c becomes the byte u = c + 128; one
+// byte permute places two such bytes under the f16 pattern 0x64.., whose
+// value is 1024 + u, and subtracting 1152 leaves c (every step exact).
+template <int KVT>
+__device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    if constexpr (KVT == KV_INT8) {
+        const uint32_t u = w ^ 0x80808080u;
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        uint32_t a, b;
+        asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(a) : "r"(u), "r"(0x64646464u));
+        asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(b) : "r"(u), "r"(0x64646464u));
+        __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+        __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+        lo = *reinterpret_cast<uint32_t*>(&ha);
+        hi = *reinterpret_cast<uint32_t*>(&hb);
+    } else {
+        lo = e4m3x2_to_f16x2((uint16_t)(w & 0xFFFF));
+        hi = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+    }
+}
+
+template <int KVT>
+struct Codec;
+template <>
+struct Codec<KV_FP8> {
+    static constexpr float QMAX = 448.f;
+    __device__ __forceinline__ static float value(uint32_t c) { return e4m3_to_f32(c); }
+    __device__ __forceinline__ static uint32_t encode(float x) { return f32_to_e4m3(x); }
+};
+template <>
+struct Codec<KV_INT8> {
+    static constexpr float QMAX = 127.f;
+    __device__ __forceinline__ static float value(uint32_t c) { return s8_to_f32(c); }
+    __device__ __forceinline__ static uint32_t encode(float x) { return f32_to_s8(x); }
+};
+
 // The block's new scale from its current one (`old`, already 0 when the call
 // starts the block at offset 0) and the absmax `a` of the new values; when it
 // grows, the older rows (offsets < first) are re-encoded through
 // load_old(o) / store_old(o, codes), 4 codes per lane.  One full warp.
-template <typename LoadOld, typename StoreOld>
-__device__ __forceinline__ float fp8_rescale(float old, float a, int first, LoadOld load_old, StoreOld store_old) {
-    float s = __fdiv_rn(a, 448.0f);
+template <int KVT, typename LoadOld, typename StoreOld>
+__device__ __forceinline__ float q8_rescale(float old, float a, int first, LoadOld load_old, StoreOld store_old) {
+    using Q = Codec<KVT>;
+    float s = __fdiv_rn(a, Q::QMAX);
     if (old > s) s = old;
     if (s > old && old > 0.f) {
 #pragma unroll 1
@@ -44,8 +95,8 @@ __device__ __forceinline__ float fp8_rescale(float old, float a, int first, Load
             uint32_t nw = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float v = e4m3_to_f32((w >> (8 * e)) & 0xFF);
-                nw |= f32_to_e4m3(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
+                const float v = Q::value((w >> (8 * e)) & 0xFF);
+                nw |= Q::encode(__fdiv_rn(__fmul_rn(v, old), s)) << (8 * e);
             }
             store_old(o, nw);
         }
@@ -53,14 +104,15 @@ __device__ __forceinline__ float fp8_rescale(float old, float a, int first, Load
     return s;
 }
 
-// 4 bf16 values (packed in w) -> 4 codes E4M3(x / s); all +0 when s == 0.
-__device__ __forceinline__ uint32_t fp8_encode4(uint2 w, float s) {
+// 4 bf16 values (packed in w) -> 4 codes Q(x / s); all 0 when s == 0.
+template <int KVT>
+__device__ __forceinline__ uint32_t q8_encode4(uint2 w, float s) {
     const float x[4] = {bf16_bits_to_f32(w.x & 0xFFFF), bf16_bits_to_f32(w.x >> 16), bf16_bits_to_f32(w.y & 0xFFFF),
                         bf16_bits_to_f32(w.y >> 16)};
     uint32_t nw = 0;
     if (s != 0.f) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) nw |= f32_to_e4m3(__fdiv_rn(x[e], s)) << (8 * e);
+        for (int e = 0; e < 4; ++e) nw |= Codec<KVT>::encode(__fdiv_rn(x[e], s)) << (8 * e);
     }
     return nw;
 }
@@ -82,8 +134,8 @@ __device__ __forceinline__ float warp_max(float a) {
 // `page` (rows of 128 codes) at offsets off_of(j), for one (block, kv head)
 // with scale *scale_p; `first` is the smallest offset written.  One full warp;
 // lane owns bytes 4*lane .. 4*lane+3 of every row.  Returns the new scale.
-template <typename OffFn>
-__device__ __forceinline__ float fp8_quantise_run(uint8_t* __restrict__ page, float* __restrict__ scale_p,
+template <int KVT, typename OffFn>
+__device__ __forceinline__ float q8_quantise_run(uint8_t* __restrict__ page, float* __restrict__ scale_p,
                                                  const uint16_t* __restrict__ src, int64_t src_stride, int r,
                                                  int first, OffFn off_of) {
     const int lane = threadIdx.x & 31;
@@ -93,12 +145,12 @@ __device__ __forceinline__ float fp8_quantise_run(uint8_t* __restrict__ page, fl
     a = warp_max(a);
     const float old = (first == 0) ? 0.f : *scale_p;
     uint32_t* rows = reinterpret_cast<uint32_t*>(page);
-    const float s = fp8_rescale(
+    const float s = q8_rescale<KVT>(
         old, a, first, [&](int o) { return rows[o * 32 + lane]; },
         [&](int o, uint32_t nw) { rows[o * 32 + lane] = nw; });
 #pragma unroll 1
     for (int j = 0; j < r; ++j)
-        rows[off_of(j) * 32 + lane] = fp8_encode4(*reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4), s);
+        rows[off_of(j) * 32 + lane] = q8_encode4<KVT>(*reinterpret_cast<const uint2*>(src + j * src_stride + lane * 4), s);
     __syncwarp();
     if (lane == 0) *scale_p = s;
     return s;

@@ -145,10 +145,10 @@ class PagedDecodeLayer:
                  device="cuda"):
         self.num_blocks, self.Hq, self.Hkv, self.d, self.bs, self.kv = num_blocks, Hq, Hkv, d, bs, kv
         self.device = torch.device(device)
-        dt = torch.uint8 if kv == "fp8" else torch.bfloat16
+        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
         self.k_cache = torch.zeros((num_blocks, Hkv, bs, d), dtype=dt, device=self.device)
         self.v_cache = torch.zeros((num_blocks, Hkv, bs, d), dtype=dt, device=self.device)
-        if kv == "fp8":
+        if kv != "bf16":
             self.k_scale = torch.zeros((num_blocks, Hkv), dtype=torch.float32, device=self.device)
             self.v_scale = torch.zeros((num_blocks, Hkv), dtype=torch.float32, device=self.device)
         else:

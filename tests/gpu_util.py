@@ -9,10 +9,11 @@ from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
 
 BF16_TOL = 1e-2     # max |err| of bf16-cache attention outputs
 FP8_TOL = 5e-2      # max |err| of fp8-cache outputs against the oracle on the stored fp8 cache
+INT8_TOL = 1e-2     # int8 cache: codes are exact in f16, so the bf16 output bound applies
 
 
 def tol(w):
-    return FP8_TOL if w.kv == "fp8" else BF16_TOL
+    return {"fp8": FP8_TOL, "int8": INT8_TOL}.get(w.kv, BF16_TOL)
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:
@@ -55,4 +56,4 @@ def gpu_out_f64(layer, seqs=None):
 def cache_bytes(t: torch.Tensor) -> np.ndarray:
     if t.dtype == torch.bfloat16:
         return t.cpu().view(torch.int16).numpy().view(np.uint16)
-    return t.cpu().numpy()
+    return t.cpu().numpy().view(np.uint8)

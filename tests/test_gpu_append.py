@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("name,kw", [("tiny", {}), ("8b", dict(B=6, seq_len=700)),
                                      ("70b", dict(B=8, seq_len=400)),
-                                     ("fp8prefix", dict(B=6, seq_len=600))])
+                                     ("fp8prefix", dict(B=6, seq_len=600)),
+                                     ("8b-int8", dict(B=6, seq_len=700))])
 def test_workload_caches_bit_exact(name, kw):
     w = workloads.make(name, **kw)
     layer = run_gpu(w)
@@ -21,7 +22,7 @@ def test_workload_caches_bit_exact(name, kw):
     assert pa.pa_get_device_error() == 0
     assert np.array_equal(cache_bytes(layer.k_cache), st.cache.k.reshape(layer.k_cache.shape))
     assert np.array_equal(cache_bytes(layer.v_cache), st.cache.v.reshape(layer.v_cache.shape))
-    if w.kv == "fp8":
+    if w.kv != "bf16":
         assert np.array_equal(layer.k_scale.cpu().numpy().view(np.uint32), st.cache.k_scale.view(np.uint32))
         assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), st.cache.v_scale.view(np.uint32))
 
@@ -35,11 +36,11 @@ class Pair:
 
     def __init__(self, nb, hkv, d, bs, kv):
         self.o = oracle.Cache(nb, hkv, d, bs, kv)
-        dt = torch.uint8 if kv == "fp8" else torch.bfloat16
+        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
         self.k = torch.zeros((nb, hkv, bs, d), dtype=dt, device="cuda")
         self.v = torch.zeros_like(self.k)
-        self.ks = torch.zeros((nb, hkv), dtype=torch.float32, device="cuda") if kv == "fp8" else None
-        self.vs = torch.zeros_like(self.ks) if kv == "fp8" else None
+        self.ks = torch.zeros((nb, hkv), dtype=torch.float32, device="cuda") if kv != "bf16" else None
+        self.vs = torch.zeros_like(self.ks) if kv != "bf16" else None
 
     def append(self, k, v, slots):
         slots = np.asarray(slots, np.int64)
@@ -69,10 +70,11 @@ def test_bf16_scatter_with_skips(d, bs):
     assert pa.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
 @pytest.mark.parametrize("bs", [16, 32])
-def test_fp8_growth_restart_and_runs(bs):
+def test_one_byte_growth_restart_and_runs(bs, kv):
     rng = np.random.default_rng(bs)
-    p = Pair(6, 2, 128, bs, "fp8")
+    p = Pair(6, 2, 128, bs, kv)
     # a prefill run across three blocks, with a skipped token in the middle of the call
     k = _bf16(rng.standard_normal((2 * bs + 5, 2, 128)))
     slots = np.concatenate([np.arange(bs, 3 * bs), [-1], np.arange(4 * bs, 4 * bs + 4)])
@@ -99,9 +101,10 @@ def test_fp8_growth_restart_and_runs(bs):
     assert pa.pa_get_device_error() == 0
 
 
-def test_fp8_one_token_per_sequence_many_blocks():
+@pytest.mark.parametrize("kv", ["fp8", "int8"])
+def test_one_byte_one_token_per_sequence_many_blocks(kv):
     rng = np.random.default_rng(11)
-    p = Pair(64, 4, 128, 32, "fp8")
+    p = Pair(64, 4, 128, 32, kv)
     hist = _bf16(rng.standard_normal((64 * 20, 4, 128)))
     slots = np.concatenate([np.arange(b * 32, b * 32 + 20) for b in range(64)])
     p.append(hist, hist, slots)

@@ -35,7 +35,8 @@ def check(w, num_splits=0, seqs=None):
 
 
 SMALL = [("tiny", {}), ("8b", dict(B=8, seq_len=600)), ("70b", dict(B=12, seq_len=500)),
-         ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700))]
+         ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700)),
+         ("8b-int8", dict(B=8, seq_len=600))]
 
 
 @pytest.mark.parametrize("name,kw", SMALL)
@@ -76,6 +77,9 @@ SHAPES = [
     (5, 4, 4, 128, 32, "fp8"),
     (5, 8, 1, 128, 16, "fp8"),
     (5, 6, 3, 128, 32, "fp8"),
+    (5, 4, 4, 128, 32, "int8"),
+    (5, 8, 1, 128, 16, "int8"),
+    (5, 16, 2, 128, 16, "int8"),
 ]
 
 
@@ -161,7 +165,7 @@ def _sample(B, k=6):
     return sorted({0, B - 1} | set(np.random.default_rng(7).choice(B, size=k, replace=False).tolist()))
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "fp8prefix"])
+@pytest.mark.parametrize("name", ["8b", "70b", "fp8prefix", "8b-int8"])
 def test_full_size_sampled(name):
     w = workloads.make(name, device="cuda")
     seqs = _sample(w.B)

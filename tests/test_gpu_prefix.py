@@ -17,7 +17,7 @@ import paged_kv_cache_294_gb300 as pa
 import workloads
 from oracle.prefix import copy_blocks
 from paged_kv_cache_294_gb300.engine import BlockManager, PagedDecodeLayer
-from tests.gpu_util import BF16_TOL, FP8_TOL, cache_bytes, excess
+from tests.gpu_util import BF16_TOL, FP8_TOL, INT8_TOL, cache_bytes, excess
 from tests.prefix_sim import OracleManager
 
 pytestmark = pytest.mark.gpu
@@ -100,7 +100,7 @@ def _oracle(sc):
     return cache, starts, outs, tables
 
 
-@pytest.mark.parametrize("layer_name", ["8b", "fp8prefix", "tiny"])
+@pytest.mark.parametrize("layer_name", ["8b", "fp8prefix", "tiny", "8b-int8"])
 @pytest.mark.parametrize("splits", [0, 2])
 def test_prefix_cached_serving_matches_the_oracle(layer_name, splits):
     sc = workloads.serving_scenario(layer_name, steps=35)     # every sequence crosses a block boundary
@@ -111,30 +111,32 @@ def test_prefix_cached_serving_matches_the_oracle(layer_name, splits):
     # every request after the first reuses the prompt's full blocks
     assert starts == o_starts and starts[0] == 0 and all(s == 5 * sc.bs for s in starts[1:])
     assert n_copies >= 1                     # the forks shared a partly filled block
-    tol = FP8_TOL if sc.kv == "fp8" else BF16_TOL
+    tol = {"fp8": FP8_TOL, "int8": INT8_TOL}.get(sc.kv, BF16_TOL)
     for s in range(len(outs)):
         assert np.array_equal(tables[s], o_tables[s])
         assert excess(outs[s], o_outs[s], tol) <= 1.0, "step %d" % s
     assert np.array_equal(cache_bytes(layer.k_cache), cache.k)
     assert np.array_equal(cache_bytes(layer.v_cache), cache.v)
-    if sc.kv == "fp8":
+    if sc.kv != "bf16":
         assert np.array_equal(layer.k_scale.cpu().numpy().view(np.uint32), cache.k_scale.view(np.uint32))
         assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), cache.v_scale.view(np.uint32))
 
 
-@pytest.mark.parametrize("kv,d,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("fp8", 128, 32)])
+@pytest.mark.parametrize("kv,d,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("fp8", 128, 32), ("int8", 128, 16)])
 def test_copy_blocks_is_bit_exact(kv, d, bs):
     nb, hkv = 300, 4
     g = torch.Generator(device="cuda")
     g.manual_seed(17)
-    dt = torch.uint8 if kv == "fp8" else torch.bfloat16
-    k = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8)
-    v = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8)
+    dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
+    k = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
+        if dt != torch.bfloat16 else None
+    v = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
+        if dt != torch.bfloat16 else None
     if kv == "bf16":
         k = torch.randn((nb, hkv, bs, d), generator=g, device="cuda").to(dt)
         v = torch.randn((nb, hkv, bs, d), generator=g, device="cuda").to(dt)
-    ks = torch.rand((nb, hkv), generator=g, device="cuda") if kv == "fp8" else None
-    vs = torch.rand((nb, hkv), generator=g, device="cuda") if kv == "fp8" else None
+    ks = torch.rand((nb, hkv), generator=g, device="cuda") if kv != "bf16" else None
+    vs = torch.rand((nb, hkv), generator=g, device="cuda") if kv != "bf16" else None
     rng = np.random.default_rng(2)
     perm = rng.permutation(nb)
     src, dst = perm[:100].astype(np.int32), perm[100:200].astype(np.int32)

@@ -35,7 +35,8 @@ def _same_state(a, b):
 
 
 CASES = [("tiny", {}), ("8b", dict(B=8, seq_len=700)), ("70b", dict(B=12, seq_len=500)),
-         ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700))]
+         ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700)),
+         ("8b-int8", dict(B=8, seq_len=700))]
 
 
 @pytest.mark.parametrize("name,kw", CASES)
@@ -52,7 +53,8 @@ def test_fused_step_equals_append_then_decode(name, kw, splits):
 
 
 SHAPES = [(5, 8, 8, 128, 16, "bf16"), (5, 8, 1, 128, 16, "bf16"), (5, 12, 3, 64, 16, "bf16"),
-          (5, 8, 2, 64, 32, "bf16"), (5, 4, 4, 128, 32, "fp8"), (5, 8, 1, 128, 16, "fp8")]
+          (5, 8, 2, 64, 32, "bf16"), (5, 4, 4, 128, 32, "fp8"), (5, 8, 1, 128, 16, "fp8"),
+          (5, 4, 4, 128, 32, "int8"), (5, 8, 2, 128, 16, "int8")]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -61,7 +63,7 @@ def test_fused_step_shapes_offsets_and_zero_lengths(shape):
     # new tokens at offset 0 (fresh block), mid-block and last row; one empty sequence
     lens = [1, bs + 1, bs // 2, 0, 3 * bs][:B]
     w = _synthetic(B, Hq, Hkv, d, bs, lens, kv, seed=B + Hq + d + bs)
-    if kv == "fp8":
+    if kv != "bf16":
         # larger new values than the history: the block scale grows and older rows re-encode
         w.k_new = (w.k_new.float() * 7).to(torch.bfloat16)
         w.v_new = (w.v_new.float() * 3).to(torch.bfloat16)
