@@ -11,8 +11,8 @@
 // tiles of 128 tokens (128 / block_size pages, each page fetched by TMA from
 // its physical block with the 128-byte swizzle).
 //
-//   warp 0      TMA producer of the K tile ring (3 stages)
-//   warp 10     TMA producer of the V tile ring (3 stages)
+//   warp 0      TMA producer of the K tile ring (3 stages), one lane per page
+//   warp 10     TMA producer of the V tile ring (3 stages), one lane per page
 //   warp 1      owns the tensor memory; one lane issues S[j%2] = Q K_j^T
 //   warp 11     one lane issues O += P_j V_j
 //               (tcgen05.mma, A operand in tensor memory, B in shared
@@ -260,68 +260,56 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == 0 || warp == 10) {
         // ------------------------------------------------------------ producers
-        // warp 0 fills the K ring, warp 10 the V ring; each reads the block
-        // ids of its next tile one tile ahead
-        if (lane == 0) {
-            const bool is_k = warp == 0;
-            const int NS = is_k ? KST : VST;
-            const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-            uint64_t* full = is_k ? bars.kfull : bars.vfull;
-            uint64_t* empty = is_k ? bars.kempty : bars.vempty;
-            uint32_t* badw = is_k ? bars.kbad : bars.vbad;
-            const uint32_t ring = sbase + (is_k ? OFF_K : OFF_V);
-            prefetch_tensormap(map);
-            int issued[KST] = {-1, -1, -1};   // last tile loaded into each stage
-            int nxt[PPT];
-#pragma unroll
-            for (int i = 0; i < PPT; ++i) nxt[i] = (i < npages) ? table[i] : -1;
-            int st = 0, use = 0;              // stage of tile j, and how often it was used before
-            for (int j = 0; j < nT; ++j) {
-                const int pn = min(PPT, npages - j * PPT);
-                int ids[PPT];
-#pragma unroll
-                for (int i = 0; i < PPT; ++i) ids[i] = nxt[i];
-                if (j + 1 < nT) {
-                    const int p1 = (j + 1) * PPT;
-#pragma unroll
-                    for (int i = 0; i < PPT; ++i) nxt[i] = (p1 + i < npages) ? table[p1 + i] : -1;
-                }
-                uint32_t bad = 0;
-                int nvalid = 0;
-#pragma unroll
-                for (int i = 0; i < PPT; ++i) {
-                    if (i >= pn) {
-                        ids[i] = -1;
-                    } else if (ids[i] >= 0 && ids[i] < a.num_blocks) {
-                        ++nvalid;
-                    } else {
-                        ids[i] = -1;
-                        bad |= 1u << i;
-                    }
-                }
+        // warp 0 fills the K ring, warp 10 the V ring.  Lane i < PPT handles
+        // page i of each tile (its block id read one tile ahead, its two TMA
+        // boxes); lane 0 waits for the stage and posts the expected bytes.
+        const bool is_k = warp == 0;
+        const int NS = is_k ? KST : VST;
+        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+        uint64_t* full = is_k ? bars.kfull : bars.vfull;
+        uint64_t* empty = is_k ? bars.kempty : bars.vempty;
+        uint32_t* badw = is_k ? bars.kbad : bars.vbad;
+        const uint32_t ring = sbase + (is_k ? OFF_K : OFF_V);
+        const bool pl = lane < PPT;   // a page lane
+        if (lane == 0) prefetch_tensormap(map);
+        int issued[KST] = {-1, -1, -1};   // last use of each stage that was loaded
+        int nxt = (pl && lane < npages) ? table[lane] : -1;
+        int st = 0, use = 0;              // stage of tile j, and how often it was used before
+        for (int j = 0; j < nT; ++j) {
+            const int p = j * PPT + lane;
+            int id = nxt;
+            if (j + 1 < nT) nxt = (pl && p + PPT < npages) ? table[p + PPT] : -1;
+            const bool inside = pl && p < npages;
+            const bool valid = inside && id >= 0 && id < a.num_blocks;
+            const uint32_t bad = __ballot_sync(0xffffffffu, inside && !valid);
+            const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+            int ok = 1;
+            if (lane == 0) {
                 if (bad && is_k) raise_error(PA_DEVERR_BLOCK_ID);
-                if (!cta_wait(&empty[st], (use & 1) ^ 1, abort)) break;
-                badw[st] = bad;
-                mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
-                const uint32_t dst = ring + st * TILEB;
-#pragma unroll
-                for (int i = 0; i < PPT; ++i)
-                    if (ids[i] >= 0) {
-                        const int y = (ids[i] * a.Hkv + h) * BS;
-                        tma_load_2d_at(dst + i * BS * 128, map, 0, y, &full[st]);
-                        tma_load_2d_at(dst + HALF + i * BS * 128, map, 64, y, &full[st]);
-                    }
-                issued[st] = use;
-                if (++st == NS) {
-                    st = 0;
-                    ++use;
+                ok = cta_wait(&empty[st], (use & 1) ^ 1, abort) ? 1 : 0;
+                if (ok) {
+                    badw[st] = bad;
+                    mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
                 }
             }
-            if (*abort) {
-                // let this CTA's own copies land before it ends
-                for (int i = 0; i < NS; ++i)
-                    if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (valid) {
+                const uint32_t dst = ring + st * TILEB + lane * BS * 128;
+                const int y = (id * a.Hkv + h) * BS;
+                tma_load_2d_at(dst, map, 0, y, &full[st]);
+                tma_load_2d_at(dst + HALF, map, 64, y, &full[st]);
             }
+            issued[st] = use;
+            if (++st == NS) {
+                st = 0;
+                ++use;
+            }
+        }
+        if (lane == 0 && *abort) {
+            // let this CTA's own copies land before it ends
+            for (int i = 0; i < NS; ++i)
+                if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ S = Q K^T issuer
