@@ -12,22 +12,24 @@
 // its physical block with the 128-byte swizzle).
 //
 //   warp 0      TMA producer of the K tile ring (3 stages), one lane per page
-//   warp 10     TMA producer of the V tile ring (3 stages), one lane per page
+//   warp 18     TMA producer of the V tile ring (3 stages), one lane per page
 //   warp 1      owns the tensor memory; one lane issues S[j%2] = Q K_j^T
-//   warp 11     one lane issues O += P_j V_j
+//   warp 19     one lane issues O += P_j V_j
 //               (tcgen05.mma, A operand in tensor memory, B in shared
 //               memory: K tile K-major, V tile MN-major; two issuing
 //               threads because one cannot keep the tensor core busy with
 //               M=128 x N=128 instructions)
-//   warps 2-9   softmax: a thread holds one query row (its tensor-memory
-//               lane) and one 64-column half of it; keeps the running max
+//   warps 2-17  softmax: a thread holds one query row (its tensor-memory
+//               lane) and a quarter of its columns; keeps the running max
 //               m and sum l in fp32 (log2 domain), writes P (bf16) into
 //               tensor memory, rescales O only when the max grows by more
 //               than 2^8, and finally writes out = O / l.  These warps
 //               also place Q in tensor memory at the start.
 //
 // Tensor memory (32-bit columns): S0 [0,128), S1 [128,256), O [256,384)
-// in fp32; Q [384,448) and P [448,512) as bf16 pairs.  Shared memory holds
+// in fp32; Q [384,448) as bf16 pairs.  P_j (bf16 pairs) is written over the
+// S columns it came from: each softmax warp's quarter of S_j holds its
+// quarter of P_j in its first 16 columns, so P is double-buffered with S.  Shared memory holds
 // only the K and V rings, so the tensor core reads one operand per MMA from
 // it.  Every wait is bounded; on a
 // timeout the CTA records PA_DEVERR_TIMEOUT, drains its own copies and MMAs,
@@ -49,12 +51,14 @@ constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + KST * TILEB;
 constexpr int SMEM_TILES = OFF_V + VST * TILEB;   // 192 KB
 constexpr int SMEM_BYTES = SMEM_TILES + 1024;
-constexpr int NTHREADS = 384;          // K producer, QK issuer, 8 softmax warps, V producer, PV issuer
-constexpr int NSOFT = 256;
+constexpr int NSW = 16;                // softmax warps: four per tensor-memory lane quadrant
+constexpr int NSOFT = NSW * 32;
+constexpr int NCOL = TN / (NSW / 4);   // S / P / O columns one softmax warp handles (32)
+constexpr int W_KPROD = 0, W_QK = 1, W_SOFT0 = 2, W_VPROD = W_SOFT0 + NSW, W_PV = W_VPROD + 1;
+constexpr int NTHREADS = (W_PV + 1) * 32;   // 640
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 constexpr uint32_t COL_Q = 384;
-constexpr uint32_t COL_P = 448;
 constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 256)
 
 struct PrefillArgs {
@@ -69,10 +73,10 @@ struct PrefillArgs {
 
 struct Bars {
     uint64_t kfull[KST], kempty[KST], vfull[VST], vempty[VST];
-    uint64_t q_full, s_full[2], s_free[2], p_full, o_done, drain[2];
-    uint64_t pair[4];            // the two softmax warps of a lane quadrant
-    float red[2][2][128];        // partial row maxima [tile parity][half][row]
-    float red_l[2][128];         // partial row sums [half][row]
+    uint64_t q_full, s_full[2], p_full[2], o_done[2], drain[2];   // [2]: by tile parity
+    uint64_t pair[4];            // the four softmax warps of a lane quadrant
+    float red[2][4][128];        // partial row maxima [tile parity][column quarter][row]
+    float red_l[4][128];         // partial row sums [column quarter][row]
     uint32_t kbad[KST], vbad[VST];   // pages of the stage whose block id was out of range
     uint32_t tmem_base;
     int abort;
@@ -128,14 +132,12 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
         "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -235,18 +237,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars.s_full[i], 1);
-            mbar_init(&bars.s_free[i], NSOFT);
+            mbar_init(&bars.o_done[i], 1);
+            mbar_init(&bars.p_full[i], NSOFT);
         }
-        mbar_init(&bars.p_full, NSOFT);
-        mbar_init(&bars.o_done, 1);
-        for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], 64);
+        for (int i = 0; i < 4; ++i) mbar_init(&bars.pair[i], NSW / 4 * 32);
         mbar_init(&bars.q_full, NSOFT);
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
         bars.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 1) {
+    if (warp == W_QK) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&bars.tmem_base)),
                      "r"(TMEM_COLS)
@@ -258,12 +259,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tc_fence_after();
     const uint32_t tmem = bars.tmem_base;
 
-    if (warp == 0 || warp == 10) {
+    if (warp == W_KPROD || warp == W_VPROD) {
         // ------------------------------------------------------------ producers
         // warp 0 fills the K ring, warp 10 the V ring.  Lane i < PPT handles
         // page i of each tile (its block id read one tile ahead, its two TMA
         // boxes); lane 0 waits for the stage and posts the expected bytes.
-        const bool is_k = warp == 0;
+        const bool is_k = warp == W_KPROD;
         const int NS = is_k ? KST : VST;
         const CUtensorMap* map = is_k ? &tm_k : &tm_v;
         uint64_t* full = is_k ? bars.kfull : bars.vfull;
@@ -311,7 +312,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int i = 0; i < NS; ++i)
                 if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
         }
-    } else if (warp == 1) {
+    } else if (warp == W_QK) {
         // ------------------------------------------------------------ S = Q K^T issuer
         constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
         const uint64_t kd0 = smem_desc(sbase + OFF_K, 16, 1024);   // + (byte offset >> 4) per MMA
@@ -327,7 +328,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();
             }
             __syncwarp();
-            if (!(ok = cta_wait(&bars.s_free[sb], ((j >> 1) & 1) ^ 1, abort))) break;
+            // S buffer j%2 holds P_{j-2} until P_{j-2} V_{j-2} has finished
+            if (j >= 2 && !(ok = cta_wait(&bars.o_done[sb], ((j >> 1) & 1) ^ 1, abort))) break;
             tc_fence_after();
             if (lane == 0) {
                 const uint32_t d_tmem = tmem + (uint32_t)sb * TN;
@@ -351,7 +353,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_wait(&bars.drain[0], 0);
         }
         __syncwarp();
-    } else if (warp == 11) {
+    } else if (warp == W_PV) {
         // ------------------------------------------------------------ O += P V issuer
         // (a second issuing thread: one thread alone cannot issue MMAs of this
         // size as fast as the tensor core retires them)
@@ -368,15 +370,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_smem();
             }
             __syncwarp();
-            if (!(ok = cta_wait(&bars.p_full, j & 1, abort))) break;
+            if (!(ok = cta_wait(&bars.p_full[j & 1], (j >> 1) & 1, abort))) break;
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t vd = vd0 + (uint64_t)((vs * TILEB) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < TN / 16; ++kk)
-                    umma_ts(tmem + COL_O, tmem + COL_P + kk * 8, vd + (uint64_t)((kk * 2048) >> 4), ID_O,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-                umma_commit(&bars.o_done);
+                for (int kk = 0; kk < TN / 16; ++kk)   // P_j: quarter kk/2 of S buffer j%2, 16 packed columns each
+                    umma_ts(tmem + COL_O, tmem + (uint32_t)(j & 1) * TN + (kk >> 1) * NCOL + (kk & 1) * 8,
+                            vd + (uint64_t)((kk * 2048) >> 4), ID_O, (j > 0 || kk > 0) ? 1u : 0u);
+                umma_commit(&bars.o_done[j & 1]);
                 umma_commit(&bars.vempty[vs]);
             }
             __syncwarp();
@@ -392,24 +394,25 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax
-        // warps 2..9: quad = warp % 4 selects the tensor-memory lanes (query
-        // rows) the warp may access; hf selects the 64-column half of S, P
-        // and O it handles.  The two warps of a quad exchange their partial
-        // row maxima (and, at the end, row sums) through shared memory.
-        const int quad = warp & 3, hf = (warp - 2) >> 2;
+        // warps W_SOFT0 .. W_SOFT0+15: quad = warp % 4 selects the tensor-
+        // memory lanes (query rows) the warp may access; qc the quarter of the
+        // 128 columns of S, P and O it handles.  The four warps of a quad
+        // exchange their partial row maxima (and, at the end, row sums)
+        // through shared memory.
+        const int quad = warp & 3, qc = (warp - W_SOFT0) >> 2;
         const int r = quad * 32 + lane;
         const int tok = t0 + r / G, g = r % G;
         const bool valid_row = tok < C;
         const int qpos = valid_row ? L - C + tok : -1;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         {
-            // this half of the Q row -> tensor memory (bf16 pairs, element
+            // this quarter of the Q row -> tensor memory (bf16 pairs, element
             // 2i in the low half of column i)
             const uint4* src =
-                reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + hf * 8;
-            uint32_t qv[32];
+                reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + qc * 4;
+            uint32_t qv[16];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
+            for (int u = 0; u < 4; ++u) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid_row) v = __ldg(src + u);
                 qv[4 * u] = v.x;
@@ -417,93 +420,86 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qv[4 * u + 2] = v.z;
                 qv[4 * u + 3] = v.w;
             }
-            tmem_st32u(tmem + lane_off + COL_Q + hf * 32, qv);
+            tmem_st16u(tmem + lane_off + COL_Q + qc * 16, qv);
             tc_fence_before();
             mbar_arrive(&bars.q_full);
         }
         const float sl2 = a.scale_log2;
-        float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this half's sum
+        float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this quarter's sum
         bool ok = true;
         for (int j = 0; j < nT; ++j) {
             const int s = j & 1;
             if (!(ok = cta_wait(&bars.s_full[s], (j >> 1) & 1, abort))) break;
             tc_fence_after();
-            float x[64];
-            tmem_ld32(tmem + lane_off + s * TN + hf * 64, &x[0]);
-            tmem_ld32(tmem + lane_off + s * TN + hf * 64 + 32, &x[32]);
-            tc_fence_before();
-            mbar_arrive(&bars.s_free[s]);
-            const int lim = qpos - j * TN - hf * 64;   // columns c <= lim are visible to this row
-            if (lim < 63) {
+            float x[NCOL];
+            tmem_ld32(tmem + lane_off + s * TN + qc * NCOL, x);
+            const int lim = qpos - j * TN - qc * NCOL;   // columns c <= lim are visible to this row
+            if (lim < NCOL - 1) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
+                for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
             }
             float mx8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx8[i] = x[i];
 #pragma unroll
-            for (int c = 8; c < 64; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+            for (int c = 8; c < NCOL; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
             const float mxs = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
-            bars.red[j & 1][hf][r] = mxs;
+            bars.red[j & 1][qc][r] = mxs;
             mbar_arrive(&bars.pair[quad]);
             if (!(ok = cta_wait(&bars.pair[quad], j & 1, abort))) break;
-            const float m_new = fmaxf(m, fmaxf(mxs, bars.red[j & 1][hf ^ 1][r]));
+            const float mt = fmaxf(fmaxf(bars.red[j & 1][0][r], bars.red[j & 1][1][r]),
+                                   fmaxf(bars.red[j & 1][2][r], bars.red[j & 1][3][r]));
+            const float m_new = fmaxf(m, mt);
             const bool rescale = m_new > m + RESCALE_LOG2;
             const float m_next = rescale ? m_new : m;
             const float mb = (m_next == -INFINITY) ? 0.f : m_next;
-            uint32_t w[32];
+            uint32_t w[NCOL / 2];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < NCOL; c += 2) {
                 const float p0 = ex2(fmaf(x[c], sl2, -mb));
                 const float p1 = ex2(fmaf(x[c + 1], sl2, -mb));
                 ls[(c >> 1) & 3] += p0 + p1;
                 w[c >> 1] = pack_bf16x2(p0, p1);
             }
-            if (j > 0) {
-                // P_{j-1} V_{j-1} has finished: O is stable and the P buffer free
-                if (!(ok = cta_wait(&bars.o_done, (j - 1) & 1, abort))) break;
-                tc_fence_after();
-            }
             if (rescale && m != -INFINITY) {
+                // O must be stable: P_{j-1} V_{j-1} has finished
+                if (!(ok = cta_wait(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) break;
+                tc_fence_after();
                 const float alpha = ex2(m - m_new);
                 l *= alpha;
+                float o[NCOL];
+                tmem_ld32(tmem + lane_off + COL_O + qc * NCOL, o);
 #pragma unroll
-                for (int c = 0; c < 64; c += 32) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_off + COL_O + hf * 64 + c, o);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(tmem + lane_off + COL_O + hf * 64 + c, o);
-                }
+                for (int i = 0; i < NCOL; ++i) o[i] *= alpha;
+                tmem_st32(tmem + lane_off + COL_O + qc * NCOL, o);
             }
             m = m_next;
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            tmem_st32u(tmem + lane_off + COL_P + hf * 32, w);
+            // P_j over the S columns this warp has just read (its own quarter)
+            tmem_st16u(tmem + lane_off + s * TN + qc * NCOL, w);
             tc_fence_before();
-            mbar_arrive(&bars.p_full);
+            mbar_arrive(&bars.p_full[s]);
         }
-        if (ok && cta_wait(&bars.o_done, (nT - 1) & 1, abort)) {
+        if (ok && cta_wait(&bars.o_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, abort)) {
             tc_fence_after();
-            bars.red_l[hf][r] = l;
+            bars.red_l[qc][r] = l;
             mbar_arrive(&bars.pair[quad]);
             if (cta_wait(&bars.pair[quad], nT & 1, abort)) {
-                const float lt = l + bars.red_l[hf ^ 1][r];
+                const float lt = (bars.red_l[0][r] + bars.red_l[1][r]) + (bars.red_l[2][r] + bars.red_l[3][r]);
                 const float inv = lt > 0.f ? 1.f / lt : 0.f;
-                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + hf * 8;
+                uint4* dst =
+                    reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + qc * (NCOL / 8);
+                float o[NCOL];
+                tmem_ld32(tmem + lane_off + COL_O + qc * NCOL, o);
+                if (valid_row) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 32) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_off + COL_O + hf * 64 + c, o);
-                    if (valid_row) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            dst[c / 8 + v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
-                    }
+                    for (int v = 0; v < NCOL / 8; ++v)
+                        dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                            pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                            pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                            pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
                 }
             }
         }
@@ -511,7 +507,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 1) {
+    if (warp == W_QK) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
                      : "memory");
