@@ -187,6 +187,15 @@ def dist_init():
     return None, 0, 1
 
 
+def max_over_ranks(t: float, dist, device="cpu") -> float:
+    """The slowest rank's time (every rank gets it); t itself on one process."""
+    if not dist:
+        return t
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt[0])
+
+
 def cpu_oracle_baseline(w, tables, budget_s=10.0, threads=None):
     """The fp64 oracle's step (append of the new token + decode attention) on a bounded
     sample of the batch, repeated until ~budget_s of wall time.  Returns dict."""
@@ -327,11 +336,7 @@ def run_ours(args):
             ev[i][1].record(stream)
         torch.cuda.synchronize()
         t = sum(x.elapsed_time(y) for x, y in ev) / 1e3
-        if dist:
-            tt = torch.tensor([t], dtype=torch.float64, device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t = float(tt[0])
-        return t
+        return max_over_ranks(t, dist, dev)
 
     K = args.steps
     # the step: pa_decode_step (append of every new token + attention, one launch)
