@@ -97,6 +97,15 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// D (+)= A B, both operands described by shared-memory matrix descriptors
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
 // D (+)= A B with the A operand (M x K, bf16 pairs along the columns) in tensor memory
 // and B described by a shared-memory matrix descriptor
 __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -196,6 +205,62 @@ __device__ __forceinline__ void zero_tile_rows(uint32_t tile, int r0, uint32_t b
     }
 }
 
+// TMA producer of one ring of NS tile stages (one warp).  Tile j (128 tokens)
+// goes into stage j % NS.  Lane i < 128/BS handles page i of each tile: it
+// reads the page's block id one tile ahead and issues the page's two
+// 128-byte-swizzled boxes.  Lane 0 waits for the stage to be free and posts the
+// bytes to expect.  Out-of-range ids are skipped and reported in badw[stage]
+// (and, when report_bad, in the device error word).  On an abort, lane 0 waits
+// for the copies this warp issued.
+template <int BS, int NS>
+__device__ __forceinline__ void produce_ring(const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t* badw,
+                                             uint32_t ring, const int32_t* table, int nT, int npages, int num_blocks,
+                                             int Hkv, int h, bool report_bad, volatile int* abort, int lane) {
+    constexpr int PPT = TN / BS;
+    const bool pl = lane < PPT;   // a page lane
+    if (lane == 0) prefetch_tensormap(map);
+    int issued[NS];               // last use of each stage that was loaded
+#pragma unroll
+    for (int i = 0; i < NS; ++i) issued[i] = -1;
+    int nxt = (pl && lane < npages) ? table[lane] : -1;
+    int st = 0, use = 0;          // stage of tile j, and how often it was used before
+    for (int j = 0; j < nT; ++j) {
+        const int p = j * PPT + lane;
+        const int id = nxt;
+        if (j + 1 < nT) nxt = (pl && p + PPT < npages) ? table[p + PPT] : -1;
+        const bool inside = pl && p < npages;
+        const bool valid = inside && id >= 0 && id < num_blocks;
+        const uint32_t bad = __ballot_sync(0xffffffffu, inside && !valid);
+        const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
+        int ok = 1;
+        if (lane == 0) {
+            if (bad && report_bad) raise_error(PA_DEVERR_BLOCK_ID);
+            ok = cta_wait(&empty[st], (use & 1) ^ 1, abort) ? 1 : 0;
+            if (ok) {
+                badw[st] = bad;
+                mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (valid) {
+            const uint32_t dst = ring + st * TILEB + lane * BS * 128;
+            const int y = (id * Hkv + h) * BS;
+            tma_load_2d_at(dst, map, 0, y, &full[st]);
+            tma_load_2d_at(dst + HALF, map, 64, y, &full[st]);
+        }
+        issued[st] = use;
+        if (++st == NS) {
+            st = 0;
+            ++use;
+        }
+    }
+    if (lane == 0 && *abort) {
+        for (int i = 0; i < NS; ++i)
+            if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
+    }
+}
+
 template <int BS>
 __global__ void __launch_bounds__(NTHREADS, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -261,57 +326,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp == W_KPROD || warp == W_VPROD) {
         // ------------------------------------------------------------ producers
-        // warp 0 fills the K ring, warp 10 the V ring.  Lane i < PPT handles
-        // page i of each tile (its block id read one tile ahead, its two TMA
-        // boxes); lane 0 waits for the stage and posts the expected bytes.
         const bool is_k = warp == W_KPROD;
-        const int NS = is_k ? KST : VST;
-        const CUtensorMap* map = is_k ? &tm_k : &tm_v;
-        uint64_t* full = is_k ? bars.kfull : bars.vfull;
-        uint64_t* empty = is_k ? bars.kempty : bars.vempty;
-        uint32_t* badw = is_k ? bars.kbad : bars.vbad;
-        const uint32_t ring = sbase + (is_k ? OFF_K : OFF_V);
-        const bool pl = lane < PPT;   // a page lane
-        if (lane == 0) prefetch_tensormap(map);
-        int issued[KST] = {-1, -1, -1};   // last use of each stage that was loaded
-        int nxt = (pl && lane < npages) ? table[lane] : -1;
-        int st = 0, use = 0;              // stage of tile j, and how often it was used before
-        for (int j = 0; j < nT; ++j) {
-            const int p = j * PPT + lane;
-            int id = nxt;
-            if (j + 1 < nT) nxt = (pl && p + PPT < npages) ? table[p + PPT] : -1;
-            const bool inside = pl && p < npages;
-            const bool valid = inside && id >= 0 && id < a.num_blocks;
-            const uint32_t bad = __ballot_sync(0xffffffffu, inside && !valid);
-            const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
-            int ok = 1;
-            if (lane == 0) {
-                if (bad && is_k) raise_error(PA_DEVERR_BLOCK_ID);
-                ok = cta_wait(&empty[st], (use & 1) ^ 1, abort) ? 1 : 0;
-                if (ok) {
-                    badw[st] = bad;
-                    mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
-                }
-            }
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            if (valid) {
-                const uint32_t dst = ring + st * TILEB + lane * BS * 128;
-                const int y = (id * a.Hkv + h) * BS;
-                tma_load_2d_at(dst, map, 0, y, &full[st]);
-                tma_load_2d_at(dst + HALF, map, 64, y, &full[st]);
-            }
-            issued[st] = use;
-            if (++st == NS) {
-                st = 0;
-                ++use;
-            }
-        }
-        if (lane == 0 && *abort) {
-            // let this CTA's own copies land before it ends
-            for (int i = 0; i < NS; ++i)
-                if (issued[i] >= 0) mbar_wait(&full[i], issued[i] & 1);
-        }
+        if (is_k)
+            produce_ring<BS, KST>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + OFF_K, table, nT, npages,
+                                  a.num_blocks, a.Hkv, h, true, abort, lane);
+        else
+            produce_ring<BS, VST>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + OFF_V, table, nT, npages,
+                                  a.num_blocks, a.Hkv, h, false, abort, lane);
     } else if (warp == W_QK) {
         // ------------------------------------------------------------ S = Q K^T issuer
         constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
@@ -514,17 +535,301 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
+// ------------------------------------------------------------------ two query tiles per CTA
+// For chunks longer than one tile: the CTA owns 256 query rows (tiles A and
+// B, consecutive tokens) of one (sequence, kv head), so every K/V tile feeds
+// twice the MMA work.  Same warp roles as above; the softmax warps alternate
+// between the tiles, so the tensor core works on one tile while the softmax
+// works on the other.  Q_A / Q_B are in shared memory (A operand of Q K^T by
+// descriptor), the K and V rings have two stages each, and tensor memory holds
+// S_A [0,128), S_B [128,256), O_A [256,384), O_B [384,512); P_t is written
+// over the S_t quarter its warp has just read, so Q K_{j+1}^T of tile t waits
+// for P_t(j) V_j.
+constexpr int P2_OFF_Q = 0;
+constexpr int P2_OFF_K = 2 * TILEB;
+constexpr int P2_OFF_V = P2_OFF_K + 2 * TILEB;
+constexpr int P2_SMEM_BYTES = P2_OFF_V + 2 * TILEB + 1024;   // 192 KB + alignment
+
+struct Bars2 {
+    uint64_t kfull[2], kempty[2], vfull[2], vempty[2];
+    uint64_t q_full, s_full[2], p_full[2], o_done[2], drain[2];   // [2]: query tile
+    uint64_t pair[2][4];                                          // [tile][lane quadrant]
+    float red[2][2][4][128];     // partial row maxima [tile][tile parity j][column quarter][row]
+    float red_l[2][4][128];      // partial row sums [tile][column quarter][row]
+    uint32_t kbad[2], vbad[2];
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int BS>
+__global__ void __launch_bounds__(NTHREADS, 1)
+    paged_prefill2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                          const PrefillArgs a) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    __shared__ Bars2 bars;
+    const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, h = blockIdx.y;
+    const int qt = gridDim.x - 1 - blockIdx.x;  // later (longer) query tiles first
+    const int G = a.G, T = TM / G;
+
+    const int qs0 = a.q_start[b];
+    const int C = a.q_start[b + 1] - qs0;
+    const int L = a.lens[b];
+    if (C < 0 || C > L || L > a.M * BS || C > a.max_q) {
+        if (tid == 0 && h == 0 && qt == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        return;
+    }
+    const int t0 = qt * 2 * T;                  // first token of tile A
+    if (t0 >= C) return;
+    const int tv = min(2 * T, C - t0);          // valid query tokens in the two tiles
+    const int nkv = L - C + t0 + tv;            // KV positions needed: 0 .. nkv-1
+    const int nT = (nkv + TN - 1) / TN;
+    const int npages = (nkv + BS - 1) / BS;
+    const int32_t* table = a.tables + (int64_t)b * a.M;
+    volatile int* abort = &bars.abort;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars.kfull[i], 1);
+            mbar_init(&bars.kempty[i], 1);
+            mbar_init(&bars.vfull[i], 1);
+            mbar_init(&bars.vempty[i], 1);
+            mbar_init(&bars.s_full[i], 1);
+            mbar_init(&bars.o_done[i], 1);
+            mbar_init(&bars.p_full[i], NSOFT);
+            mbar_init(&bars.drain[i], 1);
+            for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[i][q], NSW / 4 * 32);
+        }
+        mbar_init(&bars.q_full, NSOFT);
+        bars.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == W_QK) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&bars.tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars.tmem_base;
+
+    if (warp == W_KPROD || warp == W_VPROD) {
+        if (warp == W_KPROD)
+            produce_ring<BS, 2>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + P2_OFF_K, table, nT, npages,
+                                a.num_blocks, a.Hkv, h, true, abort, lane);
+        else
+            produce_ring<BS, 2>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + P2_OFF_V, table, nT, npages,
+                                a.num_blocks, a.Hkv, h, false, abort, lane);
+    } else if (warp == W_QK) {
+        // ------------------------------------------------------------ S_t = Q_t K_j^T issuer
+        constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
+        const uint64_t qd0 = smem_desc(sbase + P2_OFF_Q, 16, 1024);
+        const uint64_t kd0 = smem_desc(sbase + P2_OFF_K, 16, 1024);
+        bool ok = cta_wait(&bars.q_full, 0, abort);
+        tc_fence_after();
+        for (int j = 0; ok && j < nT; ++j) {
+            const int ks = j & 1;
+            if (!(ok = cta_wait(&bars.kfull[ks], (j >> 1) & 1, abort))) break;
+            const uint32_t kbad = bars.kbad[ks];
+            if (kbad) {
+                zero_tile_rows(sbase + P2_OFF_K + ks * TILEB, TN, kbad, BS, lane);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            for (int t = 0; ok && t < 2; ++t) {
+                // S_t holds P_t(j-1) until P_t(j-1) V_{j-1} has finished
+                if (j > 0 && !(ok = cta_wait(&bars.o_done[t], (j - 1) & 1, abort))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t qd = qd0 + (uint64_t)((t * TILEB) >> 4);
+                    const uint64_t kd = kd0 + (uint64_t)((ks * TILEB) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint64_t off = (uint64_t)(((kk >> 2) * HALF + (kk & 3) * 32) >> 4);
+                        umma_ss(tmem + (uint32_t)t * TN, qd + off, kd + off, ID_S, kk > 0);
+                    }
+                    umma_commit(&bars.s_full[t]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&bars.kempty[ks]);
+            __syncwarp();
+        }
+        if (lane == 0) {
+            umma_commit(&bars.drain[0]);
+            mbar_wait(&bars.drain[0], 0);
+        }
+        __syncwarp();
+    } else if (warp == W_PV) {
+        // ------------------------------------------------------------ O_t += P_t V_j issuer
+        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
+        const uint64_t vd0 = smem_desc(sbase + P2_OFF_V, HALF, 1024);
+        bool ok = true;
+        for (int j = 0; ok && j < nT; ++j) {
+            const int vs = j & 1;
+            if (!(ok = cta_wait(&bars.vfull[vs], (j >> 1) & 1, abort))) break;
+            const int rz = (j == nT - 1) ? nkv - j * TN : TN;   // rows past the last needed position
+            const uint32_t vbad = bars.vbad[vs];
+            if (rz < TN || vbad) {
+                zero_tile_rows(sbase + P2_OFF_V + vs * TILEB, rz, vbad, BS, lane);
+                fence_proxy_async_smem();
+            }
+            __syncwarp();
+            for (int t = 0; ok && t < 2; ++t) {
+                if (!(ok = cta_wait(&bars.p_full[t], j & 1, abort))) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t vd = vd0 + (uint64_t)((vs * TILEB) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < TN / 16; ++kk)   // P_t: quarter kk/2 of S_t, 16 packed columns each
+                        umma_ts(tmem + COL_O + (uint32_t)t * TN, tmem + (uint32_t)t * TN + (kk >> 1) * NCOL + (kk & 1) * 8,
+                                vd + (uint64_t)((kk * 2048) >> 4), ID_O, (j > 0 || kk > 0) ? 1u : 0u);
+                    umma_commit(&bars.o_done[t]);
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) umma_commit(&bars.vempty[vs]);
+            __syncwarp();
+        }
+        if (lane == 0) {
+            umma_commit(&bars.drain[1]);
+            mbar_wait(&bars.drain[1], 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ softmax (both tiles)
+        const int quad = warp & 3, qc = (warp - W_SOFT0) >> 2;
+        const int r = quad * 32 + lane;
+        const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        int tok[2], qpos[2];
+        bool valid_row[2];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            tok[t] = t0 + t * T + r / G;
+            valid_row[t] = tok[t] < C;
+            qpos[t] = valid_row[t] ? L - C + tok[t] : -1;
+        }
+        const int g = r % G;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+            // this quarter of the Q row of tile t -> shared memory, 128-byte swizzled
+            const uint4* src =
+                reinterpret_cast<const uint4*>(a.q + ((int64_t)(qs0 + tok[t]) * a.Hq + h * G + g) * D) + qc * 4;
+            const uint32_t row = sbase + P2_OFF_Q + t * TILEB + (qc >> 1) * HALF + r * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (valid_row[t]) v = __ldg(src + i);
+                const int u = (qc & 1) * 4 + i;
+                st_shared_v4(row + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.q_full);
+        const float sl2 = a.scale_log2;
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        bool ok = true;
+        for (int j = 0; ok && j < nT; ++j) {
+#pragma unroll 1
+            for (int t = 0; t < 2; ++t) {
+                if (!(ok = cta_wait(&bars.s_full[t], j & 1, abort))) break;
+                tc_fence_after();
+                float x[NCOL];
+                tmem_ld32(tmem + lane_off + t * TN + qc * NCOL, x);
+                const int lim = qpos[t] - j * TN - qc * NCOL;
+                if (lim < NCOL - 1) {
+#pragma unroll
+                    for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
+                }
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = x[i];
+#pragma unroll
+                for (int c = 8; c < NCOL; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
+                const float mxs = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+                bars.red[t][j & 1][qc][r] = mxs;
+                mbar_arrive(&bars.pair[t][quad]);
+                if (!(ok = cta_wait(&bars.pair[t][quad], j & 1, abort))) break;
+                const float mt = fmaxf(fmaxf(bars.red[t][j & 1][0][r], bars.red[t][j & 1][1][r]),
+                                       fmaxf(bars.red[t][j & 1][2][r], bars.red[t][j & 1][3][r]));
+                const float m_new = fmaxf(m[t], mt);
+                const bool rescale = m_new > m[t] + RESCALE_LOG2;
+                const float m_next = rescale ? m_new : m[t];
+                const float mb = (m_next == -INFINITY) ? 0.f : m_next;
+                uint32_t w[NCOL / 2];
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int c = 0; c < NCOL; c += 2) {
+                    const float p0 = ex2(fmaf(x[c], sl2, -mb));
+                    const float p1 = ex2(fmaf(x[c + 1], sl2, -mb));
+                    ls[(c >> 1) & 3] += p0 + p1;
+                    w[c >> 1] = pack_bf16x2(p0, p1);
+                }
+                if (rescale && m[t] != -INFINITY) {
+                    // O_t must be stable: P_t(j-1) V_{j-1} has finished (Q K_j^T waited for it)
+                    if (!(ok = cta_wait(&bars.o_done[t], (j - 1) & 1, abort))) break;
+                    tc_fence_after();
+                    const float alpha = ex2(m[t] - m_new);
+                    l[t] *= alpha;
+                    float o[NCOL];
+                    tmem_ld32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
+#pragma unroll
+                    for (int i = 0; i < NCOL; ++i) o[i] *= alpha;
+                    tmem_st32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
+                }
+                m[t] = m_next;
+                l[t] += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                tmem_st16u(tmem + lane_off + t * TN + qc * NCOL, w);
+                tc_fence_before();
+                mbar_arrive(&bars.p_full[t]);
+            }
+        }
+#pragma unroll 1
+        for (int t = 0; ok && t < 2; ++t) {
+            if (!(ok = cta_wait(&bars.o_done[t], (nT - 1) & 1, abort))) break;
+            tc_fence_after();
+            bars.red_l[t][qc][r] = l[t];
+            mbar_arrive(&bars.pair[t][quad]);
+            if (!(ok = cta_wait(&bars.pair[t][quad], nT & 1, abort))) break;
+            const float lt = (bars.red_l[t][0][r] + bars.red_l[t][1][r]) + (bars.red_l[t][2][r] + bars.red_l[t][3][r]);
+            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            float o[NCOL];
+            tmem_ld32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
+            if (valid_row[t]) {
+                uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok[t]) * a.Hq + h * G + g) * D) +
+                             qc * (NCOL / 8);
+#pragma unroll
+                for (int v = 0; v < NCOL / 8; ++v)
+                    dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == W_QK) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
 template <int BS>
 cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
-    static bool attr_set[64] = {};
+    static bool attr_set[64][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(paged_prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
-    }
     PrefillArgs a;
     a.out = static_cast<__nv_bfloat16*>(L.out);
     a.q = static_cast<const __nv_bfloat16*>(L.q);
@@ -539,8 +844,23 @@ cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
     a.max_q = L.max_q;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     const int T = TM / a.G;
-    dim3 grid((unsigned)((L.max_q + T - 1) / T), (unsigned)L.Hkv, (unsigned)L.B);
-    paged_prefill_kernel<BS><<<grid, NTHREADS, SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+    // chunks longer than one 128-row tile: two tiles per CTA share each K/V tile
+    const bool two = L.max_q > T;
+    if (dev >= 0 && dev < 64 && !attr_set[dev][two]) {
+        e = two ? cudaFuncSetAttribute(paged_prefill2_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       P2_SMEM_BYTES)
+                : cudaFuncSetAttribute(paged_prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        attr_set[dev][two] = true;
+    }
+    if (two) {
+        dim3 grid((unsigned)((L.max_q + 2 * T - 1) / (2 * T)), (unsigned)L.Hkv, (unsigned)L.B);
+        paged_prefill2_kernel<BS><<<grid, NTHREADS, P2_SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+    } else {
+        dim3 grid((unsigned)((L.max_q + T - 1) / T), (unsigned)L.Hkv, (unsigned)L.B);
+        paged_prefill_kernel<BS><<<grid, NTHREADS, SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+    }
     return cudaGetLastError();
 }
 
