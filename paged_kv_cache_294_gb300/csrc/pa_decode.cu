@@ -317,8 +317,27 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* 
 template <int D>
 __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int b, int h, int nsplit, int tid,
                                            int nthr, int warp, int nwarps, int lane, void (*sync)()) {
+    // Each thread owns elements idx = tid + e * nthr of the group's G x D
+    // outputs.  The partials of a chunk of KC partitions are loaded for all
+    // of a thread's elements at once (independent loads, one round trip),
+    // and the first chunk is in flight while the weights are computed.
+    constexpr int EMAX = 8, KC = 4;    // G * D <= 8 * 128 <= EMAX * nthr for the 160-thread CTA
     const int G = a.G;
     const int64_t row0 = (int64_t)b * a.Hq + h * G;
+    const int ne = G * D;
+    float pv[EMAX][KC], acc[EMAX];
+    auto load_chunk = [&](int k0) {
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            const int idx = tid + e * nthr;
+            const int gq = idx / D, dim = idx - gq * D;
+            const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
+#pragma unroll
+            for (int kk = 0; kk < KC; ++kk)
+                pv[e][kk] = (idx < ne && k0 + kk < nsplit) ? __ldcg(op + (int64_t)(k0 + kk) * D) : 0.f;
+        }
+    };
+    load_chunk(0);
     for (int i = tid; i < G * nsplit; i += nthr) {
         const int gq = i / nsplit, k = i - gq * nsplit;
         sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
@@ -339,13 +358,28 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int 
         for (int k = lane; k < nsplit; k += 32) wr[k] = exp2f(wr[k] - mx) * inv;
     }
     sync();
-    for (int idx = tid; idx < G * D; idx += nthr) {
-        const int gq = idx / D, dim = idx - gq * D;
-        const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
-        const float* wr = sw + gq * nsplit;
-        float acc = 0.f;
-        for (int k = 0; k < nsplit; ++k) acc = fmaf(wr[k], __ldcg(op + (int64_t)k * D), acc);
-        a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc);
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
+    for (int k0 = 0; k0 < nsplit; k0 += KC) {
+        if (k0 > 0) load_chunk(k0);
+#pragma unroll
+        for (int e = 0; e < EMAX; ++e) {
+            const int idx = tid + e * nthr;
+            const int gq = idx / D;
+            if (idx < ne) {
+#pragma unroll
+                for (int kk = 0; kk < KC; ++kk)
+                    if (k0 + kk < nsplit) acc[e] = fmaf(sw[gq * nsplit + k0 + kk], pv[e][kk], acc[e]);
+            }
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < EMAX; ++e) {
+        const int idx = tid + e * nthr;
+        if (idx < ne) {
+            const int gq = idx / D, dim = idx - gq * D;
+            a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc[e]);
+        }
     }
 }
 
