@@ -59,7 +59,7 @@ typedef enum {
     PA_ERR_INVALID = 1,     /* bad argument (shape, null pointer, range, workspace too small) */
     PA_ERR_OOM = 2,         /* allocator: not enough free blocks (nothing was taken) */
     PA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed */
-    PA_ERR_UNSUPPORTED = 4  /* valid request this build does not implement (e.g. fp8 with head_dim 64) */
+    PA_ERR_UNSUPPORTED = 4  /* a valid request the library does not implement (e.g. fp8 with head_dim 64) */
 } pa_status;
 
 typedef enum {
