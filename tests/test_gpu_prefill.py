@@ -141,3 +141,37 @@ def test_unsupported_shapes_and_bad_arguments():
         pa.pa_prefill_attention(torch.empty_like(q), q, layer.k_cache, layer.v_cache, None, None,
                                 layer.block_tables, layer.seq_lens, torch.from_numpy(w.q_start).cuda(), -1,
                                 w.scale)
+
+
+def _sampled_rows_match(w, layer, got, rows):
+    caches = {}
+    for r in rows:
+        b = int(np.searchsorted(w.q_start, r, side="right") - 1)
+        C = int(w.q_start[b + 1] - w.q_start[b])
+        pos = int(w.seq_lens[b]) - C + (r - int(w.q_start[b]))
+        if b not in caches:
+            caches[b] = oracle.run.OracleStep(w, seqs=[b], tables=layer.tables_host)
+        ref = oracle.prefill_attention(caches[b].cache, w.q_chunk[r:r + 1], layer.tables_host[b:b + 1],
+                                       np.array([pos + 1]), np.array([0, 1]), w.Hq, w.scale)
+        assert excess(got[r:r + 1], ref, BF16_TOL) <= 1.0, "row %d" % r
+
+
+@pytest.mark.parametrize("layer_name", ["8b", "70b"])
+def test_bench_prefill_configuration_sampled(layer_name):
+    # the batch bench.py times: 16 sequences of 2048 cached tokens + a 2048-token chunk
+    w = workloads.make_prefill(layer_name, [2048] * 16, [2048] * 16, seed=31, device="cuda")
+    layer, got = _gpu(w)
+    rng = np.random.default_rng(1)
+    rows = sorted(set(int(x) for x in rng.integers(0, int(w.q_start[-1]), 20)) | {0, 2047, 16 * 2048 - 1})
+    _sampled_rows_match(w, layer, got, rows)
+
+
+@pytest.mark.parametrize("layer_name", ["8b", "70b"])
+def test_bench_verify_configuration_sampled(layer_name):
+    # the verify batch bench.py times: 64 sequences, U[128, 4096] cached, 4 proposals + 1
+    rng = np.random.default_rng(7)
+    ctx = [int(x) for x in rng.integers(128, 4097, 64)]
+    w = workloads.make_prefill(layer_name, ctx, [5] * 64, seed=31, device="cuda")
+    layer, got = _gpu(w)
+    rows = sorted(set(int(x) for x in np.random.default_rng(2).integers(0, int(w.q_start[-1]), 24)) | {0, 319})
+    _sampled_rows_match(w, layer, got, rows)
