@@ -402,6 +402,28 @@ def run_ours(args):
     copy_gbs = copy_bytes * K / t_copy / 1e9
     del ck, cv, cks, cvs
 
+    # host prefix cache (pa_prefix_match + pa_prefix_insert through BlockManager):
+    # 1000 requests, each one of 8 system prompts of 2304 tokens plus its own
+    # U[1, 512] tokens; admit (match + allocate), commit (insert), free
+    prefix = None
+    if not args.no_extras:
+        from paged_kv_cache_294_gb300.engine import BlockManager
+        prng = np.random.default_rng(11)
+        prompts = [[int(x) for x in prng.integers(0, 32000, 2304)] for _ in range(8)]
+        reqs = [prompts[int(prng.integers(0, 8))] + [int(x) for x in prng.integers(32000, 64000, int(prng.integers(1, 513)))]
+                for _ in range(1000)]
+        mgr = BlockManager(w.num_blocks, w.bs)
+        reused = 0
+        t0 = time.perf_counter()
+        for i, toks in enumerate(reqs):
+            reused += mgr.add(i, toks)
+            mgr.commit(i)
+            mgr.free(i)
+        t_host = time.perf_counter() - t0
+        prefix = {"requests": len(reqs), "us_per_request": 1e6 * t_host / len(reqs),
+                  "reused_token_fraction": reused / sum(len(t) for t in reqs),
+                  "calls": "BlockManager.add (pa_prefix_match + pa_block_alloc), commit (pa_prefix_insert), free"}
+
     # multi-query attention (pa_prefill_attention) on this workload's layer shape:
     # a chunked-prefill batch (16 sequences, 2048 cached + a 2048-token chunk) and
     # a speculative-verify batch (64 sequences, 4 proposals + 1, U[128, 4096] cached)
@@ -464,6 +486,7 @@ def run_ours(args):
         "attention_only": {"GBps": alg * K / t_attn / 1e9, "us": 1e6 * t_attn / K,
                            "calls": "pa_decode_attention"},
         "multi_query_attention": extras,
+        "prefix_cache_host": prefix,
         "copy_blocks": {"GBps": round(copy_gbs, 1), "frac": round(copy_gbs / hbm_peak()[0], 4),
                         "us": 1e6 * t_copy / K, "blocks": nb_copy, "bytes": copy_bytes,
                         "calls": "pa_copy_blocks (copy-on-write of whole K/V pages)"},

@@ -257,6 +257,8 @@ typedef struct pa_allocator pa_allocator;
 
 /* NULL on bad arguments (num_blocks < 0, block_size <= 0) or out of memory. */
 pa_allocator* pa_allocator_create(int num_blocks, int block_size);
+/* Releases the allocator (deferred while prefix caches created on it remain,
+ * see pa_prefix_cache_destroy). */
 void pa_allocator_destroy(pa_allocator* a);
 /* n blocks, all or nothing; ids written to out_ids[0..n-1].  PA_ERR_OOM if
  * fewer than n are free (nothing taken). */
@@ -322,7 +324,9 @@ pa_status pa_prefill_attention(void* out, const void* q, const void* k_cache, co
 typedef struct pa_prefix_cache pa_prefix_cache;
 
 pa_prefix_cache* pa_prefix_cache_create(pa_allocator* a);
-/* Drops the cache's references. */
+/* Drops the cache's references.  Caches and their allocator may be destroyed
+ * in any order: an allocator destroyed while caches created on it remain is
+ * released when the last of them is destroyed. */
 void pa_prefix_cache_destroy(pa_prefix_cache* c);
 int pa_prefix_cache_size(const pa_prefix_cache* c);
 /* The longest cached prefix of tokens[0..n_tokens): the physical blocks of

@@ -12,6 +12,7 @@
 #include <vector>
 
 #include "../../include/pa.h"
+#include "pa_host_internal.h"
 
 // Reference-counted pool of fixed-size KV blocks ("KV cache & continuous
 // batching", section "2. PagedAttention"; "LLM Serving - KV Cache, Batching,
@@ -22,7 +23,19 @@ struct pa_allocator {
     int block_size;
     std::vector<int32_t> refcnt;
     std::set<int32_t> free_ids;
+    int attached = 0;       // prefix caches created on this allocator and not yet destroyed
+    bool released = false;  // pa_allocator_destroy was called while caches were attached
 };
+
+namespace pa {
+
+void allocator_attach(pa_allocator* a) { ++a->attached; }
+
+void allocator_detach(pa_allocator* a) {
+    if (--a->attached == 0 && a->released) delete a;
+}
+
+}  // namespace pa
 
 extern "C" {
 
@@ -42,7 +55,14 @@ pa_allocator* pa_allocator_create(int num_blocks, int block_size) {
     return a;
 }
 
-void pa_allocator_destroy(pa_allocator* a) { delete a; }
+void pa_allocator_destroy(pa_allocator* a) {
+    if (!a) return;
+    if (a->attached > 0) {
+        a->released = true;   // freed by the last attached cache's destroy
+        return;
+    }
+    delete a;
+}
 
 pa_status pa_block_alloc(pa_allocator* a, int n, int32_t* out_ids) {
     if (!a || n < 0 || (n > 0 && !out_ids)) return PA_ERR_INVALID;

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "../../include/pa.h"
+#include "pa_host_internal.h"
 
 namespace {
 
@@ -73,6 +74,7 @@ pa_prefix_cache* pa_prefix_cache_create(pa_allocator* a) {
     c->alloc = a;
     c->bs = pa_allocator_block_size(a);
     c->clock = 0;
+    pa::allocator_attach(a);
     return c;
 }
 
@@ -80,6 +82,7 @@ void pa_prefix_cache_destroy(pa_prefix_cache* c) {
     if (!c) return;
     for (const Entry& e : c->entries)
         if (e.live) pa_block_free(c->alloc, &e.block, 1);
+    pa::allocator_detach(c->alloc);
     delete c;
 }
 

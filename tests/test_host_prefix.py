@@ -3,6 +3,9 @@
 Bit-exact: every match, allocation, copy-on-write decision, eviction count
 and reference count must equal the oracle's on the same operation trace.
 """
+import os
+import sys
+
 import numpy as np
 import pytest
 
@@ -11,6 +14,8 @@ import paged_kv_cache_294_gb300 as pa
 from oracle.prefix import PrefixCache, cow
 from paged_kv_cache_294_gb300.engine import BlockManager
 from tests.prefix_sim import OracleManager
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _same_pool(a_lib, a_or, nb):
@@ -172,3 +177,45 @@ def test_block_manager_evicts_cached_blocks_when_the_pool_runs_dry():
     assert m.cache.size() == o.cache.size() == 3
     assert m.add(2, list(range(8))) == o.add(2, list(range(8))) == 8   # the first two still match
     assert m.blocks[2] == o.blocks[2]
+
+
+def test_allocator_and_cache_can_be_destroyed_in_either_order():
+    lib = pa.load()
+    for cache_first in (True, False):
+        a = lib.pa_allocator_create(64, 4)
+        c = lib.pa_prefix_cache_create(a)
+        ids = np.zeros(3, np.int32)
+        assert lib.pa_block_alloc(a, 3, ids.ctypes.data) == pa.PA_OK
+        toks = np.arange(12, dtype=np.int32)
+        assert lib.pa_prefix_insert(c, toks.ctypes.data, 12, ids.ctypes.data, 3) == pa.PA_OK
+        assert lib.pa_block_free(a, ids.ctypes.data, 3) == pa.PA_OK
+        if cache_first:
+            lib.pa_prefix_cache_destroy(c)
+            assert lib.pa_allocator_num_free(a) == 64
+            lib.pa_allocator_destroy(a)
+        else:
+            lib.pa_allocator_destroy(a)      # deferred: the cache still holds references
+            lib.pa_prefix_cache_destroy(c)   # releases its blocks, then the allocator
+
+
+def test_interpreter_exit_with_live_cache_objects_in_a_cycle():
+    # objects left in a garbage cycle at exit are finalised in any order
+    code = r"""
+import sys, cProfile, numpy as np
+sys.path.insert(0, %r)
+from paged_kv_cache_294_gb300.engine import BlockManager
+rng = np.random.default_rng(11)
+prompts = [[int(x) for x in rng.integers(0, 32000, 2304)] for _ in range(8)]
+reqs = [prompts[int(rng.integers(0, 8))] + [int(x) for x in rng.integers(32000, 64000, int(rng.integers(1, 513)))]
+        for _ in range(300)]
+mgr = BlockManager(40000, 16)
+def run():
+    for i, toks in enumerate(reqs):
+        mgr.add(i, toks); mgr.commit(i); mgr.free(i)
+cProfile.run("run()", None)
+print("ok")
+""" % ROOT
+    import subprocess
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip().endswith("ok")
