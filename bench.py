@@ -410,7 +410,8 @@ def run_ours(args):
         from paged_kv_cache_294_gb300.engine import BlockManager
         prng = np.random.default_rng(11)
         prompts = [[int(x) for x in prng.integers(0, 32000, 2304)] for _ in range(8)]
-        reqs = [prompts[int(prng.integers(0, 8))] + [int(x) for x in prng.integers(32000, 64000, int(prng.integers(1, 513)))]
+        reqs = [np.array(prompts[int(prng.integers(0, 8))] +
+                         [int(x) for x in prng.integers(32000, 64000, int(prng.integers(1, 513)))], dtype=np.int32)
                 for _ in range(1000)]
         mgr = BlockManager(w.num_blocks, w.bs)
         reused = 0

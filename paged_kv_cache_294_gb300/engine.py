@@ -68,8 +68,14 @@ class BlockManager:
         self.bs = int(block_size)
         self.alloc = pa_allocator(num_blocks, block_size)
         self.cache = pa_prefix_cache(self.alloc) if prefix_caching else None
-        self.tokens: Dict[int, List[int]] = {}
+        # each sequence's tokens: an int32 buffer (grown by doubling) and its length,
+        # handed to the prefix cache without conversion
+        self._tok: Dict[int, list] = {}
         self.blocks: Dict[int, List[int]] = {}
+
+    def tokens(self, sid: int) -> np.ndarray:
+        buf, n = self._tok[sid]
+        return buf[:n]
 
     def _alloc(self, n: int) -> List[int]:
         if n <= 0:
@@ -82,30 +88,30 @@ class BlockManager:
     def add(self, sid: int, tokens: Sequence[int]) -> int:
         if sid in self.blocks:
             raise ValueError("sequence %d exists" % sid)
-        toks = [int(t) for t in tokens]
-        shared = [int(x) for x in self.cache.match(toks)] if self.cache is not None else []
+        toks = np.array(tokens, dtype=np.int32)
+        shared = self.cache.match(toks).tolist() if self.cache is not None else []
         try:
             own = self._alloc(-(-len(toks) // self.bs) - len(shared))
         except PagedAttnError:
             self.alloc.free(shared)
             raise
-        self.tokens[sid], self.blocks[sid] = toks, shared + own
+        self._tok[sid], self.blocks[sid] = [toks, len(toks)], shared + own
         return len(shared) * self.bs
 
     def commit(self, sid: int) -> None:
         if self.cache is not None:
-            self.cache.insert(self.tokens[sid], self.blocks[sid])
+            self.cache.insert(self.tokens(sid), self.blocks[sid])
 
     def fork(self, child: int, parent: int) -> None:
         if child in self.blocks:
             raise ValueError("sequence %d exists" % child)
         self.alloc.share(self.blocks[parent])
-        self.tokens[child] = list(self.tokens[parent])
+        self._tok[child] = [self.tokens(parent).copy(), len(self.tokens(parent))]
         self.blocks[child] = list(self.blocks[parent])
 
     def append(self, sid: int, token: int):
-        toks, blocks = self.tokens[sid], self.blocks[sid]
-        n = len(toks)
+        entry, blocks = self._tok[sid], self.blocks[sid]
+        n = entry[1]
         j = n // self.bs
         copy = None
         if j == len(blocks):
@@ -120,12 +126,17 @@ class BlockManager:
             if needs_copy:
                 copy = (blocks[j], dst)
             blocks[j] = dst
-        toks.append(int(token))
+        if n == len(entry[0]):
+            grown = np.empty(max(16, 2 * n), dtype=np.int32)
+            grown[:n] = entry[0][:n]
+            entry[0] = grown
+        entry[0][n] = int(token)
+        entry[1] = n + 1
         return blocks[j] * self.bs + n % self.bs, copy
 
     def free(self, sid: int) -> None:
         self.alloc.free(self.blocks.pop(sid))
-        del self.tokens[sid]
+        del self._tok[sid]
 
     def table(self, sids: Sequence[int], M: int) -> np.ndarray:
         t = np.full((len(sids), M), -1, dtype=np.int32)
@@ -137,7 +148,7 @@ class BlockManager:
         return t
 
     def lens(self, sids: Sequence[int]) -> np.ndarray:
-        return np.asarray([len(self.tokens[s]) for s in sids], dtype=np.int32)
+        return np.asarray([self._tok[s][1] for s in sids], dtype=np.int32)
 
 
 class PagedDecodeLayer:
