@@ -100,3 +100,27 @@ def test_fused_step_skips_an_invalid_last_block():
     changed = (layer.k_cache != before_k).reshape(layer.k_cache.shape[0], -1).any(dim=1).nonzero().flatten()
     allowed = {int(layer.tables_host[0, 1]), int(layer.tables_host[2, 0])}   # the other two new tokens
     assert set(int(x) for x in changed) <= allowed
+
+
+@pytest.mark.parametrize("name,kw", [("8b", dict(B=8, seq_len=700)), ("fp8prefix", dict(B=8, seq_len=700)),
+                                     ("8b-int8", dict(B=8, seq_len=700))])
+@pytest.mark.parametrize("splits", [0, 3])
+def test_fused_step_replayed_from_a_cuda_graph(name, kw, splits):
+    """pa_decode_step captured in a CUDA graph (as a serving loop replays its
+    step) writes the same cache bytes and outputs as the call made eagerly."""
+    w = workloads.make(name, **kw)
+    warm = PagedDecodeLayer.from_workload(w, "cuda")
+    warm.fused_step(num_splits=splits)   # one-time per-kernel setup happens outside the capture
+    torch.cuda.synchronize()
+    a, b = _pair(w)
+    pa.pa_get_device_error(clear=True)
+    out_a = a.fused_step(num_splits=splits).clone()
+    b.ensure_workspace(splits)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        b.fused_step(num_splits=splits)
+    graph.replay()
+    _same_state(a, b)
+    assert torch.equal(out_a.view(torch.int16), b.out.view(torch.int16))
+    assert pa.pa_get_device_error() == 0
