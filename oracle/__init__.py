@@ -19,6 +19,9 @@ Parity status of each function (what pins it, in tests/test_oracle_*.py):
   kv_append (fp8)         scale == absmax/448, round-trip bounds, brute-force encode
   int8 codec / append     numpy rint + clip on fp32 quotients, the growth / restart /
                           zero cases; attention on the int8 cache against torch
+  int4 codec / append     the same pins with 7 in place of 127, plus the nibble order
+                          (element 2j low, 2j+1 high) read back by hand; attention on
+                          the int4 cache against torch on the unpacked values
   e4m3_encode/value       nearest-value brute force over the 256-code table, format facts
   kv_bytes/blocks_for     the pages' printed per-token sizes and block counts
   sched_*                 the pages' printed iteration counts
@@ -87,6 +90,9 @@ def _load():
             "or_kv_append_int8": (i32, [P, P, P, P, P, P, P, i32, i64, i32, i32, i32]),
             "or_int8_value": (dbl, [ctypes.c_uint8]),
             "or_int8_encode": (ctypes.c_uint8, [ctypes.c_float]),
+            "or_kv_append_int4": (i32, [P, P, P, P, P, P, P, i32, i64, i32, i32, i32]),
+            "or_int4_value": (dbl, [ctypes.c_uint8]),
+            "or_int4_encode": (ctypes.c_uint8, [ctypes.c_float]),
             "or_decode_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                           i64, dbl, i32]),
             "or_decode_attention_split": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32,
@@ -143,7 +149,16 @@ def int8_encode(x: float) -> int:
     return int(_load().or_int8_encode(float(x)))
 
 
-_KV_CODE = {"bf16": 0, "fp8": 1, "int8": 2}
+def int4_value(nibble: int) -> float:
+    return float(_load().or_int4_value(int(nibble) & 0xF))
+
+
+def int4_encode(x: float) -> int:
+    """Nibble (0..15, two's complement) of clamp(rint(x), -7, 7)."""
+    return int(_load().or_int4_encode(float(x)))
+
+
+_KV_CODE = {"bf16": 0, "fp8": 1, "int8": 2, "int4": 3}
 
 
 def e4m3_encode_array(x: np.ndarray) -> np.ndarray:
@@ -257,16 +272,18 @@ def slot_mapping(tables: np.ndarray, seq: np.ndarray, pos: np.ndarray, block_siz
 
 # ---------------------------------------------------------------- cache
 class Cache:
-    """Host-side paged cache in the shared layout [num_blocks][Hkv][bs][d]."""
+    """Host-side paged cache in the shared layout [num_blocks][Hkv][bs][d]
+    (int4: [num_blocks][Hkv][bs][d / 2] bytes, two codes per byte)."""
 
     def __init__(self, num_blocks, Hkv, d, bs, kv="bf16"):
         self.num_blocks, self.Hkv, self.d, self.bs, self.kv = num_blocks, Hkv, d, bs, kv
         if kv not in _KV_CODE:
-            raise ValueError("kv must be bf16, fp8 or int8")
+            raise ValueError("kv must be bf16, fp8, int8 or int4")
         dt = np.uint8 if kv != "bf16" else np.uint16
+        row = d // 2 if kv == "int4" else d
         # np.zeros maps lazily: only pages the appends touch take memory
-        self.k = np.zeros((num_blocks, Hkv, bs, d), dtype=dt)
-        self.v = np.zeros((num_blocks, Hkv, bs, d), dtype=dt)
+        self.k = np.zeros((num_blocks, Hkv, bs, row), dtype=dt)
+        self.v = np.zeros((num_blocks, Hkv, bs, row), dtype=dt)
         if kv != "bf16":
             self.k_scale = np.zeros((num_blocks, Hkv), dtype=np.float32)
             self.v_scale = np.zeros((num_blocks, Hkv), dtype=np.float32)
@@ -279,7 +296,8 @@ class Cache:
         T = len(slots)
         lib = _load()
         if self.kv != "bf16":
-            fn = lib.or_kv_append_fp8 if self.kv == "fp8" else lib.or_kv_append_int8
+            fn = {"fp8": lib.or_kv_append_fp8, "int8": lib.or_kv_append_int8,
+                  "int4": lib.or_kv_append_int4}[self.kv]
             rc = fn(_p(self.k), _p(self.v), _p(self.k_scale), _p(self.v_scale), _p(kn), _p(vn), _p(slots), T,
                     self.num_blocks, self.Hkv, self.d, self.bs)
         else:

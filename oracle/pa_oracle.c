@@ -19,8 +19,9 @@
  *
  * Cache layout shared by both implementations (it is an interface, not
  * arithmetic): k_cache / v_cache are [num_blocks][Hkv][block_size][d]
- * elements, bf16 bit patterns or e4m3 codes; fp8 scales are [num_blocks][Hkv]
- * fp32.  block_tables is [B][M] int32, row b listing the physical block of
+ * elements: bf16 bit patterns, e4m3 or int8 codes (one byte each) or int4
+ * codes (two per byte, a row taking d / 2 bytes); the scales of the coded
+ * caches are [num_blocks][Hkv] fp32.  block_tables is [B][M] int32, row b listing the physical block of
  * logical block j of sequence b.
  *
  * Build: gcc -O2 -std=c99 -fPIC -shared -ffp-contract=off pa_oracle.c -lm
@@ -117,10 +118,55 @@ uint8_t or_int8_encode(float x) {
     return (uint8_t)(int8_t)q;
 }
 
-/* The two one-byte codecs: 1 = e4m3 (largest code value 448), 2 = int8 (127). */
-static double q8_value(int codec, uint8_t c) { return codec == 2 ? or_int8_value(c) : or_e4m3_value(c); }
-static uint8_t q8_encode(int codec, float x) { return codec == 2 ? or_int8_encode(x) : or_e4m3_encode(x); }
-static float q8_max(int codec) { return codec == 2 ? 127.0f : 448.0f; }
+/* int4 cache ([P1] "KV cache memory math": half a byte per element for
+ * int4): a code c in [-7, 7] stands for c * scale, the symmetric range, like
+ * int8's [-127, 127].  Encoding as for int8, clamped to +-7.  A code is a
+ * 4-bit two's-complement nibble; element 2j of a row sits in the low nibble
+ * of the row's byte j and element 2j+1 in its high nibble. */
+double or_int4_value(uint8_t nibble) {
+    int v = nibble & 0xF;
+    return (double)(v >= 8 ? v - 16 : v);
+}
+
+uint8_t or_int4_encode(float x) {
+    double q;
+    if (isnan(x)) return 0;
+    q = rint((double)x);
+    if (q > 7.0) q = 7.0;
+    if (q < -7.0) q = -7.0;
+    return (uint8_t)((int)q & 0xF);
+}
+
+/* The scaled codecs: 1 = e4m3 (largest code value 448), 2 = int8 (127),
+ * 3 = int4 (7). */
+static double q8_value(int codec, uint8_t c) {
+    return codec == 3 ? or_int4_value(c) : codec == 2 ? or_int8_value(c) : or_e4m3_value(c);
+}
+static uint8_t q8_encode(int codec, float x) {
+    return codec == 3 ? or_int4_encode(x) : codec == 2 ? or_int8_encode(x) : or_e4m3_encode(x);
+}
+static float q8_max(int codec) { return codec == 3 ? 7.0f : codec == 2 ? 127.0f : 448.0f; }
+
+/* Bytes of one token row of one head: d for one-byte codes, d / 2 for int4. */
+static int64_t row_bytes(int codec, int d) { return codec == 3 ? d / 2 : d; }
+
+/* The code of element i of row o of a page, and its update. */
+static uint8_t page_get(const uint8_t* page, int codec, int d, int o, int i) {
+    if (codec == 3) {
+        uint8_t b = page[(int64_t)o * (d / 2) + i / 2];
+        return (uint8_t)((i & 1) ? (b >> 4) : (b & 0xF));
+    }
+    return page[(int64_t)o * d + i];
+}
+
+static void page_set(uint8_t* page, int codec, int d, int o, int i, uint8_t c) {
+    if (codec == 3) {
+        uint8_t* b = page + (int64_t)o * (d / 2) + i / 2;
+        *b = (i & 1) ? (uint8_t)((*b & 0x0F) | ((c & 0xF) << 4)) : (uint8_t)((*b & 0xF0) | (c & 0xF));
+        return;
+    }
+    page[(int64_t)o * d + i] = c;
+}
 
 /* ------------------------------------------------------------------------ */
 /* Accounting: [P1] "KV cache memory math" and [P2] "KV memory, paging and   */
@@ -351,7 +397,7 @@ static void q8_block_head(int codec, uint8_t* cache, float* scale, const uint16_
     float old, a = 0.0f, s;
     int k, i, o;
     int64_t sidx = p * Hkv + h;
-    uint8_t* page = cache + (p * Hkv + h) * (int64_t)bs * d;
+    uint8_t* page = cache + (p * Hkv + h) * (int64_t)bs * row_bytes(codec, d);
     old = (first == 0) ? 0.0f : scale[sidx];
     for (k = 0; k < ntok; k++) {
         const uint16_t* x = src + ((int64_t)toks[k] * Hkv + h) * d;
@@ -365,16 +411,16 @@ static void q8_block_head(int codec, uint8_t* cache, float* scale, const uint16_
     if (s > old && old > 0.0f) {
         for (o = 0; o < first; o++)
             for (i = 0; i < d; i++) {
-                uint8_t* e = page + (int64_t)o * d + i;
-                float prod = (float)q8_value(codec, *e) * old;
-                *e = q8_encode(codec, prod / s);
+                float prod = (float)q8_value(codec, page_get(page, codec, d, o, i)) * old;
+                page_set(page, codec, d, o, i, q8_encode(codec, prod / s));
             }
     }
     for (k = 0; k < ntok; k++) {
         const uint16_t* x = src + ((int64_t)toks[k] * Hkv + h) * d;
         int64_t off = slots[toks[k]] % bs;
         for (i = 0; i < d; i++)
-            page[off * d + i] = (s == 0.0f) ? (uint8_t)0 : q8_encode(codec, bf16_to_float(x[i]) / s);
+            page_set(page, codec, d, (int)off, i,
+                     (s == 0.0f) ? (uint8_t)0 : q8_encode(codec, bf16_to_float(x[i]) / s));
     }
     scale[sidx] = s;
 }
@@ -427,6 +473,16 @@ int or_kv_append_int8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float*
     return q8_append(2, k_cache, v_cache, k_scale, v_scale, k_new, v_new, slots, T, num_blocks, Hkv, d, bs);
 }
 
+/* The same rule for the int4 cache with 7 in place of 127: s = max(old,
+ * fp32(absmax) / 7), codes clamp(rint(x / s), -7, 7), two per byte.  A row's
+ * d codes fill d / 2 bytes (d even). */
+int or_kv_append_int4(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float* v_scale,
+                      const uint16_t* k_new, const uint16_t* v_new, const int64_t* slots, int T,
+                      int64_t num_blocks, int Hkv, int d, int bs) {
+    if (d % 2) return -1;
+    return q8_append(3, k_cache, v_cache, k_scale, v_scale, k_new, v_new, slots, T, num_blocks, Hkv, d, bs);
+}
+
 /* ------------------------------------------------------------------------ */
 /* Decode attention: [P1] "The core insight" (the new token's query attends  */
 /* over all cached keys and values), [P2] "Hands-on" (cached attention of    */
@@ -438,15 +494,18 @@ int or_kv_append_int8(uint8_t* k_cache, uint8_t* v_cache, float* k_scale, float*
 /* Query head i of a sequence uses KV head i / G, G = Hq / Hkv (consecutive  */
 /* query heads share a KV head; the pages do not fix the mapping).  Token t  */
 /* of sequence b is row t mod bs of physical block table[b][t / bs].  For    */
-/* the fp8 / int8 cache an element's value is value(code) * scale[block]     */
-/* [head]; the attention functions' `fp8` argument is the cache type:        */
-/* 0 bf16, 1 e4m3, 2 int8.                                                   */
+/* the fp8 / int8 / int4 cache an element's value is value(code) *          */
+/* scale[block][head]; the attention functions' `fp8` argument is the cache  */
+/* type: 0 bf16, 1 e4m3, 2 int8, 3 int4.                                     */
 /* A sequence of length 0 yields a zero output row.                          */
 /* ------------------------------------------------------------------------ */
 static double kv_elem(const void* cache, const float* sc, int fp8, int64_t blk, int h, int off,
                       int i, int Hkv, int d, int bs) {
     int64_t idx = ((blk * Hkv + h) * bs + off) * (int64_t)d + i;
-    if (fp8) return q8_value(fp8, ((const uint8_t*)cache)[idx]) * (double)sc[blk * Hkv + h];
+    if (fp8) {
+        const uint8_t* page = (const uint8_t*)cache + (blk * Hkv + h) * (int64_t)bs * row_bytes(fp8, d);
+        return q8_value(fp8, page_get(page, fp8, d, off, i)) * (double)sc[blk * Hkv + h];
+    }
     return or_bf16_value(((const uint16_t*)cache)[idx]);
 }
 
