@@ -48,11 +48,15 @@ def hbm_peak():
         return FALLBACK_HBM, "fallback"
 
 
+def row_bytes(w):
+    """Bytes of one token row of one kv head: 2 per element (bf16), 1 (fp8, int8), 1/2 (int4)."""
+    return {"bf16": 2 * w.d, "int4": w.d // 2}.get(w.kv, w.d)
+
+
 def algorithmic_bytes(w):
     """K/V bytes of every cached token of every sequence (logical, once per sequence),
     plus q read and out written.  Unique-physical KV bytes reported beside it."""
-    elt = 1 if w.kv != "bf16" else 2
-    tok = 2 * w.Hkv * w.d * elt
+    tok = 2 * w.Hkv * row_bytes(w)
     lens = np.asarray(w.seq_lens, dtype=np.int64)
     qo = 2 * w.B * w.Hq * w.d * 2
     return int(lens.sum()) * tok + qo, int(lens.sum()) * tok, qo
@@ -81,14 +85,13 @@ def unique_kv_bytes(w, tables):
     """K/V bytes of distinct cached tokens: a physical block shared by several
     sequences (a common prefix) counts once, with as many tokens as its longest
     user fills.  Equals the logical count when no block is shared."""
-    elt = 1 if w.kv != "bf16" else 2
     used = {}
     for b, L in enumerate(w.seq_lens):
         L = int(L)
         for j in range(-(-L // w.bs)):
             p = int(tables[b, j])
             used[p] = max(used.get(p, 0), min(w.bs, L - j * w.bs))
-    return sum(used.values()) * 2 * w.Hkv * w.d * elt
+    return sum(used.values()) * 2 * w.Hkv * row_bytes(w)
 
 
 class ClockSampler:
@@ -224,8 +227,7 @@ def cpu_oracle_baseline(w, tables, budget_s=10.0, threads=None):
         total += time.perf_counter() - t0
         reps += 1
     lens = np.asarray(w.seq_lens, dtype=np.int64)[seqs]
-    elt = 1 if w.kv != "bf16" else 2
-    byts = int(lens.sum()) * 2 * w.Hkv * w.d * elt + 2 * len(seqs) * w.Hq * w.d * 2
+    byts = int(lens.sum()) * 2 * w.Hkv * row_bytes(w) + 2 * len(seqs) * w.Hq * w.d * 2
     per_step = total / reps
     return {"value": byts / per_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d of %d sequences (%d tokens), fp64 C oracle append+decode, %d reps, %.1f s" %
@@ -256,8 +258,7 @@ def run_reference(args):
         if i >= args.warmup:
             times.append(dt)
     lens = np.asarray(w.seq_lens, dtype=np.int64)[seqs]
-    elt = 1 if w.kv != "bf16" else 2
-    byts = int(lens.sum()) * 2 * w.Hkv * w.d * elt + 2 * len(seqs) * w.Hq * w.d * 2
+    byts = int(lens.sum()) * 2 * w.Hkv * row_bytes(w) + 2 * len(seqs) * w.Hq * w.d * 2
     t = sum(times)
     value = byts * len(times) / t / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
@@ -300,7 +301,7 @@ def run_ours(args):
     st.append()
     ref = st.decode(threads=os.cpu_count() or 1)
     err = float(np.max(np.abs(layer.out.float().cpu().numpy()[sample] - ref)))
-    tol = {"fp8": 5e-2, "int8": 1e-2}.get(w.kv, 1e-2)
+    tol = {"fp8": 5e-2, "int8": 1e-2, "int4": 1e-2}.get(w.kv, 1e-2)
     parity = {"max_abs_err": err, "tol": tol, "sequences": sample, "ok": bool(err <= tol and flags == 0)}
     if not parity["ok"]:
         print("parity check failed: %s flags=%#x" % (parity, flags), file=sys.stderr)
@@ -453,7 +454,8 @@ def run_ours(args):
     cvs = torch.ones_like(cks) if cks is not None else None
     perm = torch.from_numpy(np.random.default_rng(1).permutation(2 * nb_copy).astype(np.int32)).to(dev)
     c_src, c_dst = perm[:nb_copy].contiguous(), perm[nb_copy:].contiguous()
-    t_copy = timed(lambda: pa.pa_copy_blocks(ck, cv, cks, cvs, c_src, c_dst), K)
+    t_copy = timed(lambda: pa.pa_copy_blocks(ck, cv, cks, cvs, c_src, c_dst,
+                                             kv_dtype=pa.PA_KV_INT4 if w.kv == "int4" else None), K)
     page = ck[0].numel() * ck.element_size()
     copy_bytes = 2 * 2 * nb_copy * (page + (4 * w.Hkv if cks is not None else 0))   # K and V, read + write
     copy_gbs = copy_bytes * K / t_copy / 1e9
@@ -529,7 +531,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": 1e3 * t_step / K, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
         "dtype": {"fp8": "fp8_e4m3-cache/f16-mma/f32-softmax",
-                  "int8": "int8-cache/f16-mma/f32-softmax"}.get(w.kv, "bf16-cache/bf16-mma/f32-softmax"),
+                  "int8": "int8-cache/f16-mma/f32-softmax",
+                  "int4": "int4-cache/f16-mma/f32-softmax"}.get(w.kv, "bf16-cache/bf16-mma/f32-softmax"),
         "data": "synthetic",
         "config": {"workload": args.workload if args.batch is None else "%s-B%d" % (args.workload, w.B),
                    "desc": w.desc, "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv,

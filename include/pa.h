@@ -28,10 +28,13 @@
  *
  * Memory layout (all row-major, innermost last)
  *   k_cache, v_cache  [num_blocks][num_kv_heads][block_size][head_dim]
- *                     bf16 (PA_KV_BF16), e4m3 bytes (PA_KV_FP8_E4M3) or
- *                     two's-complement int8 codes (PA_KV_INT8).
+ *                     bf16 (PA_KV_BF16), e4m3 bytes (PA_KV_FP8_E4M3),
+ *                     two's-complement int8 codes (PA_KV_INT8) or 4-bit codes
+ *                     two per byte (PA_KV_INT4: a row is head_dim / 2 bytes,
+ *                     element 2j in the low nibble of byte j, 2j+1 in the high).
  *                     One (block, kv_head) page is contiguous.
- *   k_scale, v_scale  [num_blocks][num_kv_heads] fp32 (one-byte caches only)
+ *   k_scale, v_scale  [num_blocks][num_kv_heads] fp32 (coded caches only:
+ *                     e4m3, int8, int4)
  *   q, out            [batch][num_q_heads][head_dim] bf16
  *   k_new, v_new      [num_tokens][num_kv_heads][head_dim] bf16
  *   block_tables      [batch][max_blocks_per_seq] int32: physical block of
@@ -65,8 +68,11 @@ typedef enum {
 typedef enum {
     PA_KV_BF16 = 0,
     PA_KV_FP8_E4M3 = 1,
-    PA_KV_INT8 = 2      /* int8 codes c in [-127, 127], value c * scale ([P3] "Memory
+    PA_KV_INT8 = 2,     /* int8 codes c in [-127, 127], value c * scale ([P3] "Memory
                            Bandwidth Optimization": INT8 KV quantization) */
+    PA_KV_INT4 = 3      /* 4-bit two's-complement codes c in [-7, 7], value c * scale,
+                           two per byte ([P1] "KV cache memory math": int4 = 0.5 byte
+                           per element) */
 } pa_kv_dtype;
 
 /* Bits of the per-device error word (pa_get_device_error). */
@@ -103,13 +109,17 @@ const char* pa_status_string(pa_status s);
  * halves the cache reads): the same rule with 127 in place of 448 and the
  * code Q(y) = clamp(round-half-to-even(y), -127, 127) in place of E4M3; an
  * element's value is code * scale.
- * Precondition (one-byte caches only): the tokens a call writes into one block form one
+ * PA_KV_INT4 ([P1] "KV cache memory math": int4 takes half a byte per
+ * element): the same rule with 7 in place of 127 and Q(y) = clamp(round-half-
+ * to-even(y), -7, 7), stored as 4-bit two's complement, two codes per byte
+ * (element 2j of a row in the low nibble of byte j, 2j+1 in the high nibble).
+ * Precondition (coded caches only): the tokens a call writes into one block form one
  * run of consecutive entries of slot_mapping with increasing offsets (true for
  * one decode token per sequence and for a prefill of one sequence).  A
  * violation gives unspecified cache contents but no out-of-bounds access.
  *
  * num_blocks * num_kv_heads * block_size must be below 2^31.  head_dim in
- * {64, 128} (one-byte caches: 128), block_size in {16, 32}.  num_tokens == 0 is a no-op.
+ * {64, 128} (coded caches: 128), block_size in {16, 32}.  num_tokens == 0 is a no-op.
  * ------------------------------------------------------------------------- */
 pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                        const void* k_new, const void* v_new, const int64_t* slot_mapping,
@@ -158,11 +168,11 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
  *
  *   out[b][i][:] = sum_t softmax_t(scale * q[b][i] . K_t) V_t,
  *   t = 0 .. seq_lens[b]-1,  K_t = k_cache[block_tables[b][t / bs]][i / G][t % bs]
- * fp8 / int8: K_t and V_t elements are value(code) * scale[block][kv_head].
+ * fp8 / int8 / int4: K_t and V_t elements are value(code) * scale[block][kv_head].
  * A sequence with seq_len 0 gives a zero row.  The outputs are bf16.
  *
  * num_blocks * num_kv_heads * block_size must be below 2^31; head_dim in
- * {64, 128} (one-byte caches: 128); block_size in {16, 32}; num_q_heads a multiple of
+ * {64, 128} (coded caches: 128); block_size in {16, 32}; num_q_heads a multiple of
  * num_kv_heads with a group size of at most 8.  batch == 0 is a no-op.
  * ------------------------------------------------------------------------- */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
@@ -356,7 +366,7 @@ pa_status pa_prefix_evict(pa_prefix_cache* c, int want, int* freed);
 pa_status pa_block_cow(pa_allocator* a, int32_t block, int32_t* out_block, int* needs_copy);
 
 /* Device copy of whole blocks: for i < n, block dst[i] (every kv head's K and
- * V page, and for the fp8 cache both scales) becomes a copy of block src[i].
+ * V page, and for a coded cache both scales) becomes a copy of block src[i].
  * src / dst are device int32 arrays; no dst may appear as a src of the same
  * call.  Ids out of range are skipped (PA_DEVERR_BLOCK_ID).  Same layout
  * rules as pa_kv_append. */

@@ -7,8 +7,11 @@ library's CUDA kernels.  There is no fallback: if the library cannot be
 loaded, every call raises.
 
 Tensor layouts (row-major):
-  k_cache, v_cache  [num_blocks, Hkv, block_size, head_dim] bf16, or uint8 (e4m3 codes)
-  k_scale, v_scale  [num_blocks, Hkv] float32 (fp8 cache only)
+  k_cache, v_cache  [num_blocks, Hkv, block_size, head_dim] bf16, uint8 (e4m3 codes) or
+                    int8 (int8 codes); [num_blocks, Hkv, block_size, head_dim / 2] uint8
+                    for int4 codes (two per byte), told apart from e4m3 by the last
+                    dimension against head_dim (pa_copy_blocks: kv_dtype=PA_KV_INT4)
+  k_scale, v_scale  [num_blocks, Hkv] float32 (coded caches only)
   q, out            [B, Hq, head_dim] bf16
   k_new, v_new      [T, Hkv, head_dim] bf16
   block_tables      [B, M] int32;  seq_lens [B] int32;  slot_mapping [T] int64
@@ -25,7 +28,7 @@ import torch
 from . import _build
 
 PA_OK, PA_ERR_INVALID, PA_ERR_OOM, PA_ERR_CUDA, PA_ERR_UNSUPPORTED = range(5)
-PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_INT8 = 0, 1, 2
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_INT8, PA_KV_INT4 = 0, 1, 2, 3
 PA_DEVERR_BLOCK_ID, PA_DEVERR_SEQ_LEN, PA_DEVERR_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _lib = None
@@ -129,14 +132,23 @@ def _stream(stream) -> Optional[int]:
     return int(stream)
 
 
-def _kv_dtype(cache: torch.Tensor) -> int:
+def _kv_dtype(cache: torch.Tensor, head_dim: Optional[int] = None) -> int:
+    """Cache type from the tensor: a uint8 cache whose rows hold head_dim / 2
+    bytes holds int4 codes, one with head_dim bytes e4m3 codes."""
     if cache.dtype == torch.bfloat16:
         return PA_KV_BF16
     if cache.dtype == torch.uint8:
+        if head_dim is not None and cache.dim() == 4 and 2 * cache.shape[3] == head_dim:
+            return PA_KV_INT4
         return PA_KV_FP8_E4M3
     if cache.dtype == torch.int8:
         return PA_KV_INT8
-    raise TypeError("cache dtype must be bfloat16, uint8 (e4m3 codes) or int8")
+    raise TypeError("cache dtype must be bfloat16, uint8 (e4m3 or int4 codes) or int8")
+
+
+def _row_len(kvd: int, d: int) -> int:
+    """Last dimension of a cache tensor of type kvd for head_dim d."""
+    return d // 2 if kvd == PA_KV_INT4 else d
 
 
 def _need(t: torch.Tensor, dtype, name: str, dim: Optional[int] = None):
@@ -153,16 +165,18 @@ def pa_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional
                  v_scale: Optional[torch.Tensor], k_new: torch.Tensor, v_new: torch.Tensor,
                  slot_mapping: torch.Tensor, stream=None) -> None:
     lib = load()
-    kvd = _kv_dtype(k_cache)
     _need(k_new, torch.bfloat16, "k_new", 3)
     _need(v_new, torch.bfloat16, "v_new", 3)
     _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    d = k_new.shape[2]
+    kvd = _kv_dtype(k_cache, d)
     if kvd != PA_KV_BF16:
         _need(k_scale, torch.float32, "k_scale", 2)
         _need(v_scale, torch.float32, "v_scale", 2)
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, dc = k_cache.shape
     T = slot_mapping.shape[0]
-    if tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d) or v_cache.shape != k_cache.shape:
+    if (dc != _row_len(kvd, d) or tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d)
+            or v_cache.shape != k_cache.shape):
         raise ValueError("shape mismatch between caches, new K/V and slot_mapping")
     _check(lib.pa_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(k_new),
                             _ptr(v_new), _ptr(slot_mapping), T, nb, hkv, d, bs, kvd, _stream(stream)),
@@ -186,15 +200,16 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tenso
                         num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
                         stream=None) -> None:
     lib = load()
-    kvd = _kv_dtype(k_cache)
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
     B, hq, d = q.shape
+    kvd = _kv_dtype(k_cache, d)
     nb, hkv, bs, dc = k_cache.shape
     M = block_tables.shape[1]
-    if dc != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
+    if (dc != _row_len(kvd, d) or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B
+            or seq_lens.shape[0] != B):
         raise ValueError("shape mismatch")
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
@@ -211,7 +226,6 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
                    stream=None) -> None:
     """Append each sequence's new token (position seq_len-1) and attend, in one launch."""
     lib = load()
-    kvd = _kv_dtype(k_cache)
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(k_new, torch.bfloat16, "k_new", 3)
@@ -219,9 +233,10 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
     B, hq, d = q.shape
+    kvd = _kv_dtype(k_cache, d)
     nb, hkv, bs, dc = k_cache.shape
     M = block_tables.shape[1]
-    if (dc != d or tuple(out.shape) != (B, hq, d) or tuple(k_new.shape) != (B, hkv, d)
+    if (dc != _row_len(kvd, d) or tuple(out.shape) != (B, hq, d) or tuple(k_new.shape) != (B, hkv, d)
             or tuple(v_new.shape) != (B, hkv, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B):
         raise ValueError("shape mismatch")
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
@@ -248,15 +263,15 @@ def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: t
     P, i32 = ctypes.c_void_p, ctypes.c_int
     f.restype = i32
     f.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, P]
-    kvd = _kv_dtype(k_cache)
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
     B, hq, d = q.shape
+    kvd = _kv_dtype(k_cache, d)
     nb, hkv, bs, dc = k_cache.shape
     M = block_tables.shape[1]
-    if dc != d or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
+    if dc != _row_len(kvd, d) or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("shape mismatch")
     _check(f(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
              _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M, nb, float(scale), int(num_splits),
@@ -271,15 +286,16 @@ def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tens
     """Chunked-prefill / verify attention: sequence b's queries (rows q_start[b] ..
     q_start[b+1]-1 of q) are the last positions of its seq_lens[b] cached tokens."""
     lib = load()
-    kvd = _kv_dtype(k_cache)
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
     _need(seq_lens, torch.int32, "seq_lens", 1)
     _need(q_start, torch.int32, "q_start", 1)
-    nb, hkv, bs, d = k_cache.shape
+    d = q.shape[2]
+    kvd = _kv_dtype(k_cache, d)
+    nb, hkv, bs, dc = k_cache.shape
     B, M = block_tables.shape
-    if out.shape != q.shape or q.shape[2] != d or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
+    if out.shape != q.shape or dc != _row_len(kvd, d) or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
         raise ValueError("shape mismatch between q, out, caches, tables, lengths and q_start")
     _check(lib.pa_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                     _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _ptr(q_start), B,
@@ -288,15 +304,25 @@ def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tens
 
 
 def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
-                   v_scale: Optional[torch.Tensor], src: torch.Tensor, dst: torch.Tensor, stream=None) -> None:
-    """Block dst[i] becomes a copy of block src[i] (K and V pages, fp8 scales)."""
+                   v_scale: Optional[torch.Tensor], src: torch.Tensor, dst: torch.Tensor, stream=None,
+                   kv_dtype: Optional[int] = None) -> None:
+    """Block dst[i] becomes a copy of block src[i] (K and V pages, scales of a
+    coded cache).  A uint8 cache is taken as e4m3 codes unless kv_dtype is
+    PA_KV_INT4."""
     lib = load()
     kvd = _kv_dtype(k_cache)
+    if kv_dtype is not None:
+        if kv_dtype == PA_KV_INT4 and kvd != PA_KV_FP8_E4M3:
+            raise TypeError("an int4 cache is a uint8 tensor")
+        if kv_dtype != PA_KV_INT4 and kv_dtype != kvd:
+            raise TypeError("kv_dtype does not match the cache tensor")
+        kvd = kv_dtype
     _need(src, torch.int32, "src", 1)
     _need(dst, torch.int32, "dst", 1)
     if src.shape != dst.shape or v_cache.shape != k_cache.shape:
         raise ValueError("src/dst or cache shapes differ")
-    nb, hkv, bs, d = k_cache.shape
+    nb, hkv, bs, dc = k_cache.shape
+    d = 2 * dc if kvd == PA_KV_INT4 else dc
     _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(src), _ptr(dst),
                               int(src.shape[0]), nb, hkv, d, bs, kvd, _stream(stream)), "pa_copy_blocks")
 

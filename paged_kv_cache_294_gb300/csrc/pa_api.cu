@@ -19,7 +19,8 @@ pa_status cuda_status(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_
 
 bool shape_ok(int num_blocks, int Hkv, int d, int bs, int kv_dtype) {
     if (num_blocks <= 0 || Hkv <= 0 || bs <= 0 || d <= 0) return false;
-    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_INT8) return false;
+    if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_INT8 && kv_dtype != PA_KV_INT4)
+        return false;
     if ((int64_t)num_blocks * Hkv * bs >= (int64_t)1 << 31) return false;  // TMA row coordinate
     return true;
 }
@@ -27,7 +28,7 @@ bool shape_ok(int num_blocks, int Hkv, int d, int bs, int kv_dtype) {
 // PA_OK, PA_ERR_INVALID or PA_ERR_UNSUPPORTED for head_dim / block_size / dtype.
 pa_status kernel_shape(int d, int bs, int kv_dtype) {
     if (bs != 16 && bs != 32) return PA_ERR_UNSUPPORTED;
-    if (kv_dtype != PA_KV_BF16) return d == 128 ? PA_OK : PA_ERR_UNSUPPORTED;   // one-byte codes: a 128-byte row
+    if (kv_dtype != PA_KV_BF16) return d == 128 ? PA_OK : PA_ERR_UNSUPPORTED;   // coded rows: 128 (int4: 64) bytes
     return (d == 64 || d == 128) ? PA_OK : PA_ERR_UNSUPPORTED;
 }
 
@@ -72,7 +73,9 @@ MapCache& map_cache() {
 
 // The cache viewed as a 2-D tensor: rows = num_blocks * Hkv * bs token rows of
 // d elements; one box = bs rows x 128 bytes, written to shared memory with
-// the 128-byte swizzle (a page of head_dim 128 bf16 takes two boxes).
+// the 128-byte swizzle (a page of head_dim 128 bf16 takes two boxes).  An
+// int4 row of 128 codes is 64 bytes: the tensor is then rows / 2 lines of 128
+// bytes (two tokens each) and a box is bs / 2 lines.
 bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, CUtensorMap* out) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return false;
@@ -86,11 +89,19 @@ bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, 
             *out = c.map[i];
             return true;
         }
-    const bool q8 = dtype != PA_KV_BF16;   // one-byte codes (e4m3 or int8)
+    const bool q8 = dtype != PA_KV_BF16;   // coded: byte elements (e4m3, int8; int4 two per byte)
+    const bool i4 = dtype == PA_KV_INT4;
     const int elt = q8 ? 1 : 2;
     cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t gstride[1] = {(cuuint64_t)d * elt};
     cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)bs};
+    if (i4) {
+        gdim[0] = 128;
+        gdim[1] = (cuuint64_t)(rows / 2);
+        gstride[0] = 128;
+        box[0] = 128;
+        box[1] = (cuuint32_t)(bs / 2);
+    }
     cuuint32_t estride[2] = {1, 1};
     CUtensorMap m;
     CUresult r = enc(&m, q8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
@@ -320,10 +331,10 @@ pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_
     if (ks != PA_OK) return ks;
     if (n == 0) return PA_OK;
     if (!k_cache || !v_cache || !src || !dst || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID;
-    const bool q8 = kv_dtype != PA_KV_BF16;   // one-byte codes with scales
+    const bool q8 = kv_dtype != PA_KV_BF16;   // coded cache with scales
     if (q8 != (k_scale != nullptr) || q8 != (v_scale != nullptr)) return PA_ERR_INVALID;
     return cuda_status(pa::launch_copy_blocks(k_cache, v_cache, k_scale, v_scale, src, dst, n, num_blocks,
-                                              num_kv_heads, head_dim, block_size, q8,
+                                              num_kv_heads, head_dim, block_size, kv_dtype,
                                               static_cast<cudaStream_t>(stream)));
 }
 

@@ -1,11 +1,12 @@
 // KV append: scatter the new tokens' K/V into the paged cache through
-// slot_mapping (bf16 copy, or fp8 e4m3 quantisation with per-(block,
-// kv_head) absmax scales).
+// slot_mapping (bf16 copy, or e4m3 / int8 / int4 quantisation with
+// per-(block, kv_head) absmax scales).
 //
 // Definitions: "LLM Serving - KV Cache, Batching, Speculative Decoding",
 // section "Recall and stretch" item 3 (keys/values appended in decode);
 // "KV cache & continuous batching", sections "The core insight" and "KV cache
-// memory math" (fp8 = 1 byte per element); "LLM Inference Optimization",
+// memory math" (fp8 and int8 = 1 byte per element, int4 = half a byte);
+// "LLM Inference Optimization",
 // section "Memory Bandwidth Optimization" (KV-cache quantization).
 #include <cuda_fp8.h>
 
@@ -42,7 +43,7 @@ __global__ void __launch_bounds__(256) kv_append_bf16_kernel(
     }
 }
 
-// One-byte caches (e4m3 or int8 codes, KVT).  One warp per (token, kv_head).
+// Coded caches (e4m3, int8 or int4 codes, KVT).  One warp per (token, kv_head).
 // Only the first token of each run of consecutive tokens that land in the
 // same block does work: it quantises the whole run (at most bs tokens) for its
 // head, K then V.
@@ -74,7 +75,8 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(
         ++r;
     }
     const int first = (int)(slot - blk * bs);
-    const int64_t page = (blk * Hkv + h) * (int64_t)bs * 128;
+    constexpr int ROWB = Codec<KVT>::BITS * 128 / 8;   // bytes of one coded row of 128 elements
+    const int64_t page = (blk * Hkv + h) * (int64_t)bs * ROWB;
     const int64_t row0 = ((int64_t)t * Hkv + h) * 128;
     auto off_of = [&](int j) { return (int)(slots[t + j] % bs); };
     q8_quantise_run<KVT>(k_cache + page, k_scale + blk * Hkv + h, k_new + row0, (int64_t)Hkv * 128, r, first,
@@ -88,7 +90,9 @@ cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {
     if (L.kvt != PA_KV_BF16) {
         const int64_t warps = (int64_t)L.T * L.Hkv;
         const int blocks = (int)((warps * 32 + 255) / 256);
-        auto kern = (L.kvt == PA_KV_INT8) ? kv_append_q8_kernel<KV_INT8> : kv_append_q8_kernel<KV_FP8>;
+        auto kern = (L.kvt == PA_KV_INT4)   ? kv_append_q8_kernel<KV_INT4>
+                    : (L.kvt == PA_KV_INT8) ? kv_append_q8_kernel<KV_INT8>
+                                            : kv_append_q8_kernel<KV_FP8>;
         kern<<<blocks, 256, 0, stream>>>((uint8_t*)L.k_cache, (uint8_t*)L.v_cache, L.k_scale, L.v_scale,
                                          (const uint16_t*)L.k_new, (const uint16_t*)L.v_new, L.slots, L.T, L.Hkv,
                                          L.bs, cap);
@@ -104,7 +108,8 @@ cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream) {
 }
 
 // Whole-block copies (copy-on-write): for each pair i, every kv head's K and
-// V page of block dst[i] becomes a copy of block src[i] (and the fp8 scales).
+// V page of block dst[i] becomes a copy of block src[i] (and the scales of a
+// coded cache).
 // One thread per 16-byte unit of a block's K (and V) data.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                                                           float* __restrict__ k_scale, float* __restrict__ v_scale,
@@ -131,13 +136,17 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
 }
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
-                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool q8,
+                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, int kvt,
                                cudaStream_t stream) {
-    const int64_t units = (int64_t)Hkv * bs * d * (q8 ? 1 : 2) / 16;
+    // bytes of one token row: 2 per element (bf16), 1 (e4m3, int8), 1/2 (int4)
+    const int64_t rowb = kvt == PA_KV_BF16 ? 2 * d : (kvt == PA_KV_INT4 ? d / 2 : d);
+    const int64_t units = (int64_t)Hkv * bs * rowb / 16;
     const int64_t total = (int64_t)n * units;
     const int blocks = (int)std::min<int64_t>((total + 255) / 256, 1 << 20);
-    copy_blocks_kernel<<<blocks, 256, 0, stream>>>((uint4*)k_cache, (uint4*)v_cache, k_scale, v_scale, src, dst, n,
-                                                   units, Hkv, num_blocks);
+    copy_blocks_kernel<<<blocks, 256, 0, stream>>>((uint4*)k_cache, (uint4*)v_cache,
+                                                   kvt == PA_KV_BF16 ? nullptr : k_scale,
+                                                   kvt == PA_KV_BF16 ? nullptr : v_scale, src, dst, n, units, Hkv,
+                                                   num_blocks);
     return cudaGetLastError();
 }
 

@@ -25,9 +25,11 @@
 //     partial and base-2 log-sum-exp to the workspace and the group's last
 //     partition to finish merges them (an atomic counter per group; nothing
 //     waits on another CTA).
-// fp8 cache: e4m3 codes convert exactly to f16 in registers (q and the
-// probabilities are f16 there), the K scale folds into the scores and the V
-// scale applies per page to a fresh P.V accumulator.
+// Coded caches (e4m3, int8, int4): codes convert exactly to f16 in registers
+// (q and the probabilities are f16 there), the K scale folds into the scores
+// and the V scale applies per page to a fresh P.V accumulator.  An int4 row
+// (64 bytes) is half of a 128-byte line: the TMA map views a page as bs / 2
+// lines of two tokens each.
 #include <cuda_fp8.h>
 #include <math.h>
 
@@ -60,10 +62,12 @@ struct DecodeArgs {
 
 template <int D, int BS, int KVT>
 struct Cfg {
-    static constexpr bool FP8 = KVT != KV_BF16;   // one-byte codes (e4m3 or int8)
+    static constexpr bool FP8 = KVT != KV_BF16;   // coded cache with scales (e4m3, int8 or int4)
+    static constexpr bool I4 = KVT == KV_INT4;
     static constexpr int ELT = FP8 ? 1 : 2;
-    static constexpr int ROWB = D * ELT;       // bytes of one token row of one head
-    static constexpr int NCH = ROWB / 128;      // 128-byte column chunks = TMA boxes per page
+    static constexpr int ROWB = I4 ? D / 2 : D * ELT;   // bytes of one token row of one head
+    static constexpr int NCH = I4 ? 1 : ROWB / 128;    // TMA boxes per page (128-byte columns)
+    static constexpr int LINES = I4 ? BS / 2 : BS;     // 128-byte lines of a page's box
     static constexpr int PAGEB = BS * ROWB;     // one (block, kv_head) page of K (or V)
     static constexpr int STAGEB = 2 * PAGEB;    // K page + V page
     static constexpr int NCW = 4;               // consumer warps
@@ -73,8 +77,19 @@ struct Cfg {
     static constexpr int MT = D / 16;           // 16-row tiles of head_dim (PV)
     static constexpr int KT = BS / 16;          // 16-token steps (PV)
     static constexpr int COMBINE_FLOATS = NCW * (8 * D + 16);
-    static_assert(ROWB % 128 == 0, "rows must be whole 128-byte chunks");
+    static_assert(I4 ? ROWB == 64 : ROWB % 128 == 0, "rows must be whole 128-byte chunks (int4: half of one)");
 };
+
+// Shared address of byte `byte` of token row t of a page tile: NCH column
+// tiles of BS rows x 128 bytes, or (int4) one tile of BS / 2 lines holding
+// tokens 2L and 2L + 1 in bytes 0..63 and 64..127 of line L; 128-byte swizzle.
+template <int BS, int KVT>
+__device__ __forceinline__ uint32_t tok_addr(uint32_t tile, int t, int byte) {
+    if constexpr (KVT == KV_INT4)
+        return swz128(tile, t >> 1, ((t & 1) << 6) + byte);
+    else
+        return swz128(tile + (byte >> 7) * (BS * 128), t, byte & 127);
+}
 
 
 // ------------------------------------------------------------------ per warp
@@ -99,6 +114,16 @@ struct WarpAcc {
         for (int ks = 0; ks < D / 16; ++ks) {
             if (!valid) {
                 qa[ks][0] = qa[ks][1] = 0u;
+            } else if (KVT == KV_INT4) {
+                // step 2ch + j2 of chunk ch: lane c's elements e_i = 32ch + 8c + i in
+                // the order the nibble conversion yields them: {e0,e4},{e1,e5} then
+                // {e2,e6},{e3,e7}
+                const int ch = ks >> 1, j2 = ks & 1;
+                const uint4 w = *reinterpret_cast<const uint4*>(qrow + ch * 32 + 8 * c);
+                const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+                auto el = [&](int i) { return __uint_as_float((i & 1) ? (u[i >> 1] & 0xFFFF0000u) : (u[i >> 1] << 16)); };
+                qa[ks][0] = pack_f16x2(el(2 * j2), el(2 * j2 + 4));
+                qa[ks][1] = pack_f16x2(el(2 * j2 + 1), el(2 * j2 + 5));
             } else if (FP8) {
                 // k order inside a 16-deep step matches the e4m3 byte order 4c .. 4c+3
                 const uint2 w = *reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * c);
@@ -126,7 +151,19 @@ struct WarpAcc {
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
             const uint32_t A[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
-            if (FP8) {
+            if (KVT == KV_INT4) {
+                // one 32-bit word = 8 codes of chunk ks / 2 feeds steps ks and ks + 1
+                if (ks & 1) continue;
+                const uint32_t A1[4] = {qa[ks + 1][0], 0u, qa[ks + 1][1], 0u};
+#pragma unroll
+                for (int nt = 0; nt < C::NT; ++nt) {
+                    const uint32_t w = ld_shared_u32(tok_addr<BS, KVT>(kt, nt * 8 + g, (ks >> 1) * 16 + 4 * c));
+                    uint32_t f[4];
+                    nib8_to_f16x2(w, f);
+                    mma_f16(acc[nt], A, f[0], f[1]);
+                    mma_f16(acc[nt], A1, f[2], f[3]);
+                }
+            } else if (FP8) {
 #pragma unroll
                 for (int nt = 0; nt < C::NT; ++nt) {
                     const int t = nt * 8 + g;
@@ -191,7 +228,9 @@ struct WarpAcc {
 
         // rows past the sequence end hold stale bytes: zero them so that
         // 0-probability x non-finite garbage cannot reach the accumulator
-        if (valid < BS) {
+        // (integer codes are always finite)
+        constexpr bool ZERO_TAIL = KVT == KV_BF16 || KVT == KV_FP8;
+        if (ZERO_TAIL && valid < BS) {
             for (int idx = valid * C::ROWB / 16 + lane; idx < BS * C::ROWB / 16; idx += 32) {
                 const int row = idx / (C::ROWB / 16), u = idx % (C::ROWB / 16);
                 const uint32_t tile = vt + (u >> 3) * (BS * 128);
@@ -202,7 +241,48 @@ struct WarpAcc {
         }
 
         // ------------------------------------------------ O^T += V^T P^T
-        if (FP8) {
+        if (KVT == KV_INT4) {
+            // ldmatrix.trans of 16-bit units (4 dims of one token; a unit is 16
+            // bytes = 32 dims of a row): lane (g, c) gets tokens 2c, 2c+1 of dims
+            // 4g..4g+3 of a unit; the nibble split turns that into one A register
+            // per dim.  MMA mt = 2 * unit + jp has rows g -> dim 32 unit + 4g + 2jp
+            // and g + 8 -> that dim + 1.
+            uint32_t pb[C::KT][2];
+#pragma unroll
+            for (int kk = 0; kk < C::KT; ++kk) {
+                pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
+                pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+            }
+            // one ldmatrix.x4 covers 32 (token, unit) rows: two units of a
+            // 16-token page, or one unit of a 32-token page (matrices 2kk and
+            // 2kk + 1 are that unit's tokens 16kk .. 16kk + 15)
+            constexpr int UPL = BS == 16 ? 2 : 1;   // units per ldmatrix.x4
+#pragma unroll
+            for (int u0 = 0; u0 < D / 32; u0 += UPL) {
+                float t[2 * UPL][4];
+#pragma unroll
+                for (int i = 0; i < 2 * UPL; ++i) t[i][0] = t[i][1] = t[i][2] = t[i][3] = 0.f;
+                const int tok = BS == 16 ? (mi & 1) * 8 + r : mi * 8 + r;
+                const int unit = BS == 16 ? u0 + (mi >> 1) : u0;
+                uint32_t rr[4];
+                ldsm_x4_t(tok_addr<BS, KVT>(vt, tok, unit * 16), rr[0], rr[1], rr[2], rr[3]);
+#pragma unroll
+                for (int hm = 0; hm < 2; ++hm) {   // matrix pair (2hm, 2hm+1): tokens 0-7 and 8-15 of a k-step
+                    const int kk = BS == 16 ? 0 : hm, ti = BS == 16 ? 2 * hm : 0;
+                    uint32_t fa[4], fb[4];
+                    nib8_to_f16x2(rr[2 * hm], fa);
+                    nib8_to_f16x2(rr[2 * hm + 1], fb);
+                    const uint32_t A0[4] = {fa[0], fa[1], fb[0], fb[1]};
+                    const uint32_t A1[4] = {fa[2], fa[3], fb[2], fb[3]};
+                    mma_f16(t[ti], A0, pb[kk][0], pb[kk][1]);
+                    mma_f16(t[ti + 1], A1, pb[kk][0], pb[kk][1]);
+                }
+#pragma unroll
+                for (int i = 0; i < 2 * UPL; ++i)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[2 * u0 + i][e] = fmaf(vsc, t[i][e], o[2 * u0 + i][e]);
+            }
+        } else if (FP8) {
             uint32_t pb[C::KT][2];
 #pragma unroll
             for (int kk = 0; kk < C::KT; ++kk) {
@@ -255,7 +335,7 @@ struct WarpAcc {
                 }
             }
         }
-        if (valid < BS) fence_proxy_async_smem();  // generic writes before the next TMA fill
+        if (ZERO_TAIL && valid < BS) fence_proxy_async_smem();  // generic writes before the next TMA fill
     }
 
     // Publish this warp's state for the item-level combine.
@@ -272,7 +352,9 @@ struct WarpAcc {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int gq = 2 * c + (e & 1);
-                const int dim = FP8 ? mt * 16 + 2 * n + (e >> 1) : mt * 16 + n + 8 * (e >> 1);
+                const int dim = KVT == KV_INT4 ? 32 * (mt >> 1) + 4 * n + 2 * (mt & 1) + (e >> 1)
+                                : FP8          ? mt * 16 + 2 * n + (e >> 1)
+                                               : mt * 16 + n + 8 * (e >> 1);
                 co[(warp * 8 + gq) * D + dim] = o[mt][e];
             }
         }
@@ -406,7 +488,8 @@ struct NewRow {
 template <int D, int KVT>
 __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, int h, int phys, int off, int lane) {
     constexpr bool FP8 = KVT != KV_BF16;
-    using QC = Codec<KVT == KV_INT8 ? KV_INT8 : KV_FP8>;
+    constexpr int CK = KVT == KV_BF16 ? KV_FP8 : KVT;
+    using QC = Codec<CK>;
     NewRow r;
     const int64_t src = ((int64_t)b * a.Hkv + h) * D;
     r.kraw = r.vraw = make_uint2(0u, 0u);
@@ -421,8 +504,8 @@ __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, in
         r.vold = off == 0 ? 0.f : a.v_scale_w[(int64_t)phys * a.Hkv + h];
         r.ks = fmaxf(r.kold, __fdiv_rn(warp_max(absmax4(r.kraw)), QC::QMAX));
         r.vs = fmaxf(r.vold, __fdiv_rn(warp_max(absmax4(r.vraw)), QC::QMAX));
-        r.kc = q8_encode4<KVT == KV_INT8 ? KV_INT8 : KV_FP8>(r.kraw, r.ks);
-        r.vc = q8_encode4<KVT == KV_INT8 ? KV_INT8 : KV_FP8>(r.vraw, r.vs);
+        r.kc = q8_encode4<CK>(r.kraw, r.ks);
+        r.vc = q8_encode4<CK>(r.vraw, r.vs);
     }
     return r;
 }
@@ -431,29 +514,52 @@ template <int D, int BS, int KVT>
 __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
                                               const NewRow& r, int lane) {
     constexpr bool FP8 = KVT != KV_BF16;
-    using QC = Codec<KVT == KV_INT8 ? KV_INT8 : KV_FP8>;
+    using QC = CodecOf<KVT>;
+    constexpr uint32_t MASK = (1u << QC::BITS) - 1;
+    constexpr int ROWB = QC::BITS * D / 8;    // bytes of a coded row; lane owns QC::BITS / 2 of them
     const int64_t prow = ((int64_t)phys * a.Hkv + h) * BS;  // first row of the page
     if (FP8) {
+        // a lane's 4 codes: one 32-bit word of a one-byte row, one 16-bit word of an int4 row
+        auto ld4 = [&](uint32_t tile, int o) {
+            uint32_t w;
+            if (QC::BITS == 8)
+                w = ld_shared_u32(tok_addr<BS, KVT>(tile, o, lane * 4));
+            else {
+                unsigned short hw;
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hw) : "r"(tok_addr<BS, KVT>(tile, o, lane * 2)));
+                w = hw;
+            }
+            return w;
+        };
+        auto st4 = [&](uint32_t tile, uint8_t* gpage, int o, uint32_t nw) {
+            if (QC::BITS == 8) {
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(tok_addr<BS, KVT>(tile, o, lane * 4)), "r"(nw) : "memory");
+                reinterpret_cast<uint32_t*>(gpage)[o * 32 + lane] = nw;
+            } else {
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(tok_addr<BS, KVT>(tile, o, lane * 2)),
+                             "h"((unsigned short)nw)
+                             : "memory");
+                reinterpret_cast<uint16_t*>(gpage)[o * 32 + lane] = (uint16_t)nw;
+            }
+        };
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
             const uint32_t tile = kv == 0 ? kt : vt;
-            uint32_t* grow = reinterpret_cast<uint32_t*>((kv == 0 ? a.k_cache_w : a.v_cache_w) + prow * 128);
+            uint8_t* gpage = (kv == 0 ? a.k_cache_w : a.v_cache_w) + prow * ROWB;
             const float old = kv == 0 ? r.kold : r.vold, sn = kv == 0 ? r.ks : r.vs;
             if (sn > old && old > 0.f) {  // the scale grew: re-encode the older rows (same rule as the append)
 #pragma unroll 1
                 for (int o = 0; o < off; ++o) {
-                    const uint32_t w = ld_shared_u32(swz128(tile, o, lane * 4));
+                    const uint32_t w = ld4(tile, o);
                     uint32_t nw = 0;
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        nw |= QC::encode(__fdiv_rn(__fmul_rn(QC::value((w >> (8 * e)) & 0xFF), old), sn)) << (8 * e);
-                    asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, o, lane * 4)), "r"(nw) : "memory");
-                    grow[o * 32 + lane] = nw;
+                        nw |= QC::encode(__fdiv_rn(__fmul_rn(QC::value((w >> (QC::BITS * e)) & MASK), old), sn))
+                              << (QC::BITS * e);
+                    st4(tile, gpage, o, nw);
                 }
             }
-            const uint32_t nw = kv == 0 ? r.kc : r.vc;
-            asm volatile("st.shared.u32 [%0], %1;" ::"r"(swz128(tile, off, lane * 4)), "r"(nw) : "memory");
-            grow[off * 32 + lane] = nw;
+            st4(tile, gpage, off, kv == 0 ? r.kc : r.vc);
             if (lane == 0) (kv == 0 ? a.k_scale_w : a.v_scale_w)[(int64_t)phys * a.Hkv + h] = sn;
         }
     } else if (lane < D / 4) {
@@ -550,7 +656,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
                     if (i >= NSTAGE) alive = mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1);
                     if (alive) {
                         mbar_arrive_expect_tx(&full[s], C::STAGEB);
-                        const int y = (phys * a.Hkv + h) * BS;
+                        const int y = (phys * a.Hkv + h) * C::LINES;
                         uint8_t* stg = sgen + s * C::STAGEB;
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
@@ -674,7 +780,7 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.part_blocks = L.part_blocks;
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
-    constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : 16);
+    constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : (C::STAGEB >= 4096 ? 16 : 32));
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
     static int configured = -1;
     cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND>, SMEM, configured);
@@ -703,6 +809,9 @@ static cudaError_t launch_shape(const DecodeLaunch& L, cudaStream_t stream) {
     } else if (L.kvt == PA_KV_INT8) {
         if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_INT8, APPEND>(L, stream);
         if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_INT8, APPEND>(L, stream);
+    } else if (L.kvt == PA_KV_INT4) {
+        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_INT4, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_INT4, APPEND>(L, stream);
     } else {
         if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_BF16, APPEND>(L, stream);
         if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_BF16, APPEND>(L, stream);

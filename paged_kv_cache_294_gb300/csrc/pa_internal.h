@@ -19,7 +19,7 @@ struct AppendLaunch {
     const void* v_new;
     const int64_t* slots;
     int T, num_blocks, Hkv, d, bs;
-    int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8
+    int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8 / PA_KV_INT4
 };
 
 struct DecodeLaunch {
@@ -45,7 +45,7 @@ struct DecodeLaunch {
     int part_blocks;    // blocks per split partition
     int S;              // partitions per sequence at most (grid x)
     float scale;
-    int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8
+    int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8 / PA_KV_INT4
 };
 
 struct PrefillLaunch {
@@ -67,7 +67,7 @@ cudaError_t launch_decode(const DecodeLaunch& L, cudaStream_t stream);
 
 cudaError_t launch_wait_selftest(cudaStream_t stream);
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
-                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, bool q8,
+                               const int32_t* dst, int n, int num_blocks, int Hkv, int d, int bs, int kvt,
                                cudaStream_t stream);
 cudaError_t append_unit_error(unsigned int* v, bool clear);
 cudaError_t decode_unit_error(unsigned int* v, bool clear);

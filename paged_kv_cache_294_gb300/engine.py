@@ -14,7 +14,7 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import (PA_ERR_OOM, PA_KV_FP8_E4M3, PagedAttnError, pa_allocator, pa_block_cow, pa_copy_blocks,
+from . import (PA_ERR_OOM, PA_KV_INT4, PagedAttnError, pa_allocator, pa_block_cow, pa_copy_blocks,
                pa_decode_attention, pa_decode_resolve_splits, pa_decode_step, pa_decode_workspace_bytes,
                pa_kv_append, pa_prefix_cache, pa_slot_mapping)
 
@@ -156,9 +156,10 @@ class PagedDecodeLayer:
                  device="cuda"):
         self.num_blocks, self.Hq, self.Hkv, self.d, self.bs, self.kv = num_blocks, Hq, Hkv, d, bs, kv
         self.device = torch.device(device)
-        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
-        self.k_cache = torch.zeros((num_blocks, Hkv, bs, d), dtype=dt, device=self.device)
-        self.v_cache = torch.zeros((num_blocks, Hkv, bs, d), dtype=dt, device=self.device)
+        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8, "int4": torch.uint8}[kv]
+        row = d // 2 if kv == "int4" else d          # int4: two codes per byte
+        self.k_cache = torch.zeros((num_blocks, Hkv, bs, row), dtype=dt, device=self.device)
+        self.v_cache = torch.zeros((num_blocks, Hkv, bs, row), dtype=dt, device=self.device)
         if kv != "bf16":
             self.k_scale = torch.zeros((num_blocks, Hkv), dtype=torch.float32, device=self.device)
             self.v_scale = torch.zeros((num_blocks, Hkv), dtype=torch.float32, device=self.device)
@@ -249,7 +250,8 @@ class PagedDecodeLayer:
             return
         src = torch.tensor([p[0] for p in pairs], dtype=torch.int32).to(self.device)
         dst = torch.tensor([p[1] for p in pairs], dtype=torch.int32).to(self.device)
-        pa_copy_blocks(self.k_cache, self.v_cache, self.k_scale, self.v_scale, src, dst, stream=stream)
+        pa_copy_blocks(self.k_cache, self.v_cache, self.k_scale, self.v_scale, src, dst, stream=stream,
+                       kv_dtype=PA_KV_INT4 if self.kv == "int4" else None)
 
     def fused_step(self, q=None, k_new=None, v_new=None, out=None, num_splits: int = 0, tables=None,
                    lens=None, stream=None):

@@ -9,11 +9,11 @@ from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
 
 BF16_TOL = 1e-2     # max |err| of bf16-cache attention outputs
 FP8_TOL = 5e-2      # max |err| of fp8-cache outputs against the oracle on the stored fp8 cache
-INT8_TOL = 1e-2     # int8 cache: codes are exact in f16, so the bf16 output bound applies
+INT8_TOL = 1e-2     # int8 / int4 caches: codes are exact in f16, so the bf16 output bound applies
 
 
 def tol(w):
-    return {"fp8": FP8_TOL, "int8": INT8_TOL}.get(w.kv, BF16_TOL)
+    return {"fp8": FP8_TOL, "int8": INT8_TOL, "int4": INT8_TOL}.get(w.kv, BF16_TOL)
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:

@@ -59,14 +59,18 @@ def test_argument_errors_return_status_without_a_gpu():
                                    4, 64, 1.0, 0, None, 0, 1, None) == pa.PA_ERR_UNSUPPORTED
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 64, 4, 128, 16,
                                    4, 64, 1.0, 0, None, 0, 0, None) == pa.PA_ERR_UNSUPPORTED
-    # int8 cache (kv_dtype 2): head_dim 64 unsupported, bad kv_dtype 3 rejected
-    assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 64, 16,
-                                   4, 64, 1.0, 0, None, 0, 2, None) == pa.PA_ERR_UNSUPPORTED
+    # int8 (kv_dtype 2) and int4 (3) caches: head_dim 64 unsupported; kv_dtype 4 rejected
+    for kvd in (2, 3):
+        assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 64, 16,
+                                       4, 64, 1.0, 0, None, 0, kvd, None) == pa.PA_ERR_UNSUPPORTED
+        assert lib.pa_kv_append(None, None, None, None, None, None, None, 1, 64, 4, 64, 16, kvd,
+                                None) == pa.PA_ERR_UNSUPPORTED
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
-                                   4, 64, 1.0, 0, None, 0, 3, None) == pa.PA_ERR_INVALID
+                                   4, 64, 1.0, 0, None, 0, 4, None) == pa.PA_ERR_INVALID
     # the multi-query entry point covers the bf16 cache only
-    assert lib.pa_prefill_attention(None, None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
-                                     4, 64, 8, 1.0, 2, None) == pa.PA_ERR_UNSUPPORTED
+    for kvd in (1, 2, 3):
+        assert lib.pa_prefill_attention(None, None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
+                                         4, 64, 8, 1.0, kvd, None) == pa.PA_ERR_UNSUPPORTED
     # null pointers with a non-empty batch
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
                                    4, 64, 1.0, 0, None, 0, 0, None) == pa.PA_ERR_INVALID

@@ -14,7 +14,8 @@ pytestmark = pytest.mark.gpu
 @pytest.mark.parametrize("name,kw", [("tiny", {}), ("8b", dict(B=6, seq_len=700)),
                                      ("70b", dict(B=8, seq_len=400)),
                                      ("fp8prefix", dict(B=6, seq_len=600)),
-                                     ("8b-int8", dict(B=6, seq_len=700))])
+                                     ("8b-int8", dict(B=6, seq_len=700)),
+                                     ("8b-int4", dict(B=6, seq_len=700))])
 def test_workload_caches_bit_exact(name, kw):
     w = workloads.make(name, **kw)
     layer = run_gpu(w)
@@ -36,8 +37,8 @@ class Pair:
 
     def __init__(self, nb, hkv, d, bs, kv):
         self.o = oracle.Cache(nb, hkv, d, bs, kv)
-        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
-        self.k = torch.zeros((nb, hkv, bs, d), dtype=dt, device="cuda")
+        dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8, "int4": torch.uint8}[kv]
+        self.k = torch.zeros((nb, hkv, bs, d // 2 if kv == "int4" else d), dtype=dt, device="cuda")
         self.v = torch.zeros_like(self.k)
         self.ks = torch.zeros((nb, hkv), dtype=torch.float32, device="cuda") if kv != "bf16" else None
         self.vs = torch.zeros_like(self.ks) if kv != "bf16" else None
@@ -70,7 +71,7 @@ def test_bf16_scatter_with_skips(d, bs):
     assert pa.pa_get_device_error() == 0
 
 
-@pytest.mark.parametrize("kv", ["fp8", "int8"])
+@pytest.mark.parametrize("kv", ["fp8", "int8", "int4"])
 @pytest.mark.parametrize("bs", [16, 32])
 def test_one_byte_growth_restart_and_runs(bs, kv):
     rng = np.random.default_rng(bs)
@@ -101,7 +102,7 @@ def test_one_byte_growth_restart_and_runs(bs, kv):
     assert pa.pa_get_device_error() == 0
 
 
-@pytest.mark.parametrize("kv", ["fp8", "int8"])
+@pytest.mark.parametrize("kv", ["fp8", "int8", "int4"])
 def test_one_byte_one_token_per_sequence_many_blocks(kv):
     rng = np.random.default_rng(11)
     p = Pair(64, 4, 128, 32, kv)

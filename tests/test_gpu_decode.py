@@ -15,6 +15,7 @@ import pytest
 import torch
 
 import oracle
+import oracle.run
 import paged_kv_cache_294_gb300 as pa
 import workloads
 from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
@@ -36,7 +37,7 @@ def check(w, num_splits=0, seqs=None):
 
 SMALL = [("tiny", {}), ("8b", dict(B=8, seq_len=600)), ("70b", dict(B=12, seq_len=500)),
          ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700)),
-         ("8b-int8", dict(B=8, seq_len=600))]
+         ("8b-int8", dict(B=8, seq_len=600)), ("8b-int4", dict(B=8, seq_len=600))]
 
 
 @pytest.mark.parametrize("name,kw", SMALL)
@@ -80,6 +81,10 @@ SHAPES = [
     (5, 4, 4, 128, 32, "int8"),
     (5, 8, 1, 128, 16, "int8"),
     (5, 16, 2, 128, 16, "int8"),
+    (5, 4, 4, 128, 32, "int4"),
+    (5, 8, 1, 128, 16, "int4"),
+    (5, 16, 2, 128, 16, "int4"),
+    (5, 6, 3, 128, 32, "int4"),
 ]
 
 
@@ -158,6 +163,30 @@ def test_fp8_stale_nan_codes_past_the_end_do_not_leak():
     assert excess(got, ref, FP8_TOL) <= 1.0
 
 
+@pytest.mark.parametrize("kv,fill", [("int8", 0x7F), ("int4", 0x77)])
+@pytest.mark.parametrize("bs", [16, 32])
+def test_integer_codes_past_the_end_do_not_leak(kv, fill, bs):
+    """Integer codes are always finite, so the kernel does not clear the rows
+    past a sequence's end: the largest codes there must still weigh nothing."""
+    w = _synthetic(2, 8, 2, 128, bs, [7, 3 * bs + 5], kv=kv, seed=17 + bs)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    for b, L in enumerate(w.seq_lens):
+        blk = int(layer.tables_host[b, (L - 1) // bs])
+        layer.k_cache[blk, :, L % bs:, :] = fill
+        layer.v_cache[blk, :, L % bs:, :] = fill
+    for S in (0, 2):
+        layer.decode(num_splits=S)
+        torch.cuda.synchronize()
+        got = layer.out.float().cpu().numpy()
+        st = oracle.run.OracleStep(w, tables=layer.tables_host)
+        st.cache.k[...] = layer.k_cache.cpu().numpy().view(np.uint8)
+        st.cache.v[...] = layer.v_cache.cpu().numpy().view(np.uint8)
+        st.cache.k_scale[...] = layer.k_scale.cpu().numpy()
+        st.cache.v_scale[...] = layer.v_scale.cpu().numpy()
+        ref = oracle.decode_attention(st.cache, w.q, layer.tables_host, w.seq_lens, w.Hq, w.scale)
+        assert excess(got, ref, tol(w)) <= 1.0
+
+
 # ------------------------------------------------------------ full sizes, sampled
 
 
@@ -165,7 +194,7 @@ def _sample(B, k=6):
     return sorted({0, B - 1} | set(np.random.default_rng(7).choice(B, size=k, replace=False).tolist()))
 
 
-@pytest.mark.parametrize("name", ["8b", "70b", "fp8prefix", "8b-int8"])
+@pytest.mark.parametrize("name", ["8b", "70b", "fp8prefix", "8b-int8", "8b-int4"])
 def test_full_size_sampled(name):
     w = workloads.make(name, device="cuda")
     seqs = _sample(w.B)

@@ -100,7 +100,7 @@ def _oracle(sc):
     return cache, starts, outs, tables
 
 
-@pytest.mark.parametrize("layer_name", ["8b", "fp8prefix", "tiny", "8b-int8"])
+@pytest.mark.parametrize("layer_name", ["8b", "fp8prefix", "tiny", "8b-int8", "8b-int4"])
 @pytest.mark.parametrize("splits", [0, 2])
 def test_prefix_cached_serving_matches_the_oracle(layer_name, splits):
     sc = workloads.serving_scenario(layer_name, steps=35)     # every sequence crosses a block boundary
@@ -111,7 +111,7 @@ def test_prefix_cached_serving_matches_the_oracle(layer_name, splits):
     # every request after the first reuses the prompt's full blocks
     assert starts == o_starts and starts[0] == 0 and all(s == 5 * sc.bs for s in starts[1:])
     assert n_copies >= 1                     # the forks shared a partly filled block
-    tol = {"fp8": FP8_TOL, "int8": INT8_TOL}.get(sc.kv, BF16_TOL)
+    tol = {"fp8": FP8_TOL, "int8": INT8_TOL, "int4": INT8_TOL}.get(sc.kv, BF16_TOL)
     for s in range(len(outs)):
         assert np.array_equal(tables[s], o_tables[s])
         assert excess(outs[s], o_outs[s], tol) <= 1.0, "step %d" % s
@@ -122,15 +122,17 @@ def test_prefix_cached_serving_matches_the_oracle(layer_name, splits):
         assert np.array_equal(layer.v_scale.cpu().numpy().view(np.uint32), cache.v_scale.view(np.uint32))
 
 
-@pytest.mark.parametrize("kv,d,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("fp8", 128, 32), ("int8", 128, 16)])
+@pytest.mark.parametrize("kv,d,bs", [("bf16", 128, 16), ("bf16", 64, 32), ("fp8", 128, 32), ("int8", 128, 16),
+                                      ("int4", 128, 16), ("int4", 128, 32)])
 def test_copy_blocks_is_bit_exact(kv, d, bs):
     nb, hkv = 300, 4
     g = torch.Generator(device="cuda")
     g.manual_seed(17)
-    dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8}[kv]
-    k = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
+    dt = {"bf16": torch.bfloat16, "fp8": torch.uint8, "int8": torch.int8, "int4": torch.uint8}[kv]
+    row = d // 2 if kv == "int4" else d
+    k = torch.randint(0, 255, (nb, hkv, bs, row), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
         if dt != torch.bfloat16 else None
-    v = torch.randint(0, 255, (nb, hkv, bs, d), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
+    v = torch.randint(0, 255, (nb, hkv, bs, row), generator=g, device="cuda", dtype=torch.uint8).view(dt) \
         if dt != torch.bfloat16 else None
     if kv == "bf16":
         k = torch.randn((nb, hkv, bs, d), generator=g, device="cuda").to(dt)
@@ -143,7 +145,8 @@ def test_copy_blocks_is_bit_exact(kv, d, bs):
     k0, v0 = cache_bytes(k).copy(), cache_bytes(v).copy()
     ks0 = ks.cpu().numpy().copy() if ks is not None else None
     pa.pa_get_device_error(clear=True)
-    pa.pa_copy_blocks(k, v, ks, vs, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda())
+    pa.pa_copy_blocks(k, v, ks, vs, torch.from_numpy(src).cuda(), torch.from_numpy(dst).cuda(),
+                      kv_dtype=pa.PA_KV_INT4 if kv == "int4" else None)
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
     k0[dst], v0[dst] = k0[src], v0[src]

@@ -36,7 +36,7 @@ def _same_state(a, b):
 
 CASES = [("tiny", {}), ("8b", dict(B=8, seq_len=700)), ("70b", dict(B=12, seq_len=500)),
          ("long", dict(B=2, seq_len=3000)), ("fp8prefix", dict(B=8, seq_len=700)),
-         ("8b-int8", dict(B=8, seq_len=700))]
+         ("8b-int8", dict(B=8, seq_len=700)), ("8b-int4", dict(B=8, seq_len=700))]
 
 
 @pytest.mark.parametrize("name,kw", CASES)
@@ -54,7 +54,8 @@ def test_fused_step_equals_append_then_decode(name, kw, splits):
 
 SHAPES = [(5, 8, 8, 128, 16, "bf16"), (5, 8, 1, 128, 16, "bf16"), (5, 12, 3, 64, 16, "bf16"),
           (5, 8, 2, 64, 32, "bf16"), (5, 4, 4, 128, 32, "fp8"), (5, 8, 1, 128, 16, "fp8"),
-          (5, 4, 4, 128, 32, "int8"), (5, 8, 2, 128, 16, "int8")]
+          (5, 4, 4, 128, 32, "int8"), (5, 8, 2, 128, 16, "int8"),
+          (5, 4, 4, 128, 32, "int4"), (5, 8, 2, 128, 16, "int4")]
 
 
 @pytest.mark.parametrize("shape", SHAPES)
@@ -103,7 +104,8 @@ def test_fused_step_skips_an_invalid_last_block():
 
 
 @pytest.mark.parametrize("name,kw", [("8b", dict(B=8, seq_len=700)), ("fp8prefix", dict(B=8, seq_len=700)),
-                                     ("8b-int8", dict(B=8, seq_len=700))])
+                                     ("8b-int8", dict(B=8, seq_len=700)),
+                                     ("8b-int4", dict(B=8, seq_len=700))])
 @pytest.mark.parametrize("splits", [0, 3])
 def test_fused_step_replayed_from_a_cuda_graph(name, kw, splits):
     """pa_decode_step captured in a CUDA graph (as a serving loop replays its

@@ -41,6 +41,8 @@ CONFIGS: Dict[str, dict] = {
     "fp8prefix": dict(index=4, Hq=32, Hkv=32, d=128, bs=32, kv="fp8", B=128, num_blocks=8192),
     # the 8b workload (same seed, same inputs) on an int8 cache
     "8b-int8": dict(index=1, Hq=32, Hkv=8, d=128, bs=16, kv="int8", B=64, num_blocks=40000),
+    # and on an int4 cache (two codes per byte)
+    "8b-int4": dict(index=1, Hq=32, Hkv=8, d=128, bs=16, kv="int4", B=64, num_blocks=40000),
 }
 
 DESCRIPTIONS = {
@@ -51,6 +53,8 @@ DESCRIPTIONS = {
     "long": "long context: Hq 32 / Hkv 8, d 128, bs 16, bf16, B 4 x 131072 tokens, K scaled 0.5",
     "8b-int8": "the 8b workload on an int8 cache (per-(block, head) scales): Hq 32 / Hkv 8, d 128, bs 16, "
                "B 64, lens U[128,4096]",
+    "8b-int4": "the 8b workload on an int4 cache (4-bit codes, two per byte, per-(block, head) scales): "
+               "Hq 32 / Hkv 8, d 128, bs 16, B 64, lens U[128,4096]",
     "fp8prefix": "shared-prefix MHA, fp8 e4m3 cache: Hq=Hkv=32, d 128, bs 32, B 128 "
                  "(100 x [2048 shared + 256 own], 28 x U[256,8192])",
 }
@@ -106,7 +110,7 @@ class Workload:
     Hkv: int
     d: int
     bs: int
-    kv: str                     # "bf16", "fp8" or "int8"
+    kv: str                     # "bf16", "fp8", "int8" or "int4"
     B: int
     num_blocks: int
     M: int                      # columns of block_tables
@@ -321,7 +325,7 @@ def make(name: str, device="cpu", B: Optional[int] = None, seq_len: Optional[int
         perm = rt.permutation(num_blocks).astype(np.int32)
         tables = _tables_from_perm(lens, bs, M, perm)
         fs, fp = _history(lens)
-    elif name in ("8b", "8b-int8"):
+    elif name in ("8b", "8b-int8", "8b-int4"):
         Bn = Bfull if B is None else B
         hi = 4096 if seq_len is None else seq_len
         lens = rl.integers(128 if seq_len is None else 1, hi + 1, size=Bn).astype(np.int32)
@@ -503,11 +507,10 @@ def roofline_bytes(w: Workload) -> dict:
 
     Counts each logical token of each sequence (a shared prefix counts once per
     sequence: "logical"), and separately each distinct physical block once
-    ("unique").  Element size 2 (bf16) or 1 (fp8) plus, for fp8, one fp32
-    scale per (block, kv_head) for K and for V.
+    ("unique").  Element size 2 (bf16), 1 (fp8, int8) or 1/2 (int4) plus, for
+    the coded caches, one fp32 scale per (block, kv_head) for K and for V.
     """
-    elt = 1 if w.kv != "bf16" else 2
-    tok_bytes = 2 * w.Hkv * w.d * elt
+    tok_bytes = 2 * w.Hkv * {"bf16": 2 * w.d, "int4": w.d // 2}.get(w.kv, w.d)
     logical_tokens = int(np.sum(w.seq_lens.astype(np.int64)))
     qo = 2 * w.B * w.Hq * w.d * 2
     out = dict(logical_kv=logical_tokens * tok_bytes, q_out=qo)
