@@ -201,9 +201,29 @@ struct WarpAcc {
         }
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = exp2f(m - m_use);
+        // Lazy rescale: m is a reference point, not the running max.  It moves
+        // (and O and l are rescaled) only when a score exceeds it by more than
+        // 2^8, so that the probabilities 2^(s - m) stay below 256 (exact range
+        // for the f16 / bf16 operands) and the O rescale is skipped on almost
+        // every page.  The result is the same: O / l with l = sum 2^(s - m).
+        const bool grow = mx > m + 8.f;   // m == -inf: any finite page maximum
+        if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? mx : m;
+            const float alpha = m_new == m ? 1.f : exp2f(m - m_new);   // m == -inf: 0
+            l *= alpha;
+            m = m_new;
+            // accumulator columns are query heads 2c and 2c+1
+            const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
+            const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                o[mt][0] *= al0;
+                o[mt][1] *= al1;
+                o[mt][2] *= al0;
+                o[mt][3] *= al1;
+            }
+        }
+        const float m_use = m == -INFINITY ? 0.f : m;
         float psum = 0.f;
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
@@ -213,18 +233,7 @@ struct WarpAcc {
                 psum += sc[nt][e];
             }
         }
-        l = l * alpha + psum;
-        m = m_new;
-        // accumulator columns are query heads 2c and 2c+1
-        const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
-        const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
-#pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            o[mt][0] *= al0;
-            o[mt][1] *= al1;
-            o[mt][2] *= al0;
-            o[mt][3] *= al1;
-        }
+        l += psum;
 
         // rows past the sequence end hold stale bytes: zero them so that
         // 0-probability x non-finite garbage cannot reach the accumulator
@@ -682,11 +691,12 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
         // this head's new K/V row (and the block's scales) up front
         const bool appends = APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW;
         int app_phys = -1;
-        NewRow nr;
+        // the row waits in shared memory, not in registers, until its page arrives
+        __shared__ NewRow s_nr[APPEND ? 32 : 1];
         if (appends) {
             app_phys = trow[npages - 1];
             if (app_phys < 0 || app_phys >= a.num_blocks) app_phys = -1;
-            if (app_phys >= 0) nr = prepare_new_row<D, KVT>(a, b, h, app_phys, (len - 1) % BS, lane);
+            if (app_phys >= 0) s_nr[lane] = prepare_new_row<D, KVT>(a, b, h, app_phys, (len - 1) % BS, lane);
         }
         for (int i = warp; i < npages; i += C::NCW) {
             const int s = i % NSTAGE;
@@ -701,6 +711,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
             const uint32_t kt = sbase + s * C::STAGEB;
             const bool patched = appends && i == npages - 1 && app_phys >= 0;
             if (patched) {
+                const NewRow nr = s_nr[lane];
                 patch_new_row<D, BS, KVT>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, nr, lane);
                 if (FP8) {
                     ksc = nr.ks;

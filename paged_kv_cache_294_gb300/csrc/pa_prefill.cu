@@ -175,21 +175,6 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                  : "memory");
 }
 
-// Bounded wait that also gives up once another role of the CTA has aborted.
-__device__ __forceinline__ bool cta_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (uint32_t polls = 1; polls < (1u << 30); ++polls) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((polls & 63u) == 0) {
-            if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
-        }
-    }
-    raise_error(PA_DEVERR_TIMEOUT);
-    *abort = 1;
-    return false;
-}
 
 // Rows [r0, TN) of both 64-column halves of a tile, and every row of the
 // pages flagged in `bad`, set to zero (generic stores; one warp).
