@@ -404,31 +404,25 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* 
 
 // Log-sum-exp merge of a (sequence, kv head) group's nsplit partials, by the
 // group's last partition to finish:  out = sum_k 2^(lse_k - L) o_k.
-// `sw` holds G * nsplit floats of shared memory.
+// `sw` holds G * nsplit floats of shared memory.  A thread owns columns of 4
+// consecutive dims of one head and keeps U partitions' float4 loads in flight
+// per round trip (the first batch while the weights are computed).
 template <int D>
 __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int b, int h, int nsplit, int tid,
                                            int nthr, int warp, int nwarps, int lane, void (*sync)()) {
-    // Each thread owns elements idx = tid + e * nthr of the group's G x D
-    // outputs.  The partials of a chunk of KC partitions are loaded for all
-    // of a thread's elements at once (independent loads, one round trip),
-    // and the first chunk is in flight while the weights are computed.
-    constexpr int EMAX = 8, KC = 4;    // G * D <= 8 * 128 <= EMAX * nthr for the 160-thread CTA
+    constexpr int U = 16, D4 = D / 4;
     const int G = a.G;
     const int64_t row0 = (int64_t)b * a.Hq + h * G;
-    const int ne = G * D;
-    float pv[EMAX][KC], acc[EMAX];
-    auto load_chunk = [&](int k0) {
+    const int ncol = G * D4;
+    float4 pv[U];
+    auto load_batch = [&](int col, int k0) {
+        const int gq = col / D4, d4 = col - gq * D4;
+        const float4* op = reinterpret_cast<const float4*>(a.o_part + (row0 + gq) * a.S * D) + d4;
 #pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-            const int idx = tid + e * nthr;
-            const int gq = idx / D, dim = idx - gq * D;
-            const float* op = a.o_part + (row0 + gq) * a.S * D + dim;
-#pragma unroll
-            for (int kk = 0; kk < KC; ++kk)
-                pv[e][kk] = (idx < ne && k0 + kk < nsplit) ? __ldcg(op + (int64_t)(k0 + kk) * D) : 0.f;
-        }
+        for (int u = 0; u < U; ++u)
+            pv[u] = k0 + u < nsplit ? __ldcg(op + (int64_t)(k0 + u) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
-    load_chunk(0);
+    if (tid < ncol) load_batch(tid, 0);
     for (int i = tid; i < G * nsplit; i += nthr) {
         const int gq = i / nsplit, k = i - gq * nsplit;
         sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
@@ -449,28 +443,28 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int 
         for (int k = lane; k < nsplit; k += 32) wr[k] = exp2f(wr[k] - mx) * inv;
     }
     sync();
+    for (int col = tid; col < ncol; col += nthr) {
+        const int gq = col / D4, d4 = col - gq * D4;
+        const float* wr = sw + gq * nsplit;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k0 = 0; k0 < nsplit; k0 += U) {
+            if (k0 > 0 || col != tid) load_batch(col, k0);
 #pragma unroll
-    for (int e = 0; e < EMAX; ++e) acc[e] = 0.f;
-    for (int k0 = 0; k0 < nsplit; k0 += KC) {
-        if (k0 > 0) load_chunk(k0);
-#pragma unroll
-        for (int e = 0; e < EMAX; ++e) {
-            const int idx = tid + e * nthr;
-            const int gq = idx / D;
-            if (idx < ne) {
-#pragma unroll
-                for (int kk = 0; kk < KC; ++kk)
-                    if (k0 + kk < nsplit) acc[e] = fmaf(sw[gq * nsplit + k0 + kk], pv[e][kk], acc[e]);
+            for (int u = 0; u < U; ++u) {
+                if (k0 + u < nsplit) {
+                    const float w = wr[k0 + u];
+                    acc.x = fmaf(w, pv[u].x, acc.x);
+                    acc.y = fmaf(w, pv[u].y, acc.y);
+                    acc.z = fmaf(w, pv[u].z, acc.z);
+                    acc.w = fmaf(w, pv[u].w, acc.w);
+                }
             }
         }
-    }
-#pragma unroll
-    for (int e = 0; e < EMAX; ++e) {
-        const int idx = tid + e * nthr;
-        if (idx < ne) {
-            const int gq = idx / D, dim = idx - gq * D;
-            a.out[(row0 + gq) * D + dim] = __float2bfloat16_rn(acc[e]);
-        }
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(a.out + (row0 + gq) * D + d4 * 4) = pk;
     }
 }
 
