@@ -57,6 +57,7 @@ struct DecodeArgs {
     float* k_scale_w;
     float* v_scale_w;
     int B, Hq, Hkv, G, M, num_blocks, part_blocks, S;
+    int b_early, part_early;   // sequences b < b_early: partitions of part_early blocks
     float scale_log2;
 };
 
@@ -622,7 +623,8 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
         len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
-    const int nsplit = (nblk + a.part_blocks - 1) / a.part_blocks;  // 0 when len == 0
+    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
+    const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0
     if (split > 0 && split >= nsplit) return;
     // the sequence's blocks split evenly over its partitions (at most P each)
     const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
@@ -783,6 +785,12 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.M = L.M;
     a.num_blocks = L.num_blocks;
     a.part_blocks = L.part_blocks;
+    // Short partitions (under 128 blocks): the first half of the batch, whose
+    // CTAs start first, takes partitions up to twice as long (at most 128
+    // blocks), so fewer CTAs start and finish in the early waves and the last
+    // CTAs to start are the short ones.
+    a.b_early = L.part_blocks < 128 ? L.B / 2 : 0;
+    a.part_early = std::min(std::min(2 * L.part_blocks, 128), L.M);
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : (C::STAGEB >= 4096 ? 16 : 32));
