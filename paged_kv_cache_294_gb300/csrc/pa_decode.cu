@@ -100,6 +100,7 @@ struct WarpAcc {
     float m, l;
     float o[D / 16][4];
     uint32_t qa[D / 16][2];
+    float qbias;   // int8 cache: 1152 * sum of this lane's head's f16 q (see the QK product)
 
     __device__ __forceinline__ void reset() {
         m = -INFINITY;
@@ -134,6 +135,23 @@ struct WarpAcc {
                 qa[ks][0] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c);
                 qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c + 8);
             }
+        }
+        qbias = 0.f;
+        if (KVT == KV_INT8) {
+            // the K operand carries 1152 + c per element: the scores carry
+            // 1152 * sum_k q_k on top, summed here over the same f16 values
+            float sum = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qa[ks][j]));
+                    sum += f.x + f.y;
+                }
+            }
+            sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+            sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            qbias = kS8Bias * sum;
         }
     }
 
@@ -170,7 +188,10 @@ struct WarpAcc {
                     const int t = nt * 8 + g;
                     const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
                     uint32_t b0, b1;
-                    code4_to_f16x2<KVT>(w, b0, b1);
+                    if (KVT == KV_INT8)
+                        s8x4_to_f16x2_biased(w, b0, b1);   // qbias comes off each score below
+                    else
+                        code4_to_f16x2<KVT>(w, b0, b1);
                     mma_f16(acc[nt], A, b0, b1);
                 }
             } else {
@@ -190,12 +211,13 @@ struct WarpAcc {
         // ------------------------------------------------ online softmax
         float sc[C::NT][2];
         float mx = -INFINITY;
+        const float sb = -qbias * sl2;   // 0 but for the int8 cache
 #pragma unroll
         for (int nt = 0; nt < C::NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int tok = nt * 8 + 2 * c + e;
-                const float v = tok < valid ? acc[nt][e] * sl2 : -INFINITY;
+                const float v = tok < valid ? fmaf(acc[nt][e], sl2, sb) : -INFINITY;
                 sc[nt][e] = v;
                 mx = fmaxf(mx, v);
             }

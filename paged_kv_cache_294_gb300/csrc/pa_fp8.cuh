@@ -71,6 +71,17 @@ __device__ __forceinline__ void code4_to_f16x2(uint32_t w, uint32_t& lo, uint32_
     }
 }
 
+// four int8 codes -> two f16x2 holding 1152 + c (the step of code4_to_f16x2
+// before its subtraction; exact).  A dot product with these values exceeds the
+// one with the codes by 1152 * (sum of the other operand), a constant per
+// query head that the caller removes once per score.
+__device__ __forceinline__ void s8x4_to_f16x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
+constexpr float kS8Bias = 1152.f;
+
 // int4 code (low nibble, two's complement) -> fp32, exact.
 __device__ __forceinline__ float s4_to_f32(uint32_t code) { return (float)((int)(code << 28) >> 28); }
 
