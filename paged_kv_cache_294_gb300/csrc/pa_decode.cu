@@ -101,10 +101,15 @@ struct WarpAcc {
     float o[D / 16][4];
     uint32_t qa[D / 16][2];
     float qbias;   // int8 cache: 1152 * sum of this lane's head's f16 q (see the QK product)
+    // coded caches: O is kept in units of vref (the largest V scale so far) and
+    // psi sums the f16 probabilities P' = P * vsc / vref of this lane's head
+    // (see the P.V product); publish() turns O back into values
+    float vref, inv_vref, psi;
 
     __device__ __forceinline__ void reset() {
         m = -INFINITY;
         l = 0.f;
+        vref = inv_vref = psi = 0.f;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
@@ -234,6 +239,7 @@ struct WarpAcc {
             const float m_new = grow ? mx : m;
             const float alpha = m_new == m ? 1.f : exp2f(m - m_new);   // m == -inf: 0
             l *= alpha;
+            psi *= alpha;
             m = m_new;
             // accumulator columns are query heads 2c and 2c+1
             const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
@@ -273,27 +279,42 @@ struct WarpAcc {
         }
 
         // ------------------------------------------------ O^T += V^T P^T
+        uint32_t pq[C::KT][2];   // coded caches: P' = P * vsc / vref as f16
+        if (FP8) {
+            // O is kept in units of vref: a page with a larger V scale rescales
+            // O (and psi) once; every other page scales its probabilities
+            if (vsc > vref) {   // uniform over the warp
+                const float rs = vref / vsc;   // 0 on the first page
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) o[mt][0] *= rs, o[mt][1] *= rs, o[mt][2] *= rs, o[mt][3] *= rs;
+                psi *= rs;
+                vref = vsc;
+                inv_vref = 1.f / vsc;
+            }
+            const float ratio = vsc * inv_vref;   // 0 while every V scale seen is 0
+#pragma unroll
+            for (int kk = 0; kk < C::KT; ++kk) {
+                pq[kk][0] = pack_f16x2(sc[2 * kk][0] * ratio, sc[2 * kk][1] * ratio);
+                pq[kk][1] = pack_f16x2(sc[2 * kk + 1][0] * ratio, sc[2 * kk + 1][1] * ratio);
+                if (KVT == KV_INT8 || KVT == KV_INT4) {   // the integer codes enter P.V with an offset
+                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&pq[kk][0]));
+                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&pq[kk][1]));
+                    psi += (a0.x + a0.y) + (a1.x + a1.y);
+                }
+            }
+        }
         if (KVT == KV_INT4) {
             // ldmatrix.trans of 16-bit units (4 dims of one token; a unit is 16
             // bytes = 32 dims of a row): lane (g, c) gets tokens 2c, 2c+1 of dims
             // 4g..4g+3 of a unit; the nibble split turns that into one A register
             // per dim.  MMA mt = 2 * unit + jp has rows g -> dim 32 unit + 4g + 2jp
-            // and g + 8 -> that dim + 1.
-            uint32_t pb[C::KT][2];
-#pragma unroll
-            for (int kk = 0; kk < C::KT; ++kk) {
-                pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-            }
+            // (operand 1032 + c) and g + 8 -> that dim + 1 (operand 1152 + 16c).
             // one ldmatrix.x4 covers 32 (token, unit) rows: two units of a
             // 16-token page, or one unit of a 32-token page (matrices 2kk and
             // 2kk + 1 are that unit's tokens 16kk .. 16kk + 15)
             constexpr int UPL = BS == 16 ? 2 : 1;   // units per ldmatrix.x4
 #pragma unroll
             for (int u0 = 0; u0 < D / 32; u0 += UPL) {
-                float t[2 * UPL][4];
-#pragma unroll
-                for (int i = 0; i < 2 * UPL; ++i) t[i][0] = t[i][1] = t[i][2] = t[i][3] = 0.f;
                 const int tok = BS == 16 ? (mi & 1) * 8 + r : mi * 8 + r;
                 const int unit = BS == 16 ? u0 + (mi >> 1) : u0;
                 uint32_t rr[4];
@@ -302,28 +323,17 @@ struct WarpAcc {
                 for (int hm = 0; hm < 2; ++hm) {   // matrix pair (2hm, 2hm+1): tokens 0-7 and 8-15 of a k-step
                     const int kk = BS == 16 ? 0 : hm, ti = BS == 16 ? 2 * hm : 0;
                     uint32_t fa[4], fb[4];
-                    nib8_to_f16x2(rr[2 * hm], fa);
-                    nib8_to_f16x2(rr[2 * hm + 1], fb);
+                    nib8_to_f16x2_raw(rr[2 * hm], fa);
+                    nib8_to_f16x2_raw(rr[2 * hm + 1], fb);
                     const uint32_t A0[4] = {fa[0], fa[1], fb[0], fb[1]};
                     const uint32_t A1[4] = {fa[2], fa[3], fb[2], fb[3]};
-                    mma_f16(t[ti], A0, pb[kk][0], pb[kk][1]);
-                    mma_f16(t[ti + 1], A1, pb[kk][0], pb[kk][1]);
+                    mma_f16(o[2 * u0 + ti], A0, pq[kk][0], pq[kk][1]);
+                    mma_f16(o[2 * u0 + ti + 1], A1, pq[kk][0], pq[kk][1]);
                 }
-#pragma unroll
-                for (int i = 0; i < 2 * UPL; ++i)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) o[2 * u0 + i][e] = fmaf(vsc, t[i][e], o[2 * u0 + i][e]);
             }
         } else if (FP8) {
-            uint32_t pb[C::KT][2];
-#pragma unroll
-            for (int kk = 0; kk < C::KT; ++kk) {
-                pb[kk][0] = pack_f16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                pb[kk][1] = pack_f16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-            }
 #pragma unroll
             for (int mp = 0; mp < C::MT / 2; ++mp) {
-                float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int kk = 0; kk < C::KT; ++kk) {
                     const int t = kk * 16 + (mi & 1) * 8 + r;
@@ -334,17 +344,19 @@ struct WarpAcc {
                     const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
                     const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
                     uint32_t A0[4], A1[4];
-                    code4_to_f16x2<KVT>(x0, A0[0], A0[1]);
-                    code4_to_f16x2<KVT>(x1, A0[2], A0[3]);
-                    code4_to_f16x2<KVT>(x2, A1[0], A1[1]);
-                    code4_to_f16x2<KVT>(x3, A1[2], A1[3]);
-                    mma_f16(t0, A0, pb[kk][0], pb[kk][1]);
-                    mma_f16(t1, A1, pb[kk][0], pb[kk][1]);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    o[2 * mp][e] = fmaf(vsc, t0[e], o[2 * mp][e]);
-                    o[2 * mp + 1][e] = fmaf(vsc, t1[e], o[2 * mp + 1][e]);
+                    if (KVT == KV_INT8) {   // operands 1152 + c
+                        s8x4_to_f16x2_biased(x0, A0[0], A0[1]);
+                        s8x4_to_f16x2_biased(x1, A0[2], A0[3]);
+                        s8x4_to_f16x2_biased(x2, A1[0], A1[1]);
+                        s8x4_to_f16x2_biased(x3, A1[2], A1[3]);
+                    } else {
+                        code4_to_f16x2<KVT>(x0, A0[0], A0[1]);
+                        code4_to_f16x2<KVT>(x1, A0[2], A0[3]);
+                        code4_to_f16x2<KVT>(x2, A1[0], A1[1]);
+                        code4_to_f16x2<KVT>(x3, A1[2], A1[3]);
+                    }
+                    mma_f16(o[2 * mp], A0, pq[kk][0], pq[kk][1]);
+                    mma_f16(o[2 * mp + 1], A1, pq[kk][0], pq[kk][1]);
                 }
             }
         } else {
@@ -375,6 +387,27 @@ struct WarpAcc {
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
         const int g = lane >> 2, c = lane & 3, n = lane >> 2;
+        if (FP8) {
+            // back from units of vref; the integer codes' offsets (times the sum
+            // of the probabilities they met) come off, int4's odd dims were x16
+            psi += __shfl_xor_sync(0xffffffffu, psi, 1);
+            psi += __shfl_xor_sync(0xffffffffu, psi, 2);
+            const float ps0 = __shfl_sync(0xffffffffu, psi, 8 * c), ps1 = __shfl_sync(0xffffffffu, psi, 8 * c + 4);
+#pragma unroll
+            for (int mt = 0; mt < D / 16; ++mt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ps = (e & 1) ? ps1 : ps0;
+                    if (KVT == KV_INT8)
+                        o[mt][e] = (o[mt][e] - kS8Bias * ps) * vref;
+                    else if (KVT == KV_INT4)
+                        o[mt][e] = (e >> 1) ? (o[mt][e] - kS4BiasHi * ps) * (vref * 0.0625f)
+                                            : (o[mt][e] - kS4BiasLo * ps) * vref;
+                    else
+                        o[mt][e] *= vref;
+                }
+            }
+        }
         if (c == 0) {
             cm[warp * 8 + g] = m;
             cl[warp * 8 + g] = l;

@@ -116,6 +116,19 @@ __device__ __forceinline__ void nib8_to_f16x2(uint32_t w, uint32_t (&f)[4]) {
     }
 }
 
+// The same eight codes before the final subtraction / scaling (exact): f[0],
+// f[2] hold 1032 + c (nibbles 0, 4 and 2, 6), f[1], f[3] hold 1152 + 16c
+// (nibbles 1, 5 and 3, 7).  The caller removes the offsets and the factor 16
+// after the products are summed.
+__device__ __forceinline__ void nib8_to_f16x2_raw(uint32_t w, uint32_t (&f)[4]) {
+    const uint32_t w8 = w >> 8;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(f[0]) : "r"(w), "r"(0x000F000Fu), "r"(0x64086408u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(f[1]) : "r"(w), "r"(0x00F000F0u), "r"(0x64806480u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(f[2]) : "r"(w8), "r"(0x000F000Fu), "r"(0x64086408u));
+    asm("lop3.b32 %0, %1, %2, %3, 0x6a;" : "=r"(f[3]) : "r"(w8), "r"(0x00F000F0u), "r"(0x64806480u));
+}
+constexpr float kS4BiasLo = 1032.f, kS4BiasHi = 1152.f;
+
 // BITS: bits per code; a lane's four codes pack into BITS * 4 bits, code e at
 // bit BITS * e (int4: the nibble order of the row).
 template <int KVT>
