@@ -50,9 +50,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 struct MapKey {
     const void* ptr;
     int64_t rows;
-    int d, bs, dtype, device;
+    int d, box_tok, dtype, device;
     bool operator==(const MapKey& o) const {
-        return ptr == o.ptr && rows == o.rows && d == o.d && bs == o.bs && dtype == o.dtype &&
+        return ptr == o.ptr && rows == o.rows && d == o.d && box_tok == o.box_tok && dtype == o.dtype &&
                device == o.device;
     }
 };
@@ -72,16 +72,17 @@ MapCache& map_cache() {
 }
 
 // The cache viewed as a 2-D tensor: rows = num_blocks * Hkv * bs token rows of
-// d elements; one box = bs rows x 128 bytes, written to shared memory with
-// the 128-byte swizzle (a page of head_dim 128 bf16 takes two boxes).  An
-// int4 row of 128 codes is 64 bytes: the tensor is then rows / 2 lines of 128
-// bytes (two tokens each) and a box is bs / 2 lines.
-bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, CUtensorMap* out) {
+// d elements; one box = box_tok rows x 128 bytes (a page, or the adjacent
+// pages of several kv heads of one block), written to shared memory with the
+// 128-byte swizzle (head_dim 128 bf16 takes two boxes per row range).  An int4
+// row of 128 codes is 64 bytes: the tensor is then rows / 2 lines of 128 bytes
+// (two tokens each) and a box is box_tok / 2 lines.
+bool encode_cache_map(const void* base, int64_t rows, int d, int box_tok, int dtype, CUtensorMap* out) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
     if (!enc) return false;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
-    const MapKey k{base, rows, d, bs, dtype, dev};
+    const MapKey k{base, rows, d, box_tok, dtype, dev};
     MapCache& c = map_cache();
     std::lock_guard<std::mutex> lock(c.mu);
     for (int i = 0; i < MapCache::N; ++i)
@@ -94,13 +95,13 @@ bool encode_cache_map(const void* base, int64_t rows, int d, int bs, int dtype, 
     const int elt = q8 ? 1 : 2;
     cuuint64_t gdim[2] = {(cuuint64_t)d, (cuuint64_t)rows};
     cuuint64_t gstride[1] = {(cuuint64_t)d * elt};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)bs};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)box_tok};
     if (i4) {
         gdim[0] = 128;
         gdim[1] = (cuuint64_t)(rows / 2);
         gstride[0] = 128;
         box[0] = 128;
-        box[1] = (cuuint32_t)(bs / 2);
+        box[1] = (cuuint32_t)(box_tok / 2);
     }
     cuuint32_t estride[2] = {1, 1};
     CUtensorMap m;
@@ -195,14 +196,17 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
         return (int)ceil_div(M, part_blocks_for(M, S));
     }
     // Automatic: about two waves of the three CTAs an SM holds, assuming the
-    // tables are half full on average; a partition holds 32 .. 128 blocks
-    // (enough pages per CTA to amortise its start-up, few enough to keep the
-    // last wave short).
+    // tables are half full on average; a CTA streams 32 .. 128 pages (enough
+    // to amortise its start-up, few enough to keep the last wave short).  A
+    // CTA covers two kv heads when their count is even, so its partition is
+    // half as many blocks.
+    const int hpc = num_kv_heads % 2 == 0 ? 2 : 1;
     const int64_t pages = (int64_t)batch * num_kv_heads * M / 2;
     const int64_t target = (int64_t)device_sms() * 6;
     int64_t P = ceil_div(pages, target);
     if (P < 32) P = 32;
     if (P > 128) P = 128;
+    P = ceil_div(P, hpc);
     if (P > M) P = M;
     if (ceil_div(M, P) > kMaxSplits) P = ceil_div(M, kMaxSplits);
     return (int)ceil_div(M, P);
@@ -251,12 +255,16 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_INVALID;
 
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
+    // two kv heads per CTA when their count is even: one box holds a block's
+    // pages of both
+    const int hpc = num_kv_heads % 2 == 0 ? 2 : 1;
     CUtensorMap tm_k, tm_v;
-    if (!encode_cache_map(k_cache, rows, head_dim, block_size, kv_dtype, &tm_k) ||
-        !encode_cache_map(v_cache, rows, head_dim, block_size, kv_dtype, &tm_v))
+    if (!encode_cache_map(k_cache, rows, head_dim, hpc * block_size, kv_dtype, &tm_k) ||
+        !encode_cache_map(v_cache, rows, head_dim, hpc * block_size, kv_dtype, &tm_v))
         return PA_ERR_CUDA;
 
     pa::DecodeLaunch L;
+    L.hpc = hpc;
     L.out = out;
     L.q = q;
     L.k_scale = k_scale;

@@ -61,7 +61,9 @@ struct DecodeArgs {
     float scale_log2;
 };
 
-template <int D, int BS, int KVT>
+// HPC: kv heads per CTA.  The pages of one block for consecutive kv heads
+// are adjacent in the cache, so one copy fetches a block for HPC heads.
+template <int D, int BS, int KVT, int HPC = 1>
 struct Cfg {
     static constexpr bool FP8 = KVT != KV_BF16;   // coded cache with scales (e4m3, int8 or int4)
     static constexpr bool I4 = KVT == KV_INT4;
@@ -70,8 +72,10 @@ struct Cfg {
     static constexpr int NCH = I4 ? 1 : ROWB / 128;    // TMA boxes per page (128-byte columns)
     static constexpr int LINES = I4 ? BS / 2 : BS;     // 128-byte lines of a page's box
     static constexpr int PAGEB = BS * ROWB;     // one (block, kv_head) page of K (or V)
-    static constexpr int STAGEB = 2 * PAGEB;    // K page + V page
+    static constexpr int STAGEB = 2 * HPC * PAGEB;   // a block's K pages, then its V pages, for HPC heads
+    static constexpr int CHS = HPC * BS * 128;  // stride of the 128-byte column tiles of a stage's K (or V)
     static constexpr int NCW = 4;               // consumer warps
+    static constexpr int WPH = NCW / HPC;       // consumer warps per kv head
     static constexpr int NTHREADS = (NCW + 1) * 32;
     static constexpr int NT = BS / 8;           // 8-token column tiles per page (QK)
     static constexpr int KS = D / 16;           // 16-deep steps over head_dim (QK)
@@ -82,21 +86,23 @@ struct Cfg {
 };
 
 // Shared address of byte `byte` of token row t of a page tile: NCH column
-// tiles of BS rows x 128 bytes, or (int4) one tile of BS / 2 lines holding
-// tokens 2L and 2L + 1 in bytes 0..63 and 64..127 of line L; 128-byte swizzle.
-template <int BS, int KVT>
+// tiles of BS rows x 128 bytes, CHS bytes apart, or (int4) one tile of BS / 2
+// lines holding tokens 2L and 2L + 1 in bytes 0..63 and 64..127 of line L;
+// 128-byte swizzle.
+template <int BS, int KVT, int CHS>
 __device__ __forceinline__ uint32_t tok_addr(uint32_t tile, int t, int byte) {
     if constexpr (KVT == KV_INT4)
         return swz128(tile, t >> 1, ((t & 1) << 6) + byte);
     else
-        return swz128(tile + (byte >> 7) * (BS * 128), t, byte & 127);
+        return swz128(tile + (byte >> 7) * CHS, t, byte & 127);
 }
 
 
 // ------------------------------------------------------------------ per warp
-template <int D, int BS, int KVT>
+template <int D, int BS, int KVT, int HPC>
 struct WarpAcc {
     static constexpr bool FP8 = KVT != KV_BF16;
+    static constexpr int CHS = Cfg<D, BS, KVT, HPC>::CHS;
     float m, l;
     float o[D / 16][4];
     uint32_t qa[D / 16][2];
@@ -164,7 +170,7 @@ struct WarpAcc {
     // the number of its tokens inside the sequence, sl2 = scale * log2(e)
     // (times the K scale for fp8), vsc the V scale (fp8).
     __device__ __forceinline__ void page(uint32_t kt, uint32_t vt, int valid, float sl2, float vsc, int lane) {
-        using C = Cfg<D, BS, KVT>;
+        using C = Cfg<D, BS, KVT, HPC>;
         const int g = lane >> 2, c = lane & 3;
         const int mi = lane >> 3, r = lane & 7;
 
@@ -181,7 +187,7 @@ struct WarpAcc {
                 const uint32_t A1[4] = {qa[ks + 1][0], 0u, qa[ks + 1][1], 0u};
 #pragma unroll
                 for (int nt = 0; nt < C::NT; ++nt) {
-                    const uint32_t w = ld_shared_u32(tok_addr<BS, KVT>(kt, nt * 8 + g, (ks >> 1) * 16 + 4 * c));
+                    const uint32_t w = ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, nt * 8 + g, (ks >> 1) * 16 + 4 * c));
                     uint32_t f[4];
                     nib8_to_f16x2(w, f);
                     mma_f16(acc[nt], A, f[0], f[1]);
@@ -201,7 +207,7 @@ struct WarpAcc {
                 }
             } else {
                 const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
-                const uint32_t ktile = kt + (jg >> 3) * (BS * 128);
+                const uint32_t ktile = kt + (jg >> 3) * C::CHS;
 #pragma unroll
                 for (int p = 0; p < C::NT / 2; ++p) {
                     const int t = (2 * p + (mi >> 1)) * 8 + r;
@@ -271,7 +277,7 @@ struct WarpAcc {
         if (ZERO_TAIL && valid < BS) {
             for (int idx = valid * C::ROWB / 16 + lane; idx < BS * C::ROWB / 16; idx += 32) {
                 const int row = idx / (C::ROWB / 16), u = idx % (C::ROWB / 16);
-                const uint32_t tile = vt + (u >> 3) * (BS * 128);
+                const uint32_t tile = vt + (u >> 3) * C::CHS;
                 asm volatile("st.shared.v4.u32 [%0], {%1,%1,%1,%1};" ::"r"(swz128(tile, row, (u & 7) * 16)), "r"(0u)
                              : "memory");
             }
@@ -318,7 +324,7 @@ struct WarpAcc {
                 const int tok = BS == 16 ? (mi & 1) * 8 + r : mi * 8 + r;
                 const int unit = BS == 16 ? u0 + (mi >> 1) : u0;
                 uint32_t rr[4];
-                ldsm_x4_t(tok_addr<BS, KVT>(vt, tok, unit * 16), rr[0], rr[1], rr[2], rr[3]);
+                ldsm_x4_t(tok_addr<BS, KVT, CHS>(vt, tok, unit * 16), rr[0], rr[1], rr[2], rr[3]);
 #pragma unroll
                 for (int hm = 0; hm < 2; ++hm) {   // matrix pair (2hm, 2hm+1): tokens 0-7 and 8-15 of a k-step
                     const int kk = BS == 16 ? 0 : hm, ti = BS == 16 ? 2 * hm : 0;
@@ -369,7 +375,7 @@ struct WarpAcc {
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
                 const int jg = 2 * mt + (mi & 1);
-                const uint32_t vtile = vt + (jg >> 3) * (BS * 128);
+                const uint32_t vtile = vt + (jg >> 3) * C::CHS;
 #pragma unroll
                 for (int kk = 0; kk < C::KT; ++kk) {
                     const int t = kk * 16 + (mi >> 1) * 8 + r;
@@ -426,28 +432,31 @@ struct WarpAcc {
     }
 };
 
-// Item-level combine of the consumer warps' states, then the output: bf16 out
+// CTA-level combine of the consumer warps' states, then the output: bf16 out
 // for a one-partition sequence, else the partition's normalised partial and
-// base-2 log-sum-exp.  Threads tid < nthr take part.
-template <int D, int NCW>
+// base-2 log-sum-exp.  Kv head h0 + hh is combined from warps hh * WPH ..
+// hh * WPH + WPH - 1.  Threads tid < nthr take part.
+template <int D, int WPH, int HPC>
 __device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* cm, const float* cl, const float* co,
-                                              int b, int h, int split, int nsplit, int tid, int nthr) {
+                                              int b, int h0, int split, int nsplit, int tid, int nthr) {
     const int G = a.G;
-    for (int idx = tid; idx < G * D; idx += nthr) {
-        const int gq = idx / D, dim = idx - gq * D;
+    for (int idx = tid; idx < HPC * G * D; idx += nthr) {
+        const int hg = idx / D, dim = idx - hg * D;
+        const int hh = hg / G, gq = hg - hh * G;
+        const int w0 = hh * WPH;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, cm[w * 8 + gq]);
+        for (int w = w0; w < w0 + WPH; ++w) M = fmaxf(M, cm[w * 8 + gq]);
         float L = 0.f, O = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < NCW; ++w) {
+            for (int w = w0; w < w0 + WPH; ++w) {
                 const float f = exp2f(cm[w * 8 + gq] - M);
                 L += cl[w * 8 + gq] * f;
                 O += co[(w * 8 + gq) * D + dim] * f;
             }
         }
-        const int64_t row = (int64_t)b * a.Hq + h * G + gq;
+        const int64_t row = (int64_t)b * a.Hq + (h0 + hh) * G + gq;
         const float val = (M == -INFINITY) ? 0.f : O / L;
         if (nsplit <= 1) {
             a.out[row * D + dim] = __float2bfloat16_rn(val);
@@ -458,17 +467,16 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* 
     }
 }
 
-// Log-sum-exp merge of a (sequence, kv head) group's nsplit partials, by the
+// Log-sum-exp merge of a group's nsplit partials (the G query heads of each
+// of the CTA's kv heads: rows row0 .. row0 + G - 1 of the output), by the
 // group's last partition to finish:  out = sum_k 2^(lse_k - L) o_k.
 // `sw` holds G * nsplit floats of shared memory.  A thread owns columns of 4
-// consecutive dims of one head and keeps U partitions' float4 loads in flight
+// consecutive dims of one row and keeps U partitions' float4 loads in flight
 // per round trip (the first batch while the weights are computed).
 template <int D>
-__device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int b, int h, int nsplit, int tid,
-                                           int nthr, int warp, int nwarps, int lane, void (*sync)()) {
+__device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int64_t row0, int G, int nsplit,
+                                           int tid, int nthr, int warp, int nwarps, int lane, void (*sync)()) {
     constexpr int U = 16, D4 = D / 4;
-    const int G = a.G;
-    const int64_t row0 = (int64_t)b * a.Hq + h * G;
     const int ncol = G * D4;
     float4 pv[U];
     auto load_batch = [&](int col, int k0) {
@@ -569,10 +577,11 @@ __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, in
     return r;
 }
 
-template <int D, int BS, int KVT>
+template <int D, int BS, int KVT, int HPC>
 __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
                                               const NewRow& r, int lane) {
     constexpr bool FP8 = KVT != KV_BF16;
+    constexpr int CHS = Cfg<D, BS, KVT, HPC>::CHS;
     using QC = CodecOf<KVT>;
     constexpr uint32_t MASK = (1u << QC::BITS) - 1;
     constexpr int ROWB = QC::BITS * D / 8;    // bytes of a coded row; lane owns QC::BITS / 2 of them
@@ -582,20 +591,20 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
         auto ld4 = [&](uint32_t tile, int o) {
             uint32_t w;
             if (QC::BITS == 8)
-                w = ld_shared_u32(tok_addr<BS, KVT>(tile, o, lane * 4));
+                w = ld_shared_u32(tok_addr<BS, KVT, CHS>(tile, o, lane * 4));
             else {
                 unsigned short hw;
-                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hw) : "r"(tok_addr<BS, KVT>(tile, o, lane * 2)));
+                asm volatile("ld.shared.u16 %0, [%1];" : "=h"(hw) : "r"(tok_addr<BS, KVT, CHS>(tile, o, lane * 2)));
                 w = hw;
             }
             return w;
         };
         auto st4 = [&](uint32_t tile, uint8_t* gpage, int o, uint32_t nw) {
             if (QC::BITS == 8) {
-                asm volatile("st.shared.u32 [%0], %1;" ::"r"(tok_addr<BS, KVT>(tile, o, lane * 4)), "r"(nw) : "memory");
+                asm volatile("st.shared.u32 [%0], %1;" ::"r"(tok_addr<BS, KVT, CHS>(tile, o, lane * 4)), "r"(nw) : "memory");
                 reinterpret_cast<uint32_t*>(gpage)[o * 32 + lane] = nw;
             } else {
-                asm volatile("st.shared.u16 [%0], %1;" ::"r"(tok_addr<BS, KVT>(tile, o, lane * 2)),
+                asm volatile("st.shared.u16 [%0], %1;" ::"r"(tok_addr<BS, KVT, CHS>(tile, o, lane * 2)),
                              "h"((unsigned short)nw)
                              : "memory");
                 reinterpret_cast<uint16_t*>(gpage)[o * 32 + lane] = (uint16_t)nw;
@@ -623,10 +632,10 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
         }
     } else if (lane < D / 4) {
         const int ct = (lane * 4) / 64, byte = (lane * 4 % 64) * 2;
-        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(kt + ct * BS * 128, off, byte)), "r"(r.kraw.x),
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(kt + ct * CHS, off, byte)), "r"(r.kraw.x),
                      "r"(r.kraw.y)
                      : "memory");
-        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(vt + ct * BS * 128, off, byte)), "r"(r.vraw.x),
+        asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(swz128(vt + ct * CHS, off, byte)), "r"(r.vraw.x),
                      "r"(r.vraw.y)
                      : "memory");
         *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(a.k_cache_w) + (prow + off) * D + lane * 4) = r.kraw;
@@ -635,17 +644,19 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
     __syncwarp();
 }
 
-template <int D, int BS, int KVT, int NSTAGE, bool APPEND>
-__global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
+template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC>
+__global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeArgs a) {
-    using C = Cfg<D, BS, KVT>;
+    using C = Cfg<D, BS, KVT, HPC>;
     constexpr bool FP8 = C::FP8;
     constexpr int BAR_OFF = NSTAGE * C::STAGEB;
+    constexpr int WPH = C::WPH;
     static_assert(C::COMBINE_FLOATS * 4 <= NSTAGE * C::STAGEB, "combine area must fit in the stages");
-    // stage s is always consumed by warp s % NCW, so no waiter can run two
-    // phases ahead of a stage's oldest unconsumed fill (parity waits alias)
-    static_assert(NSTAGE % Cfg<D, BS, KVT>::NCW == 0, "ring depth must be a multiple of the consumer warps");
+    // stage s is always consumed by warps hh * WPH + s % WPH (one per kv head),
+    // so no waiter can run two phases ahead of a stage's oldest unconsumed
+    // fill (parity waits alias)
+    static_assert(NSTAGE % WPH == 0, "ring depth must be a multiple of the consumer warps per head");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
@@ -653,13 +664,14 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
     uint64_t* full = reinterpret_cast<uint64_t*>(sgen + BAR_OFF);
     uint64_t* empty = full + NSTAGE;
 
-    const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    const int split = blockIdx.x, b = blockIdx.z;
+    const int h0 = blockIdx.y * HPC;   // this CTA's kv heads: h0 .. h0 + HPC - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], HPC);   // released once per kv head
         }
         fence_mbar_init();
     }
@@ -674,7 +686,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
     int len = a.lens[b];
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
-        if (threadIdx.x == 0 && split == 0 && h == 0) raise_error(PA_DEVERR_SEQ_LEN);
+        if (threadIdx.x == 0 && split == 0 && h0 == 0) raise_error(PA_DEVERR_SEQ_LEN);
         len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
@@ -689,7 +701,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
     if (split > 0 && warp == C::NCW && lane < npages) phys0 = trow[lane];
     __syncthreads();
 
-    WarpAcc<D, BS, KVT> st;
+    WarpAcc<D, BS, KVT, HPC> st;
     st.reset();
     if (warp == C::NCW) {
         if (lane == 0) {
@@ -716,14 +728,15 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
                     if (i >= NSTAGE) alive = mbar_wait(&empty[s], ((i / NSTAGE) - 1) & 1);
                     if (alive) {
                         mbar_arrive_expect_tx(&full[s], C::STAGEB);
-                        const int y = (phys * a.Hkv + h) * C::LINES;
+                        // one box: the block's rows for kv heads h0 .. h0 + HPC - 1
+                        const int y = (phys * a.Hkv + h0) * C::LINES;
                         uint8_t* stg = sgen + s * C::STAGEB;
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
-                            tma_load_2d(stg + ch * BS * 128, &tm_k, ch * (128 / C::ELT), y, &full[s]);
+                            tma_load_2d(stg + ch * C::CHS, &tm_k, ch * (128 / C::ELT), y, &full[s]);
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
-                            tma_load_2d(stg + C::PAGEB + ch * BS * 128, &tm_v, ch * (128 / C::ELT), y, &full[s]);
+                            tma_load_2d(stg + HPC * C::PAGEB + ch * C::CHS, &tm_v, ch * (128 / C::ELT), y, &full[s]);
                     }
                 }
             }
@@ -736,20 +749,22 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
             }
         }
     } else {
+        // consumer warp: kv head h = h0 + hh, pages i with i mod WPH == wi
+        const int hh = warp / WPH, wi = warp - hh * WPH, h = h0 + hh;
         const int g = lane >> 2;
         st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
         // fused step: the warp that consumes the page holding position len-1 fetches
-        // this head's new K/V row (and the block's scales) up front
-        const bool appends = APPEND && split == nsplit - 1 && npages > 0 && warp == (npages - 1) % C::NCW;
+        // its head's new K/V row (and the block's scales) up front
+        const bool appends = APPEND && split == nsplit - 1 && npages > 0 && wi == (npages - 1) % WPH;
         int app_phys = -1;
         // the row waits in shared memory, not in registers, until its page arrives
-        __shared__ NewRow s_nr[APPEND ? 32 : 1];
+        __shared__ NewRow s_nr[APPEND ? HPC : 1][32];
         if (appends) {
             app_phys = trow[npages - 1];
             if (app_phys < 0 || app_phys >= a.num_blocks) app_phys = -1;
-            if (app_phys >= 0) s_nr[lane] = prepare_new_row<D, KVT>(a, b, h, app_phys, (len - 1) % BS, lane);
+            if (app_phys >= 0) s_nr[hh][lane] = prepare_new_row<D, KVT>(a, b, h, app_phys, (len - 1) % BS, lane);
         }
-        for (int i = warp; i < npages; i += C::NCW) {
+        for (int i = wi; i < npages; i += WPH) {
             const int s = i % NSTAGE;
             float ksc = 1.f, vsc = 1.f;
             if (FP8) {
@@ -759,18 +774,19 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
                 vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
             }
             if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
-            const uint32_t kt = sbase + s * C::STAGEB;
+            // this head's rows of the stage: line hh * LINES of each column tile
+            const uint32_t kt = sbase + s * C::STAGEB + hh * C::LINES * 128;
+            const uint32_t vt = kt + HPC * C::PAGEB;
             const bool patched = appends && i == npages - 1 && app_phys >= 0;
             if (patched) {
-                const NewRow nr = s_nr[lane];
-                patch_new_row<D, BS, KVT>(a, h, app_phys, (len - 1) % BS, kt, kt + C::PAGEB, nr, lane);
+                const NewRow nr = s_nr[hh][lane];
+                patch_new_row<D, BS, KVT, HPC>(a, h, app_phys, (len - 1) % BS, kt, vt, nr, lane);
                 if (FP8) {
                     ksc = nr.ks;
                     vsc = nr.vs;
                 }
             }
-            st.page(kt, kt + C::PAGEB, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc,
-                    lane);
+            st.page(kt, vt, min(BS, len - (j0 + i) * BS), FP8 ? a.scale_log2 * ksc : a.scale_log2, vsc, lane);
             if (patched) fence_proxy_async_smem();  // generic writes before the next TMA fill
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
@@ -783,21 +799,24 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT>::NTHREADS, 3)
     float* co = cl + C::NCW * 8;
     if (warp < C::NCW) st.publish(cm, cl, co, warp, lane);
     __syncthreads();
-    combine_store<D, C::NCW>(a, cm, cl, co, b, h, split, nsplit, threadIdx.x, C::NTHREADS);
+    combine_store<D, WPH, HPC>(a, cm, cl, co, b, h0, split, nsplit, threadIdx.x, C::NTHREADS);
     if (nsplit <= 1) return;
 
+    // the group: this CTA's kv heads of sequence b, counted per head set
+    const int grp = b * (a.Hkv / HPC) + blockIdx.y;
     __shared__ int s_last;
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) {
-        const int old = atomicAdd(&a.counters[b * a.Hkv + h], 1);
+        const int old = atomicAdd(&a.counters[grp], 1);
         s_last = (old == nsplit - 1);
     }
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    merge_group<D>(a, cm, b, h, nsplit, threadIdx.x, C::NTHREADS, warp, C::NCW + 1, lane, sync_cta);
-    if (threadIdx.x == 0) a.counters[b * a.Hkv + h] = 0;
+    merge_group<D>(a, cm, (int64_t)b * a.Hq + h0 * a.G, HPC * a.G, nsplit, threadIdx.x, C::NTHREADS, warp,
+                   C::NCW + 1, lane, sync_cta);
+    if (threadIdx.x == 0) a.counters[grp] = 0;
 }
 
 // ------------------------------------------------------------------ launch
@@ -814,9 +833,9 @@ static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
     return cudaSuccess;
 }
 
-template <int D, int BS, int KVT, bool APPEND>
+template <int D, int BS, int KVT, bool APPEND, int HPC>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
-    using C = Cfg<D, BS, KVT>;
+    using C = Cfg<D, BS, KVT, HPC>;
     DecodeArgs a;
     a.out = (__nv_bfloat16*)L.out;
     a.q = (const uint16_t*)L.q;
@@ -840,24 +859,24 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.M = L.M;
     a.num_blocks = L.num_blocks;
     a.part_blocks = L.part_blocks;
-    // Short partitions (under 128 blocks): the first half of the batch, whose
-    // CTAs start first, takes partitions up to twice as long (at most 128
-    // blocks), so fewer CTAs start and finish in the early waves and the last
-    // CTAs to start are the short ones.
-    a.b_early = L.part_blocks < 128 ? L.B / 2 : 0;
-    a.part_early = std::min(std::min(2 * L.part_blocks, 128), L.M);
+    // Short partitions (under 128 pages per CTA): the first half of the
+    // batch, whose CTAs start first, takes partitions up to twice as long (at
+    // most 128 pages per CTA), so fewer CTAs start and finish in the early
+    // waves and the last CTAs to start are the short ones.
+    a.b_early = L.part_blocks * HPC < 128 ? L.B / 2 : 0;
+    a.part_early = std::min(std::min(2 * L.part_blocks, 128 / HPC), L.M);
     a.S = L.S;
     a.scale_log2 = L.scale * 1.4426950408889634f;
-    constexpr int NST = (C::STAGEB >= 16384) ? 4 : (C::STAGEB >= 8192 ? 8 : (C::STAGEB >= 4096 ? 16 : 32));
+    constexpr int NST = 65536 / C::STAGEB;   // 64 KB of stages
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
     static int configured = -1;
-    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND>, SMEM, configured);
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC>, SMEM, configured);
     if (e != cudaSuccess) return e;
     // programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel (typically this step's append) finishes; they wait for it
     // in griddep_wait() before reading any input
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.S, L.Hkv, L.B);
+    cfg.gridDim = dim3(L.S, L.Hkv / HPC, L.B);
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
@@ -866,25 +885,32 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND>, *L.tm_k, *L.tm_v, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC>, *L.tm_k, *L.tm_v, a);
+}
+
+// Kv heads per CTA: 2 when the count is even (the tensor maps' boxes then
+// span two heads' pages), else 1.
+template <int D, int BS, int KVT, bool APPEND>
+static cudaError_t launch_heads(const DecodeLaunch& L, cudaStream_t stream) {
+    return L.hpc == 2 ? launch_typed<D, BS, KVT, APPEND, 2>(L, stream) : launch_typed<D, BS, KVT, APPEND, 1>(L, stream);
 }
 
 template <bool APPEND>
 static cudaError_t launch_shape(const DecodeLaunch& L, cudaStream_t stream) {
     if (L.kvt == PA_KV_FP8_E4M3) {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_FP8, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_FP8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 16) return launch_heads<128, 16, KV_FP8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_heads<128, 32, KV_FP8, APPEND>(L, stream);
     } else if (L.kvt == PA_KV_INT8) {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_INT8, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_INT8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 16) return launch_heads<128, 16, KV_INT8, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_heads<128, 32, KV_INT8, APPEND>(L, stream);
     } else if (L.kvt == PA_KV_INT4) {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_INT4, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_INT4, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 16) return launch_heads<128, 16, KV_INT4, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_heads<128, 32, KV_INT4, APPEND>(L, stream);
     } else {
-        if (L.d == 128 && L.bs == 16) return launch_typed<128, 16, KV_BF16, APPEND>(L, stream);
-        if (L.d == 128 && L.bs == 32) return launch_typed<128, 32, KV_BF16, APPEND>(L, stream);
-        if (L.d == 64 && L.bs == 16) return launch_typed<64, 16, KV_BF16, APPEND>(L, stream);
-        if (L.d == 64 && L.bs == 32) return launch_typed<64, 32, KV_BF16, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 16) return launch_heads<128, 16, KV_BF16, APPEND>(L, stream);
+        if (L.d == 128 && L.bs == 32) return launch_heads<128, 32, KV_BF16, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 16) return launch_heads<64, 16, KV_BF16, APPEND>(L, stream);
+        if (L.d == 64 && L.bs == 32) return launch_heads<64, 32, KV_BF16, APPEND>(L, stream);
     }
     return cudaErrorInvalidValue;
 }

@@ -43,6 +43,7 @@ struct DecodeLaunch {
     float* v_scale_w;
     int B, Hq, Hkv, d, bs, M, num_blocks;
     int part_blocks;    // blocks per split partition
+    int hpc;            // kv heads per CTA (1 or 2); the tensor maps' boxes span hpc heads' pages
     int S;              // partitions per sequence at most (grid x)
     float scale;
     int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8 / PA_KV_INT4
