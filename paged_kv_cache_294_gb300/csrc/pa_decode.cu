@@ -667,6 +667,10 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     const int split = blockIdx.x, b = blockIdx.z;
     const int h0 = blockIdx.y * HPC;   // this CTA's kv heads: h0 .. h0 + HPC - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // a partition this sequence can never use (a table holds at most M blocks):
+    // leave before any set-up or load
+    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
+    if (split > 0 && split >= (a.M + pblk - 1) / pblk) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -690,7 +694,6 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
         len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
-    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
     const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0
     if (split > 0 && split >= nsplit) return;
     // the sequence's blocks split evenly over its partitions (at most P each)

@@ -241,3 +241,25 @@ def test_consecutive_calls_with_different_shapes():
         w = _synthetic(B, 16, 4, 128, 16, lens, seed=B)
         for S in (0, 1, 4):
             check(w, S)
+
+
+@pytest.mark.parametrize("kv", ["fp8", "int8", "int4"])
+def test_coded_blocks_with_zero_scales(kv):
+    """Blocks whose K or V values are all zero get scale 0 and codes 0.  The
+    kernel keeps O in units of the largest V scale seen so far: a sequence whose
+    first page has V scale 0 and whose later pages do not, one whose every V is
+    zero, and one whose K is zero (uniform weights) must all match the oracle."""
+    w = _synthetic(4, 8, 2, 128, 16, [40, 33, 70, 5], kv=kv, seed=31)
+    seq, pos = np.asarray(w.fill_seq), np.asarray(w.fill_pos)
+    vf, kf = w.v_fill.clone(), w.k_fill.clone()
+    vf[torch.from_numpy((seq == 0) & (pos < 16))] = 0      # sequence 0: first block's V only
+    vf[torch.from_numpy(seq == 1)] = 0                      # sequence 1: every V
+    kf[torch.from_numpy(seq == 2)] = 0                      # sequence 2: every K
+    w.v_fill, w.k_fill = vf, kf
+    w.v_new = w.v_new.clone()
+    w.k_new = w.k_new.clone()
+    w.v_new[1] = 0
+    w.k_new[2] = 0
+    for S in (0, 2):
+        layer, _ = check(w, S)
+    assert torch.all(layer.out[1].float() == 0)
