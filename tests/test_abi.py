@@ -94,8 +94,13 @@ def test_split_planning():
     ws = pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 64)
     assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4)
     assert pa.pa_decode_resolve_splits(4, 8, 8192, 4096) == 512      # at most 512 partitions
-    # automatic choice keeps partitions between 32 and 128 blocks
-    for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (4, 8, 8192), (128, 32, 256), (4, 2, 7)]:
+    # automatic choice: a CTA streams 32 .. 128 pages; it covers two kv heads
+    # when their count is even, so its partition is half as many blocks
+    for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (4, 8, 8192), (128, 32, 256), (4, 2, 7), (64, 3, 256),
+                      (300, 1, 512)]:
         S = pa.pa_decode_resolve_splits(B, Hkv, M, 0)
         P = -(-M // S)
-        assert 1 <= S <= M and (P >= min(32, M)) and P <= 128
+        hpc = 2 if Hkv % 2 == 0 else 1
+        assert 1 <= S <= M
+        assert P == M or P * hpc >= 32
+        assert P * hpc <= 128 + hpc - 1
