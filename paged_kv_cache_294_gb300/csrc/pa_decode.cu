@@ -9,27 +9,32 @@
 // head i / G.  Scores, softmax and P.V stay on chip ("LLM Inference
 // Optimization", section "FlashAttention") with an fp32 online softmax.
 //
-// One CTA per (partition of P blocks, kv head, sequence).  A CTA has 5 warps:
-//   * warp 4, the producer, issues TMA tile loads of each page's K and V
-//     (one (block, kv head) page = bs rows x head_dim) into a ring of shared
-//     memory stages written with the 128-byte swizzle; completion is counted
-//     in bytes on one mbarrier per stage;
-//   * warps 0-3 consume the pages round-robin.  Per page a warp forms
-//     S^T = Q K^T with m16n8k16 MMAs (the G query heads of the group are the
-//     M rows, the page's tokens the N columns, head_dim the K depth; q lives
-//     in registers), updates its fp32 online softmax in registers and
-//     accumulates O^T += V^T P^T with MMAs whose B operand is the probability
-//     tile taken straight from the score registers;
-//   * the consumer warps' states merge in shared memory; a one-partition
+// One CTA per (partition of P blocks, pair of kv heads, sequence); one kv
+// head per CTA when their count is odd.  The pages of one block for
+// consecutive kv heads are adjacent in the cache, so one copy fetches a block
+// for both heads.  A CTA has 5 warps:
+//   * warp 4, the producer, issues TMA tile loads of each block's K and V rows
+//     for the CTA's heads into a ring of shared-memory stages written with the
+//     128-byte swizzle; completion is counted in bytes on one mbarrier per
+//     stage;
+//   * warps 0-3 consume the pages, two warps per kv head taking alternate
+//     pages.  Per page a warp forms S^T = Q K^T with m16n8k16 MMAs (the G query
+//     heads of the group are the M rows, the page's tokens the N columns,
+//     head_dim the K depth; q lives in registers), updates its fp32 online
+//     softmax in registers and accumulates O^T += V^T P^T with MMAs whose B
+//     operand is the probability tile taken straight from the score registers;
+//   * each head's warp states merge in shared memory; a one-partition
 //     sequence writes bf16 out, otherwise the partition writes its normalised
-//     partial and base-2 log-sum-exp to the workspace and the group's last
+//     partials and base-2 log-sum-exps to the workspace and the group's last
 //     partition to finish merges them (an atomic counter per group; nothing
 //     waits on another CTA).
 // Coded caches (e4m3, int8, int4): codes convert exactly to f16 in registers
-// (q and the probabilities are f16 there), the K scale folds into the scores
-// and the V scale applies per page to a fresh P.V accumulator.  An int4 row
-// (64 bytes) is half of a 128-byte line: the TMA map views a page as bs / 2
-// lines of two tokens each.
+// (q and the probabilities are f16 there).  The K scale folds into the
+// scores; the V scale folds into the probabilities relative to the largest V
+// scale seen so far, so P.V accumulates straight into O.  The integer codes
+// enter the products with a constant offset that comes off per score (K) or
+// once per CTA (V).  An int4 row (64 bytes) is half of a 128-byte line: the
+// TMA map views a page as bs / 2 lines of two tokens each.
 #include <cuda_fp8.h>
 #include <math.h>
 
