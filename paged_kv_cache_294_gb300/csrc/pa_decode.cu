@@ -583,8 +583,8 @@ __device__ __forceinline__ NewRow prepare_new_row(const DecodeArgs& a, int b, in
 }
 
 template <int D, int BS, int KVT, int HPC>
-__device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
-                                              const NewRow& r, int lane) {
+__device__ __forceinline__ void patch_new_row_body(const DecodeArgs& a, int h, int phys, int off, uint32_t kt,
+                                                   uint32_t vt, const NewRow& r, int lane) {
     constexpr bool FP8 = KVT != KV_BF16;
     constexpr int CHS = Cfg<D, BS, KVT, HPC>::CHS;
     using QC = CodecOf<KVT>;
@@ -649,6 +649,25 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
     __syncwarp();
 }
 
+// The coded caches' patch (with the re-encode of older rows when the block
+// scale grows) runs out of line: it runs once per CTA, and inlined into the
+// page loop it cost that loop about 8% (register allocation and scheduling).
+// The bf16 patch is a few stores and stays inline.
+template <int D, int BS, int KVT, int HPC>
+__device__ __noinline__ void patch_new_row_call(const DecodeArgs& a, int h, int phys, int off, uint32_t kt,
+                                                uint32_t vt, const NewRow& r, int lane) {
+    patch_new_row_body<D, BS, KVT, HPC>(a, h, phys, off, kt, vt, r, lane);
+}
+
+template <int D, int BS, int KVT, int HPC>
+__device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int phys, int off, uint32_t kt, uint32_t vt,
+                                              const NewRow& r, int lane) {
+    if constexpr (KVT == KV_BF16)
+        patch_new_row_body<D, BS, KVT, HPC>(a, h, phys, off, kt, vt, r, lane);
+    else
+        patch_new_row_call<D, BS, KVT, HPC>(a, h, phys, off, kt, vt, r, lane);
+}
+
 template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC>
 __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -668,6 +687,14 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     uint8_t* sgen = smem_raw + (sbase - raw_u32);
     uint64_t* full = reinterpret_cast<uint64_t*>(sgen + BAR_OFF);
     uint64_t* empty = full + NSTAGE;
+    // Coded caches: the (K, V) scales per head of the pages of a 32-page batch,
+    // in two slots (batch n in slot n % 2), each published by the producer at
+    // the batch's start with one arrival on its barrier.  A slot is rewritten
+    // two batches later, when every page of its batch has been released (the
+    // ring holds at most 32 pages).
+    __shared__ float2 batch_sc[FP8 ? 2 : 1][32][HPC];
+    __shared__ uint64_t batch_bar[2];
+    static_assert(NSTAGE <= 32, "a batch slot is reused only after its pages are released");
 
     const int split = blockIdx.x, b = blockIdx.z;
     const int h0 = blockIdx.y * HPC;   // this CTA's kv heads: h0 .. h0 + HPC - 1
@@ -682,6 +709,8 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], HPC);   // released once per kv head
         }
+        mbar_init(&batch_bar[0], 1);
+        mbar_init(&batch_bar[1], 1);
         fence_mbar_init();
     }
     // Inputs may come from the preceding kernel in the stream (this step's
@@ -717,15 +746,43 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
             prefetch_tensormap(&tm_v);
         }
         bool alive = true;
-        for (int base = 0; base < npages; base += 32) {
-            int myphys = 0;
+        int issued = 0;   // lane 0: pages whose copies were issued
+        // batch n's block ids (and, coded caches, scales): loaded during batch
+        // n - 1, so that neither a copy nor the consumers wait for them
+        auto load_batch = [&](int base, int& phys, float (&ks)[HPC], float (&vs)[HPC]) {
+            phys = 0;
+#pragma unroll
+            for (int hh = 0; hh < HPC; ++hh) ks[hh] = vs[hh] = 1.f;
             if (base + lane < npages) {
-                myphys = base == 0 ? phys0 : trow[base + lane];
-                if (myphys < 0 || myphys >= a.num_blocks) {
+                phys = base == 0 ? phys0 : trow[base + lane];   // batch 0's came with the length
+                if (phys < 0 || phys >= a.num_blocks) {
                     raise_error(PA_DEVERR_BLOCK_ID);
-                    myphys = -1;  // loads read block 0; nothing is written through it
+                    phys = -1;  // loads read block 0; nothing is written through it
+                }
+                if (FP8) {
+                    const int64_t si = (int64_t)(phys < 0 ? 0 : phys) * a.Hkv + h0;
+#pragma unroll
+                    for (int hh = 0; hh < HPC; ++hh) {
+                        ks[hh] = a.k_scale[si + hh];
+                        vs[hh] = a.v_scale[si + hh];
+                    }
                 }
             }
+        };
+        int myphys;
+        float mks[HPC], mvs[HPC];
+        load_batch(0, myphys, mks, mvs);
+        for (int base = 0; base < npages; base += 32) {
+            const int nb = base / 32;
+            if (FP8) {   // this batch's scales for the consumers
+#pragma unroll
+                for (int hh = 0; hh < HPC; ++hh) batch_sc[nb & 1][lane][hh] = make_float2(mks[hh], mvs[hh]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&batch_bar[nb & 1]);
+            }
+            int nphys = 0;
+            float nks[HPC], nvs[HPC];
+            if (base + 32 < npages) load_batch(base + 32, nphys, nks, nvs);
             const int cnt = min(32, npages - base);
             for (int k = 0; k < cnt; ++k) {
                 const int phys_raw = __shfl_sync(0xffffffffu, myphys, k);
@@ -745,14 +802,21 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
 #pragma unroll
                         for (int ch = 0; ch < C::NCH; ++ch)
                             tma_load_2d(stg + HPC * C::PAGEB + ch * C::CHS, &tm_v, ch * (128 / C::ELT), y, &full[s]);
+                        issued = i + 1;
                     }
                 }
+            }
+            myphys = nphys;
+#pragma unroll
+            for (int hh = 0; hh < HPC; ++hh) {
+                mks[hh] = nks[hh];
+                mvs[hh] = nvs[hh];
             }
         }
         // every issued load lands before the shared memory is reused or released
         if (lane == 0) {
-            for (int s = 0; s < NSTAGE && s < npages; ++s) {
-                const int last = s + ((npages - 1 - s) / NSTAGE) * NSTAGE;
+            for (int s = 0; s < NSTAGE && s < issued; ++s) {
+                const int last = s + ((issued - 1 - s) / NSTAGE) * NSTAGE;
                 mbar_wait(&full[s], (last / NSTAGE) & 1);
             }
         }
@@ -775,11 +839,12 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
         for (int i = wi; i < npages; i += WPH) {
             const int s = i % NSTAGE;
             float ksc = 1.f, vsc = 1.f;
-            if (FP8) {
-                int phys = trow[i];
-                if (phys < 0 || phys >= a.num_blocks) phys = 0;
-                ksc = a.k_scale[(int64_t)phys * a.Hkv + h];
-                vsc = a.v_scale[(int64_t)phys * a.Hkv + h];
+            if (FP8) {   // the batch's scales, published at the batch's start
+                const int nb = i / 32;
+                if ((i & 31) == wi && !mbar_wait(&batch_bar[nb & 1], (nb >> 1) & 1)) break;   // warp's first page of it
+                const float2 sv = batch_sc[nb & 1][i & 31][hh];
+                ksc = sv.x;
+                vsc = sv.y;
             }
             if (!mbar_wait(&full[s], (i / NSTAGE) & 1)) break;
             // this head's rows of the stage: line hh * LINES of each column tile
