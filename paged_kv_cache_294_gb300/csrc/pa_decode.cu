@@ -878,15 +878,17 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     // the group: this CTA's kv heads of sequence b, counted per head set
     const int grp = b * (a.Hkv / HPC) + blockIdx.y;
     __shared__ int s_last;
-    __threadfence();
-    __syncthreads();
+    __syncthreads();   // every thread's partial stores precede the count
     if (threadIdx.x == 0) {
-        const int old = atomicAdd(&a.counters[grp], 1);
+        // one acquire-release count: it releases this CTA's partials (ordered
+        // before it by the barrier) and, for the group's last partition,
+        // acquires the others' (the barrier below passes that on)
+        int old;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(&a.counters[grp]) : "memory");
         s_last = (old == nsplit - 1);
     }
     __syncthreads();
     if (!s_last) return;
-    __threadfence();
     merge_group<D>(a, cm, (int64_t)b * a.Hq + h0 * a.G, HPC * a.G, nsplit, threadIdx.x, C::NTHREADS, warp,
                    C::NCW + 1, lane, sync_cta);
     if (threadIdx.x == 0) a.counters[grp] = 0;
