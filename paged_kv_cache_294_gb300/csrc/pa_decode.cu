@@ -351,16 +351,17 @@ struct WarpAcc {
                     const int unit = 2 * mp + (mi >> 1);
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4_t(swz128(vt, t, unit * 16), r0, r1, r2, r3);
-                    // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes
-                    const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
-                    const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
+                    // r = {v[2c][2n], v[2c][2n+1], v[2c+1][2n], v[2c+1][2n+1]} bytes;
+                    // the A operand wants the even bytes, then the odd ones
                     uint32_t A0[4], A1[4];
                     if (KVT == KV_INT8) {   // operands 1152 + c
-                        s8x4_to_f16x2_biased(x0, A0[0], A0[1]);
-                        s8x4_to_f16x2_biased(x1, A0[2], A0[3]);
-                        s8x4_to_f16x2_biased(x2, A1[0], A1[1]);
-                        s8x4_to_f16x2_biased(x3, A1[2], A1[3]);
+                        s8x4_eo_to_f16x2_biased(r0, A0[0], A0[1]);
+                        s8x4_eo_to_f16x2_biased(r1, A0[2], A0[3]);
+                        s8x4_eo_to_f16x2_biased(r2, A1[0], A1[1]);
+                        s8x4_eo_to_f16x2_biased(r3, A1[2], A1[3]);
                     } else {
+                        const uint32_t x0 = prmt(r0, 0x3120), x1 = prmt(r1, 0x3120);
+                        const uint32_t x2 = prmt(r2, 0x3120), x3 = prmt(r3, 0x3120);
                         code4_to_f16x2<KVT>(x0, A0[0], A0[1]);
                         code4_to_f16x2<KVT>(x1, A0[2], A0[3]);
                         code4_to_f16x2<KVT>(x2, A1[0], A1[1]);

@@ -80,6 +80,13 @@ __device__ __forceinline__ void s8x4_to_f16x2_biased(uint32_t w, uint32_t& lo, u
     asm("prmt.b32 %0, %1, %2, 0x4140;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
     asm("prmt.b32 %0, %1, %2, 0x4342;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
 }
+// The same values with the even bytes (0, 2) in lo and the odd bytes (1, 3)
+// in hi: a byte reorder and the conversion in the same two permutes.
+__device__ __forceinline__ void s8x4_eo_to_f16x2_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    asm("prmt.b32 %0, %1, %2, 0x4240;" : "=r"(lo) : "r"(u), "r"(0x64646464u));
+    asm("prmt.b32 %0, %1, %2, 0x4341;" : "=r"(hi) : "r"(u), "r"(0x64646464u));
+}
 constexpr float kS8Bias = 1152.f;
 
 // int4 code (low nibble, two's complement) -> fp32, exact.
