@@ -235,8 +235,12 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
         return PA_ERR_INVALID;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID;
     if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
-    if (batch > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;  // grid z / y
     if ((int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31) return PA_ERR_INVALID;
+    {   // one CTA per work item: at most S x (kv-head sets) x batch of them
+        const int64_t items = (int64_t)pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits) *
+                              (num_kv_heads % 2 == 0 ? num_kv_heads / 2 : num_kv_heads) * batch;
+        if (items > INT32_MAX) return PA_ERR_UNSUPPORTED;
+    }
     const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
     if (ks != PA_OK) return ks;
     if (!(scale == scale)) return PA_ERR_INVALID;  // NaN

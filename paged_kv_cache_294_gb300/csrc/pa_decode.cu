@@ -542,8 +542,84 @@ __device__ __forceinline__ void sync_cta() { __syncthreads(); }
 
 __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 : (len > cap ? cap : len); }
 
+// Work items.  Sequence b of nblk blocks has max(1, ceil(nblk / pblk))
+// partitions for each of the NH = Hkv / HPC kv-head sets (pblk = part_early
+// for b < b_early, else part_blocks).  The grid lists only these items:
+// first partition 0 of every (sequence, head set), CTA r = b * NH + head set,
+// mapped without any lookup; then the later partitions, sequence by sequence,
+// then by head set, then by partition, which a CTA finds with one warp scan
+// over the lengths.  CTAs past the last item have nothing to do, so no CTA
+// slot goes to a partition past its sequence's end.
+struct WorkItem {
+    int b, hs, split, raw_len;   // b < 0: no item
+};
+
+template <int BS>
+__device__ __forceinline__ int partitions_of(const DecodeArgs& a, int b, int raw_len) {
+    const int nblk = (clamp_len(raw_len, a.M * BS) + BS - 1) / BS;
+    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
+    return max(1, (nblk + pblk - 1) / pblk);
+}
+
+// Later partition r (counted from the first item after the B * NH partitions
+// 0).  Called by one full warp.  Lane L covers sequences c0 + 8L .. c0 + 8L + 7
+// of each 256-sequence chunk; all of a chunk's lengths are loaded before the
+// scan.
+template <int BS, int HPC>
+__device__ __forceinline__ WorkItem find_later_item(const DecodeArgs& a, int r, int lane) {
+    const int NH = a.Hkv / HPC;
+    WorkItem it{-1, 0, 0, 0};
+    int base = 0;   // items of the chunks before this one
+    for (int c0 = 0; c0 < a.B; c0 += 256) {
+        int raw[8], ns[8], mine = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int bb = c0 + 8 * lane + k;
+            raw[k] = bb < a.B ? a.lens[bb] : 0;
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int bb = c0 + 8 * lane + k;
+            ns[k] = bb < a.B ? partitions_of<BS>(a, bb, raw[k]) - 1 : 0;   // partitions after the first
+            mine += ns[k] * NH;
+        }
+        int inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        const int total = __shfl_sync(0xffffffffu, inc, 31);
+        if (r < base + total) {
+            const int src = __ffs(__ballot_sync(0xffffffffu, r < base + inc)) - 1;
+            if (lane == src) {
+                int off = r - (base + inc - mine);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int cnt = ns[k] * NH;
+                    if (it.b < 0 && off < cnt) {
+                        const int n = max(ns[k], 1);
+                        it.b = c0 + 8 * lane + k;
+                        it.hs = off / n;
+                        it.split = 1 + off - it.hs * n;
+                        it.raw_len = raw[k];
+                    }
+                    off -= cnt;
+                }
+            }
+            it.b = __shfl_sync(0xffffffffu, it.b, src);
+            it.hs = __shfl_sync(0xffffffffu, it.hs, src);
+            it.split = __shfl_sync(0xffffffffu, it.split, src);
+            it.raw_len = __shfl_sync(0xffffffffu, it.raw_len, src);
+            return it;
+        }
+        base += total;
+    }
+    return it;
+}
+
 // ========================================================================
-// grid (partitions, kv heads, sequences)
+// grid: the work items (see find_item), one CTA each
 // ========================================================================
 // Fused step.  The warp that consumes the page holding sequence b's position
 // len-1 prepares this head's new row when the CTA starts (fp8: the block's new
@@ -697,13 +773,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     __shared__ uint64_t batch_bar[2];
     static_assert(NSTAGE <= 32, "a batch slot is reused only after its pages are released");
 
-    const int split = blockIdx.x, b = blockIdx.z;
-    const int h0 = blockIdx.y * HPC;   // this CTA's kv heads: h0 .. h0 + HPC - 1
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // a partition this sequence can never use (a table holds at most M blocks):
-    // leave before any set-up or load
-    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
-    if (split > 0 && split >= (a.M + pblk - 1) / pblk) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -718,26 +788,42 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     // append): wait for it before the first global read.
     griddep_wait();
 
-    // partition 0 starts at block 0: its producer fetches the first table
-    // entries alongside the length (entries past the sequence are not used)
+    __shared__ WorkItem s_item;
+    const int nfirst = a.B * (a.Hkv / HPC);
+    const bool first = (int)blockIdx.x < nfirst;   // partition 0 of (b, head set)
     int phys0 = 0;
-    if (split == 0 && warp == C::NCW && lane < a.M) phys0 = a.tables[(int64_t)b * a.M + lane];
-    int len = a.lens[b];
+    if (warp == C::NCW) {
+        if (first) {
+            const int b0 = blockIdx.x / (a.Hkv / HPC);
+            // partition 0 starts at block 0: the first table entries come
+            // alongside the length (entries past the sequence are not used)
+            if (lane < a.M) phys0 = a.tables[(int64_t)b0 * a.M + lane];
+            if (lane == 0) s_item = WorkItem{b0, (int)blockIdx.x - b0 * (a.Hkv / HPC), 0, a.lens[b0]};
+        } else {
+            const WorkItem it = find_later_item<BS, HPC>(a, blockIdx.x - nfirst, lane);
+            if (lane == 0) s_item = it;
+        }
+    }
+    __syncthreads();   // also publishes the barrier initialisation
+    const WorkItem it = s_item;
+    if (it.b < 0) return;   // past the last item
+    const int b = it.b, split = it.split;
+    const int h0 = it.hs * HPC;   // this CTA's kv heads: h0 .. h0 + HPC - 1
+    int len = it.raw_len;
     const int cap = a.M * BS;
     if (len < 0 || len > cap) {
         if (threadIdx.x == 0 && split == 0 && h0 == 0) raise_error(PA_DEVERR_SEQ_LEN);
         len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
-    const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0
-    if (split > 0 && split >= nsplit) return;
+    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
+    const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0 (one item, no pages)
     // the sequence's blocks split evenly over its partitions (at most P each)
     const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
     const int j0 = split * pb;
     const int npages = max(0, min(nblk, j0 + pb) - j0);
     const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
-    if (split > 0 && warp == C::NCW && lane < npages) phys0 = trow[lane];
-    __syncthreads();
+    if (!first && warp == C::NCW && lane < npages) phys0 = trow[lane];
 
     WarpAcc<D, BS, KVT, HPC> st;
     st.reset();
@@ -755,7 +841,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
 #pragma unroll
             for (int hh = 0; hh < HPC; ++hh) ks[hh] = vs[hh] = 1.f;
             if (base + lane < npages) {
-                phys = base == 0 ? phys0 : trow[base + lane];   // batch 0's came with the length
+                phys = base == 0 ? phys0 : trow[base + lane];   // batch 0's were loaded at the start
                 if (phys < 0 || phys >= a.num_blocks) {
                     raise_error(PA_DEVERR_BLOCK_ID);
                     phys = -1;  // loads read block 0; nothing is written through it
@@ -868,16 +954,22 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     }
 
     __syncthreads();  // pipeline drained: the stage memory becomes the combine area
+    // the item again, from shared memory: none of it stays in registers
+    // across the page loop
+    const WorkItem ie = s_item;
+    const int eb = ie.b, eh0 = ie.hs * HPC, esplit = ie.split;
+    const int ensplit = (((clamp_len(ie.raw_len, cap) + BS - 1) / BS) + (eb < a.b_early ? a.part_early : a.part_blocks) - 1) /
+                        (eb < a.b_early ? a.part_early : a.part_blocks);
     float* cm = reinterpret_cast<float*>(sgen);
     float* cl = cm + C::NCW * 8;
     float* co = cl + C::NCW * 8;
     if (warp < C::NCW) st.publish(cm, cl, co, warp, lane);
     __syncthreads();
-    combine_store<D, WPH, HPC>(a, cm, cl, co, b, h0, split, nsplit, threadIdx.x, C::NTHREADS);
-    if (nsplit <= 1) return;
+    combine_store<D, WPH, HPC>(a, cm, cl, co, eb, eh0, esplit, ensplit, threadIdx.x, C::NTHREADS);
+    if (ensplit <= 1) return;
 
     // the group: this CTA's kv heads of sequence b, counted per head set
-    const int grp = b * (a.Hkv / HPC) + blockIdx.y;
+    const int grp = eb * (a.Hkv / HPC) + ie.hs;
     __shared__ int s_last;
     __syncthreads();   // every thread's partial stores precede the count
     if (threadIdx.x == 0) {
@@ -886,11 +978,11 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
         // acquires the others' (the barrier below passes that on)
         int old;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(old) : "l"(&a.counters[grp]) : "memory");
-        s_last = (old == nsplit - 1);
+        s_last = (old == ensplit - 1);
     }
     __syncthreads();
     if (!s_last) return;
-    merge_group<D>(a, cm, (int64_t)b * a.Hq + h0 * a.G, HPC * a.G, nsplit, threadIdx.x, C::NTHREADS, warp,
+    merge_group<D>(a, cm, (int64_t)eb * a.Hq + eh0 * a.G, HPC * a.G, ensplit, threadIdx.x, C::NTHREADS, warp,
                    C::NCW + 1, lane, sync_cta);
     if (threadIdx.x == 0) a.counters[grp] = 0;
 }
@@ -952,7 +1044,8 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     // previous kernel (typically this step's append) finishes; they wait for it
     // in griddep_wait() before reading any input
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.S, L.Hkv / HPC, L.B);
+    // an upper bound on the work items: every sequence at most S partitions
+    cfg.gridDim = dim3((unsigned)L.S * (unsigned)(L.Hkv / HPC) * (unsigned)L.B);
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
