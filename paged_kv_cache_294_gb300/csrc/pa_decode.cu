@@ -544,12 +544,15 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 
 // Work items.  Sequence b of nblk blocks has max(1, ceil(nblk / pblk))
 // partitions for each of the NH = Hkv / HPC kv-head sets (pblk = part_early
-// for b < b_early, else part_blocks).  The grid lists only these items:
-// first partition 0 of every (sequence, head set), CTA r = b * NH + head set,
-// mapped without any lookup; then the later partitions, sequence by sequence,
-// then by head set, then by partition, which a CTA finds with one warp scan
-// over the lengths.  CTAs past the last item have nothing to do, so no CTA
-// slot goes to a partition past its sequence's end.
+// for b < b_early, else part_blocks).  For batches of up to 256 sequences the
+// grid lists only these items: first partition 0 of every (sequence, head
+// set), CTA r = b * NH + head set, mapped without any lookup; then the later
+// partitions, sequence by sequence, then by head set, then by partition,
+// which a CTA finds with one warp scan over the lengths.  CTAs past the last
+// item have nothing to do, so no CTA slot goes to a partition past its
+// sequence's end.  Larger batches take every (sequence, head set, partition
+// < S) in that order, with no scan; a partition past its sequence's end
+// leaves once it has read the length.
 struct WorkItem {
     int b, hs, split, raw_len;   // b < 0: no item
 };
@@ -561,16 +564,17 @@ __device__ __forceinline__ int partitions_of(const DecodeArgs& a, int b, int raw
     return max(1, (nblk + pblk - 1) / pblk);
 }
 
+constexpr int kScanMaxBatch = 256;
+
 // Later partition r (counted from the first item after the B * NH partitions
-// 0).  Called by one full warp.  Lane L covers sequences c0 + 8L .. c0 + 8L + 7
-// of each 256-sequence chunk; all of a chunk's lengths are loaded before the
-// scan.
+// 0), B <= kScanMaxBatch.  Called by one full warp.  Lane L covers sequences
+// 8L .. 8L + 7; all lengths are loaded before the scan.
 template <int BS, int HPC>
 __device__ __forceinline__ WorkItem find_later_item(const DecodeArgs& a, int r, int lane) {
     const int NH = a.Hkv / HPC;
     WorkItem it{-1, 0, 0, 0};
-    int base = 0;   // items of the chunks before this one
-    for (int c0 = 0; c0 < a.B; c0 += 256) {
+    {
+        constexpr int c0 = 0, base = 0;
         int raw[8], ns[8], mine = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -611,9 +615,7 @@ __device__ __forceinline__ WorkItem find_later_item(const DecodeArgs& a, int r, 
             it.hs = __shfl_sync(0xffffffffu, it.hs, src);
             it.split = __shfl_sync(0xffffffffu, it.split, src);
             it.raw_len = __shfl_sync(0xffffffffu, it.raw_len, src);
-            return it;
         }
-        base += total;
     }
     return it;
 }
@@ -774,6 +776,14 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     static_assert(NSTAGE <= 32, "a batch slot is reused only after its pages are released");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool scan = a.B <= kScanMaxBatch;
+    if (!scan) {
+        // a partition this sequence can never use (a table holds at most M
+        // blocks): leave before any set-up or load
+        const int b0 = blockIdx.x / a.S / (a.Hkv / HPC), split0 = blockIdx.x % a.S;
+        const int pblk0 = b0 < a.b_early ? a.part_early : a.part_blocks;
+        if (split0 > 0 && split0 >= (a.M + pblk0 - 1) / pblk0) return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NSTAGE; ++s) {
@@ -789,18 +799,23 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     griddep_wait();
 
     __shared__ WorkItem s_item;
-    const int nfirst = a.B * (a.Hkv / HPC);
-    const bool first = (int)blockIdx.x < nfirst;   // partition 0 of (b, head set)
+    const int NH = a.Hkv / HPC;
+    // partition 0 of (b, head set): mapped directly, the table read with the length
+    const bool first = scan ? (int)blockIdx.x < a.B * NH : (int)blockIdx.x % a.S == 0;
     int phys0 = 0;
     if (warp == C::NCW) {
-        if (first) {
-            const int b0 = blockIdx.x / (a.Hkv / HPC);
+        if (!scan) {
+            const int q = blockIdx.x / a.S, b0 = q / NH;
+            if (first && lane < a.M) phys0 = a.tables[(int64_t)b0 * a.M + lane];
+            if (lane == 0) s_item = WorkItem{b0, q - b0 * NH, (int)blockIdx.x - q * a.S, a.lens[b0]};
+        } else if (first) {
+            const int b0 = blockIdx.x / NH;
             // partition 0 starts at block 0: the first table entries come
             // alongside the length (entries past the sequence are not used)
             if (lane < a.M) phys0 = a.tables[(int64_t)b0 * a.M + lane];
-            if (lane == 0) s_item = WorkItem{b0, (int)blockIdx.x - b0 * (a.Hkv / HPC), 0, a.lens[b0]};
+            if (lane == 0) s_item = WorkItem{b0, (int)blockIdx.x - b0 * NH, 0, a.lens[b0]};
         } else {
-            const WorkItem it = find_later_item<BS, HPC>(a, blockIdx.x - nfirst, lane);
+            const WorkItem it = find_later_item<BS, HPC>(a, blockIdx.x - a.B * NH, lane);
             if (lane == 0) s_item = it;
         }
     }
@@ -818,6 +833,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     const int nblk = (len + BS - 1) / BS;
     const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
     const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0 (one item, no pages)
+    if (split > 0 && split >= nsplit) return;     // (larger batches) past the sequence's end
     // the sequence's blocks split evenly over its partitions (at most P each)
     const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
     const int j0 = split * pb;
