@@ -63,6 +63,7 @@ struct DecodeArgs {
     float* v_scale_w;
     int B, Hq, Hkv, G, M, num_blocks, part_blocks, S;
     int b_early, part_early;   // sequences b < b_early: partitions of part_early blocks
+    int scan;                  // 1: the grid lists work items only (see find_later_item)
     float scale_log2;
 };
 
@@ -544,13 +545,15 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 
 // Work items.  Sequence b of nblk blocks has max(1, ceil(nblk / pblk))
 // partitions for each of the NH = Hkv / HPC kv-head sets (pblk = part_early
-// for b < b_early, else part_blocks).  For batches of up to 256 sequences the
-// grid lists only these items: first partition 0 of every (sequence, head
+// for b < b_early, else part_blocks).  For batches of up to 256 sequences and
+// at most 32 partitions (where partitions past a sequence's end are a large
+// share of S * NH * B and each would hold a CTA slot for a while) the grid
+// lists only these items: first partition 0 of every (sequence, head
 // set), CTA r = b * NH + head set, mapped without any lookup; then the later
 // partitions, sequence by sequence, then by head set, then by partition,
 // which a CTA finds with one warp scan over the lengths.  CTAs past the last
 // item have nothing to do, so no CTA slot goes to a partition past its
-// sequence's end.  Larger batches take every (sequence, head set, partition
+// sequence's end.  Other launches take every (sequence, head set, partition
 // < S) in that order, with no scan; a partition past its sequence's end
 // leaves once it has read the length.
 struct WorkItem {
@@ -776,7 +779,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     static_assert(NSTAGE <= 32, "a batch slot is reused only after its pages are released");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool scan = a.B <= kScanMaxBatch;
+    const bool scan = a.scan != 0;
     if (!scan) {
         // a partition this sequence can never use (a table holds at most M
         // blocks): leave before any set-up or load
@@ -1050,6 +1053,7 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.b_early = L.part_blocks * HPC < 128 ? L.B / 2 : 0;
     a.part_early = std::min(std::min(2 * L.part_blocks, 128 / HPC), L.M);
     a.S = L.S;
+    a.scan = L.B <= kScanMaxBatch && L.S <= 32;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     constexpr int NST = 65536 / C::STAGEB;   // 64 KB of stages
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
