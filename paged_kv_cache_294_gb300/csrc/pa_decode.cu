@@ -575,51 +575,46 @@ constexpr int kScanMaxBatch = 256;
 template <int BS, int HPC>
 __device__ __forceinline__ WorkItem find_later_item(const DecodeArgs& a, int r, int lane) {
     const int NH = a.Hkv / HPC;
+    int raw[8], ns[8], mine = 0;   // ns: partitions after the first
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int bb = 8 * lane + k;
+        raw[k] = bb < a.B ? a.lens[bb] : 0;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int bb = 8 * lane + k;
+        ns[k] = bb < a.B ? partitions_of<BS>(a, bb, raw[k]) - 1 : 0;
+        mine += ns[k] * NH;
+    }
+    int inc = mine;   // inclusive scan of the lanes' item counts
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += t;
+    }
     WorkItem it{-1, 0, 0, 0};
-    {
-        constexpr int c0 = 0, base = 0;
-        int raw[8], ns[8], mine = 0;
+    if (r >= __shfl_sync(0xffffffffu, inc, 31)) return it;   // past the last item
+    const int src = __ffs(__ballot_sync(0xffffffffu, r < inc)) - 1;
+    if (lane == src) {
+        int off = r - (inc - mine);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const int bb = c0 + 8 * lane + k;
-            raw[k] = bb < a.B ? a.lens[bb] : 0;
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int bb = c0 + 8 * lane + k;
-            ns[k] = bb < a.B ? partitions_of<BS>(a, bb, raw[k]) - 1 : 0;   // partitions after the first
-            mine += ns[k] * NH;
-        }
-        int inc = mine;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += t;
-        }
-        const int total = __shfl_sync(0xffffffffu, inc, 31);
-        if (r < base + total) {
-            const int src = __ffs(__ballot_sync(0xffffffffu, r < base + inc)) - 1;
-            if (lane == src) {
-                int off = r - (base + inc - mine);
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int cnt = ns[k] * NH;
-                    if (it.b < 0 && off < cnt) {
-                        const int n = max(ns[k], 1);
-                        it.b = c0 + 8 * lane + k;
-                        it.hs = off / n;
-                        it.split = 1 + off - it.hs * n;
-                        it.raw_len = raw[k];
-                    }
-                    off -= cnt;
-                }
+            const int cnt = ns[k] * NH;
+            if (it.b < 0 && off < cnt) {
+                const int n = max(ns[k], 1);
+                it.b = 8 * lane + k;
+                it.hs = off / n;
+                it.split = 1 + off - it.hs * n;
+                it.raw_len = raw[k];
             }
-            it.b = __shfl_sync(0xffffffffu, it.b, src);
-            it.hs = __shfl_sync(0xffffffffu, it.hs, src);
-            it.split = __shfl_sync(0xffffffffu, it.split, src);
-            it.raw_len = __shfl_sync(0xffffffffu, it.raw_len, src);
+            off -= cnt;
         }
     }
+    it.b = __shfl_sync(0xffffffffu, it.b, src);
+    it.hs = __shfl_sync(0xffffffffu, it.hs, src);
+    it.split = __shfl_sync(0xffffffffu, it.split, src);
+    it.raw_len = __shfl_sync(0xffffffffu, it.raw_len, src);
     return it;
 }
 

@@ -235,6 +235,20 @@ def test_large_ragged_batch(S):
     check(w, S)
 
 
+@pytest.mark.parametrize("B", [255, 256, 257])
+@pytest.mark.parametrize("Hq,Hkv", [(8, 2), (6, 3)])
+@pytest.mark.parametrize("S", [0, 3])
+def test_work_item_grid_edges(B, Hq, Hkv, S):
+    """Batches at the edge of the one-warp work-item scan (every lane's eight
+    sequences in use; one sequence more than it covers, which takes the direct
+    grid), with empty, one-block and multi-partition lengths mixed, one or two
+    kv heads per CTA; every output compared."""
+    rng = np.random.default_rng(B * 7 + Hkv + S)
+    lens = [int(x) for x in rng.choice([0, 1, 16, 17, 200, 700], size=B)]
+    w = _synthetic(B, Hq, Hkv, 64, 16, lens, seed=B + Hkv)
+    check(w, S)
+
+
 def test_consecutive_calls_with_different_shapes():
     """Consecutive calls with different batch shapes on one workspace stay correct."""
     for B, lens in ((7, [5, 300, 17, 1, 0, 64, 900]), (3, [2000, 3, 40])):
