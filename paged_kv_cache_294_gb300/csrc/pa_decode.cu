@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     const int nblk = (len + BS - 1) / BS;
     const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
     const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0 (one item, no pages)
-    if (split > 0 && split >= nsplit) return;     // (larger batches) past the sequence's end
+    if (split > 0 && split >= nsplit) return;     // (direct grid) past the sequence's end
     // the sequence's blocks split evenly over its partitions (at most P each)
     const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
     const int j0 = split * pb;
