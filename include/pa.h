@@ -173,7 +173,10 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
  *
  * num_blocks * num_kv_heads * block_size must be below 2^31; head_dim in
  * {64, 128} (coded caches: 128); block_size in {16, 32}; num_q_heads a multiple of
- * num_kv_heads with a group size of at most 8.  batch == 0 is a no-op.
+ * num_kv_heads with a group size of at most 8.  batch == 0 is a no-op.  The
+ * launch has one CTA per (sequence, kv-head set, partition), a kv-head set
+ * being two heads when num_kv_heads is even, else one: S * sets * batch must
+ * stay below 2^31 (PA_ERR_UNSUPPORTED otherwise).
  * ------------------------------------------------------------------------- */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, const void* v_cache,
                               const float* k_scale, const float* v_scale,
