@@ -77,6 +77,11 @@ def test_argument_errors_return_status_without_a_gpu():
     # pool too large for 32-bit TMA rows
     assert lib.pa_kv_append(None, None, None, None, None, None, None, 1, 1 << 27, 8, 128, 16, 0,
                             None) == pa.PA_ERR_INVALID
+    # more than 2^31 - 1 work items (S x kv-head sets x batch): rejected before any pointer is read
+    S = pa.pa_decode_resolve_splits(1 << 26, 8, 64, 8)
+    assert S == 8 and S * 4 * (1 << 26) > 2 ** 31 - 1
+    assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1 << 26, 32, 8, 128, 16,
+                                   64, 64, 1.0, 8, None, 0, 0, None) == pa.PA_ERR_UNSUPPORTED
     # empty work is a no-op
     assert lib.pa_kv_append(None, None, None, None, None, None, None, 0, 64, 2, 64, 16, 0, None) == pa.PA_OK
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 0, 8, 4, 128, 16,
