@@ -47,11 +47,16 @@ class OracleStep:
     seqs: evaluate only these batch rows (their blocks are written from every
     history token that lands in them, so each block's contents, and for fp8
     its scale, are exactly those of the full workload).
+    tables: block tables another implementation used for this workload.  The
+    oracle always builds its own (its allocator replaying the workload's
+    trace) and only checks that they are the same.
     """
 
     def __init__(self, w, seqs: Optional[Sequence[int]] = None, tables: Optional[np.ndarray] = None):
         self.w = w
-        self.tables = tables_of(w) if tables is None else tables
+        self.tables = tables_of(w)
+        if tables is not None and not np.array_equal(np.asarray(tables), self.tables):
+            raise AssertionError("the given block tables differ from the oracle's own for this workload")
         self.seqs = np.arange(w.B) if seqs is None else np.asarray(sorted(set(int(s) for s in seqs)))
         lens = np.asarray(w.seq_lens, dtype=np.int32)
         used = set()

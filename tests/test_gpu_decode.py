@@ -1,9 +1,9 @@
 """pa_decode_attention through the C ABI against the fp64 oracle.
 
-Tolerance: max |err| <= 1e-2 for the bf16 cache, <= 5e-2 for the fp8 cache
-(against the oracle evaluated on the stored fp8 cache); where the bf16
-output grid is coarser than that bound (|ref| >= 2, resp. >= 8) one bf16 ulp
-of the reference.  Small cases compare
+Tolerance per output: max(atol, half a bf16 spacing of the reference +
+2^-10), atol = 1e-2 for the bf16 cache and 5e-2 for the fp8 cache (against
+the oracle evaluated on the stored fp8 cache); the half spacing only exceeds
+atol where |ref| >= 4 (resp. >= 16), since the outputs are bf16.  Small cases compare
 every output; full-size cases (the benchmark's shapes and launch
 configuration) compare sampled sequences, each computed by the oracle from
 the same seeded inputs.
@@ -170,20 +170,22 @@ def test_integer_codes_past_the_end_do_not_leak(kv, fill, bs):
     past a sequence's end: the largest codes there must still weigh nothing."""
     w = _synthetic(2, 8, 2, 128, bs, [7, 3 * bs + 5], kv=kv, seed=17 + bs)
     layer = PagedDecodeLayer.from_workload(w, "cuda")
+    st = oracle.run.OracleStep(w, tables=layer.tables_host)
+    st.append()
     for b, L in enumerate(w.seq_lens):
         blk = int(layer.tables_host[b, (L - 1) // bs])
+        # the same codes past the end in both caches (the step's append never
+        # touches rows past its own)
         layer.k_cache[blk, :, L % bs:, :] = fill
         layer.v_cache[blk, :, L % bs:, :] = fill
+        st.cache.k[blk, :, L % bs:, :] = fill
+        st.cache.v[blk, :, L % bs:, :] = fill
+    layer.append_step()
+    ref = st.decode()
     for S in (0, 2):
         layer.decode(num_splits=S)
         torch.cuda.synchronize()
         got = layer.out.float().cpu().numpy()
-        st = oracle.run.OracleStep(w, tables=layer.tables_host)
-        st.cache.k[...] = layer.k_cache.cpu().numpy().view(np.uint8)
-        st.cache.v[...] = layer.v_cache.cpu().numpy().view(np.uint8)
-        st.cache.k_scale[...] = layer.k_scale.cpu().numpy()
-        st.cache.v_scale[...] = layer.v_scale.cpu().numpy()
-        ref = oracle.decode_attention(st.cache, w.q, layer.tables_host, w.seq_lens, w.Hq, w.scale)
         assert excess(got, ref, tol(w)) <= 1.0
 
 

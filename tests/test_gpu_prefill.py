@@ -26,7 +26,7 @@ def _gpu(w, max_q=None, tables=None, layer=None):
 
 def _oracle(w, tables):
     st = oracle.run.OracleStep(w, tables=tables)
-    return oracle.prefill_attention(st.cache, w.q_chunk, tables, w.seq_lens, w.q_start, w.Hq, w.scale,
+    return oracle.prefill_attention(st.cache, w.q_chunk, st.tables, w.seq_lens, w.q_start, w.Hq, w.scale,
                                     threads=8)
 
 
@@ -65,7 +65,7 @@ def test_long_chunk_sampled_rows():
         if b not in caches:
             caches[b] = oracle.run.OracleStep(w, seqs=[b], tables=layer.tables_host)
         st = caches[b]
-        ref = oracle.prefill_attention(st.cache, w.q_chunk[r:r + 1], layer.tables_host[b:b + 1],
+        ref = oracle.prefill_attention(st.cache, w.q_chunk[r:r + 1], st.tables[b:b + 1],
                                        np.array([pos + 1]), np.array([0, 1]), w.Hq, w.scale)
         assert excess(got[r:r + 1], ref, BF16_TOL) <= 1.0, "row %d" % r
 
@@ -87,7 +87,7 @@ def test_stale_nan_rows_and_blocks_are_never_read_into_outputs():
             layer.v_cache[blk] = nan
     _, got = _gpu(w, layer=layer)
     st = oracle.run.OracleStep(w, tables=layer.tables_host)
-    ref = oracle.prefill_attention(st.cache, w.q_chunk, layer.tables_host, w.seq_lens, w.q_start, w.Hq, w.scale)
+    ref = oracle.prefill_attention(st.cache, w.q_chunk, st.tables, w.seq_lens, w.q_start, w.Hq, w.scale)
     assert np.isfinite(got).all()
     assert excess(got, ref, BF16_TOL) <= 1.0
 
@@ -151,7 +151,7 @@ def _sampled_rows_match(w, layer, got, rows):
         pos = int(w.seq_lens[b]) - C + (r - int(w.q_start[b]))
         if b not in caches:
             caches[b] = oracle.run.OracleStep(w, seqs=[b], tables=layer.tables_host)
-        ref = oracle.prefill_attention(caches[b].cache, w.q_chunk[r:r + 1], layer.tables_host[b:b + 1],
+        ref = oracle.prefill_attention(caches[b].cache, w.q_chunk[r:r + 1], caches[b].tables[b:b + 1],
                                        np.array([pos + 1]), np.array([0, 1]), w.Hq, w.scale)
         assert excess(got[r:r + 1], ref, BF16_TOL) <= 1.0, "row %d" % r
 
