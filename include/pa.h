@@ -226,9 +226,13 @@ pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void
  *   - Requests whose workspace (pa_decode_workspace_bytes) exceeds
  *     PA_STATIC_WORKSPACE_BYTES return PA_ERR_INVALID and launch nothing;
  *     use pa_decode_attention with a caller workspace for those.
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, which may load the library's device code); make
- *     that first call on each device before any stream capture.
+ *   - Arguments are checked exactly as pa_decode_attention checks them, and
+ *     a refused call queues no work at all.
+ *   - The first call in a device's context looks up the array's device
+ *     address (cudaGetSymbolAddress, which may load the library's device
+ *     code) and keeps it for that context; after cudaDeviceReset the next
+ *     call looks it up again.  Make the first call on each device (and the
+ *     first after a reset) before any stream capture.
  *   - Every call uses the same array: each call zeroes its counter words with
  *     cudaMemsetAsync on `stream` before the kernel, and calls whose work
  *     overlaps on the GPU (other streams, other threads) race on the array
@@ -368,6 +372,33 @@ pa_status pa_prefix_evict(pa_prefix_cache* c, int want, int* freed);
  * pa_copy_blocks.  PA_ERR_OOM if no block is free (nothing changed). */
 pa_status pa_block_cow(pa_allocator* a, int32_t block, int32_t* out_block, int* needs_copy);
 
+/* Admit a sequence of n_tokens tokens ([P1] "2. PagedAttention" and "4.
+ * Prefix caching"): blocks[0 .. *n_blocks) receives
+ * pa_blocks_for_tokens(n_tokens, bs) physical blocks, first the longest
+ * cached prefix of `tokens` (pa_prefix_match; c may be NULL: no reuse), then
+ * fresh blocks (lowest free ids).  When the pool is short, blocks only the
+ * cache still references are evicted first (pa_prefix_evict).  The caller
+ * holds one reference on each listed block.  *first_new_pos = the first
+ * position whose KV the caller must still write (matched blocks x bs).
+ * All or nothing: PA_ERR_OOM leaves the allocator and cache references as
+ * they were (*n_blocks = 0).  PA_ERR_INVALID if the blocks needed exceed
+ * max_blocks, c belongs to another allocator, or a pointer is NULL. */
+pa_status pa_seq_admit(pa_allocator* a, pa_prefix_cache* c, const int32_t* tokens, int64_t n_tokens,
+                       int32_t* blocks, int max_blocks, int* n_blocks, int64_t* first_new_pos);
+
+/* Reserve the slot of token position `pos` in a sequence holding
+ * blocks[0 .. *n_blocks) (capacity max_blocks).  If pos opens a new block
+ * (pos / bs == *n_blocks) a fresh block is appended (*n_blocks grows by one);
+ * otherwise the block holding pos goes through pa_block_cow, and when it was
+ * shared, blocks[] names the private copy and *copy_src / *copy_dst the page
+ * copy the caller must run (pa_copy_blocks) before writing the slot (both -1
+ * when no copy is needed).  *slot = block * bs + pos % bs.  A pool that is
+ * short first gives up blocks only the cache references (c may be NULL).
+ * PA_ERR_OOM if no block can be had (nothing changed); PA_ERR_INVALID if
+ * pos < 0, pos / bs > *n_blocks or pos / bs >= max_blocks. */
+pa_status pa_seq_append_slot(pa_allocator* a, pa_prefix_cache* c, int32_t* blocks, int* n_blocks, int max_blocks,
+                             int64_t pos, int64_t* slot, int32_t* copy_src, int32_t* copy_dst);
+
 /* Device copy of whole blocks: for i < n, block dst[i] (every kv head's K and
  * V page, and for a coded cache both scales) becomes a copy of block src[i].
  * src / dst are device int32 arrays; no dst may appear as a src of the same
@@ -396,6 +427,16 @@ uint64_t pa_kv_bytes(int layers, int kv_heads, int head_dim, int dtype_bits, int
 pa_status pa_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
                           const int32_t* seq_ids, const int32_t* positions, int num_tokens,
                           int block_size, int64_t* slots);
+
+/* The slot of each sequence's new token in a decode step: position
+ * seq_lens[b] - 1 (the new token counts in its sequence's length), mapped as
+ * pa_slot_mapping maps it ([P1] "2. PagedAttention").  slots[b] = -1 where
+ * seq_lens[b] <= 0 (the sequence gets no token; pa_kv_append skips it).
+ * block_tables [batch][max_blocks_per_seq] and seq_lens [batch] are host
+ * arrays; slots [batch] is written by the call.  PA_ERR_INVALID if a
+ * position lies beyond its table row or an argument is bad. */
+pa_status pa_step_slots(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                        int block_size, int64_t* slots);
 
 /* Unit-time scheduler simulator ([P2] "Static versus continuous scheduling"
  * and "Hands-on"): mode 0 = static cohorts of `slots` requests (each cohort

@@ -65,6 +65,8 @@ def load(build_if_missing: bool = True):
                                       ctypes.c_float, i32, P, sz, i32, P]),
         "pa_decode_step": (i32, [P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                  ctypes.c_float, i32, P, sz, i32, P]),
+        "pa_decode_attention_static_ws": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                ctypes.c_float, i32, i32, P]),
         "pa_prefill_attention": (i32, [P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, i32,
                                        ctypes.c_float, i32, P]),
         "pa_get_device_error": (i32, [P, i32]),
@@ -89,6 +91,9 @@ def load(build_if_missing: bool = True):
         "pa_blocks_for_tokens": (i64, [i64, i32]),
         "pa_kv_bytes": (u64, [i32, i32, i32, i32, i64, i64]),
         "pa_slot_mapping": (i32, [P, i32, P, P, i32, i32, P]),
+        "pa_step_slots": (i32, [P, i32, P, i32, i32, P]),
+        "pa_seq_admit": (i32, [P, P, P, i64, P, i32, P, P]),
+        "pa_seq_append_slot": (i32, [P, P, P, P, i32, i64, P, P, P]),
         "pa_sched_simulate": (i32, [P, i32, i32, i32, P]),
         "pa_sched_continuous_kv": (i32, [P, P, P, i32, i32, i64, i32, P, P, P, P, P]),
     }
@@ -124,10 +129,12 @@ def _np_ptr(a: Optional[np.ndarray]):
     return a.ctypes.data
 
 
-def _stream(stream) -> Optional[int]:
+def _stream(stream, device=None) -> Optional[int]:
     if stream is None:
-        return torch.cuda.current_stream().cuda_stream
+        return torch.cuda.current_stream(device).cuda_stream
     if isinstance(stream, torch.cuda.Stream):
+        if device is not None and stream.device != device:
+            raise ValueError("stream is on %s, the call's tensors on %s" % (stream.device, device))
         return stream.cuda_stream
     return int(stream)
 
@@ -160,6 +167,31 @@ def _need(t: torch.Tensor, dtype, name: str, dim: Optional[int] = None):
         raise ValueError("%s must have %d dimensions" % (name, dim))
 
 
+def _one_device(ref: torch.Tensor, **tensors) -> torch.device:
+    """The call's device: ref's.  Every other tensor argument (None skipped)
+    must be a CUDA tensor on that same device, checked before anything is
+    launched (a host or foreign-device pointer handed to a kernel or a TMA
+    map would be read by the GPU)."""
+    dev = ref.device
+    if dev.type != "cuda":
+        raise ValueError("tensor arguments must be CUDA tensors")
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if not isinstance(t, torch.Tensor) or not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % name)
+        if t.device != dev:
+            raise ValueError("%s is on %s, the call's other tensors on %s" % (name, t.device, dev))
+    return dev
+
+
+def _call(dev: torch.device, what: str, fn, *args, stream=None):
+    """Run a device entry point with `dev` current, on `stream` (default: the
+    current torch stream of dev), and raise on a non-OK status."""
+    with torch.cuda.device(dev):
+        _check(fn(*args, _stream(stream, dev)), what)
+
+
 # ------------------------------------------------------------------ device ops
 def pa_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
                  v_scale: Optional[torch.Tensor], k_new: torch.Tensor, v_new: torch.Tensor,
@@ -178,9 +210,10 @@ def pa_kv_append(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional
     if (dc != _row_len(kvd, d) or tuple(k_new.shape) != (T, hkv, d) or tuple(v_new.shape) != (T, hkv, d)
             or v_cache.shape != k_cache.shape):
         raise ValueError("shape mismatch between caches, new K/V and slot_mapping")
-    _check(lib.pa_kv_append(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(k_new),
-                            _ptr(v_new), _ptr(slot_mapping), T, nb, hkv, d, bs, kvd, _stream(stream)),
-           "pa_kv_append")
+    dev = _one_device(k_new, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale, v_new=v_new,
+                      slot_mapping=slot_mapping)
+    _call(dev, "pa_kv_append", lib.pa_kv_append, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+          _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), T, nb, hkv, d, bs, kvd, stream=stream)
 
 
 def pa_decode_resolve_splits(batch: int, num_kv_heads: int, max_blocks_per_seq: int,
@@ -212,11 +245,11 @@ def pa_decode_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tenso
             or seq_lens.shape[0] != B):
         raise ValueError("shape mismatch")
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.pa_decode_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                   _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d,
-                                   bs, M, nb, float(scale), int(num_splits), _ptr(workspace), ws,
-                                   kvd, _stream(stream)),
-           "pa_decode_attention")
+    dev = _one_device(q, out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                      block_tables=block_tables, seq_lens=seq_lens, workspace=workspace)
+    _call(dev, "pa_decode_attention", lib.pa_decode_attention, _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M, nb,
+          float(scale), int(num_splits), _ptr(workspace), ws, kvd, stream=stream)
 
 
 def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -240,11 +273,11 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
             or tuple(v_new.shape) != (B, hkv, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B):
         raise ValueError("shape mismatch")
     ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.pa_decode_step(_ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                              _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv,
-                              d, bs, M, nb, float(scale), int(num_splits), _ptr(workspace), ws, kvd,
-                              _stream(stream)),
-           "pa_decode_step")
+    dev = _one_device(q, out=out, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale,
+                      v_scale=v_scale, block_tables=block_tables, seq_lens=seq_lens, workspace=workspace)
+    _call(dev, "pa_decode_step", lib.pa_decode_step, _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
+          _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M,
+          nb, float(scale), int(num_splits), _ptr(workspace), ws, kvd, stream=stream)
 
 
 PA_STATIC_WORKSPACE_BYTES = 16 << 20
@@ -259,10 +292,6 @@ def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: t
     allocate device memory (the library's own PA_STATIC_WORKSPACE_BYTES array
     is used; calls sharing it must not overlap on the GPU)."""
     lib = load()
-    f = lib.pa_decode_attention_static_ws
-    P, i32 = ctypes.c_void_p, ctypes.c_int
-    f.restype = i32
-    f.argtypes = [P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32, ctypes.c_float, i32, i32, P]
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
@@ -273,10 +302,11 @@ def pa_decode_attention_static_ws(out: torch.Tensor, q: torch.Tensor, k_cache: t
     M = block_tables.shape[1]
     if dc != _row_len(kvd, d) or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("shape mismatch")
-    _check(f(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-             _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M, nb, float(scale), int(num_splits),
-             kvd, _stream(stream)),
-           "pa_decode_attention_static_ws")
+    dev = _one_device(q, out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                      block_tables=block_tables, seq_lens=seq_lens)
+    _call(dev, "pa_decode_attention_static_ws", lib.pa_decode_attention_static_ws, _ptr(out), _ptr(q),
+          _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq,
+          hkv, d, bs, M, nb, float(scale), int(num_splits), kvd, stream=stream)
 
 
 def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -297,10 +327,11 @@ def pa_prefill_attention(out: torch.Tensor, q: torch.Tensor, k_cache: torch.Tens
     B, M = block_tables.shape
     if out.shape != q.shape or dc != _row_len(kvd, d) or q_start.shape[0] != B + 1 or seq_lens.shape[0] != B:
         raise ValueError("shape mismatch between q, out, caches, tables, lengths and q_start")
-    _check(lib.pa_prefill_attention(_ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                    _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _ptr(q_start), B,
-                                    q.shape[1], hkv, d, bs, M, nb, int(max_q_len), float(scale), kvd,
-                                    _stream(stream)), "pa_prefill_attention")
+    dev = _one_device(q, out=out, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale,
+                      block_tables=block_tables, seq_lens=seq_lens, q_start=q_start)
+    _call(dev, "pa_prefill_attention", lib.pa_prefill_attention, _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+          _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), _ptr(q_start), B, q.shape[1], hkv, d,
+          bs, M, nb, int(max_q_len), float(scale), kvd, stream=stream)
 
 
 def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Optional[torch.Tensor],
@@ -323,8 +354,9 @@ def pa_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: Option
         raise ValueError("src/dst or cache shapes differ")
     nb, hkv, bs, dc = k_cache.shape
     d = 2 * dc if kvd == PA_KV_INT4 else dc
-    _check(lib.pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(src), _ptr(dst),
-                              int(src.shape[0]), nb, hkv, d, bs, kvd, _stream(stream)), "pa_copy_blocks")
+    dev = _one_device(src, dst=dst, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale, v_scale=v_scale)
+    _call(dev, "pa_copy_blocks", lib.pa_copy_blocks, _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+          _ptr(src), _ptr(dst), int(src.shape[0]), nb, hkv, d, bs, kvd, stream=stream)
 
 
 def pa_get_device_error(clear: bool = True) -> int:
@@ -473,6 +505,49 @@ def pa_slot_mapping(block_tables: np.ndarray, seq_ids: np.ndarray, positions: np
     _check(load().pa_slot_mapping(_np_ptr(t), int(t.shape[1]), _np_ptr(s), _np_ptr(p), int(len(s)),
                                   int(block_size), _np_ptr(out)), "pa_slot_mapping")
     return out[: len(s)]
+
+
+def pa_step_slots(block_tables: np.ndarray, seq_lens: np.ndarray, block_size: int) -> np.ndarray:
+    """Slot of each sequence's new token (position seq_len - 1); -1 where seq_len <= 0."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    n = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    if t.ndim != 2 or n.shape != (t.shape[0],):
+        raise ValueError("block_tables must be [B, M] and seq_lens [B]")
+    out = np.zeros(max(len(n), 1), dtype=np.int64)
+    _check(load().pa_step_slots(_np_ptr(t), int(t.shape[1]), _np_ptr(n), int(len(n)), int(block_size),
+                                _np_ptr(out)), "pa_step_slots")
+    return out[: len(n)]
+
+
+def pa_seq_admit(a: pa_allocator, c: Optional[pa_prefix_cache], tokens: np.ndarray, blocks: np.ndarray):
+    """Blocks for a new sequence (cached prefix first, then fresh ones) written
+    into the int32 buffer `blocks`; returns (number of blocks, first position
+    whose KV the caller must write)."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    if blocks.dtype != np.int32 or not blocks.flags["C_CONTIGUOUS"]:
+        raise TypeError("blocks must be a contiguous int32 buffer")
+    n = ctypes.c_int(0)
+    first = ctypes.c_int64(0)
+    _check(load().pa_seq_admit(a.handle, c.handle if c is not None else None, _np_ptr(t) if t.size else None,
+                               int(t.size), _np_ptr(blocks) if blocks.size else None, int(blocks.size),
+                               ctypes.byref(n), ctypes.byref(first)), "pa_seq_admit")
+    return int(n.value), int(first.value)
+
+
+def pa_seq_append_slot(a: pa_allocator, c: Optional[pa_prefix_cache], blocks: np.ndarray, n_blocks: int, pos: int):
+    """Reserve position pos of a sequence holding blocks[:n_blocks] (int32 buffer,
+    updated in place); returns (slot, new n_blocks, (src, dst) page copy or None)."""
+    if blocks.dtype != np.int32 or not blocks.flags["C_CONTIGUOUS"]:
+        raise TypeError("blocks must be a contiguous int32 buffer")
+    n = ctypes.c_int(int(n_blocks))
+    slot = ctypes.c_int64(0)
+    src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+    _check(load().pa_seq_append_slot(a.handle, c.handle if c is not None else None,
+                                     _np_ptr(blocks) if blocks.size else None, ctypes.byref(n), int(blocks.size),
+                                     int(pos), ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst)),
+           "pa_seq_append_slot")
+    copy = (int(src.value), int(dst.value)) if src.value >= 0 else None
+    return int(slot.value), int(n.value), copy
 
 
 def pa_sched_simulate(out_lens: Sequence[int], slots: int, mode: int) -> int:

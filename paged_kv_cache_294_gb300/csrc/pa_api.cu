@@ -221,15 +221,15 @@ size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, i
 
 }  // extern "C"
 
-namespace {
+namespace pa {
 
-// Shared by pa_decode_attention (k_new == NULL) and pa_decode_step.
-pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
-                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
-                      const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
-                      void* workspace, size_t workspace_bytes, int kv_dtype, void* stream, const void* k_new,
-                      const void* v_new) {
+// Every check of a decode call's arguments but the workspace's.  PA_OK for a
+// call that may launch (batch == 0 included: it launches nothing).
+pa_status decode_check(const void* out, const void* q, const void* k_cache, const void* v_cache,
+                       const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                       const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                       int kv_dtype, const void* k_new, const void* v_new) {
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || num_splits < 0 ||
         !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
         return PA_ERR_INVALID;
@@ -253,6 +253,24 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     if (q8 && (!k_scale || !v_scale)) return PA_ERR_INVALID;
     if ((k_new != nullptr) != (v_new != nullptr)) return PA_ERR_INVALID;
     if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID;
+    return PA_OK;
+}
+
+}  // namespace pa
+
+namespace {
+
+// Shared by pa_decode_attention (k_new == NULL) and pa_decode_step.
+pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                      const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                      void* workspace, size_t workspace_bytes, int kv_dtype, void* stream, const void* k_new,
+                      const void* v_new) {
+    const pa_status chk = pa::decode_check(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
+                                           num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                           num_blocks, scale, num_splits, kv_dtype, k_new, v_new);
+    if (chk != PA_OK || batch == 0) return chk;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
     const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
                                                   max_blocks_per_seq, num_splits);

@@ -141,6 +141,25 @@ pa_status pa_slot_mapping(const int32_t* block_tables, int max_blocks_per_seq,
     return PA_OK;
 }
 
+pa_status pa_step_slots(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                        int block_size, int64_t* slots) {
+    if (batch < 0 || block_size <= 0 || max_blocks_per_seq < 0) return PA_ERR_INVALID;
+    if (batch == 0) return PA_OK;
+    if (!block_tables || !seq_lens || !slots) return PA_ERR_INVALID;
+    for (int b = 0; b < batch; ++b) {
+        const int32_t len = seq_lens[b];
+        if (len <= 0) {   // no token this step
+            slots[b] = -1;
+            continue;
+        }
+        const int p = len - 1;   // the new token is the sequence's last position
+        if (p / block_size >= max_blocks_per_seq) return PA_ERR_INVALID;
+        const int32_t blk = block_tables[(int64_t)b * max_blocks_per_seq + p / block_size];
+        slots[b] = (int64_t)blk * block_size + p % block_size;
+    }
+    return PA_OK;
+}
+
 pa_status pa_sched_simulate(const int64_t* out_lens, int n, int slots, int mode, int64_t* iters) {
     if (n < 0 || slots <= 0 || (mode != 0 && mode != 1) || !iters || (n > 0 && !out_lens))
         return PA_ERR_INVALID;

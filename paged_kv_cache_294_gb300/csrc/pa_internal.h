@@ -8,6 +8,8 @@
 
 #include <algorithm>
 
+#include "../../include/pa.h"
+
 namespace pa {
 
 struct AppendLaunch {
@@ -60,6 +62,14 @@ struct PrefillLaunch {
     int B, Hq, Hkv, bs, M, num_blocks, max_q;
     float scale;
 };
+
+// Checks of a decode call's arguments other than its workspace (pa_api.cu);
+// returns the status the call would return, PA_OK if it may launch.
+pa_status decode_check(const void* out, const void* q, const void* k_cache, const void* v_cache, const float* k_scale,
+                       const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens, int batch,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                       int num_blocks, float scale, int num_splits, int kv_dtype, const void* k_new,
+                       const void* v_new);
 
 cudaError_t launch_kv_append(const AppendLaunch& L, cudaStream_t stream);
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream);

@@ -201,4 +201,79 @@ pa_status pa_block_cow(pa_allocator* a, int32_t block, int32_t* out_block, int* 
     return PA_OK;
 }
 
+namespace {
+
+// n fresh blocks into out; when the pool is short, blocks only the prefix
+// cache still holds are evicted first.  All or nothing.
+pa_status alloc_evicting(pa_allocator* a, pa_prefix_cache* c, int n, int32_t* out) {
+    if (n <= 0) return PA_OK;
+    const int shortfall = n - pa_allocator_num_free(a);
+    if (shortfall > 0 && c) {
+        int freed = 0;
+        pa_prefix_evict(c, shortfall, &freed);
+    }
+    return pa_block_alloc(a, n, out);
+}
+
+}  // namespace
+
+pa_status pa_seq_admit(pa_allocator* a, pa_prefix_cache* c, const int32_t* tokens, int64_t n_tokens,
+                       int32_t* blocks, int max_blocks, int* n_blocks, int64_t* first_new_pos) {
+    if (!a || n_tokens < 0 || max_blocks < 0 || !n_blocks || !first_new_pos || (n_tokens > 0 && !tokens))
+        return PA_ERR_INVALID;
+    if (c && c->alloc != a) return PA_ERR_INVALID;
+    const int bs = pa_allocator_block_size(a);
+    const int64_t need = pa_blocks_for_tokens(n_tokens, bs);
+    if (need > max_blocks || (need > 0 && !blocks)) return PA_ERR_INVALID;
+    int shared = 0;
+    if (c && need > 0) {
+        const pa_status s = pa_prefix_match(c, tokens, n_tokens, blocks, (int)need, &shared);
+        if (s != PA_OK) return s;
+    }
+    const pa_status s = alloc_evicting(a, c, (int)need - shared, blocks + shared);
+    if (s != PA_OK) {
+        if (shared) pa_block_free(a, blocks, shared);   // give the matched references back
+        *n_blocks = 0;
+        *first_new_pos = 0;
+        return s;
+    }
+    *n_blocks = (int)need;
+    *first_new_pos = (int64_t)shared * bs;
+    return PA_OK;
+}
+
+pa_status pa_seq_append_slot(pa_allocator* a, pa_prefix_cache* c, int32_t* blocks, int* n_blocks, int max_blocks,
+                             int64_t pos, int64_t* slot, int32_t* copy_src, int32_t* copy_dst) {
+    if (!a || !n_blocks || !slot || !copy_src || !copy_dst || pos < 0 || *n_blocks < 0 ||
+        (*n_blocks > 0 && !blocks))
+        return PA_ERR_INVALID;
+    if (c && c->alloc != a) return PA_ERR_INVALID;
+    const int bs = pa_allocator_block_size(a);
+    const int64_t j = pos / bs;
+    if (j > *n_blocks || j >= max_blocks || !blocks) return PA_ERR_INVALID;
+    *copy_src = *copy_dst = -1;
+    if (j == *n_blocks) {   // the position opens a new block
+        const pa_status s = alloc_evicting(a, c, 1, blocks + j);
+        if (s != PA_OK) return s;
+        *n_blocks += 1;
+    } else {                // it lands in a block the sequence holds: write only a private one
+        int32_t dst = -1;
+        int needs_copy = 0;
+        pa_status s = pa_block_cow(a, blocks[j], &dst, &needs_copy);
+        if (s == PA_ERR_OOM && c) {
+            int freed = 0;
+            pa_prefix_evict(c, 1, &freed);
+            if (freed > 0) s = pa_block_cow(a, blocks[j], &dst, &needs_copy);
+        }
+        if (s != PA_OK) return s;
+        if (needs_copy) {
+            *copy_src = blocks[j];
+            *copy_dst = dst;
+        }
+        blocks[j] = dst;
+    }
+    *slot = (int64_t)blocks[j] * bs + pos % bs;
+    return PA_OK;
+}
+
 }  // extern "C"

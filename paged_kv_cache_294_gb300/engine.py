@@ -14,9 +14,9 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import (PA_ERR_OOM, PA_KV_INT4, PagedAttnError, pa_allocator, pa_block_cow, pa_copy_blocks,
-               pa_decode_attention, pa_decode_resolve_splits, pa_decode_step, pa_decode_workspace_bytes,
-               pa_kv_append, pa_prefix_cache, pa_slot_mapping)
+from . import (PA_KV_INT4, pa_allocator, pa_blocks_for_tokens, pa_copy_blocks, pa_decode_attention,
+               pa_decode_resolve_splits, pa_decode_step, pa_decode_workspace_bytes, pa_kv_append, pa_prefix_cache,
+               pa_seq_admit, pa_seq_append_slot, pa_slot_mapping, pa_step_slots)
 
 
 def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[int], M: int):
@@ -44,10 +44,29 @@ def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[
     return tables, alloc
 
 
+class _BlockLists:
+    """Read-only view of BlockManager's per-sequence block buffers as lists."""
+
+    def __init__(self, bufs):
+        self._bufs = bufs
+
+    def __contains__(self, sid) -> bool:
+        return sid in self._bufs
+
+    def __getitem__(self, sid) -> List[int]:
+        buf, n = self._bufs[sid]
+        return [int(x) for x in buf[:n]]
+
+    def __len__(self) -> int:
+        return len(self._bufs)
+
+
 class BlockManager:
     """Block tables of live sequences over a pa_allocator, with prefix caching
     and copy-on-write ("KV cache & continuous batching", sections
-    "2. PagedAttention" and "4. Prefix caching").
+    "2. PagedAttention" and "4. Prefix caching").  Every block decision is
+    the library's (pa_seq_admit, pa_seq_append_slot, pa_prefix_insert); this
+    class keeps each sequence's tokens and blocks in int32 buffers.
 
     add(sid, tokens)     reuses the longest cached prefix, allocates blocks for
                          the rest and returns the first position whose KV the
@@ -55,9 +74,9 @@ class BlockManager:
     commit(sid)          caches the sequence's full blocks (after their KV is
                          written);
     fork(child, parent)  the child shares every block of the parent;
-    append(sid, token)   reserves the next token's slot: a fresh block at a
-                         block boundary, else the block it lands in after
-                         pa_block_cow; returns (slot, (src, dst) or None), the
+    append(sid, token)   reserves the next token's slot: a fresh block when the
+                         token opens one, else the block it lands in after
+                         copy-on-write; returns (slot, (src, dst) or None), the
                          pair naming a block copy the caller must run (with
                          pa_copy_blocks) before writing;
     free(sid)            drops the sequence's references.
@@ -68,83 +87,68 @@ class BlockManager:
         self.bs = int(block_size)
         self.alloc = pa_allocator(num_blocks, block_size)
         self.cache = pa_prefix_cache(self.alloc) if prefix_caching else None
-        # each sequence's tokens: an int32 buffer (grown by doubling) and its length,
-        # handed to the prefix cache without conversion
+        # each sequence's tokens and blocks: an int32 buffer (grown by doubling)
+        # and its used length, handed to the library without conversion
         self._tok: Dict[int, list] = {}
-        self.blocks: Dict[int, List[int]] = {}
+        self._blk: Dict[int, list] = {}
+        self.blocks = _BlockLists(self._blk)
 
     def tokens(self, sid: int) -> np.ndarray:
         buf, n = self._tok[sid]
         return buf[:n]
 
-    def _alloc(self, n: int) -> List[int]:
-        if n <= 0:
-            return []
-        short = n - self.alloc.num_free()
-        if short > 0 and self.cache is not None:
-            self.cache.evict(short)
-        return [int(x) for x in self.alloc.alloc(n)]
+    @staticmethod
+    def _room(entry, extra: int = 1):
+        """Grow a [buffer, used] pair so that `extra` more entries fit."""
+        buf, n = entry
+        if n + extra > len(buf):
+            grown = np.empty(max(16, 2 * len(buf), n + extra), dtype=np.int32)
+            grown[:n] = buf[:n]
+            entry[0] = grown
 
     def add(self, sid: int, tokens: Sequence[int]) -> int:
-        if sid in self.blocks:
+        if sid in self._blk:
             raise ValueError("sequence %d exists" % sid)
         toks = np.array(tokens, dtype=np.int32)
-        shared = self.cache.match(toks).tolist() if self.cache is not None else []
-        try:
-            own = self._alloc(-(-len(toks) // self.bs) - len(shared))
-        except PagedAttnError:
-            self.alloc.free(shared)
-            raise
-        self._tok[sid], self.blocks[sid] = [toks, len(toks)], shared + own
-        return len(shared) * self.bs
+        buf = np.empty(max(4, pa_blocks_for_tokens(len(toks), self.bs)), dtype=np.int32)
+        n, first = pa_seq_admit(self.alloc, self.cache, toks, buf)
+        self._tok[sid], self._blk[sid] = [toks, len(toks)], [buf, n]
+        return first
 
     def commit(self, sid: int) -> None:
         if self.cache is not None:
-            self.cache.insert(self.tokens(sid), self.blocks[sid])
+            buf, n = self._blk[sid]
+            self.cache.insert(self.tokens(sid), buf[:n])
 
     def fork(self, child: int, parent: int) -> None:
-        if child in self.blocks:
+        if child in self._blk:
             raise ValueError("sequence %d exists" % child)
-        self.alloc.share(self.blocks[parent])
+        buf, n = self._blk[parent]
+        self.alloc.share(buf[:n])
         self._tok[child] = [self.tokens(parent).copy(), len(self.tokens(parent))]
-        self.blocks[child] = list(self.blocks[parent])
+        self._blk[child] = [buf[:max(n, 4)].copy(), n]
 
     def append(self, sid: int, token: int):
-        entry, blocks = self._tok[sid], self.blocks[sid]
-        n = entry[1]
-        j = n // self.bs
-        copy = None
-        if j == len(blocks):
-            blocks.append(self._alloc(1)[0])
-        else:
-            try:
-                dst, needs_copy = pa_block_cow(self.alloc, blocks[j])
-            except PagedAttnError as e:
-                if e.status != PA_ERR_OOM or self.cache is None or self.cache.evict(1) == 0:
-                    raise
-                dst, needs_copy = pa_block_cow(self.alloc, blocks[j])
-            if needs_copy:
-                copy = (blocks[j], dst)
-            blocks[j] = dst
-        if n == len(entry[0]):
-            grown = np.empty(max(16, 2 * n), dtype=np.int32)
-            grown[:n] = entry[0][:n]
-            entry[0] = grown
-        entry[0][n] = int(token)
-        entry[1] = n + 1
-        return blocks[j] * self.bs + n % self.bs, copy
+        tok, blk = self._tok[sid], self._blk[sid]
+        self._room(blk)
+        slot, blk[1], copy = pa_seq_append_slot(self.alloc, self.cache, blk[0], blk[1], tok[1])
+        self._room(tok)
+        tok[0][tok[1]] = int(token)
+        tok[1] += 1
+        return slot, copy
 
     def free(self, sid: int) -> None:
-        self.alloc.free(self.blocks.pop(sid))
+        buf, n = self._blk.pop(sid)
+        self.alloc.free(buf[:n])
         del self._tok[sid]
 
     def table(self, sids: Sequence[int], M: int) -> np.ndarray:
         t = np.full((len(sids), M), -1, dtype=np.int32)
         for i, sid in enumerate(sids):
-            b = self.blocks[sid]
-            if len(b) > M:
+            buf, n = self._blk[sid]
+            if n > M:
                 raise ValueError("table wider than M")
-            t[i, : len(b)] = b
+            t[i, :n] = buf[:n]
         return t
 
     def lens(self, sids: Sequence[int]) -> np.ndarray:
@@ -174,10 +178,8 @@ class PagedDecodeLayer:
         self.block_tables = torch.from_numpy(self.tables_host).to(self.device)
         self.seq_lens = torch.from_numpy(self.lens_host).to(self.device)
         self.B, self.M = self.tables_host.shape
-        # the new token of each sequence sits at position len - 1
-        self.step_slots_host = pa_slot_mapping(self.tables_host, np.arange(self.B, dtype=np.int32),
-                                               np.maximum(self.lens_host - 1, 0).astype(np.int32), self.bs)
-        self.step_slots_host[self.lens_host <= 0] = -1
+        # the slot of each sequence's new token (its last position; -1 for empty sequences)
+        self.step_slots_host = pa_step_slots(self.tables_host, self.lens_host, self.bs)
         self.step_slots = torch.from_numpy(self.step_slots_host).to(self.device)
 
     def ensure_workspace(self, num_splits: int = 0) -> torch.Tensor:

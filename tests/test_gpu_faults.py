@@ -85,3 +85,37 @@ def test_bounded_wait_gives_up_and_reports():
     layer.step()
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
+
+
+def test_every_tensor_argument_must_be_on_the_calls_device():
+    """A host tensor among CUDA ones (a cache, a scale, a workspace, a table)
+    is refused before any launch: the kernel or its TMA map would otherwise
+    be handed a host pointer."""
+    layer = _layer("fp8prefix", B=2, seq_len=100)
+    ws = layer.ensure_workspace(0)
+    before = layer.out.clone()
+    host = {"k_cache": layer.k_cache.cpu(), "k_scale": layer.k_scale.cpu(), "workspace": ws.cpu(),
+            "block_tables": layer.block_tables.cpu()}
+    for name, t in host.items():
+        kw = dict(k_cache=layer.k_cache, k_scale=layer.k_scale, workspace=ws, block_tables=layer.block_tables)
+        kw[name] = t
+        with pytest.raises(ValueError, match=name):
+            pa.pa_decode_attention(layer.out, layer.q, kw["k_cache"], layer.v_cache, kw["k_scale"], layer.v_scale,
+                                   kw["block_tables"], layer.seq_lens, layer.scale, 0, kw["workspace"])
+        with pytest.raises(ValueError, match=name):
+            pa.pa_decode_step(layer.out, layer.q, layer.k_new, layer.v_new, kw["k_cache"], layer.v_cache,
+                              kw["k_scale"], layer.v_scale, kw["block_tables"], layer.seq_lens, layer.scale, 0,
+                              kw["workspace"])
+        if name != "workspace":
+            with pytest.raises(ValueError, match=name):
+                pa.pa_decode_attention_static_ws(layer.out, layer.q, kw["k_cache"], layer.v_cache, kw["k_scale"],
+                                                 layer.v_scale, kw["block_tables"], layer.seq_lens, layer.scale)
+    with pytest.raises(ValueError, match="k_cache"):
+        pa.pa_kv_append(layer.k_cache.cpu(), layer.v_cache, layer.k_scale, layer.v_scale, layer.k_new,
+                        layer.v_new, layer.step_slots)
+    with pytest.raises(ValueError, match="v_scale"):
+        pa.pa_copy_blocks(layer.k_cache, layer.v_cache, layer.k_scale, layer.v_scale.cpu(),
+                          torch.zeros(1, dtype=torch.int32, device="cuda"),
+                          torch.ones(1, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(before.view(torch.int16), layer.out.view(torch.int16))

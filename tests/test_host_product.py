@@ -158,3 +158,58 @@ def test_continuous_kv_matches_oracle():
         assert a.num_free() == o.num_free()
     r = pa.pa_sched_continuous_kv(pa.pa_allocator(1000, 16), [0] * 5, [5, 20, 10, 15, 10], 3)
     assert r["iters"] == 20
+
+
+@pytest.mark.parametrize("name,kw", [("tiny", {}), ("8b", dict(B=16)), ("70b", dict(B=40)),
+                                     ("fp8prefix", dict(B=12, seq_len=600))])
+def test_step_slots_match_oracle(name, kw):
+    """The decode step's slots (the new token at position len - 1) equal the
+    oracle's, including -1 for empty sequences."""
+    w = workloads.make(name, **kw)
+    tables = oracle.run.tables_of(w)
+    lens = np.asarray(w.seq_lens, np.int32).copy()
+    lens[:: 5] = 0                      # some sequences get no token this step
+    w.seq_lens = lens
+    st = oracle.run.OracleStep(w, seqs=[0], tables=tables)
+    assert np.array_equal(pa.pa_step_slots(tables, lens, w.bs), st.step_slots)
+
+
+def test_step_slots_reject_positions_beyond_the_table():
+    tables = np.arange(6, dtype=np.int32).reshape(2, 3)
+    assert list(pa.pa_step_slots(tables, np.array([48, 1], np.int32), 16)) == [2 * 16 + 15, 3 * 16]
+    with pytest.raises(pa.PagedAttnError):
+        pa.pa_step_slots(tables, np.array([49, 1], np.int32), 16)
+
+
+def test_seq_admit_and_append_slot_errors_leave_state_unchanged():
+    a = pa.pa_allocator(3, 4)
+    c = pa.pa_prefix_cache(a)
+    buf = np.zeros(8, np.int32)
+    assert pa.pa_seq_admit(a, c, np.arange(9), buf) == (3, 0)           # 9 tokens: 3 blocks
+    c.insert(np.arange(9), buf[:3])
+    with pytest.raises(pa.PagedAttnError) as e:                          # needs 3 fresh: only cached ones
+        pa.pa_seq_admit(a, None, np.arange(100, 109), np.zeros(8, np.int32))
+    assert e.value.status == pa.PA_ERR_OOM and a.num_free() == 0
+    with pytest.raises(pa.PagedAttnError) as e:                          # too small a buffer
+        pa.pa_seq_admit(a, c, np.arange(9), np.zeros(2, np.int32))
+    assert e.value.status == pa.PA_ERR_INVALID
+    # position 12 opens block 3, but none is free and no cache may give one up
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.pa_seq_append_slot(a, None, buf, 3, 12)
+    assert e.value.status == pa.PA_ERR_OOM and list(buf[:3]) == [0, 1, 2]
+    with pytest.raises(pa.PagedAttnError) as e:                          # a hole in the block list
+        pa.pa_seq_append_slot(a, c, buf, 3, 16)
+    assert e.value.status == pa.PA_ERR_INVALID
+    # position 5 lands in block 1, which the cache shares (only full blocks are
+    # cached: blocks 0 and 1): copy-on-write needs a block, none is free and the
+    # cache can give up none (the sequence still holds both) -> OOM, unchanged
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.pa_seq_append_slot(a, c, buf, 3, 5)
+    assert e.value.status == pa.PA_ERR_OOM
+    assert [a.refcount(i) for i in range(3)] == [2, 2, 1] and list(buf[:3]) == [0, 1, 2]
+    # position 9 lands in block 2, held by the sequence alone: written in place
+    assert pa.pa_seq_append_slot(a, c, buf, 3, 9) == (2 * 4 + 1, 3, None)
+    # free the sequence and re-admit the same tokens: the two cached blocks match
+    a.free(buf[:3])
+    assert pa.pa_seq_admit(a, c, np.arange(9), buf) == (3, 8)
+    assert list(buf[:2]) == [0, 1]
