@@ -437,7 +437,7 @@ def e2e_measure(bn, layer, K, world, alg):
     return e2e, serial
 
 
-def measure_workload(bn, name, world, local, sweep=None):
+def measure_workload(bn, name, world, local, sweep=None, cuda_core=False):
     """Build one workload, check its step against the oracle on every output,
     then time it.  Returns the workload's entry of the JSON line."""
     import oracle.run
@@ -521,6 +521,32 @@ def measure_workload(bn, name, world, local, sweep=None):
         rows.append({"splits": "auto (%d)" % S, "us": entry["us_per_step"], "GBps": entry["roofline"]["achieved"],
                      "frac": entry["roofline"]["frac"], "max_err_over_bound": parity["max_err_over_bound"]})
         entry["split_sweep"] = rows
+    if cuda_core:
+        # the same kernel with its CUDA-core page step (packed fp32 FMAs) in place
+        # of the tensor-core MMAs: parity first, then the same timings
+        os.environ["PA_DECODE_FMA"] = "1"
+        try:
+            pa.pa_get_device_error(clear=True)
+            layer.fused_step(num_splits=args.splits)
+            torch.cuda.synchronize()
+            par = parity_full(w, layer.out, ref, pa.pa_get_device_error())
+            if not par["ok"]:
+                print("parity check failed on %s (CUDA-core step): %s" % (name, par), file=sys.stderr)
+                sys.exit(3)
+            with ClockSampler(local) as fclocks:
+                tf_step = bn.timed(lambda: layer.fused_step(num_splits=args.splits), K)
+                tf_attn = bn.timed(lambda: layer.decode(num_splits=args.splits), K)
+            bn.clock_lines.extend(fclocks.lines)
+        finally:
+            del os.environ["PA_DECODE_FMA"]
+        g = (uniq + qo_bytes) * K / tf_step / 1e9
+        entry["cuda_core_variant"] = {
+            "what": "PA_DECODE_FMA=1: the page step's Q.K^T and P.V as packed fp32 FMAs on the CUDA cores "
+                    "instead of m16n8k16 MMAs; same kernel otherwise",
+            "step_us": 1e6 * tf_step / K, "step_GBps": round(g, 1), "frac": round(g / peak, 4),
+            "attention_only_us": 1e6 * tf_attn / K,
+            "tensor_core_step_us": entry["us_per_step"], "tensor_core_attention_only_us": entry["attention_only"]["us"],
+            "parity": par}
     cpu = None
     if name == bn.headline and world == 1 and not args.no_cpu_baseline and bn.rank == 0:
         cpu = cpu_oracle_baseline(w, layer.tables_host, budget_s=args.cpu_seconds)
@@ -578,12 +604,13 @@ def measure_extras(bn):
 
     # multi-query attention (pa_prefill_attention): a chunked-prefill batch (16
     # sequences, 2048 cached + a 2048-token chunk) and a speculative-verify batch
-    # (64 sequences, 4 proposals + 1, U[128, 4096] cached), 8b and 70b layers
+    # (64 sequences, 4 proposals + 1, U[128, 4096] cached), 8b and 70b layers on
+    # the bf16 cache, the 8b layer on the int8 and int4 caches
     mq = {}
     rng = np.random.default_rng(7)
     cases = {"prefill": ([2048] * 16, [2048] * 16),
              "verify": ([int(x) for x in rng.integers(128, 4097, 64)], [5] * 64)}
-    for layer_name in ("8b", "70b"):
+    for layer_name in ("8b", "70b", "8b-int8", "8b-int4"):
         for case, (ctx, chunk) in cases.items():
             pw = workloads.make_prefill(layer_name, ctx, chunk, seed=31, device=dev)
             pl = PagedDecodeLayer.from_workload(pw, dev)
@@ -630,7 +657,8 @@ def run_ours(args):
     wall0 = time.perf_counter()
     for name in names:
         sweep = SPLIT_SWEEP if (name == "long" and args.workload == "all" and args.batch is None) else None
-        entries[name], c = measure_workload(bn, name, world, local, sweep)
+        cuda_core = name in ("8b", "70b") and args.workload == "all" and args.batch is None
+        entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core)
         cpu = c or cpu
     extras = measure_extras(bn) if not args.no_extras else {}
     wall = time.perf_counter() - wall0

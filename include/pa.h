@@ -311,8 +311,12 @@ int pa_allocator_refcount(const pa_allocator* a, int32_t id);
  *   max_q_len     host bound on every C_b (sizes the grid)
  *   other arguments as for pa_decode_attention (no workspace).
  *
- * Supported: bf16 cache, head_dim 128, block_size 16 or 32, G dividing 128
- * (PA_ERR_UNSUPPORTED otherwise).  A sequence with C_b < 0, C_b > seq_lens[b],
+ * Every cache type (bf16, e4m3, int8, int4; the coded ones with k_scale /
+ * v_scale, PA_ERR_INVALID without) at head_dim 128, block_size 16 or 32, G
+ * dividing 128 (PA_ERR_UNSUPPORTED otherwise).  A coded cache's codes are
+ * expanded exactly to f16 and the tensor cores then take q and the
+ * probabilities as f16 too, so q must lie in the f16 range (|q| < 65504).
+ * A sequence with C_b < 0, C_b > seq_lens[b],
  * seq_lens[b] > max_blocks_per_seq * block_size or C_b > max_q_len is
  * skipped (PA_DEVERR_SEQ_LEN); out-of-range block ids raise
  * PA_DEVERR_BLOCK_ID and leave that sequence's outputs unspecified (finite).

@@ -37,6 +37,7 @@
 // TMA map views a page as bs / 2 lines of two tokens each.
 #include <cuda_fp8.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "pa_device.cuh"
 #include "pa_fp8.cuh"
@@ -271,6 +272,10 @@ struct WarpAcc {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 sc[nt][e] = exp2f(sc[nt][e] - m_use);
+                // bf16 cache: l sums the probabilities as the P.V product sees
+                // them (bf16), so the output is a convex combination of V rows
+                // whose weights carry the rounding
+                if (!FP8) sc[nt][e] = __bfloat162float(__float2bfloat16_rn(sc[nt][e]));
                 psum += sc[nt][e];
             }
         }
@@ -435,6 +440,194 @@ struct WarpAcc {
                                                : mt * 16 + n + 8 * (e >> 1);
                 co[(warp * 8 + gq) * D + dim] = o[mt][e];
             }
+        }
+    }
+};
+
+// The same page step on the CUDA cores (bf16 cache, head_dim 128, 16-token
+// pages, G query heads per kv head fixed at compile time): S = Q K^T, the
+// lazy-rescaled fp32 online softmax and O += P V, with packed two-wide fp32
+// FMAs (fma.rn.f32x2) in place of the tensor-core MMAs.  It exists so that
+// the two contractions can be timed against each other on the same kernel;
+// PA_DECODE_FMA=1 selects it (see launch_heads).
+//   Q K^T: lane (t, h) = (lane / 2, lane % 2) forms token t's G scores over
+//     half h of head_dim, with q read as fp32 from shared memory (this head's
+//     copy, [G][8 chunks of 8 dims][2 halves][8 floats]); the halves add with
+//     one shuffle.
+//   P V: lane owns dims 4 lane .. 4 lane + 3 of O for the G heads.  Token t's
+//     probabilities reach every lane through the first 1 KB of this head's K
+//     rows of the stage, which Q K^T no longer needs, as {p, p} pairs.  Rows
+//     past the sequence's end are skipped, never multiplied.
+template <int D, int BS, int HPC, int G>
+struct WarpAccFma {
+    static_assert(D == 128 && BS == 16 && (G == 4 || G == 8), "CUDA-core variant: d 128, 16-token pages, G 4 or 8");
+    static constexpr int CHS = Cfg<D, BS, KV_BF16, HPC>::CHS;
+    static_assert(BS * G * 8 <= BS * 128, "the probabilities fit in the head's K rows of one column tile");
+    static constexpr int QS_BYTES = G * D * 4;   // this head's fp32 q
+    float m[G], l[G];
+    float o[G][4];
+    uint32_t qs;   // shared address of this head's fp32 q
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+            o[g][0] = o[g][1] = o[g][2] = o[g][3] = 0.f;
+        }
+    }
+
+    // q rows of the head's G query heads (qrow: bf16 [G][D] in global memory)
+    // into the head's shared copy, written by the head's first warp; every
+    // warp of the head then meets at named barrier `bar`.
+    __device__ __forceinline__ void load_q(const uint16_t* qrow, uint32_t qs_head, bool writer, int bar, int nthr,
+                                           int lane) {
+        qs = qs_head;
+        if (writer) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint2 w = *reinterpret_cast<const uint2*>(qrow + g * D + lane * 4);
+                const int d0 = lane * 4, half = d0 >> 6, j = (d0 & 63) >> 3, e = d0 & 7;
+                const uint32_t a = qs + (((g * 8 + j) * 2 + half) * 8 + e) * 4;
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(__uint_as_float(w.x << 16)),
+                             "f"(__uint_as_float(w.x & 0xFFFF0000u)), "f"(__uint_as_float(w.y << 16)),
+                             "f"(__uint_as_float(w.y & 0xFFFF0000u))
+                             : "memory");
+            }
+        }
+        // literal barrier ids (1 per head) keep the kernel's barrier count at 3
+        if (bar == 1)
+            asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+        else
+            asm volatile("bar.sync 2, %0;" ::"r"(nthr) : "memory");
+    }
+
+    static __device__ __forceinline__ void fma2(float2& acc, float2 a, float2 b) {
+        uint64_t d, x, y;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(acc.x), "f"(acc.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+        asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(x), "l"(y));
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(d));
+    }
+
+    static __device__ __forceinline__ float2 bf2(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    }
+
+    __device__ __forceinline__ void page(uint32_t kt, uint32_t vt, int valid, float sl2, float, int lane) {
+        const int t = lane >> 1, h = lane & 1;
+        // ------------------------------------------------ S^T = Q K^T
+        float2 acc[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) acc[g] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            uint32_t k0, k1, k2, k3;
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(k0), "=r"(k1), "=r"(k2), "=r"(k3)
+                         : "r"(swz128(kt + h * CHS, t, j * 16)));
+            const float2 kp0 = bf2(k0), kp1 = bf2(k1), kp2 = bf2(k2), kp3 = bf2(k3);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const uint32_t qa = qs + ((g * 8 + j) * 2 + h) * 32;
+                float4 q0, q1;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(q0.x), "=f"(q0.y), "=f"(q0.z), "=f"(q0.w)
+                             : "r"(qa));
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(q1.x), "=f"(q1.y), "=f"(q1.z), "=f"(q1.w)
+                             : "r"(qa + 16));
+                fma2(acc[g], make_float2(q0.x, q0.y), kp0);
+                fma2(acc[g], make_float2(q0.z, q0.w), kp1);
+                fma2(acc[g], make_float2(q1.x, q1.y), kp2);
+                fma2(acc[g], make_float2(q1.z, q1.w), kp3);
+            }
+        }
+        // ------------------------------------------------ online softmax
+        float sc[G];
+        bool grow = false;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float sv = acc[g].x + acc[g].y;
+            sv += __shfl_xor_sync(0xffffffffu, sv, 1);
+            sc[g] = t < valid ? sv * sl2 : -INFINITY;
+            grow |= sc[g] > m[g] + 8.f;   // m == -inf: any finite score
+        }
+        // Lazy rescale, as in WarpAcc: the reference m moves only when a score
+        // exceeds it by more than 2^8
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float pm = sc[g];
+#pragma unroll
+                for (int o2 = 2; o2 < 32; o2 <<= 1) pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, o2));
+                const float m_new = pm > m[g] + 8.f ? pm : m[g];
+                const float alpha = m_new == m[g] ? 1.f : exp2f(m[g] - m_new);   // m == -inf: 0
+                l[g] *= alpha;
+                o[g][0] *= alpha;
+                o[g][1] *= alpha;
+                o[g][2] *= alpha;
+                o[g][3] *= alpha;
+                m[g] = m_new;
+            }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            sc[g] = exp2f(sc[g] - (m[g] == -INFINITY ? 0.f : m[g]));
+            if (h == 0) l[g] += sc[g];
+        }
+        __syncwarp();   // every lane's K reads are done: the rows take the probabilities
+        // layout [G / 2 head pairs][BS tokens] of {p_g, p_g, p_g+1, p_g+1}
+        if (h == 0) {
+#pragma unroll
+            for (int g = 0; g < G; g += 2)
+                asm volatile("st.shared.v4.f32 [%0], {%1, %1, %2, %2};" ::"r"(kt + ((g / 2) * BS + t) * 16),
+                             "f"(sc[g]), "f"(sc[g + 1])
+                             : "memory");
+        }
+        __syncwarp();
+        // ------------------------------------------------ O += P V
+        const uint32_t vcol = vt + (lane >> 4) * CHS;
+        const int vbyte = (lane * 8) & 127;
+#pragma unroll
+        for (int tt = 0; tt < BS; ++tt) {
+            if (tt < valid) {
+                uint32_t v0, v1;
+                asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v0), "=r"(v1) : "r"(swz128(vcol, tt, vbyte)));
+                const float2 vp0 = bf2(v0), vp1 = bf2(v1);
+#pragma unroll
+                for (int g = 0; g < G; g += 2) {
+                    float4 pp;
+                    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                                 : "=f"(pp.x), "=f"(pp.y), "=f"(pp.z), "=f"(pp.w)
+                                 : "r"(kt + ((g / 2) * BS + tt) * 16));
+                    float2 a0 = make_float2(o[g][0], o[g][1]), a1 = make_float2(o[g][2], o[g][3]);
+                    float2 b0 = make_float2(o[g + 1][0], o[g + 1][1]), b1 = make_float2(o[g + 1][2], o[g + 1][3]);
+                    fma2(a0, make_float2(pp.x, pp.y), vp0);
+                    fma2(a1, make_float2(pp.x, pp.y), vp1);
+                    fma2(b0, make_float2(pp.z, pp.w), vp0);
+                    fma2(b1, make_float2(pp.z, pp.w), vp1);
+                    o[g][0] = a0.x, o[g][1] = a0.y, o[g][2] = a1.x, o[g][3] = a1.y;
+                    o[g + 1][0] = b0.x, o[g + 1][1] = b0.y, o[g + 1][2] = b1.x, o[g + 1][3] = b1.y;
+                }
+            }
+        }
+        fence_proxy_async_smem();   // generic writes into the stage before its next TMA fill
+    }
+
+    __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int warp, int lane) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float ls = l[g];
+#pragma unroll
+            for (int o2 = 1; o2 < 32; o2 <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o2);
+            if (lane == 0) {
+                cm[warp * 8 + g] = m[g];
+                cl[warp * 8 + g] = ls;
+            }
+            *reinterpret_cast<float4*>(co + (warp * 8 + g) * D + lane * 4) =
+                make_float4(o[g][0], o[g][1], o[g][2], o[g][3]);
         }
     }
 };
@@ -745,11 +938,23 @@ __device__ __forceinline__ void patch_new_row(const DecodeArgs& a, int h, int ph
         patch_new_row_call<D, BS, KVT, HPC>(a, h, phys, off, kt, vt, r, lane);
 }
 
-template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC>
+// GF = 0: tensor-core page step (WarpAcc); GF = G: the CUDA-core page step
+// (WarpAccFma) for exactly G query heads per kv head.
+template <int D, int BS, int KVT, int HPC, int GF, bool CUDA_CORES = (GF > 0 && KVT == KV_BF16)>
+struct AccOf {
+    using type = WarpAcc<D, BS, KVT, HPC>;
+};
+template <int D, int BS, int KVT, int HPC, int GF>
+struct AccOf<D, BS, KVT, HPC, GF, true> {
+    using type = WarpAccFma<D, BS, HPC, GF>;
+};
+
+template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC, int GF = 0>
 __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeArgs a) {
     using C = Cfg<D, BS, KVT, HPC>;
+    using Acc = typename AccOf<D, BS, KVT, HPC, GF>::type;
     constexpr bool FP8 = C::FP8;
     constexpr int BAR_OFF = NSTAGE * C::STAGEB;
     constexpr int WPH = C::WPH;
@@ -839,7 +1044,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
     if (!first && warp == C::NCW && lane < npages) phys0 = trow[lane];
 
-    WarpAcc<D, BS, KVT, HPC> st;
+    Acc st;
     st.reset();
     if (warp == C::NCW) {
         if (lane == 0) {
@@ -924,8 +1129,14 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     } else {
         // consumer warp: kv head h = h0 + hh, pages i with i mod WPH == wi
         const int hh = warp / WPH, wi = warp - hh * WPH, h = h0 + hh;
-        const int g = lane >> 2;
-        st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
+        if constexpr (GF > 0) {
+            // the head's q in shared memory (after the barriers), written by its first warp
+            const uint32_t qs_head = sbase + BAR_OFF + 2 * NSTAGE * 8 + hh * Acc::QS_BYTES;
+            st.load_q(a.q + ((int64_t)b * a.Hq + h * GF) * D, qs_head, wi == 0, 1 + hh, WPH * 32, lane);
+        } else {
+            const int g = lane >> 2;
+            st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
+        }
         // fused step: the warp that consumes the page holding position len-1 fetches
         // its head's new K/V row (and the block's scales) up front
         const bool appends = APPEND && split == nsplit - 1 && npages > 0 && wi == (npages - 1) % WPH;
@@ -1015,7 +1226,7 @@ static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
     return cudaSuccess;
 }
 
-template <int D, int BS, int KVT, bool APPEND, int HPC>
+template <int D, int BS, int KVT, bool APPEND, int HPC, int GF = 0>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     using C = Cfg<D, BS, KVT, HPC>;
     DecodeArgs a;
@@ -1051,9 +1262,11 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.scan = L.B <= kScanMaxBatch && L.S <= 32;
     a.scale_log2 = L.scale * 1.4426950408889634f;
     constexpr int NST = 65536 / C::STAGEB;   // 64 KB of stages
-    constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + 1024;
+    // the CUDA-core page step keeps each head's q (fp32) after the barriers
+    constexpr int QS = GF > 0 ? HPC * GF * D * 4 : 0;
+    constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + QS + 1024;
     static int configured = -1;
-    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC>, SMEM, configured);
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF>, SMEM, configured);
     if (e != cudaSuccess) return e;
     // programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel (typically this step's append) finishes; they wait for it
@@ -1069,13 +1282,32 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC>, *L.tm_k, *L.tm_v, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF>, *L.tm_k, *L.tm_v, a);
+}
+
+// PA_DECODE_FMA=1 in the environment selects the CUDA-core page step
+// (WarpAccFma) where it exists (bf16 cache, head_dim 128, 16-token pages,
+// G = 4 or 8); the tensor-core step is the default.  A measurement switch:
+// both give the same quantity within the parity bound.
+static bool fma_requested() {
+    const char* e = getenv("PA_DECODE_FMA");
+    return e && e[0] == '1';
 }
 
 // Kv heads per CTA: 2 when the count is even (the tensor maps' boxes then
 // span two heads' pages), else 1.
 template <int D, int BS, int KVT, bool APPEND>
 static cudaError_t launch_heads(const DecodeLaunch& L, cudaStream_t stream) {
+    if constexpr (KVT == KV_BF16 && D == 128 && BS == 16) {
+        const int G = L.Hq / L.Hkv;
+        if (fma_requested() && (G == 4 || G == 8)) {
+            if (L.hpc == 2)
+                return G == 4 ? launch_typed<D, BS, KVT, APPEND, 2, 4>(L, stream)
+                              : launch_typed<D, BS, KVT, APPEND, 2, 8>(L, stream);
+            return G == 4 ? launch_typed<D, BS, KVT, APPEND, 1, 4>(L, stream)
+                          : launch_typed<D, BS, KVT, APPEND, 1, 8>(L, stream);
+        }
+    }
     return L.hpc == 2 ? launch_typed<D, BS, KVT, APPEND, 2>(L, stream) : launch_typed<D, BS, KVT, APPEND, 1>(L, stream);
 }
 

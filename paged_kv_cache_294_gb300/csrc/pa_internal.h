@@ -54,6 +54,8 @@ struct DecodeLaunch {
 struct PrefillLaunch {
     void* out;          // bf16 [total_q][Hq][d]
     const void* q;      // bf16 [total_q][Hq][d]
+    const float* k_scale;   // coded caches: [num_blocks][Hkv]
+    const float* v_scale;
     const int32_t* tables;
     const int32_t* lens;
     const int32_t* q_start;   // [B + 1]
@@ -61,6 +63,7 @@ struct PrefillLaunch {
     const CUtensorMap* tm_v;
     int B, Hq, Hkv, bs, M, num_blocks, max_q;
     float scale;
+    int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8 / PA_KV_INT4
 };
 
 // Checks of a decode call's arguments other than its workspace (pa_api.cu);

@@ -26,6 +26,16 @@
 //               than 2^8, and finally writes out = O / l.  These warps
 //               also place Q in tensor memory at the start.
 //
+// Coded caches (e4m3, int8, int4 codes with one fp32 scale per (block, kv
+// head)): the producers land each page's codes in the upper part of its
+// stage, and four more warps (20-23; two for K, two for V) expand them in
+// place to exact f16 values in the layout a bf16 tile would have.  The MMAs
+// then run on f16 operands (Q, K, P, V all f16).  The K producer also passes
+// each page's K and V scales through a four-slot ring; the softmax folds the
+// K scale into the scores and the V scale into the probabilities, relative to
+// the largest V scale of the tile's sequence seen so far (vref), so O
+// accumulates in units of vref and is rescaled when vref grows.
+//
 // Tensor memory (32-bit columns): S0 [0,128), S1 [128,256), O [256,384)
 // in fp32; Q [384,448) as bf16 pairs.  P_j (bf16 pairs) is written over the
 // S columns it came from: each softmax warp's quarter of S_j holds its
@@ -35,6 +45,7 @@
 // timeout the CTA records PA_DEVERR_TIMEOUT, drains its own copies and MMAs,
 // frees the tensor memory and ends.
 #include "pa_device.cuh"
+#include "pa_fp8.cuh"
 #include "pa_internal.h"
 
 namespace pa {
@@ -55,7 +66,22 @@ constexpr int NSW = 16;                // softmax warps: four per tensor-memory 
 constexpr int NSOFT = NSW * 32;
 constexpr int NCOL = TN / (NSW / 4);   // S / P / O columns one softmax warp handles (32)
 constexpr int W_KPROD = 0, W_QK = 1, W_SOFT0 = 2, W_VPROD = W_SOFT0 + NSW, W_PV = W_VPROD + 1;
+constexpr int W_KCONV = W_PV + 1, W_VCONV = W_KCONV + 2;   // coded caches: code -> f16 warps
 constexpr int NTHREADS = (W_PV + 1) * 32;   // 640
+constexpr int NCONV = 64;                   // threads expanding one K (or V) tile
+constexpr int SC_SLOTS = 4;                 // scale ring (coded caches), by tile index
+
+// Per cache type: threads per CTA and where a stage holds the raw codes
+// before they are expanded in place (one-byte codes: the upper half, which
+// row r of the f16 tile's upper half overwrites only after the same thread
+// has read raw row r; int4 codes: the last 8 KB, read whole before any write).
+template <int KVT>
+struct PfCfg {
+    static constexpr bool CODED = KVT != KV_BF16;
+    static constexpr int NT = CODED ? NTHREADS + 4 * 32 : NTHREADS;
+    static constexpr int RAW_OFF = KVT == KV_INT4 ? TILEB - TN * 64 : HALF;
+    static constexpr int ROWB = KVT == KV_INT4 ? 64 : 128;   // raw bytes of one token row
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_O = 256;
 constexpr uint32_t COL_Q = 384;
@@ -64,6 +90,8 @@ constexpr float RESCALE_LOG2 = 8.f;    // lazy rescale threshold (a factor of 25
 struct PrefillArgs {
     __nv_bfloat16* out;
     const __nv_bfloat16* q;
+    const float* k_scale;    // coded caches: [num_blocks][Hkv]
+    const float* v_scale;
     const int32_t* tables;
     const int32_t* lens;
     const int32_t* q_start;
@@ -78,6 +106,10 @@ struct Bars {
     float red[2][4][128];        // partial row maxima [tile parity][column quarter][row]
     float red_l[4][128];         // partial row sums [column quarter][row]
     uint32_t kbad[KST], vbad[VST];   // pages of the stage whose block id was out of range
+    uint64_t kconv[KST], vconv[VST]; // coded caches: the stage's f16 tile is ready
+    uint64_t krd, vrd;               // int4: the converter group has read the tile's codes
+    uint64_t sc_full[SC_SLOTS], sc_empty[SC_SLOTS];
+    float2 sc[SC_SLOTS][TN / 16];    // (K, V) scale of each page of a tile (coded caches)
     uint32_t tmem_base;
     int abort;
 };
@@ -95,6 +127,12 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr uint32_t instr_desc(int M, int N, int b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
+}
+
+// the same for f16 A and B (format code 0 at bits 7 and 10): the coded caches'
+// codes expand to f16 exactly, and Q and P are f16 to match
+__host__ __device__ constexpr uint32_t instr_desc_f16(int M, int N, int b_mn) {
+    return (1u << 4) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // D (+)= A B, both operands described by shared-memory matrix descriptors
@@ -170,6 +208,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// two bf16 values -> the same two values as f16 (round to nearest; exact
+// for the f16 normal range)
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
+    return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -190,6 +234,100 @@ __device__ __forceinline__ void zero_tile_rows(uint32_t tile, int r0, uint32_t b
     }
 }
 
+// eight int4 codes (nibbles 0..7 of w, element j in nibble j) -> four f16x2
+// in element order: {e0, e1}, {e2, e3}, {e4, e5}, {e6, e7}; exact.
+__device__ __forceinline__ void nib8_to_f16x2_ordered(uint32_t w, uint32_t (&o)[4]) {
+    uint32_t f[4];
+    nib8_to_f16x2(w, f);   // {e0, e4}, {e1, e5}, {e2, e6}, {e3, e7}
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o[0]) : "r"(f[0]), "r"(f[1]));
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o[1]) : "r"(f[2]), "r"(f[3]));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o[2]) : "r"(f[0]), "r"(f[1]));
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o[3]) : "r"(f[2]), "r"(f[3]));
+}
+
+// Shared address of the 16-byte f16 unit holding dims 8u .. 8u + 7 of row r
+// of a tile (two 64-column halves of 128 rows x 128 bytes, 128-byte swizzle:
+// the layout a bf16 tile loaded by TMA has).
+__device__ __forceinline__ uint32_t f16_unit(uint32_t tile, int r, int u) {
+    return tile + (u >> 3) * HALF + r * 128 + (((u & 7) ^ (r & 7)) << 4);
+}
+
+// Expand a stage's raw codes (landed by TMA at PfCfg::RAW_OFF, 128-byte
+// swizzled) in place into exact f16 values.  Thread i < NCONV of the
+// converter group; int4 codes: `rd` is the group's read barrier (count
+// NCONV), in phase `rd_parity` for this tile.  Returns false on an abort.
+template <int KVT>
+__device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, uint32_t rd_parity,
+                                            volatile int* abort) {
+    const uint32_t raw = tile + PfCfg<KVT>::RAW_OFF;
+    if constexpr (KVT == KV_INT4) {
+        // line i holds tokens 2i (bytes 0..63) and 2i + 1 (bytes 64..127);
+        // 16-byte chunk c: token 2i + c / 4, dims 32 (c % 4) .. + 31.  Every
+        // line is read before any f16 row is written (the f16 rows overlap
+        // other threads' lines): the group meets at a bounded barrier wait.
+        uint4 ch[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(ch[c].x), "=r"(ch[c].y), "=r"(ch[c].z), "=r"(ch[c].w)
+                         : "r"(raw + i * 128 + ((c ^ (i & 7)) << 4)));
+        mbar_arrive(rd);
+        if (!cta_wait(rd, rd_parity, abort)) return false;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const int r = 2 * i + (c >> 2);
+            const uint32_t w[4] = {ch[c].x, ch[c].y, ch[c].z, ch[c].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {   // word k: dims 32 (c % 4) + 8 k .. + 7
+                uint32_t o[4];
+                nib8_to_f16x2_ordered(w[k], o);
+                st_shared_v4(f16_unit(tile, r, 4 * (c & 3) + k), o[0], o[1], o[2], o[3]);
+            }
+        }
+    } else {
+        // rows i and i + 64: each thread reads its raw row whole before it
+        // writes the row's f16 units (the upper half's row r lies on raw row r)
+#pragma unroll 1
+        for (int r = i; r < TN; r += NCONV) {
+            uint4 ch[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(ch[c].x), "=r"(ch[c].y), "=r"(ch[c].z), "=r"(ch[c].w)
+                             : "r"(raw + r * 128 + ((c ^ (r & 7)) << 4)));
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {   // chunk c: dims 16 c .. 16 c + 15 -> units 2c, 2c + 1
+                uint32_t a0, a1, b0, b1, c0, c1, d0, d1;
+                code4_to_f16x2<KVT>(ch[c].x, a0, a1);
+                code4_to_f16x2<KVT>(ch[c].y, b0, b1);
+                code4_to_f16x2<KVT>(ch[c].z, c0, c1);
+                code4_to_f16x2<KVT>(ch[c].w, d0, d1);
+                st_shared_v4(f16_unit(tile, r, 2 * c), a0, a1, b0, b1);
+                st_shared_v4(f16_unit(tile, r, 2 * c + 1), c0, c1, d0, d1);
+            }
+        }
+    }
+    fence_proxy_async_smem();   // the f16 tile, written by generic stores, is read by the tensor core
+    return true;
+}
+
+// Converter group (two warps): for each tile j of the ring, wait for its raw
+// codes, expand them, and arrive on conv[stage].  Ends early on an abort.
+template <int KVT, int NS>
+__device__ __forceinline__ void convert_ring(uint64_t* full, uint64_t* conv, uint64_t* rd, uint32_t ring, int nT,
+                                             int i, volatile int* abort) {
+    int st = 0, use = 0;
+    for (int j = 0; j < nT; ++j) {
+        if (!cta_wait(&full[st], use & 1, abort)) return;
+        if (!expand_tile<KVT>(ring + st * TILEB, i, rd, j & 1, abort)) return;
+        mbar_arrive(&conv[st]);
+        if (++st == NS) {
+            st = 0;
+            ++use;
+        }
+    }
+}
+
 // TMA producer of one ring of NS tile stages (one warp).  Tile j (128 tokens)
 // goes into stage j % NS.  Lane i < 128/BS handles page i of each tile: it
 // reads the page's block id one tile ahead and issues the page's two
@@ -197,42 +335,80 @@ __device__ __forceinline__ void zero_tile_rows(uint32_t tile, int r0, uint32_t b
 // bytes to expect.  Out-of-range ids are skipped and reported in badw[stage]
 // (and, when report_bad, in the device error word).  On an abort, lane 0 waits
 // for the copies this warp issued.
-template <int BS, int NS>
+// Coded caches: the codes of page i land at PfCfg::RAW_OFF + i * BS * ROWB
+// (one box per page), and when `sc` is given (the K producer) each page's
+// (K, V) scales are published through the scale ring: slot j % SC_SLOTS,
+// sc_full arrived once the tile's scales are written, sc_empty arrived by
+// every softmax thread once it has read them.
+template <int BS, int NS, int KVT>
 __device__ __forceinline__ void produce_ring(const CUtensorMap* map, uint64_t* full, uint64_t* empty, uint32_t* badw,
                                              uint32_t ring, const int32_t* table, int nT, int npages, int num_blocks,
-                                             int Hkv, int h, bool report_bad, volatile int* abort, int lane) {
+                                             int Hkv, int h, bool report_bad, volatile int* abort, int lane,
+                                             float2 (*sc)[TN / 16] = nullptr, uint64_t* sc_full = nullptr,
+                                             uint64_t* sc_empty = nullptr, const float* k_scale = nullptr,
+                                             const float* v_scale = nullptr) {
     constexpr int PPT = TN / BS;
+    constexpr bool CODED = PfCfg<KVT>::CODED;
+    constexpr uint32_t PAGE_BYTES = CODED ? (uint32_t)BS * PfCfg<KVT>::ROWB : 2u * BS * 128u;
     const bool pl = lane < PPT;   // a page lane
     if (lane == 0) prefetch_tensormap(map);
     int issued[NS];               // last use of each stage that was loaded
 #pragma unroll
     for (int i = 0; i < NS; ++i) issued[i] = -1;
     int nxt = (pl && lane < npages) ? table[lane] : -1;
+    // scales of the next tile's page, loaded alongside its block id
+    auto load_sc = [&](int id) {
+        return (id >= 0 && id < num_blocks) ? make_float2(k_scale[(int64_t)id * Hkv + h], v_scale[(int64_t)id * Hkv + h])
+                                            : make_float2(0.f, 0.f);
+    };
+    float2 nsc = make_float2(0.f, 0.f);
+    if (sc) nsc = load_sc(nxt);
     int st = 0, use = 0;          // stage of tile j, and how often it was used before
     for (int j = 0; j < nT; ++j) {
         const int p = j * PPT + lane;
         const int id = nxt;
-        if (j + 1 < nT) nxt = (pl && p + PPT < npages) ? table[p + PPT] : -1;
+        const float2 psc = nsc;
+        if (j + 1 < nT) {
+            nxt = (pl && p + PPT < npages) ? table[p + PPT] : -1;
+            if (sc) nsc = load_sc(nxt);
+        }
         const bool inside = pl && p < npages;
         const bool valid = inside && id >= 0 && id < num_blocks;
         const uint32_t bad = __ballot_sync(0xffffffffu, inside && !valid);
         const int nvalid = __popc(__ballot_sync(0xffffffffu, valid));
         int ok = 1;
+        if (sc) {
+            // the tile's scales into ring slot j % SC_SLOTS, once its last reader is done
+            const int slot = j % SC_SLOTS;
+            if (lane == 0 && j >= SC_SLOTS) ok = cta_wait(&sc_empty[slot], ((j / SC_SLOTS) - 1) & 1, abort) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            if (pl) sc[slot][lane] = valid ? psc : make_float2(0.f, 0.f);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sc_full[slot]);
+        }
         if (lane == 0) {
             if (bad && report_bad) raise_error(PA_DEVERR_BLOCK_ID);
             ok = cta_wait(&empty[st], (use & 1) ^ 1, abort) ? 1 : 0;
             if (ok) {
                 badw[st] = bad;
-                mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * 2u * BS * 128u);
+                mbar_arrive_expect_tx(&full[st], (uint32_t)nvalid * PAGE_BYTES);
             }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (valid) {
-            const uint32_t dst = ring + st * TILEB + lane * BS * 128;
-            const int y = (id * Hkv + h) * BS;
-            tma_load_2d_at(dst, map, 0, y, &full[st]);
-            tma_load_2d_at(dst + HALF, map, 64, y, &full[st]);
+            if constexpr (CODED) {
+                // one box of BS rows (int4: BS / 2 lines of two rows) of the page's codes
+                constexpr int LINES = KVT == KV_INT4 ? BS / 2 : BS;
+                const uint32_t dst = ring + st * TILEB + PfCfg<KVT>::RAW_OFF + lane * BS * PfCfg<KVT>::ROWB;
+                tma_load_2d_at(dst, map, 0, (id * Hkv + h) * LINES, &full[st]);
+            } else {
+                const uint32_t dst = ring + st * TILEB + lane * BS * 128;
+                const int y = (id * Hkv + h) * BS;
+                tma_load_2d_at(dst, map, 0, y, &full[st]);
+                tma_load_2d_at(dst + HALF, map, 64, y, &full[st]);
+            }
         }
         issued[st] = use;
         if (++st == NS) {
@@ -246,11 +422,12 @@ __device__ __forceinline__ void produce_ring(const CUtensorMap* map, uint64_t* f
     }
 }
 
-template <int BS>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int BS, int KVT>
+__global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const PrefillArgs a) {
     constexpr int PPT = TN / BS;  // pages per KV tile
+    constexpr bool CODED = PfCfg<KVT>::CODED;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Bars bars;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -294,6 +471,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_init(&bars.q_full, NSOFT);
         mbar_init(&bars.drain[0], 1);
         mbar_init(&bars.drain[1], 1);
+        for (int i = 0; i < KST; ++i) mbar_init(&bars.kconv[i], NCONV);
+        for (int i = 0; i < VST; ++i) mbar_init(&bars.vconv[i], NCONV);
+        mbar_init(&bars.krd, NCONV);
+        mbar_init(&bars.vrd, NCONV);
+        for (int i = 0; i < SC_SLOTS; ++i) {
+            mbar_init(&bars.sc_full[i], 1);
+            mbar_init(&bars.sc_empty[i], NSOFT);
+        }
         bars.abort = 0;
         fence_mbar_init();
     }
@@ -312,22 +497,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     if (warp == W_KPROD || warp == W_VPROD) {
         // ------------------------------------------------------------ producers
         const bool is_k = warp == W_KPROD;
+        if (is_k) {
+            if constexpr (CODED)
+                produce_ring<BS, KST, KVT>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + OFF_K, table, nT, npages,
+                                           a.num_blocks, a.Hkv, h, true, abort, lane, bars.sc, bars.sc_full,
+                                           bars.sc_empty, a.k_scale, a.v_scale);
+            else
+                produce_ring<BS, KST, KVT>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + OFF_K, table, nT, npages,
+                                           a.num_blocks, a.Hkv, h, true, abort, lane);
+        } else {
+            produce_ring<BS, VST, KVT>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + OFF_V, table, nT, npages,
+                                       a.num_blocks, a.Hkv, h, false, abort, lane);
+        }
+    } else if (CODED && warp >= W_KCONV) {
+        // ------------------------------------------------------------ code -> f16 expansion
+        const bool is_k = warp < W_VCONV;
+        const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
         if (is_k)
-            produce_ring<BS, KST>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + OFF_K, table, nT, npages,
-                                  a.num_blocks, a.Hkv, h, true, abort, lane);
+            convert_ring<KVT, KST>(bars.kfull, bars.kconv, &bars.krd, sbase + OFF_K, nT, i, abort);
         else
-            produce_ring<BS, VST>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + OFF_V, table, nT, npages,
-                                  a.num_blocks, a.Hkv, h, false, abort, lane);
+            convert_ring<KVT, VST>(bars.vfull, bars.vconv, &bars.vrd, sbase + OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
         // ------------------------------------------------------------ S = Q K^T issuer
-        constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
+        constexpr uint32_t ID_S = CODED ? instr_desc_f16(TM, TN, 0) : instr_desc(TM, TN, 0);
+        uint64_t* kready = CODED ? bars.kconv : bars.kfull;
         const uint64_t kd0 = smem_desc(sbase + OFF_K, 16, 1024);   // + (byte offset >> 4) per MMA
         bool ok = cta_wait(&bars.q_full, 0, abort);
         tc_fence_after();
         int ks = 0, kuse = 0;   // K stage of tile j and its use count
         for (int j = 0; ok && j < nT; ++j) {
             const int sb = j & 1;
-            if (!(ok = cta_wait(&bars.kfull[ks], kuse & 1, abort))) break;
+            if (!(ok = cta_wait(&kready[ks], kuse & 1, abort))) break;
             const uint32_t kbad = bars.kbad[ks];
             if (kbad) {
                 zero_tile_rows(sbase + OFF_K + ks * TILEB, TN, kbad, BS, lane);
@@ -363,12 +563,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // ------------------------------------------------------------ O += P V issuer
         // (a second issuing thread: one thread alone cannot issue MMAs of this
         // size as fast as the tensor core retires them)
-        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
+        constexpr uint32_t ID_O = CODED ? instr_desc_f16(TM, D, 1) : instr_desc(TM, D, 1);
+        uint64_t* vready = CODED ? bars.vconv : bars.vfull;
         const uint64_t vd0 = smem_desc(sbase + OFF_V, HALF, 1024);
         bool ok = true;
         int vs = 0, vuse = 0;   // V stage of tile j and its use count
         for (int j = 0; ok && j < nT; ++j) {
-            if (!(ok = cta_wait(&bars.vfull[vs], vuse & 1, abort))) break;
+            if (!(ok = cta_wait(&vready[vs], vuse & 1, abort))) break;
             const int rz = (j == nT - 1) ? nkv - j * TN : TN;   // rows past the last needed position
             const uint32_t vbad = bars.vbad[vs];
             if (rz < TN || vbad) {
@@ -426,21 +627,48 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 qv[4 * u + 2] = v.z;
                 qv[4 * u + 3] = v.w;
             }
+            if constexpr (CODED) {   // f16 operands throughout
+#pragma unroll
+                for (int i = 0; i < 16; ++i) qv[i] = bf16x2_to_f16x2(qv[i]);
+            }
             tmem_st16u(tmem + lane_off + COL_Q + qc * 16, qv);
             tc_fence_before();
             mbar_arrive(&bars.q_full);
         }
         const float sl2 = a.scale_log2;
         float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this quarter's sum
+        // coded caches: O is kept in units of vref, the largest V scale seen
+        float vref = 0.f, inv_vref = 0.f;
         bool ok = true;
         for (int j = 0; j < nT; ++j) {
             const int s = j & 1;
+            // coded caches: this tile's page scales (K on the scores, V on the probabilities)
+            constexpr int PQ = CODED ? (NCOL + BS - 1) / BS : 1;   // pages under this thread's columns
+            float sl2k[PQ], vr[PQ];
+            float vmax = 0.f;
+            if constexpr (CODED) {
+                const int slot = j % SC_SLOTS;
+                if (!(ok = cta_wait(&bars.sc_full[slot], (j / SC_SLOTS) & 1, abort))) break;
+#pragma unroll
+                for (int i = 0; i < PPT; ++i) vmax = fmaxf(vmax, bars.sc[slot][i].y);
+#pragma unroll
+                for (int i = 0; i < PQ; ++i) {
+                    const float2 sv = bars.sc[slot][(qc * NCOL) / BS + i];
+                    sl2k[i] = sl2 * sv.x;
+                    vr[i] = sv.y;
+                }
+                mbar_arrive(&bars.sc_empty[slot]);
+            }
             if (!(ok = cta_wait(&bars.s_full[s], (j >> 1) & 1, abort))) break;
             tc_fence_after();
             float x[NCOL];
             tmem_ld32(tmem + lane_off + s * TN + qc * NCOL, x);
             const int lim = qpos - j * TN - qc * NCOL;   // columns c <= lim are visible to this row
-            if (lim < NCOL - 1) {
+            if constexpr (CODED) {
+                // scores in log2 units (K scale of the column's page), masked after scaling
+#pragma unroll
+                for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+            } else if (lim < NCOL - 1) {
 #pragma unroll
                 for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
             }
@@ -450,7 +678,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
             for (int c = 8; c < NCOL; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
             const float mxs = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+                                    fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * (CODED ? 1.f : sl2);
             bars.red[j & 1][qc][r] = mxs;
             mbar_arrive(&bars.pair[quad]);
             if (!(ok = cta_wait(&bars.pair[quad], j & 1, abort))) break;
@@ -462,23 +690,47 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             const float mb = (m_next == -INFINITY) ? 0.f : m_next;
             uint32_t w[NCOL / 2];
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int c = 0; c < NCOL; c += 2) {
-                const float p0 = ex2(fmaf(x[c], sl2, -mb));
-                const float p1 = ex2(fmaf(x[c + 1], sl2, -mb));
-                ls[(c >> 1) & 3] += p0 + p1;
-                w[c >> 1] = pack_bf16x2(p0, p1);
+            // coded caches: a larger V scale than any before moves vref (O rescales below)
+            const float vref_old = vref;
+            if (CODED && vmax > vref) {
+                vref = vmax;
+                inv_vref = 1.f / vmax;
             }
-            if (rescale && m != -INFINITY) {
+            if constexpr (CODED) {
+                // P' = P * vsc / vref as f16 (exact codes times these probabilities
+                // accumulate O in units of vref); l sums P itself
+#pragma unroll
+                for (int c = 0; c < NCOL; c += 2) {
+                    const float p0 = ex2(x[c] - mb), p1 = ex2(x[c + 1] - mb);
+                    const float ratio = vr[c / BS] * inv_vref;   // 0 while every V scale seen is 0
+                    ls[(c >> 1) & 3] += p0 + p1;
+                    w[c >> 1] = pack_f16x2(p0 * ratio, p1 * ratio);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < NCOL; c += 2) {
+                    // l sums the probabilities as the P V product sees them (bf16):
+                    // the output is then a convex combination of V rows whose weights
+                    // carry the rounding, so its error scales with the spread of V
+                    // rather than with |V|
+                    const uint32_t pk = pack_bf16x2(ex2(fmaf(x[c], sl2, -mb)), ex2(fmaf(x[c + 1], sl2, -mb)));
+                    ls[(c >> 1) & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+                    w[c >> 1] = pk;
+                }
+            }
+            const bool mrescale = rescale && m != -INFINITY;
+            const bool vrescale = CODED && vref > vref_old && vref_old > 0.f;
+            if (mrescale || vrescale) {
                 // O must be stable: P_{j-1} V_{j-1} has finished
                 if (!(ok = cta_wait(&bars.o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort))) break;
                 tc_fence_after();
-                const float alpha = ex2(m - m_new);
-                l *= alpha;
+                const float alpha = mrescale ? ex2(m - m_new) : 1.f;
+                if (mrescale) l *= alpha;
+                const float f = vrescale ? alpha * (vref_old * inv_vref) : alpha;
                 float o[NCOL];
                 tmem_ld32(tmem + lane_off + COL_O + qc * NCOL, o);
 #pragma unroll
-                for (int i = 0; i < NCOL; ++i) o[i] *= alpha;
+                for (int i = 0; i < NCOL; ++i) o[i] *= f;
                 tmem_st32(tmem + lane_off + COL_O + qc * NCOL, o);
             }
             m = m_next;
@@ -494,7 +746,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(&bars.pair[quad]);
             if (cta_wait(&bars.pair[quad], nT & 1, abort)) {
                 const float lt = (bars.red_l[0][r] + bars.red_l[1][r]) + (bars.red_l[2][r] + bars.red_l[3][r]);
-                const float inv = lt > 0.f ? 1.f / lt : 0.f;
+                // coded caches: O is in units of vref
+                const float inv = lt > 0.f ? (CODED ? vref : 1.f) / lt : 0.f;
                 uint4* dst =
                     reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D) + qc * (NCOL / 8);
                 float o[NCOL];
@@ -542,14 +795,20 @@ struct Bars2 {
     float red[2][2][4][128];     // partial row maxima [tile][tile parity j][column quarter][row]
     float red_l[2][4][128];      // partial row sums [tile][column quarter][row]
     uint32_t kbad[2], vbad[2];
+    uint64_t kconv[2], vconv[2];     // coded caches: the stage's f16 tile is ready
+    uint64_t krd, vrd;               // int4: the converter group has read the tile's codes
+    uint64_t sc_full[SC_SLOTS], sc_empty[SC_SLOTS];
+    float2 sc[SC_SLOTS][TN / 16];    // (K, V) scale of each page of a tile (coded caches)
     uint32_t tmem_base;
     int abort;
 };
 
-template <int BS>
-__global__ void __launch_bounds__(NTHREADS, 1)
+template <int BS, int KVT>
+__global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
     paged_prefill2_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                           const PrefillArgs a) {
+    constexpr int PPT = TN / BS;  // pages per KV tile
+    constexpr bool CODED = PfCfg<KVT>::CODED;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     __shared__ Bars2 bars;
     const uint32_t sbase = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -585,6 +844,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_init(&bars.p_full[i], NSOFT);
             mbar_init(&bars.drain[i], 1);
             for (int q = 0; q < 4; ++q) mbar_init(&bars.pair[i][q], NSW / 4 * 32);
+            mbar_init(&bars.kconv[i], NCONV);
+            mbar_init(&bars.vconv[i], NCONV);
+        }
+        mbar_init(&bars.krd, NCONV);
+        mbar_init(&bars.vrd, NCONV);
+        for (int i = 0; i < SC_SLOTS; ++i) {
+            mbar_init(&bars.sc_full[i], 1);
+            mbar_init(&bars.sc_empty[i], NSOFT);
         }
         mbar_init(&bars.q_full, NSOFT);
         bars.abort = 0;
@@ -603,22 +870,37 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t tmem = bars.tmem_base;
 
     if (warp == W_KPROD || warp == W_VPROD) {
-        if (warp == W_KPROD)
-            produce_ring<BS, 2>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + P2_OFF_K, table, nT, npages,
-                                a.num_blocks, a.Hkv, h, true, abort, lane);
+        if (warp == W_KPROD) {
+            if constexpr (CODED)
+                produce_ring<BS, 2, KVT>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + P2_OFF_K, table, nT,
+                                         npages, a.num_blocks, a.Hkv, h, true, abort, lane, bars.sc, bars.sc_full,
+                                         bars.sc_empty, a.k_scale, a.v_scale);
+            else
+                produce_ring<BS, 2, KVT>(&tm_k, bars.kfull, bars.kempty, bars.kbad, sbase + P2_OFF_K, table, nT,
+                                         npages, a.num_blocks, a.Hkv, h, true, abort, lane);
+        } else {
+            produce_ring<BS, 2, KVT>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + P2_OFF_V, table, nT, npages,
+                                     a.num_blocks, a.Hkv, h, false, abort, lane);
+        }
+    } else if (CODED && warp >= W_KCONV) {
+        // ------------------------------------------------------------ code -> f16 expansion
+        const bool is_k = warp < W_VCONV;
+        const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
+        if (is_k)
+            convert_ring<KVT, 2>(bars.kfull, bars.kconv, &bars.krd, sbase + P2_OFF_K, nT, i, abort);
         else
-            produce_ring<BS, 2>(&tm_v, bars.vfull, bars.vempty, bars.vbad, sbase + P2_OFF_V, table, nT, npages,
-                                a.num_blocks, a.Hkv, h, false, abort, lane);
+            convert_ring<KVT, 2>(bars.vfull, bars.vconv, &bars.vrd, sbase + P2_OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
         // ------------------------------------------------------------ S_t = Q_t K_j^T issuer
-        constexpr uint32_t ID_S = instr_desc(TM, TN, 0);
+        constexpr uint32_t ID_S = CODED ? instr_desc_f16(TM, TN, 0) : instr_desc(TM, TN, 0);
+        uint64_t* kready = CODED ? bars.kconv : bars.kfull;
         const uint64_t qd0 = smem_desc(sbase + P2_OFF_Q, 16, 1024);
         const uint64_t kd0 = smem_desc(sbase + P2_OFF_K, 16, 1024);
         bool ok = cta_wait(&bars.q_full, 0, abort);
         tc_fence_after();
         for (int j = 0; ok && j < nT; ++j) {
             const int ks = j & 1;
-            if (!(ok = cta_wait(&bars.kfull[ks], (j >> 1) & 1, abort))) break;
+            if (!(ok = cta_wait(&kready[ks], (j >> 1) & 1, abort))) break;
             const uint32_t kbad = bars.kbad[ks];
             if (kbad) {
                 zero_tile_rows(sbase + P2_OFF_K + ks * TILEB, TN, kbad, BS, lane);
@@ -652,12 +934,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         __syncwarp();
     } else if (warp == W_PV) {
         // ------------------------------------------------------------ O_t += P_t V_j issuer
-        constexpr uint32_t ID_O = instr_desc(TM, D, 1);
+        constexpr uint32_t ID_O = CODED ? instr_desc_f16(TM, D, 1) : instr_desc(TM, D, 1);
+        uint64_t* vready = CODED ? bars.vconv : bars.vfull;
         const uint64_t vd0 = smem_desc(sbase + P2_OFF_V, HALF, 1024);
         bool ok = true;
         for (int j = 0; ok && j < nT; ++j) {
             const int vs = j & 1;
-            if (!(ok = cta_wait(&bars.vfull[vs], (j >> 1) & 1, abort))) break;
+            if (!(ok = cta_wait(&vready[vs], (j >> 1) & 1, abort))) break;
             const int rz = (j == nT - 1) ? nkv - j * TN : TN;   // rows past the last needed position
             const uint32_t vbad = bars.vbad[vs];
             if (rz < TN || vbad) {
@@ -711,6 +994,12 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int i = 0; i < 4; ++i) {
                 uint4 v = make_uint4(0, 0, 0, 0);
                 if (valid_row[t]) v = __ldg(src + i);
+                if constexpr (CODED) {   // f16 operands throughout
+                    v.x = bf16x2_to_f16x2(v.x);
+                    v.y = bf16x2_to_f16x2(v.y);
+                    v.z = bf16x2_to_f16x2(v.z);
+                    v.w = bf16x2_to_f16x2(v.w);
+                }
                 const int u = (qc & 1) * 4 + i;
                 st_shared_v4(row + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
             }
@@ -719,8 +1008,27 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         mbar_arrive(&bars.q_full);
         const float sl2 = a.scale_log2;
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        // coded caches: O_t is kept in units of vref[t], the largest V scale seen
+        float vref[2] = {0.f, 0.f}, inv_vref[2] = {0.f, 0.f};
         bool ok = true;
         for (int j = 0; ok && j < nT; ++j) {
+            // coded caches: this K/V tile's page scales, shared by both query tiles
+            constexpr int PQ = CODED ? (NCOL + BS - 1) / BS : 1;   // pages under this thread's columns
+            float sl2k[PQ], vr[PQ];
+            float vmax = 0.f;
+            if constexpr (CODED) {
+                const int slot = j % SC_SLOTS;
+                if (!(ok = cta_wait(&bars.sc_full[slot], (j / SC_SLOTS) & 1, abort))) break;
+#pragma unroll
+                for (int i = 0; i < PPT; ++i) vmax = fmaxf(vmax, bars.sc[slot][i].y);
+#pragma unroll
+                for (int i = 0; i < PQ; ++i) {
+                    const float2 sv = bars.sc[slot][(qc * NCOL) / BS + i];
+                    sl2k[i] = sl2 * sv.x;
+                    vr[i] = sv.y;
+                }
+                mbar_arrive(&bars.sc_empty[slot]);
+            }
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 if (!(ok = cta_wait(&bars.s_full[t], j & 1, abort))) break;
@@ -728,7 +1036,11 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 float x[NCOL];
                 tmem_ld32(tmem + lane_off + t * TN + qc * NCOL, x);
                 const int lim = qpos[t] - j * TN - qc * NCOL;
-                if (lim < NCOL - 1) {
+                if constexpr (CODED) {
+                    // scores in log2 units (K scale of the column's page), masked after scaling
+#pragma unroll
+                    for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+                } else if (lim < NCOL - 1) {
 #pragma unroll
                     for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
                 }
@@ -738,7 +1050,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 #pragma unroll
                 for (int c = 8; c < NCOL; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], x[c]);
                 const float mxs = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+                                        fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * (CODED ? 1.f : sl2);
                 bars.red[t][j & 1][qc][r] = mxs;
                 mbar_arrive(&bars.pair[t][quad]);
                 if (!(ok = cta_wait(&bars.pair[t][quad], j & 1, abort))) break;
@@ -750,23 +1062,42 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 const float mb = (m_next == -INFINITY) ? 0.f : m_next;
                 uint32_t w[NCOL / 2];
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int c = 0; c < NCOL; c += 2) {
-                    const float p0 = ex2(fmaf(x[c], sl2, -mb));
-                    const float p1 = ex2(fmaf(x[c + 1], sl2, -mb));
-                    ls[(c >> 1) & 3] += p0 + p1;
-                    w[c >> 1] = pack_bf16x2(p0, p1);
+                const float vref_old = vref[t];
+                if (CODED && vmax > vref[t]) {
+                    vref[t] = vmax;
+                    inv_vref[t] = 1.f / vmax;
                 }
-                if (rescale && m[t] != -INFINITY) {
+                if constexpr (CODED) {
+                    // P' = P * vsc / vref as f16; l sums P itself
+#pragma unroll
+                    for (int c = 0; c < NCOL; c += 2) {
+                        const float p0 = ex2(x[c] - mb), p1 = ex2(x[c + 1] - mb);
+                        const float ratio = vr[c / BS] * inv_vref[t];   // 0 while every V scale seen is 0
+                        ls[(c >> 1) & 3] += p0 + p1;
+                        w[c >> 1] = pack_f16x2(p0 * ratio, p1 * ratio);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < NCOL; c += 2) {
+                        // l sums the bf16 probabilities the P V product uses
+                        const uint32_t pk = pack_bf16x2(ex2(fmaf(x[c], sl2, -mb)), ex2(fmaf(x[c + 1], sl2, -mb)));
+                        ls[(c >> 1) & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+                        w[c >> 1] = pk;
+                    }
+                }
+                const bool mrescale = rescale && m[t] != -INFINITY;
+                const bool vrescale = CODED && vref[t] > vref_old && vref_old > 0.f;
+                if (mrescale || vrescale) {
                     // O_t must be stable: P_t(j-1) V_{j-1} has finished (Q K_j^T waited for it)
                     if (!(ok = cta_wait(&bars.o_done[t], (j - 1) & 1, abort))) break;
                     tc_fence_after();
-                    const float alpha = ex2(m[t] - m_new);
-                    l[t] *= alpha;
+                    const float alpha = mrescale ? ex2(m[t] - m_new) : 1.f;
+                    if (mrescale) l[t] *= alpha;
+                    const float f = vrescale ? alpha * (vref_old * inv_vref[t]) : alpha;
                     float o[NCOL];
                     tmem_ld32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
 #pragma unroll
-                    for (int i = 0; i < NCOL; ++i) o[i] *= alpha;
+                    for (int i = 0; i < NCOL; ++i) o[i] *= f;
                     tmem_st32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
                 }
                 m[t] = m_next;
@@ -784,7 +1115,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             mbar_arrive(&bars.pair[t][quad]);
             if (!(ok = cta_wait(&bars.pair[t][quad], nT & 1, abort))) break;
             const float lt = (bars.red_l[t][0][r] + bars.red_l[t][1][r]) + (bars.red_l[t][2][r] + bars.red_l[t][3][r]);
-            const float inv = lt > 0.f ? 1.f / lt : 0.f;
+            // coded caches: O_t is in units of vref[t]
+            const float inv = lt > 0.f ? (CODED ? vref[t] : 1.f) / lt : 0.f;
             float o[NCOL];
             tmem_ld32(tmem + lane_off + COL_O + t * TN + qc * NCOL, o);
             if (valid_row[t]) {
@@ -809,8 +1141,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     }
 }
 
-template <int BS>
+template <int BS, int KVT>
 cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
+    constexpr int NT = PfCfg<KVT>::NT;
     static bool attr_set[64][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -818,6 +1151,8 @@ cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
     PrefillArgs a;
     a.out = static_cast<__nv_bfloat16*>(L.out);
     a.q = static_cast<const __nv_bfloat16*>(L.q);
+    a.k_scale = L.k_scale;
+    a.v_scale = L.v_scale;
     a.tables = L.tables;
     a.lens = L.lens;
     a.q_start = L.q_start;
@@ -832,28 +1167,39 @@ cudaError_t launch_typed(const PrefillLaunch& L, cudaStream_t stream) {
     // chunks longer than one 128-row tile: two tiles per CTA share each K/V tile
     const bool two = L.max_q > T;
     if (dev >= 0 && dev < 64 && !attr_set[dev][two]) {
-        e = two ? cudaFuncSetAttribute(paged_prefill2_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = two ? cudaFuncSetAttribute(paged_prefill2_kernel<BS, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        P2_SMEM_BYTES)
-                : cudaFuncSetAttribute(paged_prefill_kernel<BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                : cudaFuncSetAttribute(paged_prefill_kernel<BS, KVT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        SMEM_BYTES);
         if (e != cudaSuccess) return e;
         attr_set[dev][two] = true;
     }
     if (two) {
         dim3 grid((unsigned)((L.max_q + 2 * T - 1) / (2 * T)), (unsigned)L.Hkv, (unsigned)L.B);
-        paged_prefill2_kernel<BS><<<grid, NTHREADS, P2_SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+        paged_prefill2_kernel<BS, KVT><<<grid, NT, P2_SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
     } else {
         dim3 grid((unsigned)((L.max_q + T - 1) / T), (unsigned)L.Hkv, (unsigned)L.B);
-        paged_prefill_kernel<BS><<<grid, NTHREADS, SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
+        paged_prefill_kernel<BS, KVT><<<grid, NT, SMEM_BYTES, stream>>>(*L.tm_k, *L.tm_v, a);
     }
     return cudaGetLastError();
+}
+
+template <int BS>
+cudaError_t launch_kv(const PrefillLaunch& L, cudaStream_t stream) {
+    switch (L.kvt) {
+        case PA_KV_BF16: return launch_typed<BS, KV_BF16>(L, stream);
+        case PA_KV_FP8_E4M3: return launch_typed<BS, KV_FP8>(L, stream);
+        case PA_KV_INT8: return launch_typed<BS, KV_INT8>(L, stream);
+        case PA_KV_INT4: return launch_typed<BS, KV_INT4>(L, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const PrefillLaunch& L, cudaStream_t stream) {
-    if (L.bs == 16) return launch_typed<16>(L, stream);
-    if (L.bs == 32) return launch_typed<32>(L, stream);
+    if (L.bs == 16) return launch_kv<16>(L, stream);
+    if (L.bs == 32) return launch_kv<32>(L, stream);
     return cudaErrorInvalidValue;
 }
 

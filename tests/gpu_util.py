@@ -37,6 +37,17 @@ def allowed_err(ref: np.ndarray, atol: float) -> np.ndarray:
     return np.maximum(atol, 0.5 * bf16_ulp(ref) + ROUND_EPS)
 
 
+def worst(got: np.ndarray, ref: np.ndarray, atol: float) -> str:
+    """The output furthest outside (or closest to) its bound, for failure messages."""
+    if not got.size:
+        return "no outputs"
+    r = np.abs(got - ref) / allowed_err(ref, atol)
+    i = np.unravel_index(int(np.argmax(r)), r.shape)
+    return "worst at %s: ref %.6g got %.6g |err| %.3g bound %.3g (%.3f of it)" % (
+        tuple(int(x) for x in i), float(ref[i]), float(got[i]), float(abs(got[i] - ref[i])),
+        float(allowed_err(ref[i], atol)), float(r[i]))
+
+
 def excess(got: np.ndarray, ref: np.ndarray, atol: float) -> float:
     """max over outputs of |got - ref| / allowed_err; parity holds when <= 1."""
     return float(np.max(np.abs(got - ref) / allowed_err(ref, atol))) if got.size else 0.0

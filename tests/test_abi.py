@@ -67,10 +67,13 @@ def test_argument_errors_return_status_without_a_gpu():
                                 None) == pa.PA_ERR_UNSUPPORTED
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
                                    4, 64, 1.0, 0, None, 0, 4, None) == pa.PA_ERR_INVALID
-    # the multi-query entry point covers the bf16 cache only
-    for kvd in (1, 2, 3):
-        assert lib.pa_prefill_attention(None, None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
+    # the multi-query entry point: every cache type at head_dim 128 (coded ones
+    # need their scales), head_dim 64 unsupported
+    for kvd in (0, 1, 2, 3):
+        assert lib.pa_prefill_attention(None, None, None, None, None, None, None, None, None, 1, 8, 4, 64, 16,
                                          4, 64, 8, 1.0, kvd, None) == pa.PA_ERR_UNSUPPORTED
+        assert lib.pa_prefill_attention(None, None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
+                                         4, 64, 8, 1.0, kvd, None) == pa.PA_ERR_INVALID
     # null pointers with a non-empty batch
     assert lib.pa_decode_attention(None, None, None, None, None, None, None, None, 1, 8, 4, 128, 16,
                                    4, 64, 1.0, 0, None, 0, 0, None) == pa.PA_ERR_INVALID
@@ -101,11 +104,15 @@ def test_split_planning():
     assert pa.pa_decode_resolve_splits(4, 8, 8192, 4096) == 512      # at most 512 partitions
     # automatic choice: a CTA streams 32 .. 128 pages; it covers two kv heads
     # when their count is even, so its partition is half as many blocks
-    for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (4, 8, 8192), (128, 32, 256), (4, 2, 7), (64, 3, 256),
-                      (300, 1, 512)]:
+    for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (128, 32, 256), (4, 2, 7), (64, 3, 256), (300, 1, 512)]:
         S = pa.pa_decode_resolve_splits(B, Hkv, M, 0)
         P = -(-M // S)
         hpc = 2 if Hkv % 2 == 0 else 1
         assert 1 <= S <= M
         assert P == M or P * hpc >= 32
         assert P * hpc <= 128 + hpc - 1
+    # few (sequence, head set) groups with long tables: one wave of long
+    # partitions (the device's SM count decides the exact number; without a
+    # device the library assumes 148)
+    S = pa.pa_decode_resolve_splits(4, 8, 8192, 0)
+    assert 4 * 4 * S <= 3 * 152 and S >= 16 and -(-8192 // S) * 2 >= 256

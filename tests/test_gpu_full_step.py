@@ -22,7 +22,7 @@ import oracle.run
 import paged_kv_cache_294_gb300 as pa
 import workloads
 from paged_kv_cache_294_gb300.engine import PagedDecodeLayer
-from tests.gpu_util import cache_bytes, excess, tol
+from tests.gpu_util import cache_bytes, excess, tol, worst
 
 pytestmark = pytest.mark.gpu
 
@@ -39,8 +39,7 @@ def _compare(w, layer, ref, what):
     got = layer.out.float().cpu().numpy().astype(np.float64)
     assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), what
-    ex = excess(got, ref, tol(w))
-    assert ex <= 1.0, (what, ex, float(np.max(np.abs(got - ref))))
+    assert excess(got, ref, tol(w)) <= 1.0, (what, worst(got, ref, tol(w)))
 
 
 @pytest.mark.parametrize("name", ["8b", "70b", "long", "fp8prefix", "8b-int8", "8b-int4"])

@@ -474,11 +474,13 @@ class PrefillWorkload(Workload):
 
 
 def make_prefill(layer: str, ctx: List[int], chunk: List[int], seed: int = 11, device="cpu",
-                 Hq: Optional[int] = None, Hkv: Optional[int] = None, bs: Optional[int] = None) -> PrefillWorkload:
+                 Hq: Optional[int] = None, Hkv: Optional[int] = None, bs: Optional[int] = None,
+                 kv: Optional[str] = None) -> PrefillWorkload:
     """Sequences with ctx[b] earlier tokens and a chunk of chunk[b] query tokens
-    (seq_len = ctx + chunk) on one layer's shape (bf16 cache), tables from a
-    seeded permutation of the pool."""
+    (seq_len = ctx + chunk) on one layer's shape and cache type (or `kv`),
+    tables from a seeded permutation of the pool."""
     cfg = dict(CONFIGS[layer])
+    kv = cfg["kv"] if kv is None else kv
     Hq = cfg["Hq"] if Hq is None else Hq
     Hkv = cfg["Hkv"] if Hkv is None else Hkv
     bs = cfg["bs"] if bs is None else bs
@@ -494,7 +496,7 @@ def make_prefill(layer: str, ctx: List[int], chunk: List[int], seed: int = 11, d
     vals = _values(seed, len(fs), B, Hq, Hkv, d, device)
     q_start = np.concatenate([[0], np.cumsum(np.asarray(chunk, dtype=np.int64))]).astype(np.int32)
     q_chunk = randn_bf16((int(q_start[-1]), Hq, d), seed, 40, device)
-    return PrefillWorkload(name="prefill-" + layer, Hq=Hq, Hkv=Hkv, d=d, bs=bs, kv="bf16", B=B,
+    return PrefillWorkload(name="prefill-" + layer, Hq=Hq, Hkv=Hkv, d=d, bs=bs, kv=kv, B=B,
                            num_blocks=num_blocks, M=M, scale=1.0 / math.sqrt(d), seq_lens=lens,
                            block_tables=tables, trace=None, target_rids=None, fill_seq=fs, fill_pos=fp,
                            desc="prefill chunks %s over contexts %s" % (list(chunk)[:4], list(ctx)[:4]),
