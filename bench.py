@@ -437,7 +437,7 @@ def e2e_measure(bn, layer, K, world, alg):
     return e2e, serial
 
 
-def measure_workload(bn, name, world, local, sweep=None, cuda_core=False):
+def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared=False):
     """Build one workload, check its step against the oracle on every output,
     then time it.  Returns the workload's entry of the JSON line."""
     import oracle.run
@@ -546,6 +546,31 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False):
             "step_us": 1e6 * tf_step / K, "step_GBps": round(g, 1), "frac": round(g / peak, 4),
             "attention_only_us": 1e6 * tf_attn / K,
             "tensor_core_step_us": entry["us_per_step"], "tensor_core_attention_only_us": entry["attention_only"]["us"],
+            "parity": par}
+    if shared:
+        # the step through pa_decode_step_shared: the blocks several sequences
+        # share are read once per chunk of 8 / G of them (plan: pa_share_plan)
+        plan = layer.plan_sharing()
+        pa.pa_get_device_error(clear=True)
+        layer.shared_step(num_splits=args.splits)
+        torch.cuda.synchronize()
+        par = parity_full(w, layer.out, ref, pa.pa_get_device_error())
+        if not par["ok"]:
+            print("parity check failed on %s (shared prefixes): %s" % (name, par), file=sys.stderr)
+            sys.exit(3)
+        with ClockSampler(local) as sclocks:
+            ts_step = bn.timed(lambda: layer.shared_step(num_splits=args.splits), K)
+            ts_attn = bn.timed(lambda: layer.shared_step(append=False, num_splits=args.splits), K)
+        bn.clock_lines.extend(sclocks.lines)
+        g = (uniq + qo_bytes) * K / ts_step / 1e9
+        entry["shared_prefix_step"] = {
+            "calls": "pa_share_plan (host) + pa_decode_step_shared (one launch)",
+            "chunks": len(plan["chunk_blocks"]), "shared_blocks": plan["max_chunk_blocks"],
+            "sequences_sharing": int((plan["chunk_of"] >= 0).sum()),
+            "us_per_step": 1e6 * ts_step / K, "value": round(world * alg * K / ts_step / 1e9, 2), "unit": UNIT,
+            "seq_steps_per_s": world * w.B * K / ts_step, "attention_only_us": 1e6 * ts_attn / K,
+            "roofline": {"bound": "hbm", "achieved": round(g, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(g / peak, 4), "peak_source": peak_kind, "bytes": "distinct K/V + q + out"},
             "parity": par}
     cpu = None
     if name == bn.headline and world == 1 and not args.no_cpu_baseline and bn.rank == 0:
@@ -658,7 +683,8 @@ def run_ours(args):
     for name in names:
         sweep = SPLIT_SWEEP if (name == "long" and args.workload == "all" and args.batch is None) else None
         cuda_core = name in ("8b", "70b") and args.workload == "all" and args.batch is None
-        entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core)
+        entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core,
+                                            shared=name == "fp8prefix" and args.batch is None)
         cpu = c or cpu
     extras = measure_extras(bn) if not args.no_extras else {}
     wall = time.perf_counter() - wall0

@@ -149,7 +149,9 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
  * (base-2 log-sum-exp of the scaled scores); then merge counters int32
  * [batch][num_kv_heads].  The workspace must be zero-filled before its
  * first use; every call that completes leaves the counters at zero again
- * (after a PA_DEVERR_TIMEOUT, zero it again).  Calls that share a workspace
+ * (after a PA_DEVERR_TIMEOUT, zero it again).  The counters' place follows
+ * from the layout (batch, heads, S): a workspace reused for a request of
+ * another layout must be zero-filled again.  Calls that share a workspace
  * must not overlap on the device.
  * ------------------------------------------------------------------------- */
 int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits);
@@ -247,6 +249,65 @@ pa_status pa_decode_attention_static_ws(void* out, const void* q, const void* k_
                                         int num_kv_heads, int head_dim, int block_size,
                                         int max_blocks_per_seq, int num_blocks, float scale,
                                         int num_splits, int kv_dtype, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Shared prefixes in one decode step ([P3] "KV Cache Management": 100
+ * requests with one system prompt share its KV; [P1] "4. Prefix caching").
+ *
+ * When several sequences' tables name the same physical blocks for their
+ * first positions, pa_decode_step_shared reads those blocks once per chunk
+ * of up to PA_SHARE_MAX_ROWS / G sequences instead of once per sequence: a
+ * chunk's work item takes its members' query heads as the rows of one
+ * contraction over the shared pages and writes one (partial, log-sum-exp)
+ * per member and head, which the split-K merge combines with the member's
+ * own pages.  The outputs are the same attention (within the parity bound;
+ * the summation order differs from pa_decode_step's).
+ *
+ * The plan (pa_share_plan builds it on the host from the block tables and
+ * lengths; the caller copies its arrays to the device):
+ *   chunk_of       [batch] int32: chunk of sequence b, -1 for none
+ *   chunk_members  [n_chunks][PA_SHARE_MAX_ROWS] int32: member sequences, -1 padded
+ *   chunk_blocks   [n_chunks] int32: shared blocks of the chunk, taken from
+ *                  its first member's table row
+ * Requirements (checked on the device; a sequence or member that fails them
+ * is attended without sharing and PA_DEVERR_BLOCK_ID is set): b appears once
+ * in chunk chunk_of[b]; 1 <= chunk_blocks[c] <= max_chunk_blocks and
+ * chunk_blocks[c] <= (seq_lens[b] - 1) / block_size for every member (the
+ * shared blocks lie before each member's newest token); a chunk holds at most
+ * PA_SHARE_MAX_ROWS / (num_q_heads / num_kv_heads) members.  The caller
+ * guarantees that the members' tables agree on those blocks (pa_share_plan's
+ * plans do); if they do not, the members attend the first member's blocks.
+ * ------------------------------------------------------------------------- */
+#define PA_SHARE_MAX_ROWS 8
+
+/* Build a plan: sequences whose first physical block is the same form a
+ * group; its shared length is the number of leading blocks every member holds
+ * at the same positions, capped by each member's (seq_lens - 1) / block_size;
+ * groups sharing at least max(min_blocks, 1) blocks are cut, in batch order,
+ * into chunks of group_rows sequences (group_rows = PA_SHARE_MAX_ROWS / G for
+ * the decode launch; below 2 nothing is shared).  Host arrays; at most
+ * max_chunks chunks (later groups are left unshared).  *max_chunk_blocks =
+ * the largest chunk_blocks. */
+pa_status pa_share_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                        int block_size, int group_rows, int min_blocks, int32_t* chunk_of, int32_t* chunk_members,
+                        int32_t* chunk_blocks, int max_chunks, int* n_chunks, int* max_chunk_blocks);
+
+/* Workspace for pa_decode_step_shared: pa_decode_workspace_bytes' layout
+ * with room for the chunk partials (max_chunk_blocks as passed to the step). */
+size_t pa_decode_shared_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int num_splits, int max_chunk_blocks);
+
+/* pa_decode_step (k_new / v_new given) or pa_decode_attention (both NULL)
+ * with the plan above (device arrays; n_chunks == 0 reads none of them).
+ * Other arguments, layouts and errors as pa_decode_step; the workspace must
+ * hold pa_decode_shared_workspace_bytes. */
+pa_status pa_decode_step_shared(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                                const int32_t* seq_lens, const int32_t* chunk_of, const int32_t* chunk_members,
+                                const int32_t* chunk_blocks, int n_chunks, int max_chunk_blocks, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                                void* workspace, size_t workspace_bytes, int kv_dtype, void* stream);
 
 /* Read (and optionally clear) the current device's error word; synchronises
  * the device.  *flags receives an OR of PA_DEVERR_* bits set since the last

@@ -94,6 +94,10 @@ def load(build_if_missing: bool = True):
         "pa_step_slots": (i32, [P, i32, P, i32, i32, P]),
         "pa_seq_admit": (i32, [P, P, P, i64, P, i32, P, P]),
         "pa_seq_append_slot": (i32, [P, P, P, P, i32, i64, P, P, P]),
+        "pa_share_plan": (i32, [P, i32, P, i32, i32, i32, i32, P, P, P, i32, P, P]),
+        "pa_decode_shared_workspace_bytes": (sz, [i32, i32, i32, i32, i32, i32, i32]),
+        "pa_decode_step_shared": (i32, [P, P, P, P, P, P, P, P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                        i32, i32, ctypes.c_float, i32, P, sz, i32, P]),
         "pa_sched_simulate": (i32, [P, i32, i32, i32, P]),
         "pa_sched_continuous_kv": (i32, [P, P, P, i32, i32, i64, i32, P, P, P, P, P]),
     }
@@ -278,6 +282,81 @@ def pa_decode_step(out: torch.Tensor, q: torch.Tensor, k_new: torch.Tensor, v_ne
     _call(dev, "pa_decode_step", lib.pa_decode_step, _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache),
           _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens), B, hq, hkv, d, bs, M,
           nb, float(scale), int(num_splits), _ptr(workspace), ws, kvd, stream=stream)
+
+
+PA_SHARE_MAX_ROWS = 8
+
+
+def pa_share_plan(block_tables: np.ndarray, seq_lens: np.ndarray, block_size: int, group_rows: int,
+                  min_blocks: int = 1, max_chunks: Optional[int] = None) -> dict:
+    """Shared-prefix plan (host): dict(chunk_of [B], chunk_members [n, PA_SHARE_MAX_ROWS],
+    chunk_blocks [n], max_chunk_blocks); chunk_of[b] = PA_SHARE_MAX_ROWS * chunk + slot or -1."""
+    t = np.ascontiguousarray(block_tables, dtype=np.int32)
+    n = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    B = len(n)
+    if t.ndim != 2 or t.shape[0] != B:
+        raise ValueError("block_tables must be [B, M] and seq_lens [B]")
+    cap = B if max_chunks is None else int(max_chunks)
+    chunk_of = np.full(max(B, 1), -1, np.int32)
+    members = np.full((max(cap, 1), PA_SHARE_MAX_ROWS), -1, np.int32)
+    blocks = np.zeros(max(cap, 1), np.int32)
+    nc, mx = ctypes.c_int(0), ctypes.c_int(0)
+    _check(load().pa_share_plan(_np_ptr(t) if B else None, int(t.shape[1]), _np_ptr(n) if B else None, B,
+                                int(block_size), int(group_rows), int(min_blocks), _np_ptr(chunk_of),
+                                _np_ptr(members), _np_ptr(blocks), cap, ctypes.byref(nc), ctypes.byref(mx)),
+           "pa_share_plan")
+    return dict(chunk_of=chunk_of[:B], chunk_members=members[: nc.value], chunk_blocks=blocks[: nc.value],
+                max_chunk_blocks=int(mx.value))
+
+
+def pa_decode_shared_workspace_bytes(batch: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                                     max_blocks_per_seq: int, num_splits: int, max_chunk_blocks: int) -> int:
+    return int(load().pa_decode_shared_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                       max_blocks_per_seq, num_splits, max_chunk_blocks))
+
+
+def pa_decode_step_shared(out: torch.Tensor, q: torch.Tensor, k_new: Optional[torch.Tensor],
+                          v_new: Optional[torch.Tensor], k_cache: torch.Tensor, v_cache: torch.Tensor,
+                          k_scale: Optional[torch.Tensor], v_scale: Optional[torch.Tensor], block_tables: torch.Tensor,
+                          seq_lens: torch.Tensor, chunk_of: torch.Tensor, chunk_members: torch.Tensor,
+                          chunk_blocks: torch.Tensor, max_chunk_blocks: int, scale: float, num_splits: int = 0,
+                          workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """The decode step (k_new / v_new given) or attention alone (both None) with
+    shared prefixes read once per chunk of sequences (plan from pa_share_plan,
+    its arrays on the device)."""
+    lib = load()
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(chunk_of, torch.int32, "chunk_of", 1)
+    _need(chunk_members, torch.int32, "chunk_members", 2)
+    _need(chunk_blocks, torch.int32, "chunk_blocks", 1)
+    if (k_new is None) != (v_new is None):
+        raise ValueError("k_new and v_new are given together")
+    B, hq, d = q.shape
+    kvd = _kv_dtype(k_cache, d)
+    nb, hkv, bs, dc = k_cache.shape
+    M = block_tables.shape[1]
+    n_chunks = int(chunk_blocks.shape[0])
+    if (dc != _row_len(kvd, d) or tuple(out.shape) != (B, hq, d) or block_tables.shape[0] != B
+            or seq_lens.shape[0] != B or chunk_of.shape[0] != B
+            or tuple(chunk_members.shape) != (n_chunks, PA_SHARE_MAX_ROWS)):
+        raise ValueError("shape mismatch")
+    if k_new is not None:
+        _need(k_new, torch.bfloat16, "k_new", 3)
+        _need(v_new, torch.bfloat16, "v_new", 3)
+        if tuple(k_new.shape) != (B, hkv, d) or tuple(v_new.shape) != (B, hkv, d):
+            raise ValueError("shape mismatch")
+    ws = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    dev = _one_device(q, out=out, k_new=k_new, v_new=v_new, k_cache=k_cache, v_cache=v_cache, k_scale=k_scale,
+                      v_scale=v_scale, block_tables=block_tables, seq_lens=seq_lens, chunk_of=chunk_of,
+                      chunk_members=chunk_members, chunk_blocks=chunk_blocks, workspace=workspace)
+    _call(dev, "pa_decode_step_shared", lib.pa_decode_step_shared, _ptr(out), _ptr(q), _ptr(k_new), _ptr(v_new),
+          _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), _ptr(seq_lens),
+          _ptr(chunk_of), _ptr(chunk_members) if n_chunks else None, _ptr(chunk_blocks) if n_chunks else None,
+          n_chunks, int(max_chunk_blocks), B, hq, hkv, d, bs, M, nb, float(scale), int(num_splits), _ptr(workspace),
+          ws, kvd, stream=stream)
 
 
 PA_STATIC_WORKSPACE_BYTES = 16 << 20

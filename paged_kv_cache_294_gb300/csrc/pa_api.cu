@@ -272,21 +272,41 @@ pa_status decode_check(const void* out, const void* q, const void* k_cache, cons
 
 namespace {
 
-// Shared by pa_decode_attention (k_new == NULL) and pa_decode_step.
+// Chunk partitions per chunk item set for a shared-prefix launch: chunks of up
+// to max_chunk_blocks blocks in partitions of at most part_blocks.
+int chunk_parts_for(int max_blocks_per_seq, int S, int max_chunk_blocks) {
+    return max_chunk_blocks > 0 ? (int)ceil_div(max_chunk_blocks, part_blocks_for(max_blocks_per_seq, S)) : 0;
+}
+
+// The shared-prefix plan of one launch (n_chunks == 0: none).
+struct SharePlan {
+    const int32_t* chunk_of = nullptr;
+    const int32_t* chunk_members = nullptr;
+    const int32_t* chunk_blocks = nullptr;
+    int n_chunks = 0, max_chunk_blocks = 0;
+};
+
+// Shared by pa_decode_attention (k_new == NULL), pa_decode_step and
+// pa_decode_step_shared (plan.n_chunks > 0).
 pa_status decode_impl(void* out, const void* q, const void* k_cache, const void* v_cache,
                       const float* k_scale, const float* v_scale, const int32_t* block_tables,
                       const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads, int head_dim,
                       int block_size, int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
                       void* workspace, size_t workspace_bytes, int kv_dtype, void* stream, const void* k_new,
-                      const void* v_new) {
+                      const void* v_new, const SharePlan& plan = SharePlan()) {
     const pa_status chk = pa::decode_check(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
                                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
                                            num_blocks, scale, num_splits, kv_dtype, k_new, v_new);
     if (chk != PA_OK || batch == 0) return chk;
     const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
-    const size_t need = pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
-                                                  max_blocks_per_seq, num_splits);
+    const int cparts = plan.n_chunks > 0 ? chunk_parts_for(max_blocks_per_seq, S, plan.max_chunk_blocks) : 0;
+    const size_t need = plan.n_chunks > 0
+                            ? pa_decode_shared_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                               max_blocks_per_seq, num_splits, plan.max_chunk_blocks)
+                            : pa_decode_workspace_bytes(batch, num_q_heads, num_kv_heads, head_dim,
+                                                        max_blocks_per_seq, num_splits);
     if (!workspace || workspace_bytes < need || !aligned16(workspace)) return PA_ERR_INVALID;
+    const int Sw = S + cparts;   // partial slots per output row
 
     const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
     // two kv heads per CTA when their count is even: one box holds a block's
@@ -308,9 +328,9 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     L.o_part = nullptr;
     L.lse = nullptr;
     {
-        const WsLayout wl = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, S);
+        const WsLayout wl = ws_layout(batch, num_q_heads, num_kv_heads, head_dim, Sw);
         char* base = static_cast<char*>(workspace);
-        if (S > 1) {
+        if (Sw > 1) {
             L.o_part = reinterpret_cast<float*>(base + wl.o_off);
             L.lse = reinterpret_cast<float*>(base + wl.lse_off);
         }
@@ -335,6 +355,13 @@ pa_status decode_impl(void* out, const void* q, const void* k_cache, const void*
     L.v_cache_w = const_cast<void*>(v_cache);
     L.k_scale_w = const_cast<float*>(k_scale);
     L.v_scale_w = const_cast<float*>(v_scale);
+    L.Sw = Sw;
+    L.chunk_of = plan.chunk_of;
+    L.chunk_members = plan.chunk_members;
+    L.chunk_blocks = plan.chunk_blocks;
+    L.n_chunks = plan.n_chunks;
+    L.chunk_parts = cparts;
+    L.max_chunk_blocks = plan.max_chunk_blocks;
     return cuda_status(pa::launch_decode(L, static_cast<cudaStream_t>(stream)));
 }
 
@@ -363,6 +390,45 @@ pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void
     return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
                        scale, num_splits, workspace, workspace_bytes, kv_dtype, stream, k_new, v_new);
+}
+
+size_t pa_decode_shared_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int max_blocks_per_seq, int num_splits, int max_chunk_blocks) {
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_chunk_blocks < 0) return 0;
+    const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
+    return ws_layout(batch, num_q_heads, num_kv_heads, head_dim,
+                     S + chunk_parts_for(max_blocks_per_seq, S, max_chunk_blocks))
+        .total;
+}
+
+pa_status pa_decode_step_shared(void* out, const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale, const int32_t* block_tables,
+                                const int32_t* seq_lens, const int32_t* chunk_of, const int32_t* chunk_members,
+                                const int32_t* chunk_blocks, int n_chunks, int max_chunk_blocks, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
+                                void* workspace, size_t workspace_bytes, int kv_dtype, void* stream) {
+    if (n_chunks < 0 || max_chunk_blocks < 0) return PA_ERR_INVALID;
+    if (n_chunks > 0) {
+        if (!chunk_of || !chunk_members || !chunk_blocks || max_chunk_blocks < 1 ||
+            max_chunk_blocks > max_blocks_per_seq)
+            return PA_ERR_INVALID;
+        // chunk items: n_chunks x kv-head sets x chunk partitions must fit the grid with the rest
+        const int S = pa_decode_resolve_splits(batch, num_kv_heads, max_blocks_per_seq, num_splits);
+        const int64_t sets = num_kv_heads % 2 == 0 ? num_kv_heads / 2 : num_kv_heads;
+        if ((int64_t)n_chunks * sets * chunk_parts_for(max_blocks_per_seq, S, max_chunk_blocks) +
+                (int64_t)S * sets * batch > INT32_MAX)
+            return PA_ERR_UNSUPPORTED;
+    }
+    SharePlan plan;
+    plan.chunk_of = chunk_of;
+    plan.chunk_members = chunk_members;
+    plan.chunk_blocks = chunk_blocks;
+    plan.n_chunks = n_chunks;
+    plan.max_chunk_blocks = n_chunks > 0 ? max_chunk_blocks : 0;
+    return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch, num_q_heads,
+                       num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, num_splits,
+                       workspace, workspace_bytes, kv_dtype, stream, k_new, v_new, plan);
 }
 
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,

@@ -66,6 +66,13 @@ struct DecodeArgs {
     int b_early, part_early;   // sequences b < b_early: partitions of part_early blocks
     int scan;                  // 1: the grid lists work items only (see find_later_item)
     float scale_log2;
+    int Sw;                    // partial slots per output row in the workspace
+    // shared prefixes (SHARED launches): chunk_of[b] = PA_SHARE_MAX_ROWS * c + slot
+    // of sequence b in chunk c, -1 for none; chunk c's members and shared blocks
+    const int32_t* chunk_of;
+    const int32_t* chunk_members;
+    const int32_t* chunk_blocks;
+    int n_chunks, chunk_parts, max_chunk_blocks;
 };
 
 // HPC: kv heads per CTA.  The pages of one block for consecutive kv heads
@@ -661,8 +668,8 @@ __device__ __forceinline__ void combine_store(const DecodeArgs& a, const float* 
         if (nsplit <= 1) {
             a.out[row * D + dim] = __float2bfloat16_rn(val);
         } else {
-            a.o_part[(row * a.S + split) * D + dim] = val;
-            if (dim == 0) a.lse[row * a.S + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
+            a.o_part[(row * a.Sw + split) * D + dim] = val;
+            if (dim == 0) a.lse[row * a.Sw + split] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
         }
     }
 }
@@ -681,7 +688,7 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int6
     float4 pv[U];
     auto load_batch = [&](int col, int k0) {
         const int gq = col / D4, d4 = col - gq * D4;
-        const float4* op = reinterpret_cast<const float4*>(a.o_part + (row0 + gq) * a.S * D) + d4;
+        const float4* op = reinterpret_cast<const float4*>(a.o_part + (row0 + gq) * a.Sw * D) + d4;
 #pragma unroll
         for (int u = 0; u < U; ++u)
             pv[u] = k0 + u < nsplit ? __ldcg(op + (int64_t)(k0 + u) * D4) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -689,7 +696,7 @@ __device__ __forceinline__ void merge_group(const DecodeArgs& a, float* sw, int6
     if (tid < ncol) load_batch(tid, 0);
     for (int i = tid; i < G * nsplit; i += nthr) {
         const int gq = i / nsplit, k = i - gq * nsplit;
-        sw[i] = __ldcg(&a.lse[(row0 + gq) * a.S + k]);
+        sw[i] = __ldcg(&a.lse[(row0 + gq) * a.Sw + k]);
     }
     sync();
     for (int gq = warp; gq < G; gq += nwarps) {
@@ -751,7 +758,42 @@ __device__ __forceinline__ int clamp_len(int len, int cap) { return len < 0 ? 0 
 // leaves once it has read the length.
 struct WorkItem {
     int b, hs, split, raw_len;   // b < 0: no item
+    int sh;                      // leading blocks attended by b's chunk (0: none)
+    int chunk;                   // >= 0: a chunk item (b = its first member)
 };
+
+// Shared prefixes: the blocks of sequence b (clamped length len) that its
+// chunk attends, or 0.  The same test decides, in b's own items and in its
+// chunk's item, whether b takes part, so both count the same partials: b is
+// member slot k of chunk c (chunk_of[b] = 8c + k, chunk_members[8c + k] = b,
+// k < 8 / G, c < n_chunks) and the chunk's blocks lie before b's newest
+// token.  A plan that fails it sets PA_DEVERR_BLOCK_ID; b is then attended
+// without sharing.
+template <int BS>
+__device__ __forceinline__ int shared_blocks_of(const DecodeArgs& a, int b, int len) {
+    const int v = a.chunk_of[b];
+    if (v < 0) return 0;
+    const int c = v / PA_SHARE_MAX_ROWS, k = v % PA_SHARE_MAX_ROWS;
+    int cb = 0;
+    const bool ok = c < a.n_chunks && k < PA_SHARE_MAX_ROWS / a.G && a.chunk_members[v] == b &&
+                    (cb = a.chunk_blocks[c]) >= 1 && cb <= a.max_chunk_blocks && cb <= a.M && len >= 1 &&
+                    cb <= (len - 1) / BS;
+    if (!ok) {
+        raise_error(PA_DEVERR_BLOCK_ID);
+        return 0;
+    }
+    return cb;
+}
+
+// Partials of sequence b's output rows: its own partitions (blocks sh ..
+// nblk - 1 in partitions of at most pblk) and, with a shared prefix, its
+// chunk's partitions (sh blocks in partitions of at most part_blocks).
+__device__ __forceinline__ int own_parts(int nblk, int sh, int pblk) {
+    return (nblk - sh + pblk - 1) / pblk;
+}
+__device__ __forceinline__ int chunk_parts_of(const DecodeArgs& a, int sh) {
+    return sh > 0 ? (sh + a.part_blocks - 1) / a.part_blocks : 0;
+}
 
 template <int BS>
 __device__ __forceinline__ int partitions_of(const DecodeArgs& a, int b, int raw_len) {
@@ -786,7 +828,7 @@ __device__ __forceinline__ WorkItem find_later_item(const DecodeArgs& a, int r, 
         const int t = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += t;
     }
-    WorkItem it{-1, 0, 0, 0};
+    WorkItem it{-1, 0, 0, 0, 0, -1};
     if (r >= __shfl_sync(0xffffffffu, inc, 31)) return it;   // past the last item
     const int src = __ffs(__ballot_sync(0xffffffffu, r < inc)) - 1;
     if (lane == src) {
@@ -949,7 +991,81 @@ struct AccOf<D, BS, KVT, HPC, GF, true> {
     using type = WarpAccFma<D, BS, HPC, GF>;
 };
 
-template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC, int GF = 0>
+// Epilogue of a chunk item: the CTA's rows (member m's query head g at row
+// m * G + g of each kv head) go out as partial p of their member's output
+// rows, in the slot after the member's own partitions; then each member's
+// merge counter counts the partial, and the CTA merges every member whose
+// partials it completed.
+template <int D, int BS, int WPH, int HPC>
+__device__ __noinline__ void chunk_epilogue(const DecodeArgs& a, const float* cm, const float* cl, const float* co,
+                                            const int* members, int cb, int h0, int hs, int p, int warp, int lane) {
+    constexpr int NTHR = (4 + 1) * 32;
+    const int G = a.G, NH = a.Hkv / HPC, R = PA_SHARE_MAX_ROWS / G;
+    __shared__ int s_slot[PA_SHARE_MAX_ROWS], s_tot[PA_SHARE_MAX_ROWS];
+    __shared__ unsigned s_last;
+    const int tid = threadIdx.x;
+    if (tid < R) {
+        const int bm = members[tid];
+        if (bm >= 0) {
+            const int nb = (clamp_len(a.lens[bm], a.M * BS) + BS - 1) / BS;
+            const int own = own_parts(nb, cb, bm < a.b_early ? a.part_early : a.part_blocks);
+            s_slot[tid] = own + p;
+            s_tot[tid] = own + chunk_parts_of(a, cb);
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < HPC * R * G * D; idx += NTHR) {
+        const int hr = idx / D, dim = idx - hr * D;
+        const int hh = hr / (R * G), r = hr - hh * (R * G);
+        const int m = r / G, gq = r - m * G;
+        const int bm = members[m];
+        if (bm < 0) continue;
+        const int w0 = hh * WPH;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = w0; w < w0 + WPH; ++w) M = fmaxf(M, cm[w * 8 + r]);
+        float L = 0.f, O = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = w0; w < w0 + WPH; ++w) {
+                const float f = exp2f(cm[w * 8 + r] - M);
+                L += cl[w * 8 + r] * f;
+                O += co[(w * 8 + r) * D + dim] * f;
+            }
+        }
+        const int64_t row = (int64_t)bm * a.Hq + (h0 + hh) * G + gq;
+        a.o_part[(row * a.Sw + s_slot[m]) * D + dim] = (M == -INFINITY) ? 0.f : O / L;
+        if (dim == 0) a.lse[row * a.Sw + s_slot[m]] = (M == -INFINITY) ? -INFINITY : M + log2f(L);
+    }
+    __syncthreads();   // every thread's partial stores precede the counts
+    if (tid == 0) {
+        unsigned last = 0;
+        for (int m = 0; m < R; ++m) {
+            const int bm = members[m];
+            if (bm < 0) continue;
+            int old;
+            asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;"
+                         : "=r"(old)
+                         : "l"(&a.counters[bm * NH + hs])
+                         : "memory");
+            if (old == s_tot[m] - 1) last |= 1u << m;
+        }
+        s_last = last;
+    }
+    __syncthreads();
+    // the merge scratch: the combine area, free once the partials are out
+    float* sw = const_cast<float*>(cm);
+    for (unsigned last = s_last; last; last &= last - 1) {
+        const int m = __ffs(last) - 1, bm = members[m];
+        merge_group<D>(a, sw, (int64_t)bm * a.Hq + h0 * G, HPC * G, s_tot[m], tid, NTHR, warp, 5, lane, sync_cta);
+        if (tid == 0) a.counters[bm * NH + hs] = 0;
+        __syncthreads();
+    }
+}
+
+// SHARED: the launch also lists chunk items (shared prefixes) ahead of the
+// sequences' own items, always on the direct grid.
+template <int D, int BS, int KVT, int NSTAGE, bool APPEND, int HPC, int GF = 0, bool SHARED = false>
 __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const DecodeArgs a) {
@@ -979,11 +1095,15 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     static_assert(NSTAGE <= 32, "a batch slot is reused only after its pages are released");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool scan = a.scan != 0;
-    if (!scan) {
+    const bool scan = !SHARED && a.scan != 0;
+    // SHARED: the first n_chunks * NH * chunk_parts CTAs are chunk items
+    const int n_citems = SHARED ? a.n_chunks * (a.Hkv / HPC) * a.chunk_parts : 0;
+    const bool is_chunk = SHARED && (int)blockIdx.x < n_citems;
+    const int rid = (int)blockIdx.x - n_citems;   // regular item index
+    if (!scan && !is_chunk) {
         // a partition this sequence can never use (a table holds at most M
         // blocks): leave before any set-up or load
-        const int b0 = blockIdx.x / a.S / (a.Hkv / HPC), split0 = blockIdx.x % a.S;
+        const int b0 = rid / a.S / (a.Hkv / HPC), split0 = rid % a.S;
         const int pblk0 = b0 < a.b_early ? a.part_early : a.part_blocks;
         if (split0 > 0 && split0 >= (a.M + pblk0 - 1) / pblk0) return;
     }
@@ -1002,21 +1122,46 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     griddep_wait();
 
     __shared__ WorkItem s_item;
+    __shared__ int s_members[PA_SHARE_MAX_ROWS];   // chunk items: member sequences that take part (-1: none)
     const int NH = a.Hkv / HPC;
-    // partition 0 of (b, head set): mapped directly, the table read with the length
-    const bool first = scan ? (int)blockIdx.x < a.B * NH : (int)blockIdx.x % a.S == 0;
+    // partition 0 of (b, head set): mapped directly, the table read with the
+    // length (not with shared prefixes: a sequence's own blocks start later)
+    const bool first = !SHARED && (scan ? (int)blockIdx.x < a.B * NH : (int)blockIdx.x % a.S == 0);
     int phys0 = 0;
     if (warp == C::NCW) {
-        if (!scan) {
-            const int q = blockIdx.x / a.S, b0 = q / NH;
+        if (is_chunk) {
+            const int per = NH * a.chunk_parts;
+            const int c = (int)blockIdx.x / per, hs = ((int)blockIdx.x % per) / a.chunk_parts,
+                      p = (int)blockIdx.x % a.chunk_parts;
+            const int cb = a.chunk_blocks[c];
+            // member slot `lane`: the sequence takes part when its own items
+            // count this chunk's partials (the same test, shared_blocks_of)
+            int mb = -1;
+            if (lane < PA_SHARE_MAX_ROWS / a.G) {
+                const int bm = a.chunk_members[c * PA_SHARE_MAX_ROWS + lane];
+                if (bm >= 0 && bm < a.B && a.chunk_of[bm] == c * PA_SHARE_MAX_ROWS + lane &&
+                    shared_blocks_of<BS>(a, bm, clamp_len(a.lens[bm], a.M * BS)) == cb)
+                    mb = bm;
+            }
+            if (lane < PA_SHARE_MAX_ROWS) s_members[lane] = mb;
+            const int lead = __shfl_sync(0xffffffffu, mb, __ffs(__ballot_sync(0xffffffffu, mb >= 0)) - 1);
+            const bool any = __any_sync(0xffffffffu, mb >= 0);
+            // the first member's table row names the shared blocks; every page is full
+            if (lane == 0) s_item = WorkItem{any ? lead : -1, hs, p, cb * BS, cb, c};
+        } else if (!scan) {
+            const int q = rid / a.S, b0 = q / NH;
             if (first && lane < a.M) phys0 = a.tables[(int64_t)b0 * a.M + lane];
-            if (lane == 0) s_item = WorkItem{b0, q - b0 * NH, (int)blockIdx.x - q * a.S, a.lens[b0]};
+            if (lane == 0) {
+                const int l0 = a.lens[b0];
+                const int sh0 = SHARED ? shared_blocks_of<BS>(a, b0, clamp_len(l0, a.M * BS)) : 0;
+                s_item = WorkItem{b0, q - b0 * NH, rid - q * a.S, l0, sh0, -1};
+            }
         } else if (first) {
             const int b0 = blockIdx.x / NH;
             // partition 0 starts at block 0: the first table entries come
             // alongside the length (entries past the sequence are not used)
             if (lane < a.M) phys0 = a.tables[(int64_t)b0 * a.M + lane];
-            if (lane == 0) s_item = WorkItem{b0, (int)blockIdx.x - b0 * NH, 0, a.lens[b0]};
+            if (lane == 0) s_item = WorkItem{b0, (int)blockIdx.x - b0 * NH, 0, a.lens[b0], 0, -1};
         } else {
             const WorkItem it = find_later_item<BS, HPC>(a, blockIdx.x - a.B * NH, lane);
             if (lane == 0) s_item = it;
@@ -1034,13 +1179,18 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
         len = clamp_len(len, cap);
     }
     const int nblk = (len + BS - 1) / BS;
-    const int pblk = b < a.b_early ? a.part_early : a.part_blocks;
-    const int nsplit = (nblk + pblk - 1) / pblk;  // 0 when len == 0 (one item, no pages)
+    // a chunk item covers the chunk's sh blocks; a sequence's own items its blocks sh .. nblk - 1
+    const int sh = SHARED ? it.sh : 0;
+    const bool chunk = SHARED && it.chunk >= 0;
+    const int base = chunk ? 0 : sh;
+    const int span = chunk ? sh : nblk - sh;
+    const int pblk = chunk ? a.part_blocks : (b < a.b_early ? a.part_early : a.part_blocks);
+    const int nsplit = (span + pblk - 1) / pblk;  // 0 when len == 0 (one item, no pages)
     if (split > 0 && split >= nsplit) return;     // (direct grid) past the sequence's end
-    // the sequence's blocks split evenly over its partitions (at most P each)
-    const int pb = nsplit > 0 ? (nblk + nsplit - 1) / nsplit : 0;
-    const int j0 = split * pb;
-    const int npages = max(0, min(nblk, j0 + pb) - j0);
+    // the blocks split evenly over the partitions (at most P each)
+    const int pb = nsplit > 0 ? (span + nsplit - 1) / nsplit : 0;
+    const int j0 = base + split * pb;
+    const int npages = max(0, min(base + span, j0 + pb) - j0);
     const int32_t* trow = a.tables + (int64_t)b * a.M + j0;
     if (!first && warp == C::NCW && lane < npages) phys0 = trow[lane];
 
@@ -1133,13 +1283,18 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
             // the head's q in shared memory (after the barriers), written by its first warp
             const uint32_t qs_head = sbase + BAR_OFF + 2 * NSTAGE * 8 + hh * Acc::QS_BYTES;
             st.load_q(a.q + ((int64_t)b * a.Hq + h * GF) * D, qs_head, wi == 0, 1 + hh, WPH * 32, lane);
+        } else if (chunk) {
+            // row g: query head g % G of member g / G
+            const int g = lane >> 2, m = g / a.G;
+            const int bm = m < PA_SHARE_MAX_ROWS / a.G ? s_members[m] : -1;
+            st.load_q(a.q + ((int64_t)max(bm, 0) * a.Hq + h * a.G + g % a.G) * D, bm >= 0, lane & 3);
         } else {
             const int g = lane >> 2;
             st.load_q(a.q + ((int64_t)b * a.Hq + h * a.G + g) * D, g < a.G, lane & 3);
         }
         // fused step: the warp that consumes the page holding position len-1 fetches
         // its head's new K/V row (and the block's scales) up front
-        const bool appends = APPEND && split == nsplit - 1 && npages > 0 && wi == (npages - 1) % WPH;
+        const bool appends = APPEND && !chunk && split == nsplit - 1 && npages > 0 && wi == (npages - 1) % WPH;
         int app_phys = -1;
         // the row waits in shared memory, not in registers, until its page arrives
         __shared__ NewRow s_nr[APPEND ? HPC : 1][32];
@@ -1183,13 +1338,21 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
     // across the page loop
     const WorkItem ie = s_item;
     const int eb = ie.b, eh0 = ie.hs * HPC, esplit = ie.split;
-    const int ensplit = (((clamp_len(ie.raw_len, cap) + BS - 1) / BS) + (eb < a.b_early ? a.part_early : a.part_blocks) - 1) /
-                        (eb < a.b_early ? a.part_early : a.part_blocks);
     float* cm = reinterpret_cast<float*>(sgen);
     float* cl = cm + C::NCW * 8;
     float* co = cl + C::NCW * 8;
     if (warp < C::NCW) st.publish(cm, cl, co, warp, lane);
     __syncthreads();
+    if constexpr (SHARED) {
+        if (ie.chunk >= 0) {
+            chunk_epilogue<D, BS, WPH, HPC>(a, cm, cl, co, s_members, ie.sh, eh0, ie.hs, esplit, warp, lane);
+            return;
+        }
+    }
+    // the sequence's partials: its own partitions and, with a shared prefix, its chunk's
+    const int esh = SHARED ? ie.sh : 0;
+    const int ensplit = own_parts((clamp_len(ie.raw_len, cap) + BS - 1) / BS, esh,
+                                  eb < a.b_early ? a.part_early : a.part_blocks) + chunk_parts_of(a, esh);
     combine_store<D, WPH, HPC>(a, cm, cl, co, eb, eh0, esplit, ensplit, threadIdx.x, C::NTHREADS);
     if (ensplit <= 1) return;
 
@@ -1226,7 +1389,7 @@ static cudaError_t set_smem_once(K kernel, int smem, int& configured_device) {
     return cudaSuccess;
 }
 
-template <int D, int BS, int KVT, bool APPEND, int HPC, int GF = 0>
+template <int D, int BS, int KVT, bool APPEND, int HPC, int GF = 0, bool SHARED = false>
 static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     using C = Cfg<D, BS, KVT, HPC>;
     DecodeArgs a;
@@ -1261,19 +1424,33 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     a.S = L.S;
     a.scan = L.B <= kScanMaxBatch && L.S <= 32;
     a.scale_log2 = L.scale * 1.4426950408889634f;
+    a.Sw = L.Sw;
+    a.chunk_of = L.chunk_of;
+    a.chunk_members = L.chunk_members;
+    a.chunk_blocks = L.chunk_blocks;
+    a.n_chunks = SHARED ? L.n_chunks : 0;
+    a.chunk_parts = L.chunk_parts;
+    a.max_chunk_blocks = L.max_chunk_blocks;
+    if (SHARED) {
+        // every partition count follows from (length, shared blocks): no early doubling, direct grid
+        a.b_early = 0;
+        a.scan = 0;
+    }
     constexpr int NST = 65536 / C::STAGEB;   // 64 KB of stages
     // the CUDA-core page step keeps each head's q (fp32) after the barriers
     constexpr int QS = GF > 0 ? HPC * GF * D * 4 : 0;
     constexpr int SMEM = NST * C::STAGEB + 2 * NST * 8 + QS + 1024;
     static int configured = -1;
-    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF>, SMEM, configured);
+    cudaError_t e = set_smem_once(paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF, SHARED>, SMEM, configured);
     if (e != cudaSuccess) return e;
     // programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel (typically this step's append) finishes; they wait for it
     // in griddep_wait() before reading any input
     cudaLaunchConfig_t cfg = {};
     // an upper bound on the work items: every sequence at most S partitions
-    cfg.gridDim = dim3((unsigned)L.S * (unsigned)(L.Hkv / HPC) * (unsigned)L.B);
+    // (shared prefixes: the chunk items first)
+    cfg.gridDim = dim3((unsigned)L.S * (unsigned)(L.Hkv / HPC) * (unsigned)L.B +
+                       (SHARED ? (unsigned)L.n_chunks * (unsigned)(L.Hkv / HPC) * (unsigned)L.chunk_parts : 0u));
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
@@ -1282,7 +1459,8 @@ static cudaError_t launch_typed(const DecodeLaunch& L, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF>, *L.tm_k, *L.tm_v, a);
+    return cudaLaunchKernelEx(&cfg, paged_decode_kernel<D, BS, KVT, NST, APPEND, HPC, GF, SHARED>, *L.tm_k, *L.tm_v,
+                              a);
 }
 
 // PA_DECODE_FMA=1 in the environment selects the CUDA-core page step
@@ -1298,6 +1476,9 @@ static bool fma_requested() {
 // span two heads' pages), else 1.
 template <int D, int BS, int KVT, bool APPEND>
 static cudaError_t launch_heads(const DecodeLaunch& L, cudaStream_t stream) {
+    if (L.n_chunks > 0)   // shared prefixes
+        return L.hpc == 2 ? launch_typed<D, BS, KVT, APPEND, 2, 0, true>(L, stream)
+                          : launch_typed<D, BS, KVT, APPEND, 1, 0, true>(L, stream);
     if constexpr (KVT == KV_BF16 && D == 128 && BS == 16) {
         const int G = L.Hq / L.Hkv;
         if (fma_requested() && (G == 4 || G == 8)) {

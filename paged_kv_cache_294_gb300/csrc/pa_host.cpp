@@ -160,6 +160,68 @@ pa_status pa_step_slots(const int32_t* block_tables, int max_blocks_per_seq, con
     return PA_OK;
 }
 
+pa_status pa_share_plan(const int32_t* block_tables, int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                        int block_size, int group_rows, int min_blocks, int32_t* chunk_of, int32_t* chunk_members,
+                        int32_t* chunk_blocks, int max_chunks, int* n_chunks, int* max_chunk_blocks) {
+    if (batch < 0 || block_size <= 0 || max_blocks_per_seq <= 0 || max_chunks < 0 || !n_chunks ||
+        !max_chunk_blocks || group_rows < 0 || group_rows > PA_SHARE_MAX_ROWS)
+        return PA_ERR_INVALID;
+    *n_chunks = 0;
+    *max_chunk_blocks = 0;
+    if (batch == 0) return PA_OK;
+    if (!block_tables || !seq_lens || !chunk_of || (max_chunks > 0 && (!chunk_members || !chunk_blocks)))
+        return PA_ERR_INVALID;
+    const int M = max_blocks_per_seq;
+    auto row = [&](int b) { return block_tables + (int64_t)b * M; };
+    // blocks of b that hold only positions before its newest token (the one
+    // a decode step appends): they are complete and the step never writes them
+    std::vector<int> cap((size_t)batch);
+    for (int b = 0; b < batch; ++b) {
+        chunk_of[b] = -1;
+        const int64_t len = seq_lens[b];
+        cap[b] = len >= 1 ? (int)std::min<int64_t>((len - 1) / block_size, M) : 0;
+    }
+    if (group_rows < 2) return PA_OK;   // one sequence per chunk shares nothing
+    // groups: sequences whose first physical block is the same, in batch order
+    std::vector<int> order;
+    for (int b = 0; b < batch; ++b)
+        if (cap[b] >= std::max(min_blocks, 1)) order.push_back(b);
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return row(x)[0] < row(y)[0]; });
+    int nc = 0, mx = 0;
+    for (size_t i = 0; i < order.size();) {
+        size_t e = i + 1;
+        while (e < order.size() && row(order[e])[0] == row(order[i])[0]) ++e;
+        if (e - i >= 2) {
+            // the blocks every member holds at the same positions as the first
+            const int first = order[i];
+            int L = cap[first];
+            for (size_t k = i + 1; k < e; ++k) {
+                const int b = order[k];
+                int c = 0;
+                const int lim = std::min(L, cap[b]);
+                while (c < lim && row(b)[c] == row(first)[c]) ++c;
+                L = c;
+            }
+            if (L >= std::max(min_blocks, 1)) {
+                for (size_t k = i; k < e && nc < max_chunks; k += group_rows, ++nc) {
+                    chunk_blocks[nc] = L;
+                    for (int r = 0; r < PA_SHARE_MAX_ROWS; ++r) {
+                        const size_t m = k + r;
+                        const bool in = r < group_rows && m < e;
+                        chunk_members[(int64_t)nc * PA_SHARE_MAX_ROWS + r] = in ? order[m] : -1;
+                        if (in) chunk_of[order[m]] = nc * PA_SHARE_MAX_ROWS + r;   // chunk and slot
+                    }
+                }
+                mx = std::max(mx, L);
+            }
+        }
+        i = e;
+    }
+    *n_chunks = nc;
+    *max_chunk_blocks = mx;
+    return PA_OK;
+}
+
 pa_status pa_sched_simulate(const int64_t* out_lens, int n, int slots, int mode, int64_t* iters) {
     if (n < 0 || slots <= 0 || (mode != 0 && mode != 1) || !iters || (n > 0 && !out_lens))
         return PA_ERR_INVALID;

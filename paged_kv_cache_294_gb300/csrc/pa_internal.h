@@ -49,6 +49,12 @@ struct DecodeLaunch {
     int S;              // partitions per sequence at most (grid x)
     float scale;
     int kvt;            // PA_KV_BF16 / PA_KV_FP8_E4M3 / PA_KV_INT8 / PA_KV_INT4
+    int Sw;             // partial slots per output row in the workspace (S without shared prefixes)
+    // shared prefixes (n_chunks > 0): the plan of pa_decode_step_shared
+    const int32_t* chunk_of = nullptr;
+    const int32_t* chunk_members = nullptr;
+    const int32_t* chunk_blocks = nullptr;
+    int n_chunks = 0, chunk_parts = 0, max_chunk_blocks = 0;
 };
 
 struct PrefillLaunch {

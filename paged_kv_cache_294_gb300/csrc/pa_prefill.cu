@@ -208,6 +208,17 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// acc + lo + hi for the two bf16 halves of pk, in fp32: a mixed-precision
+// FMA with 1.0 takes each 16-bit half as it is
+__device__ __forceinline__ float add_bf16_halves(float acc, uint32_t pk) {
+    unsigned short lo, hi;
+    asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(pk));
+    const unsigned short one = 0x3F80;   // bf16 1.0
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(lo), "h"(one));
+    asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(hi), "h"(one));
+    return acc;
+}
+
 // two bf16 values -> the same two values as f16 (round to nearest; exact
 // for the f16 normal range)
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                     // carry the rounding, so its error scales with the spread of V
                     // rather than with |V|
                     const uint32_t pk = pack_bf16x2(ex2(fmaf(x[c], sl2, -mb)), ex2(fmaf(x[c + 1], sl2, -mb)));
-                    ls[(c >> 1) & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+                    ls[(c >> 1) & 3] = add_bf16_halves(ls[(c >> 1) & 3], pk);
                     w[c >> 1] = pk;
                 }
             }
@@ -1081,7 +1092,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                     for (int c = 0; c < NCOL; c += 2) {
                         // l sums the bf16 probabilities the P V product uses
                         const uint32_t pk = pack_bf16x2(ex2(fmaf(x[c], sl2, -mb)), ex2(fmaf(x[c + 1], sl2, -mb)));
-                        ls[(c >> 1) & 3] += __uint_as_float(pk << 16) + __uint_as_float(pk & 0xFFFF0000u);
+                        ls[(c >> 1) & 3] = add_bf16_halves(ls[(c >> 1) & 3], pk);
                         w[c >> 1] = pk;
                     }
                 }

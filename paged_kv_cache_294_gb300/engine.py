@@ -14,9 +14,10 @@ from typing import Dict, List, Optional, Sequence
 import numpy as np
 import torch
 
-from . import (PA_KV_INT4, pa_allocator, pa_blocks_for_tokens, pa_copy_blocks, pa_decode_attention,
-               pa_decode_resolve_splits, pa_decode_step, pa_decode_workspace_bytes, pa_kv_append, pa_prefix_cache,
-               pa_seq_admit, pa_seq_append_slot, pa_slot_mapping, pa_step_slots)
+from . import (PA_KV_INT4, PA_SHARE_MAX_ROWS, pa_allocator, pa_blocks_for_tokens, pa_copy_blocks,
+               pa_decode_attention, pa_decode_resolve_splits, pa_decode_shared_workspace_bytes, pa_decode_step,
+               pa_decode_step_shared, pa_decode_workspace_bytes, pa_kv_append, pa_prefix_cache, pa_seq_admit,
+               pa_seq_append_slot, pa_share_plan, pa_slot_mapping, pa_step_slots)
 
 
 def replay_trace(trace, num_blocks: int, block_size: int, target_rids: Sequence[int], M: int):
@@ -245,6 +246,37 @@ class PagedDecodeLayer:
         """pa_kv_append of the new tokens, then pa_decode_attention (two launches)."""
         self.append_step(stream=stream)
         return self.decode(num_splits=num_splits, stream=stream)
+
+    # ---------------------------------------------------------------- shared prefixes
+    def plan_sharing(self, min_blocks: int = 1):
+        """Plan the shared prefixes of the current batch (pa_share_plan on the
+        host tables) and place the plan on the device; returns the plan."""
+        plan = pa_share_plan(self.tables_host, self.lens_host, self.bs, PA_SHARE_MAX_ROWS // (self.Hq // self.Hkv),
+                             min_blocks)
+        self.share_plan = plan
+        self.chunk_of = torch.from_numpy(plan["chunk_of"]).to(self.device)
+        self.chunk_members = torch.from_numpy(plan["chunk_members"].reshape(-1, PA_SHARE_MAX_ROWS)).to(self.device)
+        self.chunk_blocks = torch.from_numpy(plan["chunk_blocks"]).to(self.device)
+        return plan
+
+    def ensure_shared_workspace(self, num_splits: int = 0) -> torch.Tensor:
+        need = pa_decode_shared_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits,
+                                                self.share_plan["max_chunk_blocks"])
+        if self.workspace is None or self.workspace.numel() < need:
+            # zero-filled: the split-K counters must start at zero (calls keep them there)
+            self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
+        return self.workspace
+
+    def shared_step(self, append: bool = True, out=None, num_splits: int = 0, stream=None):
+        """The decode step (or attention alone) through pa_decode_step_shared with
+        the plan of plan_sharing."""
+        ws = self.ensure_shared_workspace(num_splits)
+        out = self.out if out is None else out
+        pa_decode_step_shared(out, self.q, self.k_new if append else None, self.v_new if append else None,
+                              self.k_cache, self.v_cache, self.k_scale, self.v_scale, self.block_tables,
+                              self.seq_lens, self.chunk_of, self.chunk_members, self.chunk_blocks,
+                              self.share_plan["max_chunk_blocks"], self.scale, num_splits, ws, stream=stream)
+        return out
 
     def copy_blocks(self, pairs, stream=None):
         """Run the block copies BlockManager.append asked for (copy-on-write)."""
