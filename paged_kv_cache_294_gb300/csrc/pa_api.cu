@@ -196,10 +196,12 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
         return (int)ceil_div(M, part_blocks_for(M, S));
     }
     // Automatic: about two waves of the three CTAs an SM holds, assuming the
-    // tables are half full on average; a CTA streams 32 .. 128 pages (enough
-    // to amortise its start-up, few enough to keep the last wave short).  A
-    // CTA covers two kv heads when their count is even, so its partition is
-    // half as many blocks.
+    // tables are half full on average; a CTA streams 32 .. 256 pages (enough
+    // to amortise its start-up, few enough to keep the last wave short; the
+    // many (sequence, head set) groups of large batches already fill the GPU,
+    // so more partitions there only add merges: shared-prefix fp8 batch 344
+    // -> 328 us at 256 pages against 128).  A CTA covers two kv heads when
+    // their count is even, so its partition is half as many blocks.
     const int hpc = num_kv_heads % 2 == 0 ? 2 : 1;
     // Few (sequence, kv-head set) groups (long contexts): one wave of long
     // partitions instead.  The CTAs start together and stream evenly, and
@@ -217,7 +219,7 @@ int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq
     const int64_t target = (int64_t)device_sms() * 6;
     int64_t P = ceil_div(pages, target);
     if (P < 32) P = 32;
-    if (P > 128) P = 128;
+    if (P > 256) P = 256;
     P = ceil_div(P, hpc);
     if (P > M) P = M;
     if (ceil_div(M, P) > kMaxSplits) P = ceil_div(M, kMaxSplits);

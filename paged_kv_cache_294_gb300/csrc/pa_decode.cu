@@ -278,7 +278,7 @@ struct WarpAcc {
         for (int nt = 0; nt < C::NT; ++nt) {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                sc[nt][e] = exp2f(sc[nt][e] - m_use);
+                sc[nt][e] = ex2_approx(sc[nt][e] - m_use);
                 // bf16 cache: l sums the probabilities as the P.V product sees
                 // them (bf16), so the output is a convex combination of V rows
                 // whose weights carry the rounding
@@ -581,7 +581,7 @@ struct WarpAccFma {
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            sc[g] = exp2f(sc[g] - (m[g] == -INFINITY ? 0.f : m[g]));
+            sc[g] = ex2_approx(sc[g] - (m[g] == -INFINITY ? 0.f : m[g]));
             if (h == 0) l[g] += sc[g];
         }
         __syncwarp();   // every lane's K reads are done: the rows take the probabilities

@@ -102,7 +102,7 @@ def test_split_planning():
     ws = pa.pa_decode_workspace_bytes(4, 32, 8, 128, 8192, 64)
     assert ws == up(4 * 32 * 64 * 128 * 4) + up(4 * 32 * 64 * 4) + up(4 * 8 * 4)
     assert pa.pa_decode_resolve_splits(4, 8, 8192, 4096) == 512      # at most 512 partitions
-    # automatic choice: a CTA streams 32 .. 128 pages; it covers two kv heads
+    # automatic choice: a CTA streams 32 .. 256 pages; it covers two kv heads
     # when their count is even, so its partition is half as many blocks
     for B, Hkv, M in [(64, 8, 256), (256, 8, 512), (128, 32, 256), (4, 2, 7), (64, 3, 256), (300, 1, 512)]:
         S = pa.pa_decode_resolve_splits(B, Hkv, M, 0)
@@ -110,7 +110,7 @@ def test_split_planning():
         hpc = 2 if Hkv % 2 == 0 else 1
         assert 1 <= S <= M
         assert P == M or P * hpc >= 32
-        assert P * hpc <= 128 + hpc - 1
+        assert P * hpc <= 256 + hpc - 1
     # few (sequence, head set) groups with long tables: one wave of long
     # partitions (the device's SM count decides the exact number; without a
     # device the library assumes 148)
