@@ -635,7 +635,7 @@ def measure_extras(bn):
     rng = np.random.default_rng(7)
     cases = {"prefill": ([2048] * 16, [2048] * 16),
              "verify": ([int(x) for x in rng.integers(128, 4097, 64)], [5] * 64)}
-    for layer_name in ("8b", "70b", "8b-int8", "8b-int4"):
+    for layer_name in args.mq_layers.split(","):
         for case, (ctx, chunk) in cases.items():
             pw = workloads.make_prefill(layer_name, ctx, chunk, seed=31, device=dev)
             pl = PagedDecodeLayer.from_workload(pw, dev)
@@ -677,18 +677,22 @@ def run_ours(args):
     bn = Bench(args, dev, dist)
     bn.rank = rank
     names = ALL_WORKLOADS if args.workload == "all" else (args.workload,)
+    if args.extras_only:
+        names = ()
     bn.headline = HEADLINE if args.workload == "all" else args.workload
     entries, cpu = {}, None
     wall0 = time.perf_counter()
     for name in names:
         sweep = SPLIT_SWEEP if (name == "long" and args.workload == "all" and args.batch is None) else None
         cuda_core = name in ("8b", "70b") and args.workload == "all" and args.batch is None
-        entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core,
-                                            shared=name == "fp8prefix" and args.batch is None)
+        entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core, shared=name == "fp8prefix")
         cpu = c or cpu
     extras = measure_extras(bn) if not args.no_extras else {}
     wall = time.perf_counter() - wall0
     if rank != 0:
+        return
+    if args.extras_only:
+        print(json.dumps(dict(extras, wall_s=wall, note="secondary measurements only (--extras-only)")))
         return
     h = entries[bn.headline]
     peak, peak_kind = hbm_peak()
@@ -728,6 +732,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the secondary measurements (block copy, host prefix cache, multi-query attention)")
+    ap.add_argument("--extras-only", action="store_true",
+                    help="only the secondary measurements (profiling their kernels)")
+    ap.add_argument("--mq-layers", default="8b,70b,8b-int8,8b-int4",
+                    help="layer shapes (workload names) of the multi-query attention measurements")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

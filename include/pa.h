@@ -139,7 +139,7 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
  * which equals the unsplit result in exact arithmetic.  The combination runs
  * inside pa_decode_attention: the last partition of a (sequence, kv head) to
  * finish merges them.  num_splits == 0 picks S from the batch shape and the
- * current device's SM count.
+ * current device's SM count (152, a GB300's, when no device is visible).
  *
  * pa_decode_resolve_splits returns the S that pa_decode_attention will use for
  * the request (0 asks for the automatic choice); the workspace must hold

@@ -119,11 +119,14 @@ bool encode_cache_map(const void* base, int64_t rows, int d, int box_tok, int dt
     return true;
 }
 
+// The current device's SM count; without a device (host-side planning), a
+// GB300's 152.
 int device_sms() {
+    constexpr int kGb300Sms = 152;
     int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kGb300Sms;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return 148;
+        return kGb300Sms;
     return sms;
 }
 

@@ -225,6 +225,27 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
     return pack_f16x2(__uint_as_float(v << 16), __uint_as_float(v & 0xFFFF0000u));
 }
 
+// Sum, in fp32, of a q row's values as the f16 operand holds them (int8 K
+// tiles carry 1152 + c: each score then carries 1152 times this sum).
+__device__ __forceinline__ float q_row_f16_sum(const __nv_bfloat16* qrow, bool valid) {
+    float sum = 0.f;
+    if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u) {
+            const uint4 v = __ldg(src + u);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t h = bf16x2_to_f16x2(w[k]);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+                sum += f.x + f.y;
+            }
+        }
+    }
+    return sum;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -267,7 +288,10 @@ __device__ __forceinline__ uint32_t f16_unit(uint32_t tile, int r, int u) {
 // swizzled) in place into exact f16 values.  Thread i < NCONV of the
 // converter group; int4 codes: `rd` is the group's read barrier (count
 // NCONV), in phase `rd_parity` for this tile.  Returns false on an abort.
-template <int KVT>
+// BIASED (int8 K tiles): the codes expand to 1152 + c (the decode kernel's
+// trick, two operations per four codes fewer); every score then carries
+// 1152 * (sum of its q row), which the softmax takes off.
+template <int KVT, bool BIASED = false>
 __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, uint32_t rd_parity,
                                             volatile int* abort) {
     const uint32_t raw = tile + PfCfg<KVT>::RAW_OFF;
@@ -309,10 +333,17 @@ __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, 
 #pragma unroll
             for (int c = 0; c < 8; ++c) {   // chunk c: dims 16 c .. 16 c + 15 -> units 2c, 2c + 1
                 uint32_t a0, a1, b0, b1, c0, c1, d0, d1;
-                code4_to_f16x2<KVT>(ch[c].x, a0, a1);
-                code4_to_f16x2<KVT>(ch[c].y, b0, b1);
-                code4_to_f16x2<KVT>(ch[c].z, c0, c1);
-                code4_to_f16x2<KVT>(ch[c].w, d0, d1);
+                if constexpr (BIASED && KVT == KV_INT8) {
+                    s8x4_to_f16x2_biased(ch[c].x, a0, a1);
+                    s8x4_to_f16x2_biased(ch[c].y, b0, b1);
+                    s8x4_to_f16x2_biased(ch[c].z, c0, c1);
+                    s8x4_to_f16x2_biased(ch[c].w, d0, d1);
+                } else {
+                    code4_to_f16x2<KVT>(ch[c].x, a0, a1);
+                    code4_to_f16x2<KVT>(ch[c].y, b0, b1);
+                    code4_to_f16x2<KVT>(ch[c].z, c0, c1);
+                    code4_to_f16x2<KVT>(ch[c].w, d0, d1);
+                }
                 st_shared_v4(f16_unit(tile, r, 2 * c), a0, a1, b0, b1);
                 st_shared_v4(f16_unit(tile, r, 2 * c + 1), c0, c1, d0, d1);
             }
@@ -324,13 +355,13 @@ __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, 
 
 // Converter group (two warps): for each tile j of the ring, wait for its raw
 // codes, expand them, and arrive on conv[stage].  Ends early on an abort.
-template <int KVT, int NS>
+template <int KVT, int NS, bool BIASED = false>
 __device__ __forceinline__ void convert_ring(uint64_t* full, uint64_t* conv, uint64_t* rd, uint32_t ring, int nT,
                                              int i, volatile int* abort) {
     int st = 0, use = 0;
     for (int j = 0; j < nT; ++j) {
         if (!cta_wait(&full[st], use & 1, abort)) return;
-        if (!expand_tile<KVT>(ring + st * TILEB, i, rd, j & 1, abort)) return;
+        if (!expand_tile<KVT, BIASED>(ring + st * TILEB, i, rd, j & 1, abort)) return;
         mbar_arrive(&conv[st]);
         if (++st == NS) {
             st = 0;
@@ -525,7 +556,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const bool is_k = warp < W_VCONV;
         const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
         if (is_k)
-            convert_ring<KVT, KST>(bars.kfull, bars.kconv, &bars.krd, sbase + OFF_K, nT, i, abort);
+            convert_ring<KVT, KST, KVT == KV_INT8>(bars.kfull, bars.kconv, &bars.krd, sbase + OFF_K, nT, i, abort);
         else
             convert_ring<KVT, VST>(bars.vfull, bars.vconv, &bars.vrd, sbase + OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
@@ -623,6 +654,11 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const bool valid_row = tok < C;
         const int qpos = valid_row ? L - C + tok : -1;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+        // a lane quadrant whose 32 rows all lie past the chunk's last query
+        // (short chunks: verify passes) computes nothing: its Q rows are zero,
+        // so its S and P rows are zero and P V leaves its O rows at zero; it
+        // only keeps pace with the barriers the other roles count it in
+        const bool live = t0 + (quad * 32) / G < C;
         {
             // this quarter of the Q row -> tensor memory (bf16 pairs, element
             // 2i in the low half of column i)
@@ -650,6 +686,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this quarter's sum
         // coded caches: O is kept in units of vref, the largest V scale seen
         float vref = 0.f, inv_vref = 0.f;
+        // int8: the offset the biased K codes add to this row's scores
+        const float kbias = KVT == KV_INT8 && live
+                                ? kS8Bias * q_row_f16_sum(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D, valid_row)
+                                : 0.f;
         bool ok = true;
         for (int j = 0; j < nT; ++j) {
             const int s = j & 1;
@@ -671,14 +711,20 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                 mbar_arrive(&bars.sc_empty[slot]);
             }
             if (!(ok = cta_wait(&bars.s_full[s], (j >> 1) & 1, abort))) break;
+            if (!live) {
+                mbar_arrive(&bars.p_full[s]);
+                continue;
+            }
             tc_fence_after();
             float x[NCOL];
             tmem_ld32(tmem + lane_off + s * TN + qc * NCOL, x);
             const int lim = qpos - j * TN - qc * NCOL;   // columns c <= lim are visible to this row
             if constexpr (CODED) {
-                // scores in log2 units (K scale of the column's page), masked after scaling
+                // scores in log2 units (K scale of the column's page; int8: the
+                // biased codes' offset off), masked after scaling
 #pragma unroll
-                for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+                for (int c = 0; c < NCOL; ++c)
+                    x[c] = (c <= lim) ? fmaf(x[c], sl2k[c / BS], -kbias * sl2k[c / BS]) : -INFINITY;
             } else if (lim < NCOL - 1) {
 #pragma unroll
                 for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
@@ -751,7 +797,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
             tc_fence_before();
             mbar_arrive(&bars.p_full[s]);
         }
-        if (ok && cta_wait(&bars.o_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, abort)) {
+        if (ok && live && cta_wait(&bars.o_done[(nT - 1) & 1], ((nT - 1) >> 1) & 1, abort)) {
             tc_fence_after();
             bars.red_l[qc][r] = l;
             mbar_arrive(&bars.pair[quad]);
@@ -898,7 +944,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const bool is_k = warp < W_VCONV;
         const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
         if (is_k)
-            convert_ring<KVT, 2>(bars.kfull, bars.kconv, &bars.krd, sbase + P2_OFF_K, nT, i, abort);
+            convert_ring<KVT, 2, KVT == KV_INT8>(bars.kfull, bars.kconv, &bars.krd, sbase + P2_OFF_K, nT, i, abort);
         else
             convert_ring<KVT, 2>(bars.vfull, bars.vconv, &bars.vrd, sbase + P2_OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
@@ -987,12 +1033,15 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const int r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int tok[2], qpos[2];
-        bool valid_row[2];
+        bool valid_row[2], live[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             tok[t] = t0 + t * T + r / G;
             valid_row[t] = tok[t] < C;
             qpos[t] = valid_row[t] ? L - C + tok[t] : -1;
+            // a lane quadrant with no row inside the chunk only keeps pace with
+            // the barriers (its Q, S, P and O rows are zero)
+            live[t] = t0 + t * T + (quad * 32) / G < C;
         }
         const int g = r % G;
 #pragma unroll
@@ -1021,6 +1070,15 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         // coded caches: O_t is kept in units of vref[t], the largest V scale seen
         float vref[2] = {0.f, 0.f}, inv_vref[2] = {0.f, 0.f};
+        // int8: the offset the biased K codes add to each tile's row scores
+        float kbias[2] = {0.f, 0.f};
+        if (KVT == KV_INT8) {
+#pragma unroll
+            for (int t = 0; t < 2; ++t)
+                if (live[t])
+                    kbias[t] = kS8Bias * q_row_f16_sum(a.q + ((int64_t)(qs0 + tok[t]) * a.Hq + h * G + g) * D,
+                                                       valid_row[t]);
+        }
         bool ok = true;
         for (int j = 0; ok && j < nT; ++j) {
             // coded caches: this K/V tile's page scales, shared by both query tiles
@@ -1043,14 +1101,20 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 if (!(ok = cta_wait(&bars.s_full[t], j & 1, abort))) break;
+                if (!live[t]) {
+                    mbar_arrive(&bars.p_full[t]);
+                    continue;
+                }
                 tc_fence_after();
                 float x[NCOL];
                 tmem_ld32(tmem + lane_off + t * TN + qc * NCOL, x);
                 const int lim = qpos[t] - j * TN - qc * NCOL;
                 if constexpr (CODED) {
-                    // scores in log2 units (K scale of the column's page), masked after scaling
+                    // scores in log2 units (K scale of the column's page; int8:
+                    // the biased codes' offset off), masked after scaling
 #pragma unroll
-                    for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+                    for (int c = 0; c < NCOL; ++c)
+                        x[c] = (c <= lim) ? fmaf(x[c], sl2k[c / BS], -kbias[t] * sl2k[c / BS]) : -INFINITY;
                 } else if (lim < NCOL - 1) {
 #pragma unroll
                     for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
@@ -1120,6 +1184,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         }
 #pragma unroll 1
         for (int t = 0; ok && t < 2; ++t) {
+            if (!live[t]) continue;
             if (!(ok = cta_wait(&bars.o_done[t], (nT - 1) & 1, abort))) break;
             tc_fence_after();
             bars.red_l[t][qc][r] = l[t];

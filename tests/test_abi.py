@@ -113,6 +113,6 @@ def test_split_planning():
         assert P * hpc <= 256 + hpc - 1
     # few (sequence, head set) groups with long tables: one wave of long
     # partitions (the device's SM count decides the exact number; without a
-    # device the library assumes 148)
+    # device the library plans for a GB300's 152 SMs)
     S = pa.pa_decode_resolve_splits(4, 8, 8192, 0)
     assert 4 * 4 * S <= 3 * 152 and S >= 16 and -(-8192 // S) * 2 >= 256
