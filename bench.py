@@ -684,6 +684,8 @@ def run_ours(args):
     wall0 = time.perf_counter()
     for name in names:
         sweep = SPLIT_SWEEP if (name == "long" and args.workload == "all" and args.batch is None) else None
+        if args.sweep_splits:
+            sweep = tuple(int(x) for x in args.sweep_splits.split(","))
         cuda_core = name in ("8b", "70b") and args.workload == "all" and args.batch is None
         entries[name], c = measure_workload(bn, name, world, local, sweep, cuda_core, shared=name == "fp8prefix")
         cpu = c or cpu
@@ -734,6 +736,8 @@ def main():
                     help="skip the secondary measurements (block copy, host prefix cache, multi-query attention)")
     ap.add_argument("--extras-only", action="store_true",
                     help="only the secondary measurements (profiling their kernels)")
+    ap.add_argument("--sweep-splits", default="",
+                    help="comma-separated split counts to time (each parity-checked) on every workload run")
     ap.add_argument("--mq-layers", default="8b,70b,8b-int8,8b-int4",
                     help="layer shapes (workload names) of the multi-query attention measurements")
     args = ap.parse_args()

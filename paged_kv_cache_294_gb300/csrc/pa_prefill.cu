@@ -944,7 +944,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const bool is_k = warp < W_VCONV;
         const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
         if (is_k)
-            convert_ring<KVT, 2, KVT == KV_INT8>(bars.kfull, bars.kconv, &bars.krd, sbase + P2_OFF_K, nT, i, abort);
+            convert_ring<KVT, 2>(bars.kfull, bars.kconv, &bars.krd, sbase + P2_OFF_K, nT, i, abort);
         else
             convert_ring<KVT, 2>(bars.vfull, bars.vconv, &bars.vrd, sbase + P2_OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
@@ -1033,15 +1033,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const int r = quad * 32 + lane;
         const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
         int tok[2], qpos[2];
-        bool valid_row[2], live[2];
+        bool valid_row[2];
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
             tok[t] = t0 + t * T + r / G;
             valid_row[t] = tok[t] < C;
             qpos[t] = valid_row[t] ? L - C + tok[t] : -1;
-            // a lane quadrant with no row inside the chunk only keeps pace with
-            // the barriers (its Q, S, P and O rows are zero)
-            live[t] = t0 + t * T + (quad * 32) / G < C;
         }
         const int g = r % G;
 #pragma unroll
@@ -1070,15 +1067,6 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         // coded caches: O_t is kept in units of vref[t], the largest V scale seen
         float vref[2] = {0.f, 0.f}, inv_vref[2] = {0.f, 0.f};
-        // int8: the offset the biased K codes add to each tile's row scores
-        float kbias[2] = {0.f, 0.f};
-        if (KVT == KV_INT8) {
-#pragma unroll
-            for (int t = 0; t < 2; ++t)
-                if (live[t])
-                    kbias[t] = kS8Bias * q_row_f16_sum(a.q + ((int64_t)(qs0 + tok[t]) * a.Hq + h * G + g) * D,
-                                                       valid_row[t]);
-        }
         bool ok = true;
         for (int j = 0; ok && j < nT; ++j) {
             // coded caches: this K/V tile's page scales, shared by both query tiles
@@ -1101,20 +1089,14 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
 #pragma unroll 1
             for (int t = 0; t < 2; ++t) {
                 if (!(ok = cta_wait(&bars.s_full[t], j & 1, abort))) break;
-                if (!live[t]) {
-                    mbar_arrive(&bars.p_full[t]);
-                    continue;
-                }
                 tc_fence_after();
                 float x[NCOL];
                 tmem_ld32(tmem + lane_off + t * TN + qc * NCOL, x);
                 const int lim = qpos[t] - j * TN - qc * NCOL;
                 if constexpr (CODED) {
-                    // scores in log2 units (K scale of the column's page; int8:
-                    // the biased codes' offset off), masked after scaling
+                    // scores in log2 units (K scale of the column's page), masked after scaling
 #pragma unroll
-                    for (int c = 0; c < NCOL; ++c)
-                        x[c] = (c <= lim) ? fmaf(x[c], sl2k[c / BS], -kbias[t] * sl2k[c / BS]) : -INFINITY;
+                    for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
                 } else if (lim < NCOL - 1) {
 #pragma unroll
                     for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
@@ -1184,7 +1166,6 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         }
 #pragma unroll 1
         for (int t = 0; ok && t < 2; ++t) {
-            if (!live[t]) continue;
             if (!(ok = cta_wait(&bars.o_done[t], (nT - 1) & 1, abort))) break;
             tc_fence_after();
             bars.red_l[t][qc][r] = l[t];
