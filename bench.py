@@ -454,6 +454,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
 
     # parity before timing: the timed launch (pa_decode_step, this split plan)
     # against the oracle on every output of every sequence
+    layer.out.fill_(float("nan"))   # a row the launch does not write fails the check
     pa.pa_get_device_error(clear=True)
     layer.fused_step(num_splits=args.splits)
     torch.cuda.synchronize()
@@ -506,6 +507,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
         rows = []
         with ClockSampler(local) as sclocks:
             for Sx in sweep:
+                layer.out.fill_(float("nan"))   # a row the launch does not write fails the check
                 pa.pa_get_device_error(clear=True)
                 layer.fused_step(num_splits=Sx)
                 torch.cuda.synchronize()
@@ -526,6 +528,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
         # of the tensor-core MMAs: parity first, then the same timings
         os.environ["PA_DECODE_FMA"] = "1"
         try:
+            layer.out.fill_(float("nan"))   # a row the launch does not write fails the check
             pa.pa_get_device_error(clear=True)
             layer.fused_step(num_splits=args.splits)
             torch.cuda.synchronize()
@@ -552,6 +555,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
         # share are read once per chunk of 8 / G of them (plan: pa_share_plan)
         plan = layer.plan_sharing()
         pa.pa_get_device_error(clear=True)
+        layer.out.fill_(float("nan"))   # a row the launch does not write fails the check
         layer.shared_step(num_splits=args.splits)
         torch.cuda.synchronize()
         par = parity_full(w, layer.out, ref, pa.pa_get_device_error())

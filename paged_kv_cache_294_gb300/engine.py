@@ -171,6 +171,7 @@ class PagedDecodeLayer:
         else:
             self.k_scale = self.v_scale = None
         self.workspace: Optional[torch.Tensor] = None
+        self._ws_key = None   # layout the workspace last served (its counters are zero for it)
 
     # ---------------------------------------------------------------- set-up
     def set_batch(self, block_tables: np.ndarray, seq_lens: np.ndarray):
@@ -183,12 +184,20 @@ class PagedDecodeLayer:
         self.step_slots_host = pa_step_slots(self.tables_host, self.lens_host, self.bs)
         self.step_slots = torch.from_numpy(self.step_slots_host).to(self.device)
 
+    def _workspace_for(self, key, need: int) -> torch.Tensor:
+        """A zero-filled workspace of at least `need` bytes for the layout `key`.
+        Calls leave the counters at zero, but their place follows from the
+        layout: a workspace that served another layout is zero-filled again."""
+        if self.workspace is None or self.workspace.numel() < need:
+            self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
+        elif key != self._ws_key:
+            self.workspace.zero_()
+        self._ws_key = key
+        return self.workspace
+
     def ensure_workspace(self, num_splits: int = 0) -> torch.Tensor:
         need = pa_decode_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits)
-        if self.workspace is None or self.workspace.numel() < need:
-            # zero-filled: the split-K counters must start at zero (calls keep them there)
-            self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
-        return self.workspace
+        return self._workspace_for(("plain", self.num_splits(num_splits), need), need)
 
     def num_splits(self, num_splits: int = 0) -> int:
         return pa_decode_resolve_splits(self.B, self.Hkv, self.M, num_splits)
@@ -260,12 +269,9 @@ class PagedDecodeLayer:
         return plan
 
     def ensure_shared_workspace(self, num_splits: int = 0) -> torch.Tensor:
-        need = pa_decode_shared_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits,
-                                                self.share_plan["max_chunk_blocks"])
-        if self.workspace is None or self.workspace.numel() < need:
-            # zero-filled: the split-K counters must start at zero (calls keep them there)
-            self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
-        return self.workspace
+        mcb = self.share_plan["max_chunk_blocks"]
+        need = pa_decode_shared_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits, mcb)
+        return self._workspace_for(("shared", self.num_splits(num_splits), mcb, need), need)
 
     def shared_step(self, append: bool = True, out=None, num_splits: int = 0, stream=None):
         """The decode step (or attention alone) through pa_decode_step_shared with

@@ -279,3 +279,23 @@ def test_coded_blocks_with_zero_scales(kv):
     for S in (0, 2):
         layer, _ = check(w, S)
     assert torch.all(layer.out[1].float() == 0)
+
+
+def test_split_count_changes_on_one_workspace():
+    """One layer, one workspace, the split count going down and up again: the
+    merge counters' place moves with the layout, so the engine zero-fills the
+    workspace whenever the layout changes (over old partials the counters
+    would be garbage and the merges would not run).  Every call must write
+    every output (poisoned with NaN first)."""
+    w = workloads.make("long", B=2, seq_len=9000)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    st, ref = oracle_out(w, tables=layer.tables_host)
+    for S in (16, 1, 2, 3, 64, 5, 0):
+        layer.out.fill_(float("nan"))
+        pa.pa_get_device_error(clear=True)
+        layer.fused_step(num_splits=S)
+        torch.cuda.synchronize()
+        assert pa.pa_get_device_error() == 0, S
+        got = layer.out.float().cpu().numpy().astype(np.float64)
+        assert np.all(np.isfinite(got)), S
+        assert excess(got, ref, tol(w)) <= 1.0, (S, worst(got, ref, tol(w)))
