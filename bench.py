@@ -247,11 +247,40 @@ def cpu_oracle_baseline(w, tables, budget_s=10.0, threads=None):
         total += time.perf_counter() - t0
         reps += 1
     per_step = total / reps
+    # the same step on one thread, once (a few seconds)
+    t0 = time.perf_counter()
+    st.append()
+    st.decode(threads=1)
+    one = time.perf_counter() - t0
     return {"value": sample_bytes(w, seqs) / per_step / 1e9, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d of %d sequences (%d tokens; the same sample as the reference arm), fp64 C oracle "
                       "append+decode, %d reps, %.1f s" % (len(seqs), w.B, int(np.sum(np.asarray(w.seq_lens)[seqs])),
                                                           reps, total),
-            "seq_steps_per_s": len(seqs) / per_step}
+            "seq_steps_per_s": len(seqs) / per_step,
+            "one_thread": {"value": sample_bytes(w, seqs) / one / 1e9, "unit": UNIT, "reps": 1},
+            "cpu": cpu_model()}
+
+
+def cpu_model():
+    """The host CPU's name as /proc/cpuinfo gives it (x86 'model name'; Arm
+    implementer / part codes), else the platform's."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                k = k.strip()
+                if k and k not in fields:
+                    fields[k] = v.strip()
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return "%s, implementer %s, part %s" % (platform.machine(), fields.get("CPU implementer", "?"),
+                                                 fields["CPU part"])
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
@@ -320,8 +349,14 @@ class Bench:
             fn()
             ev[i][1].record(self.stream)
         torch.cuda.synchronize()
-        t = sum(x.elapsed_time(y) for x, y in ev) / 1e3
+        self.last_steps_ms = [x.elapsed_time(y) for x, y in ev]
+        t = sum(self.last_steps_ms) / 1e3
         return max_over_ranks(t, self.dist, self.dev)
+
+    def step_stats(self):
+        """Median and 90th percentile of the last timed() call's steps (µs, this rank)."""
+        v = np.asarray(self.last_steps_ms) * 1e3
+        return {"median_us": float(np.median(v)), "p90_us": float(np.percentile(v, 90)), "steps": int(v.size)}
 
 
 def parity_bound(ref, tol):
@@ -471,6 +506,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
     # rewrites identical bytes (bf16) and keeps a coded block's scale
     with ClockSampler(local) as clocks:
         t_step = bn.timed(lambda: layer.fused_step(num_splits=args.splits), K)
+        step_stats = bn.step_stats()
         t_two = bn.timed(lambda: (layer.append_step(), layer.decode(num_splits=args.splits)), K)
         t_attn = bn.timed(lambda: layer.decode(num_splits=args.splits), K)
         e2e, e2e_serial = e2e_measure(bn, layer, K, world, alg)
@@ -481,7 +517,7 @@ def measure_workload(bn, name, world, local, sweep=None, cuda_core=False, shared
     traffic = ncu_traffic(name, S) if args.batch is None else None
     entry = {
         "value": round(value, 2), "unit": UNIT, "ms_per_step": 1e3 * t_step / K, "us_per_step": 1e6 * t_step / K,
-        "seq_steps_per_s": world * w.B * K / t_step,
+        "seq_steps_per_s": world * w.B * K / t_step, "step_time": step_stats,
         "config": {"workload": name if args.batch is None else "%s-B%d" % (name, w.B), "desc": w.desc,
                    "batch": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "head_dim": w.d, "block_size": w.bs, "kv": w.kv,
                    "num_splits": S, "tokens": int(np.sum(w.seq_lens)),
