@@ -188,10 +188,16 @@ class PagedDecodeLayer:
         """A zero-filled workspace of at least `need` bytes for the layout `key`.
         Calls leave the counters at zero, but their place follows from the
         layout: a workspace that served another layout is zero-filled again."""
+        filled = False
         if self.workspace is None or self.workspace.numel() < need:
             self.workspace = torch.zeros(max(need, 256), dtype=torch.uint8, device=self.device)
+            filled = True
         elif key != self._ws_key:
             self.workspace.zero_()
+            filled = True
+        if filled and self.workspace.is_cuda:
+            # the fill ran on torch's current stream; a call may come on another
+            torch.cuda.current_stream(self.workspace.device).synchronize()
         self._ws_key = key
         return self.workspace
 
