@@ -299,3 +299,30 @@ def test_split_count_changes_on_one_workspace():
         got = layer.out.float().cpu().numpy().astype(np.float64)
         assert np.all(np.isfinite(got)), S
         assert excess(got, ref, tol(w)) <= 1.0, (S, worst(got, ref, tol(w)))
+
+
+@pytest.mark.parametrize("Hq,Hkv,kv", [(64, 8, "bf16"), (32, 8, "bf16"), (8, 8, "fp8")])
+def test_max_split_count_merges_512_partials(Hq, Hkv, kv):
+    """The largest split count (512): 8192-token sequences of 512 blocks, one
+    block per partition, so the merge reads 512 partials per row (the most
+    its shared-memory weights hold: 16 rows x 512 at G = 8)."""
+    w = _synthetic(2, Hq, Hkv, 128, 16, [8192, 8000], kv, seed=Hq + Hkv)
+    assert pa.pa_decode_resolve_splits(2, Hkv, 512, 512) == 512
+    check(w, 512)
+
+
+@pytest.mark.parametrize("S", [0, 3])
+def test_all_sequences_empty(S):
+    """Every seq_len 0: every output row is zero, nothing is read from the
+    cache, and the merge counters stay at zero."""
+    w = _synthetic(5, 8, 2, 128, 16, [0, 0, 0, 0, 0], "bf16", seed=1)
+    layer = PagedDecodeLayer.from_workload(w, "cuda")
+    ws = layer.ensure_workspace(S)
+    layer.out.fill_(float("nan"))
+    pa.pa_get_device_error(clear=True)
+    layer.decode(num_splits=S)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert torch.count_nonzero(layer.out).item() == 0
+    need = pa.pa_decode_workspace_bytes(layer.B, layer.Hq, layer.Hkv, layer.d, layer.M, S)
+    assert int(ws[:need].view(torch.int32)[-((layer.B * layer.Hkv + 63) // 64 * 64):].abs().sum()) == 0
