@@ -1094,9 +1094,15 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                 tmem_ld32(tmem + lane_off + t * TN + qc * NCOL, x);
                 const int lim = qpos[t] - j * TN - qc * NCOL;
                 if constexpr (CODED) {
-                    // scores in log2 units (K scale of the column's page), masked after scaling
+                    // scores in log2 units (K scale of the column's page), masked after
+                    // scaling; only a tile the causal limit cuts pays for the mask
+                    if (lim < NCOL - 1) {
 #pragma unroll
-                    for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+                        for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] * sl2k[c / BS] : -INFINITY;
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < NCOL; ++c) x[c] *= sl2k[c / BS];
+                    }
                 } else if (lim < NCOL - 1) {
 #pragma unroll
                     for (int c = 0; c < NCOL; ++c) x[c] = (c <= lim) ? x[c] : -INFINITY;
