@@ -117,25 +117,31 @@ template <int D, int BS, int KVT, int HPC>
 struct WarpAcc {
     static constexpr bool FP8 = KVT != KV_BF16;
     static constexpr int CHS = Cfg<D, BS, KVT, HPC>::CHS;
-    float m, l;
+    // Lane (g, c) = (lane / 4, lane % 4) keeps the softmax state of query
+    // heads 2c and 2c + 1 (index e), the columns its O fragment holds: m[e] is
+    // the same in the 8 lanes of column c, l[e] and psi[e] sum this lane's
+    // tokens only (publish() adds the 8 lanes up).
+    float m[2], l[2];
     float o[D / 16][4];
-    uint32_t qa[D / 16][2];
-    float qbias;   // int8 cache: 1152 * sum of this lane's head's f16 q (see the QK product)
+    uint32_t qa[D / 16][2];   // q of head g as the Q.K^T B operand
+    float qbias[2];   // int8 cache: 1152 * sum of head 2c + e's f16 q (see the QK product)
     // coded caches: O is kept in units of vref (the largest V scale so far) and
-    // psi sums the f16 probabilities P' = P * vsc / vref of this lane's head
-    // (see the P.V product); publish() turns O back into values
-    float vref, inv_vref, psi;
+    // psi sums the f16 probabilities P' = P * vsc / vref of each head (see the
+    // P.V product); publish() turns O back into values
+    float vref, inv_vref, psi[2];
 
     __device__ __forceinline__ void reset() {
-        m = -INFINITY;
-        l = 0.f;
-        vref = inv_vref = psi = 0.f;
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+        vref = inv_vref = psi[0] = psi[1] = 0.f;
 #pragma unroll
         for (int i = 0; i < D / 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     }
 
-    // q of query head h*G + g as the MMA A operand; rows g >= G stay zero.
-    // `qrow` is a generic pointer (global or shared) to that head's bf16 row.
+    // q of query head h*G + g as the Q.K^T B operand (column g; the k order
+    // within a 16-deep step is that of the K operand's codes); columns g >= G
+    // stay zero.  `qrow` is a generic pointer (global or shared) to that
+    // head's bf16 row.
     __device__ __forceinline__ void load_q(const uint16_t* qrow, bool valid, int c) {
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -161,7 +167,7 @@ struct WarpAcc {
                 qa[ks][1] = *reinterpret_cast<const uint32_t*>(qrow + ks * 16 + 2 * c + 8);
             }
         }
-        qbias = 0.f;
+        qbias[0] = qbias[1] = 0.f;
         if (KVT == KV_INT8) {
             // the K operand carries 1152 + c per element: the scores carry
             // 1152 * sum_k q_k on top, summed here over the same f16 values
@@ -176,7 +182,9 @@ struct WarpAcc {
             }
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-            qbias = kS8Bias * sum;
+            // lanes 8c and 8c + 4 hold heads 2c and 2c + 1
+            qbias[0] = kS8Bias * __shfl_sync(0xffffffffu, sum, 8 * c);
+            qbias[1] = kS8Bias * __shfl_sync(0xffffffffu, sum, 8 * c + 4);
         }
     }
 
@@ -188,105 +196,118 @@ struct WarpAcc {
         const int g = lane >> 2, c = lane & 3;
         const int mi = lane >> 3, r = lane & 7;
 
-        // ------------------------------------------------ S^T = Q K^T
-        float acc[C::NT][4];
+        // ------------------------------------------------ S^T = K Q^T
+        // Tokens are the MMA's M (16 per m-tile) and the query heads its N:
+        // acc[kk] holds tokens 16kk + g and 16kk + g + 8 (e >> 1) of heads 2c
+        // and 2c + 1 (e & 1).  A 16-token page takes D / 16 MMAs.
+        float acc[C::KT][4];
 #pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+        for (int kk = 0; kk < C::KT; ++kk) acc[kk][0] = acc[kk][1] = acc[kk][2] = acc[kk][3] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < C::KS; ++ks) {
-            const uint32_t A[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
             if (KVT == KV_INT4) {
-                // one 32-bit word = 8 codes of chunk ks / 2 feeds steps ks and ks + 1
+                // one 32-bit word = 8 codes of chunk ks / 2 of a token feeds steps ks and ks + 1
                 if (ks & 1) continue;
-                const uint32_t A1[4] = {qa[ks + 1][0], 0u, qa[ks + 1][1], 0u};
 #pragma unroll
-                for (int nt = 0; nt < C::NT; ++nt) {
-                    const uint32_t w = ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, nt * 8 + g, (ks >> 1) * 16 + 4 * c));
-                    uint32_t f[4];
-                    nib8_to_f16x2(w, f);
-                    mma_f16(acc[nt], A, f[0], f[1]);
-                    mma_f16(acc[nt], A1, f[2], f[3]);
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    const int t = kk * 16 + g;
+                    uint32_t f0[4], f1[4];
+                    nib8_to_f16x2(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t, (ks >> 1) * 16 + 4 * c)), f0);
+                    nib8_to_f16x2(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t + 8, (ks >> 1) * 16 + 4 * c)), f1);
+                    const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
+                    const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
+                    mma_f16(acc[kk], A0, qa[ks][0], qa[ks][1]);
+                    mma_f16(acc[kk], A1, qa[ks + 1][0], qa[ks + 1][1]);
                 }
             } else if (FP8) {
 #pragma unroll
-                for (int nt = 0; nt < C::NT; ++nt) {
-                    const int t = nt * 8 + g;
-                    const uint32_t w = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
-                    uint32_t b0, b1;
-                    if (KVT == KV_INT8)
-                        s8x4_to_f16x2_biased(w, b0, b1);   // qbias comes off each score below
-                    else
-                        code4_to_f16x2<KVT>(w, b0, b1);
-                    mma_f16(acc[nt], A, b0, b1);
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    const int t = kk * 16 + g;
+                    const uint32_t w0 = ld_shared_u32(swz128(kt, t, ks * 16 + 4 * c));
+                    const uint32_t w1 = ld_shared_u32(swz128(kt, t + 8, ks * 16 + 4 * c));
+                    uint32_t A[4];
+                    if (KVT == KV_INT8) {   // qbias comes off each score below
+                        s8x4_to_f16x2_biased(w0, A[0], A[2]);
+                        s8x4_to_f16x2_biased(w1, A[1], A[3]);
+                    } else {
+                        code4_to_f16x2<KVT>(w0, A[0], A[2]);
+                        code4_to_f16x2<KVT>(w1, A[1], A[3]);
+                    }
+                    mma_f16(acc[kk], A, qa[ks][0], qa[ks][1]);
                 }
             } else {
-                const int jg = 2 * ks + (mi & 1);  // 16-byte unit along the row
+                // matrices: tokens 0-7 / 8-15 (mi & 1) x dims 8 (mi >> 1) .. of the step
+                const int jg = 2 * ks + (mi >> 1);  // 16-byte unit along the row
                 const uint32_t ktile = kt + (jg >> 3) * C::CHS;
 #pragma unroll
-                for (int p = 0; p < C::NT / 2; ++p) {
-                    const int t = (2 * p + (mi >> 1)) * 8 + r;
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(swz128(ktile, t, (jg & 7) * 16), r0, r1, r2, r3);
-                    mma_bf16(acc[2 * p], A, r0, r1);
-                    mma_bf16(acc[2 * p + 1], A, r2, r3);
+                for (int kk = 0; kk < C::KT; ++kk) {
+                    const int t = kk * 16 + (mi & 1) * 8 + r;
+                    uint32_t A[4];
+                    ldsm_x4(swz128(ktile, t, (jg & 7) * 16), A[0], A[1], A[2], A[3]);
+                    mma_bf16(acc[kk], A, qa[ks][0], qa[ks][1]);
                 }
             }
         }
 
         // ------------------------------------------------ online softmax
-        float sc[C::NT][2];
-        float mx = -INFINITY;
-        const float sb = -qbias * sl2;   // 0 but for the int8 cache
+        float sc[C::KT][4];
+        float mx[2] = {-INFINITY, -INFINITY};
+        const float sb[2] = {-qbias[0] * sl2, -qbias[1] * sl2};   // 0 but for the int8 cache
 #pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
+        for (int kk = 0; kk < C::KT; ++kk) {
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int tok = nt * 8 + 2 * c + e;
-                const float v = tok < valid ? fmaf(acc[nt][e], sl2, sb) : -INFINITY;
-                sc[nt][e] = v;
-                mx = fmaxf(mx, v);
+            for (int e = 0; e < 4; ++e) {
+                const int tok = kk * 16 + g + 8 * (e >> 1);
+                const float v = tok < valid ? fmaf(acc[kk][e], sl2, sb[e & 1]) : -INFINITY;
+                sc[kk][e] = v;
+                mx[e & 1] = fmaxf(mx[e & 1], v);
             }
         }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         // Lazy rescale: m is a reference point, not the running max.  It moves
         // (and O and l are rescaled) only when a score exceeds it by more than
         // 2^8, so that the probabilities 2^(s - m) stay below 256 (exact range
         // for the f16 / bf16 operands) and the O rescale is skipped on almost
         // every page.  The result is the same: O / l with l = sum 2^(s - m).
-        const bool grow = mx > m + 8.f;   // m == -inf: any finite page maximum
-        if (__any_sync(0xffffffffu, grow)) {
-            const float m_new = grow ? mx : m;
-            const float alpha = m_new == m ? 1.f : exp2f(m - m_new);   // m == -inf: 0
-            l *= alpha;
-            psi *= alpha;
-            m = m_new;
-            // accumulator columns are query heads 2c and 2c+1
-            const float al0 = __shfl_sync(0xffffffffu, alpha, 8 * c);
-            const float al1 = __shfl_sync(0xffffffffu, alpha, 8 * c + 4);
+        // Each lane tests its own scores (m == -inf: any finite one); only on
+        // a page where one passes does the warp form the column maxima, which
+        // the 8 lanes of a column then share as their new m.
+        if (__any_sync(0xffffffffu, mx[0] > m[0] + 8.f || mx[1] > m[1] + 8.f)) {
 #pragma unroll
-            for (int mt = 0; mt < C::MT; ++mt) {
-                o[mt][0] *= al0;
-                o[mt][1] *= al1;
-                o[mt][2] *= al0;
-                o[mt][3] *= al1;
+            for (int x = 4; x < 32; x <<= 1) {
+                mx[0] = fmaxf(mx[0], __shfl_xor_sync(0xffffffffu, mx[0], x));
+                mx[1] = fmaxf(mx[1], __shfl_xor_sync(0xffffffffu, mx[1], x));
             }
-        }
-        const float m_use = m == -INFINITY ? 0.f : m;
-        float psum = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < C::NT; ++nt) {
+            float al[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-                sc[nt][e] = ex2_approx(sc[nt][e] - m_use);
+                const float m_new = mx[e] > m[e] + 8.f ? mx[e] : m[e];
+                al[e] = m_new == m[e] ? 1.f : exp2f(m[e] - m_new);   // m == -inf: 0
+                l[e] *= al[e];
+                psi[e] *= al[e];
+                m[e] = m_new;
+            }
+            // accumulator columns are query heads 2c and 2c+1
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                o[mt][0] *= al[0];
+                o[mt][1] *= al[1];
+                o[mt][2] *= al[0];
+                o[mt][3] *= al[1];
+            }
+        }
+        const float m_use[2] = {m[0] == -INFINITY ? 0.f : m[0], m[1] == -INFINITY ? 0.f : m[1]};
+#pragma unroll
+        for (int kk = 0; kk < C::KT; ++kk) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sc[kk][e] = ex2_approx(sc[kk][e] - m_use[e & 1]);
                 // bf16 cache: l sums the probabilities as the P.V product sees
                 // them (bf16), so the output is a convex combination of V rows
                 // whose weights carry the rounding
-                if (!FP8) sc[nt][e] = __bfloat162float(__float2bfloat16_rn(sc[nt][e]));
-                psum += sc[nt][e];
+                if (!FP8) sc[kk][e] = __bfloat162float(__float2bfloat16_rn(sc[kk][e]));
+                l[e & 1] += sc[kk][e];
             }
         }
-        l += psum;
 
         // rows past the sequence end hold stale bytes: zero them so that
         // 0-probability x non-finite garbage cannot reach the accumulator
@@ -303,6 +324,8 @@ struct WarpAcc {
         }
 
         // ------------------------------------------------ O^T += V^T P^T
+        // The B operand of k-step kk (tokens 16kk .. 16kk + 15) is P^T: the
+        // (token, head) 8x8 blocks of acc[kk] transposed in registers.
         uint32_t pq[C::KT][2];   // coded caches: P' = P * vsc / vref as f16
         if (FP8) {
             // O is kept in units of vref: a page with a larger V scale rescales
@@ -311,20 +334,24 @@ struct WarpAcc {
                 const float rs = vref / vsc;   // 0 on the first page
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) o[mt][0] *= rs, o[mt][1] *= rs, o[mt][2] *= rs, o[mt][3] *= rs;
-                psi *= rs;
+                psi[0] *= rs;
+                psi[1] *= rs;
                 vref = vsc;
                 inv_vref = 1.f / vsc;
             }
             const float ratio = vsc * inv_vref;   // 0 while every V scale seen is 0
 #pragma unroll
             for (int kk = 0; kk < C::KT; ++kk) {
-                pq[kk][0] = pack_f16x2(sc[2 * kk][0] * ratio, sc[2 * kk][1] * ratio);
-                pq[kk][1] = pack_f16x2(sc[2 * kk + 1][0] * ratio, sc[2 * kk + 1][1] * ratio);
+                const uint32_t lo = pack_f16x2(sc[kk][0] * ratio, sc[kk][1] * ratio);   // token 16kk + g
+                const uint32_t hi = pack_f16x2(sc[kk][2] * ratio, sc[kk][3] * ratio);   // token 16kk + g + 8
                 if (KVT == KV_INT8 || KVT == KV_INT4) {   // the integer codes enter P.V with an offset
-                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&pq[kk][0]));
-                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&pq[kk][1]));
-                    psi += (a0.x + a0.y) + (a1.x + a1.y);
+                    const float2 a0 = __half22float2(*reinterpret_cast<const __half2*>(&lo));
+                    const float2 a1 = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+                    psi[0] += a0.x + a1.x;
+                    psi[1] += a0.y + a1.y;
                 }
+                pq[kk][0] = movm_t(lo);
+                pq[kk][1] = movm_t(hi);
             }
         }
         if (KVT == KV_INT4) {
@@ -388,8 +415,8 @@ struct WarpAcc {
             uint32_t pb[C::KT][2];
 #pragma unroll
             for (int kk = 0; kk < C::KT; ++kk) {
-                pb[kk][0] = pack_bf16x2(sc[2 * kk][0], sc[2 * kk][1]);
-                pb[kk][1] = pack_bf16x2(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+                pb[kk][0] = movm_t(pack_bf16x2(sc[kk][0], sc[kk][1]));
+                pb[kk][1] = movm_t(pack_bf16x2(sc[kk][2], sc[kk][3]));
             }
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
@@ -409,15 +436,22 @@ struct WarpAcc {
 
     // Publish this warp's state for the item-level combine.
     __device__ __forceinline__ void publish(float* cm, float* cl, float* co, int warp, int lane) {
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        // the 8 lanes of column c (lane bits 2-4) hold heads 2c and 2c + 1
+#pragma unroll
+        for (int x = 4; x < 32; x <<= 1) {
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], x);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], x);
+        }
         const int g = lane >> 2, c = lane & 3, n = lane >> 2;
         if (FP8) {
             // back from units of vref; the integer codes' offsets (times the sum
             // of the probabilities they met) come off, int4's odd dims were x16
-            psi += __shfl_xor_sync(0xffffffffu, psi, 1);
-            psi += __shfl_xor_sync(0xffffffffu, psi, 2);
-            const float ps0 = __shfl_sync(0xffffffffu, psi, 8 * c), ps1 = __shfl_sync(0xffffffffu, psi, 8 * c + 4);
+#pragma unroll
+            for (int x = 4; x < 32; x <<= 1) {
+                psi[0] += __shfl_xor_sync(0xffffffffu, psi[0], x);
+                psi[1] += __shfl_xor_sync(0xffffffffu, psi[1], x);
+            }
+            const float ps0 = psi[0], ps1 = psi[1];
 #pragma unroll
             for (int mt = 0; mt < D / 16; ++mt) {
 #pragma unroll
@@ -433,9 +467,11 @@ struct WarpAcc {
                 }
             }
         }
-        if (c == 0) {
-            cm[warp * 8 + g] = m;
-            cl[warp * 8 + g] = l;
+        if (g == 0) {
+            cm[warp * 8 + 2 * c] = m[0];
+            cm[warp * 8 + 2 * c + 1] = m[1];
+            cl[warp * 8 + 2 * c] = l[0];
+            cl[warp * 8 + 2 * c + 1] = l[1];
         }
 #pragma unroll
         for (int mt = 0; mt < D / 16; ++mt) {
@@ -1284,7 +1320,7 @@ __global__ void __launch_bounds__(Cfg<D, BS, KVT, HPC>::NTHREADS, 3)
             const uint32_t qs_head = sbase + BAR_OFF + 2 * NSTAGE * 8 + hh * Acc::QS_BYTES;
             st.load_q(a.q + ((int64_t)b * a.Hq + h * GF) * D, qs_head, wi == 0, 1 + hh, WPH * 32, lane);
         } else if (chunk) {
-            // row g: query head g % G of member g / G
+            // q column g: query head g % G of member g / G
             const int g = lane >> 2, m = g / a.G;
             const int bm = m < PA_SHARE_MAX_ROWS / a.G ? s_members[m] : -1;
             st.load_q(a.q + ((int64_t)max(bm, 0) * a.Hq + h * a.G + g % a.G) * D, bm >= 0, lane & 3);
