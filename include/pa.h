@@ -154,6 +154,10 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
  * another layout must be zero-filled again.  Calls that share a workspace
  * must not overlap on the device.
  * ------------------------------------------------------------------------- */
+/* PA_FORCE_SPLITS=n in the environment (an integer in 1 .. 512, read once, at
+ * the first call) makes every request for the automatic choice use n as if it
+ * were passed: the split sweeps of long contexts without a code change.
+ * Other values are ignored; an explicit num_splits always wins. */
 int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits);
 size_t pa_decode_workspace_bytes(int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int max_blocks_per_seq, int num_splits);
@@ -348,6 +352,15 @@ pa_status pa_block_free(pa_allocator* a, const int32_t* ids, int n);
  * Management": 100 requests sharing one system prompt).  Every id must be
  * allocated; otherwise PA_ERR_INVALID and no change. */
 pa_status pa_block_share(pa_allocator* a, const int32_t* ids, int n);
+/* Fault injection for host-side failure tests ([P1] "KV cache memory math"
+ * and [P2] "Static versus continuous scheduling": a request is refused when
+ * the pool cannot hold its blocks): the n-th later pa_block_alloc call on this
+ * allocator that asks for at least one block fails with PA_ERR_OOM and takes
+ * nothing, whatever is free; that includes the allocations made inside
+ * pa_block_cow, pa_seq_admit, pa_seq_append_slot and pa_sched_continuous_kv.
+ * One shot: later calls succeed as usual.  n <= 0 disarms it.  PA_ERR_INVALID
+ * for a NULL allocator. */
+pa_status pa_allocator_fail_nth_alloc(pa_allocator* a, int64_t n);
 int pa_allocator_num_free(const pa_allocator* a);
 int pa_allocator_num_blocks(const pa_allocator* a);
 int pa_allocator_block_size(const pa_allocator* a);
@@ -525,7 +538,11 @@ pa_status pa_sched_simulate(const int64_t* out_lens, int n, int slots, int mode,
  * admitted_at[r] / finished_at[r] = iteration of admission / completion
  * (-1 if not reached); tables (n x max_blocks_per_seq, -1 padded) and
  * lens (tokens held) of the requests still active when it stops.
- * PA_ERR_INVALID on bad arguments or if a single request can never fit. */
+ * PA_ERR_INVALID on bad arguments or if a single request can never fit.  A
+ * reservation the pool refuses although the blocks looked free (see
+ * pa_allocator_fail_nth_alloc) leaves the request at the head of the queue
+ * for the next iteration; PA_ERR_OOM if no request is running then (every
+ * block this call took has been returned). */
 pa_status pa_sched_continuous_kv(pa_allocator* a, const int64_t* prompt_lens,
                                  const int64_t* out_lens, int n, int max_num_seqs,
                                  int64_t stop_iter, int max_blocks_per_seq, int64_t* iters,

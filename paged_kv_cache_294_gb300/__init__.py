@@ -76,6 +76,7 @@ def load(build_if_missing: bool = True):
         "pa_block_alloc": (i32, [P, i32, P]),
         "pa_block_free": (i32, [P, P, i32]),
         "pa_block_share": (i32, [P, P, i32]),
+        "pa_allocator_fail_nth_alloc": (i32, [P, i64]),
         "pa_allocator_num_free": (i32, [P]),
         "pa_allocator_num_blocks": (i32, [P]),
         "pa_allocator_refcount": (i32, [P, i32]),
@@ -479,6 +480,10 @@ class pa_allocator:
 
     def num_free(self) -> int:
         return int(self._lib.pa_allocator_num_free(self._h))
+
+    def fail_nth_alloc(self, n: int) -> None:
+        """Fault injection: the n-th later allocation of at least one block fails with OOM (n <= 0 disarms)."""
+        _check(self._lib.pa_allocator_fail_nth_alloc(self._h, int(n)), "pa_allocator_fail_nth_alloc")
 
     def refcount(self, i: int) -> int:
         return int(self._lib.pa_allocator_refcount(self._h, int(i)))

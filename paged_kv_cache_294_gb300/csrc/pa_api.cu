@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -155,6 +156,19 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int d, int S) {
 // Blocks per partition for a resolved split count.
 int part_blocks_for(int M, int S) { return (int)ceil_div(M, S < 1 ? 1 : S); }
 
+// PA_FORCE_SPLITS=n (a positive integer) in the environment stands in for an
+// explicit split count wherever the automatic one is asked for; read once.
+int forced_splits() {
+    static const int n = [] {
+        const char* v = getenv("PA_FORCE_SPLITS");
+        if (!v || !*v) return 0;
+        char* end = nullptr;
+        const long x = strtol(v, &end, 10);
+        return (*end == '\0' && x > 0 && x <= kMaxSplits) ? (int)x : 0;
+    }();
+    return n;
+}
+
 }  // namespace
 
 extern "C" {
@@ -174,6 +188,7 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
                        const void* k_new, const void* v_new, const int64_t* slot_mapping,
                        int num_tokens, int num_blocks, int num_kv_heads, int head_dim,
                        int block_size, int kv_dtype, void* stream) {
+    pa::CallRange range("pa_kv_append");
     if (num_tokens < 0 || !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
         return PA_ERR_INVALID;
     const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
@@ -193,6 +208,7 @@ pa_status pa_kv_append(void* k_cache, void* v_cache, float* k_scale, float* v_sc
 int pa_decode_resolve_splits(int batch, int num_kv_heads, int max_blocks_per_seq, int num_splits) {
     if (batch <= 0 || num_kv_heads <= 0 || max_blocks_per_seq <= 0) return 1;
     const int M = max_blocks_per_seq;
+    if (num_splits <= 0) num_splits = forced_splits();
     if (num_splits > 0) {
         int S = num_splits > M ? M : num_splits;
         if (S > kMaxSplits) S = kMaxSplits;
@@ -381,6 +397,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_cache, con
                               int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
                               void* workspace, size_t workspace_bytes, int kv_dtype,
                               void* stream) {
+    pa::CallRange range("pa_decode_attention");
     return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
                        scale, num_splits, workspace, workspace_bytes, kv_dtype, stream, nullptr, nullptr);
@@ -391,6 +408,7 @@ pa_status pa_decode_step(void* out, const void* q, const void* k_new, const void
                          const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
                          int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
                          int num_splits, void* workspace, size_t workspace_bytes, int kv_dtype, void* stream) {
+    pa::CallRange range("pa_decode_step");
     if (batch > 0 && (!k_new || !v_new)) return PA_ERR_INVALID;
     return decode_impl(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
                        num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks,
@@ -413,6 +431,7 @@ pa_status pa_decode_step_shared(void* out, const void* q, const void* k_new, con
                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                                 int max_blocks_per_seq, int num_blocks, float scale, int num_splits,
                                 void* workspace, size_t workspace_bytes, int kv_dtype, void* stream) {
+    pa::CallRange range("pa_decode_step_shared");
     if (n_chunks < 0 || max_chunk_blocks < 0) return PA_ERR_INVALID;
     if (n_chunks > 0) {
         if (!chunk_of || !chunk_members || !chunk_blocks || max_chunk_blocks < 1 ||
@@ -439,6 +458,7 @@ pa_status pa_decode_step_shared(void* out, const void* q, const void* k_new, con
 pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale, const int32_t* src,
                          const int32_t* dst, int n, int num_blocks, int num_kv_heads, int head_dim, int block_size,
                          int kv_dtype, void* stream) {
+    pa::CallRange range("pa_copy_blocks");
     if (n < 0 || !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)) return PA_ERR_INVALID;
     const pa_status ks = kernel_shape(head_dim, block_size, kv_dtype);
     if (ks != PA_OK) return ks;
@@ -456,6 +476,7 @@ pa_status pa_prefill_attention(void* out, const void* q, const void* k_cache, co
                                const int32_t* seq_lens, const int32_t* q_start, int batch, int num_q_heads,
                                int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                                int num_blocks, int max_q_len, float scale, int kv_dtype, void* stream) {
+    pa::CallRange range("pa_prefill_attention");
     if (batch < 0 || num_q_heads <= 0 || max_blocks_per_seq <= 0 || max_q_len < 0 ||
         !shape_ok(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype))
         return PA_ERR_INVALID;

@@ -25,6 +25,7 @@ struct pa_allocator {
     std::set<int32_t> free_ids;
     int attached = 0;       // prefix caches created on this allocator and not yet destroyed
     bool released = false;  // pa_allocator_destroy was called while caches were attached
+    int64_t fail_in = 0;    // > 0: the fail_in-th next allocation fails (pa_allocator_fail_nth_alloc)
 };
 
 namespace pa {
@@ -66,6 +67,7 @@ void pa_allocator_destroy(pa_allocator* a) {
 
 pa_status pa_block_alloc(pa_allocator* a, int n, int32_t* out_ids) {
     if (!a || n < 0 || (n > 0 && !out_ids)) return PA_ERR_INVALID;
+    if (n > 0 && a->fail_in > 0 && --a->fail_in == 0) return PA_ERR_OOM;   // injected
     if ((size_t)n > a->free_ids.size()) return PA_ERR_OOM;
     for (int k = 0; k < n; ++k) {
         auto it = a->free_ids.begin();
@@ -97,6 +99,12 @@ pa_status pa_block_share(pa_allocator* a, const int32_t* ids, int n) {
     for (int k = 0; k < n; ++k)
         if (ids[k] < 0 || ids[k] >= a->num_blocks || a->refcnt[ids[k]] == 0) return PA_ERR_INVALID;
     for (int k = 0; k < n; ++k) a->refcnt[ids[k]]++;
+    return PA_OK;
+}
+
+pa_status pa_allocator_fail_nth_alloc(pa_allocator* a, int64_t n) {
+    if (!a) return PA_ERR_INVALID;
+    a->fail_in = n > 0 ? n : 0;
     return PA_OK;
 }
 
@@ -276,18 +284,25 @@ pa_status pa_sched_continuous_kv(pa_allocator* a, const int64_t* prompt_lens,
     }
     int64_t it = 0;
     while ((!queue.empty() || !active.empty()) && (stop_iter < 0 || it < stop_iter)) {
-        // admission: in arrival order while a sequence slot and the reservation fit
+        // admission: in arrival order while a sequence slot and the reservation fit;
+        // a reservation the pool refuses leaves the request queued, like a full pool
+        bool refused = false;
         while (!queue.empty() && (int)active.size() < max_num_seqs) {
             const int r = queue.front();
             const int64_t need = pa_blocks_for_tokens(prompt_lens[r] + out_lens[r], a->block_size);
             if ((int64_t)a->free_ids.size() < need) break;
             Req q{r, 0, std::vector<int32_t>((size_t)need)};
-            if (pa_block_alloc(a, (int)need, q.blocks.data()) != PA_OK) return PA_ERR_OOM;
+            if (pa_block_alloc(a, (int)need, q.blocks.data()) != PA_OK) {
+                refused = true;
+                break;
+            }
             active.push_back(std::move(q));
             queue.pop_front();
             if (admitted_at) admitted_at[r] = it;
         }
-        if (active.empty()) return PA_ERR_INVALID;  // head of the queue can never fit
+        // nothing can run: the pool refused the head (it holds nothing of this
+        // call now), or the head can never fit
+        if (active.empty()) return refused ? PA_ERR_OOM : PA_ERR_INVALID;
         // one decode iteration: every active request produces one token
         std::vector<Req> keep;
         keep.reserve(active.size());

@@ -6,11 +6,24 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <algorithm>
 
 #include "../../include/pa.h"
 
 namespace pa {
+
+// An NVTX range named after a C entry point, open for the host side of the
+// call (checks, planning, launch), so that a profiler's timeline shows which
+// call queued which kernels.  Without a profiler attached, a push or a pop is
+// one call through an empty hook.
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 struct AppendLaunch {
     void* k_cache;

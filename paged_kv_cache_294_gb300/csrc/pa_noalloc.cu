@@ -93,6 +93,7 @@ extern "C" pa_status pa_decode_attention_static_ws(
     const float* v_scale, const int32_t* block_tables, const int32_t* seq_lens, int batch,
     int num_q_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
     int num_blocks, float scale, int num_splits, int kv_dtype, void* stream) {
+    pa::CallRange range("pa_decode_attention_static_ws");
     // every argument check first: a refused call queues no work on the array
     const pa_status chk = pa::decode_check(out, q, k_cache, v_cache, k_scale, v_scale, block_tables, seq_lens, batch,
                                            num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
