@@ -85,6 +85,12 @@ SHAPES = [
     (5, 8, 1, 128, 16, "int4"),
     (5, 16, 2, 128, 16, "int4"),
     (5, 6, 3, 128, 32, "int4"),
+    # odd group sizes: a lane's second head column (2c + 1) is padding for some c
+    (5, 24, 8, 128, 16, "bf16"),    # G = 3
+    (5, 10, 2, 64, 16, "bf16"),     # G = 5, head_dim 64
+    (5, 12, 2, 128, 32, "fp8"),     # G = 6
+    (5, 14, 2, 128, 16, "int8"),    # G = 7
+    (5, 21, 3, 128, 32, "int4"),    # G = 7, an odd kv-head count
 ]
 
 
