@@ -124,7 +124,7 @@ struct WarpAcc {
     float m[2], l[2];
     float o[D / 16][4];
     uint32_t qa[D / 16][2];   // q of head g as the Q.K^T B operand
-    float qbias[2];   // int8 cache: 1152 * sum of head 2c + e's f16 q (see the QK product)
+    float qbias[2];   // int8 / int4 caches: the K codes' offset times head 2c + e's q (see load_q)
     // coded caches: O is kept in units of vref (the largest V scale so far) and
     // psi sums the f16 probabilities P' = P * vsc / vref of each head (see the
     // P.V product); publish() turns O back into values
@@ -150,13 +150,15 @@ struct WarpAcc {
             } else if (KVT == KV_INT4) {
                 // step 2ch + j2 of chunk ch: lane c's elements e_i = 32ch + 8c + i in
                 // the order the nibble conversion yields them: {e0,e4},{e1,e5} then
-                // {e2,e6},{e3,e7}
+                // {e2,e6},{e3,e7}.  The K operand holds 1032 + c for the even
+                // elements (low nibbles) and 1152 + 16c for the odd ones (high
+                // nibbles): q of an odd element enters as q / 16
                 const int ch = ks >> 1, j2 = ks & 1;
                 const uint4 w = *reinterpret_cast<const uint4*>(qrow + ch * 32 + 8 * c);
                 const uint32_t u[4] = {w.x, w.y, w.z, w.w};
                 auto el = [&](int i) { return __uint_as_float((i & 1) ? (u[i >> 1] & 0xFFFF0000u) : (u[i >> 1] << 16)); };
                 qa[ks][0] = pack_f16x2(el(2 * j2), el(2 * j2 + 4));
-                qa[ks][1] = pack_f16x2(el(2 * j2 + 1), el(2 * j2 + 5));
+                qa[ks][1] = pack_f16x2(el(2 * j2 + 1) * 0.0625f, el(2 * j2 + 5) * 0.0625f);
             } else if (FP8) {
                 // k order inside a 16-deep step matches the e4m3 byte order 4c .. 4c+3
                 const uint2 w = *reinterpret_cast<const uint2*>(qrow + ks * 16 + 4 * c);
@@ -168,23 +170,29 @@ struct WarpAcc {
             }
         }
         qbias[0] = qbias[1] = 0.f;
-        if (KVT == KV_INT8) {
-            // the K operand carries 1152 + c per element: the scores carry
-            // 1152 * sum_k q_k on top, summed here over the same f16 values
-            float sum = 0.f;
+        if (KVT == KV_INT8 || KVT == KV_INT4) {
+            // the K operand carries an offset per element (int8: 1152 + c;
+            // int4: 1032 + c, and 1152 + 16c against q / 16): the scores carry
+            // sum_k q_k * offset_k on top, summed here over the same f16 values
+            float sum = 0.f, sum_hi = 0.f;
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&qa[ks][j]));
-                    sum += f.x + f.y;
+                    if (KVT == KV_INT4 && j == 1)
+                        sum_hi += f.x + f.y;
+                    else
+                        sum += f.x + f.y;
                 }
             }
+            if (KVT == KV_INT4) sum = kS4BiasLo * sum + kS4BiasHi * sum_hi;
             sum += __shfl_xor_sync(0xffffffffu, sum, 1);
             sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+            if (KVT == KV_INT8) sum *= kS8Bias;
             // lanes 8c and 8c + 4 hold heads 2c and 2c + 1
-            qbias[0] = kS8Bias * __shfl_sync(0xffffffffu, sum, 8 * c);
-            qbias[1] = kS8Bias * __shfl_sync(0xffffffffu, sum, 8 * c + 4);
+            qbias[0] = __shfl_sync(0xffffffffu, sum, 8 * c);
+            qbias[1] = __shfl_sync(0xffffffffu, sum, 8 * c + 4);
         }
     }
 
@@ -212,8 +220,9 @@ struct WarpAcc {
                 for (int kk = 0; kk < C::KT; ++kk) {
                     const int t = kk * 16 + g;
                     uint32_t f0[4], f1[4];
-                    nib8_to_f16x2(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t, (ks >> 1) * 16 + 4 * c)), f0);
-                    nib8_to_f16x2(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t + 8, (ks >> 1) * 16 + 4 * c)), f1);
+                    // offset codes; qbias comes off each score below
+                    nib8_to_f16x2_raw(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t, (ks >> 1) * 16 + 4 * c)), f0);
+                    nib8_to_f16x2_raw(ld_shared_u32(tok_addr<BS, KVT, CHS>(kt, t + 8, (ks >> 1) * 16 + 4 * c)), f1);
                     const uint32_t A0[4] = {f0[0], f1[0], f0[1], f1[1]};
                     const uint32_t A1[4] = {f0[2], f1[2], f0[3], f1[3]};
                     mma_f16(acc[kk], A0, qa[ks][0], qa[ks][1]);
@@ -252,7 +261,7 @@ struct WarpAcc {
         // ------------------------------------------------ online softmax
         float sc[C::KT][4];
         float mx[2] = {-INFINITY, -INFINITY};
-        const float sb[2] = {-qbias[0] * sl2, -qbias[1] * sl2};   // 0 but for the int8 cache
+        const float sb[2] = {-qbias[0] * sl2, -qbias[1] * sl2};   // 0 but for the int8 and int4 caches
 #pragma unroll
         for (int kk = 0; kk < C::KT; ++kk) {
 #pragma unroll
