@@ -91,10 +91,9 @@ struct Cfg {
     static constexpr int NCW = 4;               // consumer warps
     static constexpr int WPH = NCW / HPC;       // consumer warps per kv head
     static constexpr int NTHREADS = (NCW + 1) * 32;
-    static constexpr int NT = BS / 8;           // 8-token column tiles per page (QK)
     static constexpr int KS = D / 16;           // 16-deep steps over head_dim (QK)
     static constexpr int MT = D / 16;           // 16-row tiles of head_dim (PV)
-    static constexpr int KT = BS / 16;          // 16-token steps (PV)
+    static constexpr int KT = BS / 16;          // 16-token row tiles (QK) and steps (PV) per page
     static constexpr int COMBINE_FLOATS = NCW * (8 * D + 16);
     static_assert(I4 ? ROWB == 64 : ROWB % 128 == 0, "rows must be whole 128-byte chunks (int4: half of one)");
 };
