@@ -29,8 +29,9 @@
 // Coded caches (e4m3, int8, int4 codes with one fp32 scale per (block, kv
 // head)): the producers land each page's codes in the upper part of its
 // stage, and four more warps (20-23; two for K, two for V) expand them in
-// place to exact f16 values in the layout a bf16 tile would have.  The MMAs
-// then run on f16 operands (Q, K, P, V all f16).  The K producer also passes
+// place to exact f16 values in the layout a bf16 tile would have (int4:
+// with each 8-dim unit in the expansion's own order, which Q and the output
+// store follow).  The MMAs then run on f16 operands (Q, K, P, V all f16).  The K producer also passes
 // each page's K and V scales through a four-slot ring; the softmax folds the
 // K scale into the scores and the V scale into the probabilities, relative to
 // the largest V scale of the tile's sequence seen so far (vref), so O
@@ -266,15 +267,34 @@ __device__ __forceinline__ void zero_tile_rows(uint32_t tile, int r0, uint32_t b
     }
 }
 
-// eight int4 codes (nibbles 0..7 of w, element j in nibble j) -> four f16x2
-// in element order: {e0, e1}, {e2, e3}, {e4, e5}, {e6, e7}; exact.
-__device__ __forceinline__ void nib8_to_f16x2_ordered(uint32_t w, uint32_t (&o)[4]) {
-    uint32_t f[4];
-    nib8_to_f16x2(w, f);   // {e0, e4}, {e1, e5}, {e2, e6}, {e3, e7}
-    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o[0]) : "r"(f[0]), "r"(f[1]));
-    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(o[1]) : "r"(f[2]), "r"(f[3]));
-    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o[2]) : "r"(f[0]), "r"(f[1]));
-    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(o[3]) : "r"(f[2]), "r"(f[3]));
+// int4 caches: the f16 K and V tiles hold each 8-dim unit in the order the
+// nibble expansion yields it, dims {0, 4, 1, 5, 2, 6, 3, 7} (four operations
+// per eight codes fewer than putting it back).  Q takes the same order, so
+// Q.K^T is unchanged; O's columns come out in it, and the output store puts
+// them back.  This turns a unit of four f16x2 words in dim order into that
+// order.
+__device__ __forceinline__ void to_nibble_order(uint32_t& x, uint32_t& y, uint32_t& z, uint32_t& w) {
+    uint32_t a, b, c, d;
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(a) : "r"(x), "r"(z));   // dims 0, 4
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(b) : "r"(x), "r"(z));   // dims 1, 5
+    asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(c) : "r"(y), "r"(w));   // dims 2, 6
+    asm("prmt.b32 %0, %1, %2, 0x7632;" : "=r"(d) : "r"(y), "r"(w));   // dims 3, 7
+    x = a;
+    y = b;
+    z = c;
+    w = d;
+}
+
+// Eight O columns of one output unit (o[0..7], int4 caches: in the nibble
+// order above) scaled by inv, as bf16 in dim order.
+template <int KVT>
+__device__ __forceinline__ uint4 out_unit(const float* o, float inv) {
+    if constexpr (KVT == KV_INT4)
+        return make_uint4(pack_bf16x2(o[0] * inv, o[2] * inv), pack_bf16x2(o[4] * inv, o[6] * inv),
+                          pack_bf16x2(o[1] * inv, o[3] * inv), pack_bf16x2(o[5] * inv, o[7] * inv));
+    else
+        return make_uint4(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv),
+                          pack_bf16x2(o[4] * inv, o[5] * inv), pack_bf16x2(o[6] * inv, o[7] * inv));
 }
 
 // Shared address of the 16-byte f16 unit holding dims 8u .. 8u + 7 of row r
@@ -313,9 +333,9 @@ __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, 
             const int r = 2 * i + (c >> 2);
             const uint32_t w[4] = {ch[c].x, ch[c].y, ch[c].z, ch[c].w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {   // word k: dims 32 (c % 4) + 8 k .. + 7
+            for (int k = 0; k < 4; ++k) {   // word k: dims 32 (c % 4) + 8 k .. + 7, in nibble order
                 uint32_t o[4];
-                nib8_to_f16x2_ordered(w[k], o);
+                nib8_to_f16x2(w[k], o);
                 st_shared_v4(f16_unit(tile, r, 4 * (c & 3) + k), o[0], o[1], o[2], o[3]);
             }
         }
@@ -678,6 +698,10 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) qv[i] = bf16x2_to_f16x2(qv[i]);
             }
+            if constexpr (KVT == KV_INT4) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) to_nibble_order(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
+            }
             tmem_st16u(tmem + lane_off + COL_Q + qc * 16, qv);
             tc_fence_before();
             mbar_arrive(&bars.q_full);
@@ -811,11 +835,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                 tmem_ld32(tmem + lane_off + COL_O + qc * NCOL, o);
                 if (valid_row) {
 #pragma unroll
-                    for (int v = 0; v < NCOL / 8; ++v)
-                        dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                            pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                            pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                            pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                    for (int v = 0; v < NCOL / 8; ++v) dst[v] = out_unit<KVT>(o + 8 * v, inv);
                 }
             }
         }
@@ -1057,6 +1077,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                     v.z = bf16x2_to_f16x2(v.z);
                     v.w = bf16x2_to_f16x2(v.w);
                 }
+                if constexpr (KVT == KV_INT4) to_nibble_order(v.x, v.y, v.z, v.w);
                 const int u = (qc & 1) * 4 + i;
                 st_shared_v4(row + ((u ^ (r & 7)) << 4), v.x, v.y, v.z, v.w);
             }
@@ -1186,11 +1207,7 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                 uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)(qs0 + tok[t]) * a.Hq + h * G + g) * D) +
                              qc * (NCOL / 8);
 #pragma unroll
-                for (int v = 0; v < NCOL / 8; ++v)
-                    dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                for (int v = 0; v < NCOL / 8; ++v) dst[v] = out_unit<KVT>(o + 8 * v, inv);
             }
         }
     }
