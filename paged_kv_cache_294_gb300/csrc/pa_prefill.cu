@@ -247,6 +247,29 @@ __device__ __forceinline__ float q_row_f16_sum(const __nv_bfloat16* qrow, bool v
     return sum;
 }
 
+// The offset that int4 K tiles holding 1032 + c (even dims, low nibbles) and
+// 1152 + 16c (odd dims, high nibbles, met by q / 16) add to each score of a q
+// row: 1032 * (sum of its even-dim f16 q) + 72 * (sum of its odd-dim ones).
+__device__ __forceinline__ float q_row_int4_bias(const __nv_bfloat16* qrow, bool valid) {
+    float even = 0.f, odd = 0.f;
+    if (valid) {
+        const uint4* src = reinterpret_cast<const uint4*>(qrow);
+#pragma unroll
+        for (int u = 0; u < D / 8; ++u) {
+            const uint4 v = __ldg(src + u);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t h = bf16x2_to_f16x2(w[k]);
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+                even += f.x;
+                odd += f.y;
+            }
+        }
+    }
+    return kS4BiasLo * even + (kS4BiasHi / 16.f) * odd;
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
@@ -335,7 +358,10 @@ __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, 
 #pragma unroll
             for (int k = 0; k < 4; ++k) {   // word k: dims 32 (c % 4) + 8 k .. + 7, in nibble order
                 uint32_t o[4];
-                nib8_to_f16x2(w[k], o);
+                if constexpr (BIASED)
+                    nib8_to_f16x2_raw(w[k], o);   // 1032 + c, 1152 + 16c: the softmax takes the offset off
+                else
+                    nib8_to_f16x2(w[k], o);
                 st_shared_v4(f16_unit(tile, r, 4 * (c & 3) + k), o[0], o[1], o[2], o[3]);
             }
         }
@@ -576,7 +602,8 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         const bool is_k = warp < W_VCONV;
         const int i = tid - (is_k ? W_KCONV : W_VCONV) * 32;
         if (is_k)
-            convert_ring<KVT, KST, KVT == KV_INT8>(bars.kfull, bars.kconv, &bars.krd, sbase + OFF_K, nT, i, abort);
+            convert_ring<KVT, KST, KVT == KV_INT8 || KVT == KV_INT4>(bars.kfull, bars.kconv, &bars.krd, sbase + OFF_K,
+                                                                     nT, i, abort);
         else
             convert_ring<KVT, VST>(bars.vfull, bars.vconv, &bars.vrd, sbase + OFF_V, nT, i, abort);
     } else if (warp == W_QK) {
@@ -699,8 +726,17 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
                 for (int i = 0; i < 16; ++i) qv[i] = bf16x2_to_f16x2(qv[i]);
             }
             if constexpr (KVT == KV_INT4) {
+                // the K tiles' odd dims hold 1152 + 16c: their q enters as q / 16
+                const __half2 s16 = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
 #pragma unroll
-                for (int u = 0; u < 4; ++u) to_nibble_order(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
+                for (int u = 0; u < 4; ++u) {
+                    to_nibble_order(qv[4 * u], qv[4 * u + 1], qv[4 * u + 2], qv[4 * u + 3]);
+#pragma unroll
+                    for (int o = 1; o < 4; o += 2) {
+                        __half2 hq = __hmul2(*reinterpret_cast<const __half2*>(&qv[4 * u + o]), s16);
+                        qv[4 * u + o] = *reinterpret_cast<uint32_t*>(&hq);
+                    }
+                }
             }
             tmem_st16u(tmem + lane_off + COL_Q + qc * 16, qv);
             tc_fence_before();
@@ -710,10 +746,12 @@ __global__ void __launch_bounds__(PfCfg<KVT>::NT, 1)
         float m = -INFINITY, l = 0.f;   // running max (scaled, log2 units) and this quarter's sum
         // coded caches: O is kept in units of vref, the largest V scale seen
         float vref = 0.f, inv_vref = 0.f;
-        // int8: the offset the biased K codes add to this row's scores
-        const float kbias = KVT == KV_INT8 && live
-                                ? kS8Bias * q_row_f16_sum(a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D, valid_row)
-                                : 0.f;
+        // int8 / int4: the offset the K tiles' offset codes add to this row's scores
+        const __nv_bfloat16* qrow = a.q + ((int64_t)(qs0 + tok) * a.Hq + h * G + g) * D;
+        const float kbias = !live               ? 0.f
+                            : KVT == KV_INT8 ? kS8Bias * q_row_f16_sum(qrow, valid_row)
+                            : KVT == KV_INT4 ? q_row_int4_bias(qrow, valid_row)
+                                             : 0.f;
         bool ok = true;
         for (int j = 0; j < nT; ++j) {
             const int s = j & 1;
