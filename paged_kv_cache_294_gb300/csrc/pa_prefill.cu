@@ -31,11 +31,12 @@
 // stage, and four more warps (20-23; two for K, two for V) expand them in
 // place to exact f16 values in the layout a bf16 tile would have (int4:
 // with each 8-dim unit in the expansion's own order, which Q and the output
-// store follow).  The MMAs then run on f16 operands (Q, K, P, V all f16).  The K producer also passes
-// each page's K and V scales through a four-slot ring; the softmax folds the
-// K scale into the scores and the V scale into the probabilities, relative to
-// the largest V scale of the tile's sequence seen so far (vref), so O
-// accumulates in units of vref and is rescaled when vref grows.
+// store follow).  The MMAs then run on f16 operands (Q, K, P, V all f16).
+// The K producer also passes each page's K and V scales through a four-slot
+// ring; the softmax folds the K scale into the scores and the V scale into
+// the probabilities, relative to the largest V scale of the tile's sequence
+// seen so far (vref), so O accumulates in units of vref and is rescaled when
+// vref grows.
 //
 // Tensor memory (32-bit columns): S0 [0,128), S1 [128,256), O [256,384)
 // in fp32; Q [384,448) as bf16 pairs.  P_j (bf16 pairs) is written over the
@@ -331,9 +332,10 @@ __device__ __forceinline__ uint32_t f16_unit(uint32_t tile, int r, int u) {
 // swizzled) in place into exact f16 values.  Thread i < NCONV of the
 // converter group; int4 codes: `rd` is the group's read barrier (count
 // NCONV), in phase `rd_parity` for this tile.  Returns false on an abort.
-// BIASED (int8 K tiles): the codes expand to 1152 + c (the decode kernel's
-// trick, two operations per four codes fewer); every score then carries
-// 1152 * (sum of its q row), which the softmax takes off.
+// BIASED (K tiles of the one-tile kernel): int8 codes expand to 1152 + c
+// (the decode kernel's trick, two operations per four codes fewer), int4
+// codes to 1032 + c and 1152 + 16c (four fewer per eight codes); every score
+// then carries a per-row offset, which the softmax takes off.
 template <int KVT, bool BIASED = false>
 __device__ __forceinline__ bool expand_tile(uint32_t tile, int i, uint64_t* rd, uint32_t rd_parity,
                                             volatile int* abort) {
