@@ -172,6 +172,7 @@ class PagedDecodeLayer:
             self.k_scale = self.v_scale = None
         self.workspace: Optional[torch.Tensor] = None
         self._ws_key = None   # layout the workspace last served (its counters are zero for it)
+        self._layouts = {}    # (B, Hq, Hkv, d, M, num_splits) -> (workspace bytes, resolved split count)
 
     # ---------------------------------------------------------------- set-up
     def set_batch(self, block_tables: np.ndarray, seq_lens: np.ndarray):
@@ -202,8 +203,15 @@ class PagedDecodeLayer:
         return self.workspace
 
     def ensure_workspace(self, num_splits: int = 0) -> torch.Tensor:
-        need = pa_decode_workspace_bytes(self.B, self.Hq, self.Hkv, self.d, self.M, num_splits)
-        return self._workspace_for(("plain", self.num_splits(num_splits), need), need)
+        # the library's answers depend only on these arguments (the split
+        # override and the SM count are fixed per process): asked once per
+        # layout instead of on every step
+        key = (self.B, self.Hq, self.Hkv, self.d, self.M, int(num_splits))
+        lay = self._layouts.get(key)
+        if lay is None:
+            lay = self._layouts[key] = (pa_decode_workspace_bytes(*key), self.num_splits(num_splits))
+        need, S = lay
+        return self._workspace_for(("plain", S, need), need)
 
     def num_splits(self, num_splits: int = 0) -> int:
         return pa_decode_resolve_splits(self.B, self.Hkv, self.M, num_splits)
