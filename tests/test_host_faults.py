@@ -142,3 +142,29 @@ def test_force_splits_from_the_environment(env, expect):
     got = [int(x) for x in run(dict(plain, PA_FORCE_SPLITS=env))]
     assert got == (expect if expect is not None else auto)
     assert auto[2] == 5
+
+
+def test_refused_copy_on_write_of_a_forked_block():
+    """A fork shares the parent's partial last block; the parent's next token
+    needs a private copy of it.  A refused copy leaves both sequences as they
+    were; with cache-only blocks to give up, the library evicts one and tries
+    again."""
+    m = BlockManager(16, 4)
+    m.add(0, list(range(6)))                          # blocks: full [0..3], partial [4, 5]
+    m.fork(1, 0)
+    before = _pool(m.alloc, 16)
+    blocks0, blocks1 = list(m.blocks[0]), list(m.blocks[1])
+    m.alloc.fail_nth_alloc(1)
+    with pytest.raises(pa.PagedAttnError) as e:       # nothing the cache could give up
+        m.append(0, 99)
+    assert e.value.status == pa.PA_ERR_OOM and _pool(m.alloc, 16) == before
+    assert list(m.blocks[0]) == blocks0 and list(m.blocks[1]) == blocks1 and len(m.tokens(0)) == 6
+    # a finished, cached sequence leaves blocks only the cache holds
+    m.add(2, list(range(100, 108)))
+    m.commit(2)
+    m.free(2)
+    assert m.cache.size() == 2
+    m.alloc.fail_nth_alloc(1)
+    slot, copy = m.append(0, 99)                      # refused once, one cached block evicted, then copied
+    assert copy is not None and copy[0] == blocks0[1] and m.cache.size() == 1
+    assert m.blocks[1] == blocks1 and m.alloc.refcount(blocks0[1]) == 1
